@@ -1,0 +1,414 @@
+/*
+ * orc.c -- the ORACLE for the speculative-decoding verify pass.
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the test suite, the package's smoke
+ * check and the CPU-baseline leg of the benchmark may load this library.  It shares no
+ * source, header, table or helper with the CUDA library and includes none of its files.
+ *
+ * Everything here is the plainest possible CPU restatement, in IEEE double precision,
+ * of what the verify pass computes.  Sources (cited by page title and section):
+ *
+ *   [P1] "100 tokens per second from a 27B model on a 24 GB AMD card" (curriculo.me),
+ *        sections "The wall" and "How speculative decoding gets past a per-token wall".
+ *   [P2] "Decode is memory-bound: the ~59 tok/s ceiling on an RTX 4090, and how
+ *        speculative decoding gets past it" (trefon.com), sections "The ceiling",
+ *        "Speculative decoding" and "Two things the math says to do".
+ *   [P3] Hacker News thread on speculative decoding (hn.shard-db.dev, item 49596054),
+ *        the comments explaining parallel verification ("D E F" example and the
+ *        [4, vocabulary_size] output tensor).
+ *
+ * Readings taken where the pages are silent are marked READING and listed in the
+ * design notes of the repository.
+ *
+ * Pins (what ties this file to something other than itself) live in tests/: brute
+ * force against a dense numpy matmul, closed forms of special cases, the worked greedy
+ * example of [P3], Monte-Carlo exactness of the sampled output distribution, the
+ * E[tokens per pass] table of [P2] and the Philox known-answer vectors.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <math.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------------------------ */
+/* Number formats, decoded from their definitions.                                      */
+/* ------------------------------------------------------------------------------------ */
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+double orc_f16_to_f64(uint16_t h)
+{
+    int sign = (h >> 15) & 1, e = (h >> 10) & 0x1f, m = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);                 /* subnormal: m * 2^-14 * 2^-10 */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + m), e - 25);     /* (1 + m/2^10) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* bfloat16: the upper half of an IEEE binary32 (8 exponent bits, bias 127, 7 fraction). */
+double orc_bf16_to_f64(uint16_t b)
+{
+    int sign = (b >> 15) & 1, e = (b >> 7) & 0xff, m = b & 0x7f;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -133);                /* m * 2^-126 * 2^-7 */
+    else if (e == 255)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(128 + m), e - 134);     /* (1 + m/2^7) * 2^(e-127) */
+    return sign ? -v : v;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Verify linear: one read of a block-quantised 4-bit weight matrix applied to the K+1  */
+/* activation columns of a verify window ([P1] "How speculative decoding gets past a     */
+/* per-token wall": the weights are read once and applied to a K-wide batch;            */
+/* [P3]: every layer runs once over all window positions).                              */
+/*                                                                                      */
+/* Weight format: 4-bit code c in 0..15 with value s * (c - 8), one fp16 scale s per 32 */
+/* consecutive inputs of an output row.  Storage (READING: the pages fix none):         */
+/*   codes [out][in/2] bytes, input 2t in the low nibble and 2t+1 in the high nibble;   */
+/*   scales[out][in/32] fp16 bit patterns.                                              */
+/* Activations x[C][in] are bfloat16 bit patterns; the result is                        */
+/*   y[c][j] = sum_i s[j][i/32] * (code[j][i] - 8) * x[c][i]                            */
+/* and a[c][j] = sum_i |s * (code - 8) * x| (the scale of the parity tolerance).        */
+/* ------------------------------------------------------------------------------------ */
+void orc_verify_linear(const uint8_t *codes, const uint16_t *scales, int64_t in_f,
+                       int64_t out_f, const uint16_t *x_bf16, int64_t C, double *y,
+                       double *a, int nthreads)
+{
+    double *x = (double *)malloc(sizeof(double) * (size_t)(C * in_f));
+    for (int64_t t = 0; t < C * in_f; ++t)
+        x[t] = orc_bf16_to_f64(x_bf16[t]);
+    if (nthreads <= 0) nthreads = 1;
+#pragma omp parallel num_threads(nthreads)
+    {
+        double *acc = (double *)malloc(sizeof(double) * (size_t)(2 * C));
+#pragma omp for schedule(static)
+        for (int64_t j = 0; j < out_f; ++j) {
+            for (int64_t c = 0; c < 2 * C; ++c) acc[c] = 0.0;
+            for (int64_t i = 0; i < in_f; ++i) {
+                uint8_t byte = codes[j * (in_f / 2) + i / 2];
+                int code = (i & 1) ? (byte >> 4) : (byte & 15);
+                double w = orc_f16_to_f64(scales[j * (in_f / 32) + i / 32]) * (double)(code - 8);
+                for (int64_t c = 0; c < C; ++c) {
+                    double t = w * x[c * in_f + i];
+                    acc[c] += t;
+                    acc[C + c] += fabs(t);
+                }
+            }
+            for (int64_t c = 0; c < C; ++c) {
+                y[c * out_f + j] = acc[c];
+                if (a) a[c * out_f + j] = acc[C + c];
+            }
+        }
+        free(acc);
+    }
+    free(x);
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Sampler: temperature, min-p and top-p ([P2] "Two things the math says to do": the    */
+/* production settings temperature 0.6, top-p 0.95, min-p 0.05; [P1] "The last mile":   */
+/* the sampled path at temperature 0.6 and top-p 0.95).                                 */
+/*                                                                                      */
+/* READING (the pages give only the constants):                                         */
+/*   1. z = logit / T, p = softmax(z) in double;                                        */
+/*   2. min-p keeps v iff p[v] >= min_p * max(p);                                       */
+/*   3. top-p orders tokens by (p descending, id ascending) and keeps the shortest      */
+/*      prefix whose mass reaches top_p, the crossing token included; top_p >= 1 keeps  */
+/*      everything;                                                                     */
+/*   4. both filters read the same un-renormalised p; the kept set is their             */
+/*      intersection, which is again a prefix of that order;                            */
+/*   5. the kept probabilities are renormalised to sum to one.                          */
+/* greedy != 0 returns the one-hot distribution of the argmax (lowest id on ties).      */
+/* The returned flags mark decisions that sit within a rounding tolerance of their      */
+/* boundary (bit 0: min-p, relative 1e-6; bit 1: top-p, 1e-5 of the mass), where an     */
+/* implementation in another precision may legitimately decide the other way.           */
+/* ------------------------------------------------------------------------------------ */
+typedef struct { double p; int64_t id; } orc_rank_t;
+
+static int orc_rank_cmp(const void *A, const void *B)
+{
+    const orc_rank_t *a = (const orc_rank_t *)A, *b = (const orc_rank_t *)B;
+    if (a->p > b->p) return -1;
+    if (a->p < b->p) return 1;
+    return (a->id < b->id) ? -1 : (a->id > b->id);
+}
+
+int orc_sampler_row(const float *logits, int64_t V, double T, double top_p, double min_p,
+                    int greedy, double *probs, int32_t *argmax_out, int64_t *n_kept_out)
+{
+    int flags = 0;
+    int64_t am = 0;
+    for (int64_t v = 1; v < V; ++v)
+        if (logits[v] > logits[am]) am = v;          /* strict: lowest id wins ties */
+    if (argmax_out) *argmax_out = (int32_t)am;
+    if (greedy) {
+        for (int64_t v = 0; v < V; ++v) probs[v] = (v == am) ? 1.0 : 0.0;
+        if (n_kept_out) *n_kept_out = 1;
+        return 0;
+    }
+    double zmax = (double)logits[am] / T, Z = 0.0;
+    for (int64_t v = 0; v < V; ++v) {
+        probs[v] = exp((double)logits[v] / T - zmax);
+        Z += probs[v];
+    }
+    for (int64_t v = 0; v < V; ++v) probs[v] /= Z;
+    double pmax = probs[am];
+
+    char *keep = (char *)calloc((size_t)V, 1);
+    for (int64_t v = 0; v < V; ++v) {
+        double thr = min_p * pmax;
+        keep[v] = probs[v] >= thr;
+        if (min_p > 0.0 && fabs(probs[v] - thr) <= 1e-6 * thr) flags |= 1;
+    }
+    if (top_p < 1.0) {
+        orc_rank_t *r = (orc_rank_t *)malloc(sizeof(orc_rank_t) * (size_t)V);
+        for (int64_t v = 0; v < V; ++v) { r[v].p = probs[v]; r[v].id = v; }
+        qsort(r, (size_t)V, sizeof(orc_rank_t), orc_rank_cmp);
+        double cum = 0.0;
+        int64_t cut = V;                              /* number of ranks top-p keeps */
+        for (int64_t t = 0; t < V; ++t) {
+            double before = cum;
+            cum += r[t].p;
+            if (cum >= top_p) {
+                cut = t + 1;
+                if (fabs(cum - top_p) < 1e-5 || fabs(before - top_p) < 1e-5) flags |= 2;
+                break;
+            }
+        }
+        for (int64_t t = cut; t < V; ++t) keep[r[t].id] = 0;
+        free(r);
+    }
+    double S = 0.0;
+    int64_t nk = 0;
+    for (int64_t v = 0; v < V; ++v)
+        if (keep[v]) { S += probs[v]; ++nk; }
+    for (int64_t v = 0; v < V; ++v) probs[v] = keep[v] ? probs[v] / S : 0.0;
+    free(keep);
+    if (n_kept_out) *n_kept_out = nk;
+    return flags;
+}
+
+void orc_sampler(const float *logits, int64_t rows, int64_t V, double T, double top_p,
+                 double min_p, int greedy, double *probs, int32_t *argmax, int64_t *n_kept,
+                 int32_t *flags, int nthreads)
+{
+    if (nthreads <= 0) nthreads = 1;
+#pragma omp parallel for num_threads(nthreads) schedule(dynamic, 1)
+    for (int64_t r = 0; r < rows; ++r)
+        flags[r] = orc_sampler_row(logits + r * V, V, T, top_p, min_p, greedy, probs + r * V,
+                                   argmax ? argmax + r : NULL, n_kept ? n_kept + r : NULL);
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1,   */
+/* 2, 3", SC'11), written from the paper's definition: a 4-word counter, a 2-word key,  */
+/* ten rounds of two 32x32->64 multiplications with the round constants, the key        */
+/* advanced by the Weyl constants between rounds.                                       */
+/* ------------------------------------------------------------------------------------ */
+void orc_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4])
+{
+    uint32_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
+    uint32_t k0 = key_in[0], k1 = key_in[1];
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) { k0 += 0x9E3779B9u; k1 += 0xBB67AE85u; }
+        uint64_t prod0 = (uint64_t)0xD2511F53u * (uint64_t)c0;
+        uint64_t prod1 = (uint64_t)0xCD9E8D57u * (uint64_t)c2;
+        uint32_t hi0 = (uint32_t)(prod0 >> 32), lo0 = (uint32_t)prod0;
+        uint32_t hi1 = (uint32_t)(prod1 >> 32), lo1 = (uint32_t)prod1;
+        uint32_t n0 = hi1 ^ c1 ^ k0, n1 = lo1, n2 = hi0 ^ c3 ^ k1, n3 = lo0;
+        c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* The uniforms of window w (absolute index) and position i (READING: the pages name no
+ * generator): key = seed, counter = (w low, w high, i, 0).  Word 0 gives the acceptance
+ * uniform u, word 1 the resampling uniform u'; each is (word >> 8) * 2^-24 in [0, 1). */
+void orc_uniforms(uint64_t seed, uint64_t window, uint32_t pos, double *u, double *u2)
+{
+    uint32_t ctr[4] = {(uint32_t)window, (uint32_t)(window >> 32), pos, 0u};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t r[4];
+    orc_philox4x32_10(ctr, key, r);
+    *u = ldexp((double)(r[0] >> 8), -24);
+    *u2 = ldexp((double)(r[1] >> 8), -24);
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Acceptance ([P1] "How speculative decoding gets past a per-token wall"; [P2]         */
+/* "Speculative decoding"; [P3] the "D E F" example).                                   */
+/*                                                                                      */
+/* Greedy (q == NULL): emit x_i while x_i equals the target's argmax at position i; at  */
+/* the first mismatch j emit argmax_j; if all k drafts match emit argmax_k.  The        */
+/* argmax comes from target_argmax when given, else from p (lowest id on ties).         */
+/*                                                                                      */
+/* Sampled: for i = 0..k-1 accept x_i iff u_i * q_i(x_i) < p_i(x_i), which is accepting */
+/* with probability min(1, p/q); at the first rejection j emit a draw from the          */
+/* normalised positive part of p_j - q_j using u'_j; if all k are accepted, the target's */
+/* own token caps the window: a draw from p_k using u'_k.                               */
+/* A draw from weights r with total R emits the smallest v whose running sum C_v        */
+/* exceeds u' * R.                                                                      */
+/*                                                                                      */
+/* Status bits (READING for inputs the pages do not consider):                          */
+/*   1 draft id outside [0, V): that position is rejected;                              */
+/*   2 q_i(x_i) == 0 for a drafted token (the test u*q < p still decides);              */
+/*   4 a probability read is NaN, infinite, negative or above one (clamped into [0,1]);  */
+/*   8 the residual has zero mass (READING: the draw falls back to p_j);                */
+/*  16 the distribution drawn from has zero mass: no token is emitted there.            */
+/* near[w] is set when a draw's u' lies within 1e-6 of either edge of the chosen        */
+/* token's interval [C_{v-1}/R, C_v/R): there another summation order may pick a        */
+/* neighbour.                                                                           */
+/* ------------------------------------------------------------------------------------ */
+static double orc_prob(float f, int *st)
+{
+    double d = (double)f;
+    if (!(d >= 0.0 && d <= 1.0)) {                 /* NaN, negative, infinite or > 1 */
+        *st |= 4;
+        if (d > 1.0) return 1.0;
+        return 0.0;
+    }
+    return d;
+}
+
+static int64_t orc_draw(const float *pr, const float *qr, int64_t V, double u2, int *st,
+                        int *near)
+{
+    double *r = (double *)malloc(sizeof(double) * (size_t)V);
+    double R = 0.0;
+    if (qr) {
+        for (int64_t v = 0; v < V; ++v) {
+            double d = orc_prob(pr[v], st) - orc_prob(qr[v], st);
+            r[v] = d > 0.0 ? d : 0.0;
+            R += r[v];
+        }
+        if (!(R > 0.0)) *st |= 8;
+    }
+    if (!qr || !(R > 0.0)) {
+        R = 0.0;
+        for (int64_t v = 0; v < V; ++v) {
+            r[v] = orc_prob(pr[v], st);
+            R += r[v];
+        }
+    }
+    int64_t tok = -1;
+    if (R > 0.0) {
+        double t = u2 * R, Cprev = 0.0, Cv = 0.0;
+        for (int64_t v = 0; v < V; ++v) {
+            Cv = Cprev + r[v];
+            if (Cv > t) { tok = v; break; }
+            Cprev = Cv;
+        }
+        if (tok < 0) {                      /* only through rounding: last nonzero weight */
+            for (int64_t v = V - 1; v >= 0; --v)
+                if (r[v] > 0.0) { tok = v; break; }
+            Cprev = R - r[tok];
+            Cv = R;
+        }
+        if (fabs(u2 - Cprev / R) < 1e-6 || fabs(u2 - Cv / R) < 1e-6) *near = 1;
+    } else {
+        *st |= 16;
+    }
+    free(r);
+    return tok;
+}
+
+static int64_t orc_argmax_row(const float *row, int64_t V, int *st)
+{
+    int64_t am = -1;
+    for (int64_t v = 0; v < V; ++v) {
+        float f = row[v];
+        if (f != f) { *st |= 4; continue; }
+        if (am < 0 || f > row[am]) am = v;
+    }
+    return am;
+}
+
+void orc_accept(const float *p, const int64_t *p_rows, const float *q, const int64_t *q_rows,
+                const int32_t *target_argmax, const int32_t *draft, int64_t n, int k,
+                int64_t V, uint64_t seed, uint64_t window_offset, const float *uniforms,
+                int32_t *out_tokens, int32_t *n_emitted, int32_t *status, int32_t *near,
+                int nthreads)
+{
+    if (nthreads <= 0) nthreads = 1;
+#pragma omp parallel for num_threads(nthreads) schedule(dynamic, 16)
+    for (int64_t w = 0; w < n; ++w) {
+        int st = 0, nr = 0, ne = 0;
+        int32_t *tok = out_tokens + w * (k + 1);
+        for (int i = 0; i <= k; ++i) tok[i] = -1;
+        const float *prow[65], *qrow[65];
+        for (int i = 0; i <= k; ++i)
+            prow[i] = p + (p_rows ? p_rows[w * (k + 1) + i] : w * (k + 1) + i) * V;
+        if (q)
+            for (int i = 0; i < k; ++i)
+                qrow[i] = q + (q_rows ? q_rows[w * k + i] : w * k + i) * V;
+        if (!q) {
+            int i = 0;
+            for (; i <= k; ++i) {
+                int64_t a = target_argmax ? target_argmax[w * (k + 1) + i]
+                                          : orc_argmax_row(prow[i], V, &st);
+                if (a < 0 || a >= V) { st |= 16; break; }   /* no usable target token */
+                if (i < k && draft[w * k + i] == a) { tok[ne++] = (int32_t)a; continue; }
+                if (i < k && (draft[w * k + i] < 0 || draft[w * k + i] >= V)) st |= 1;
+                tok[ne++] = (int32_t)a;
+                break;
+            }
+        } else {
+            int i = 0;
+            for (; i < k; ++i) {
+                double u, u2;
+                if (uniforms) {
+                    u = uniforms[(w * (k + 1) + i) * 2];
+                    u2 = uniforms[(w * (k + 1) + i) * 2 + 1];
+                } else {
+                    orc_uniforms(seed, window_offset + (uint64_t)w, (uint32_t)i, &u, &u2);
+                }
+                int32_t x = draft[w * k + i];
+                int accept = 0;
+                if (x < 0 || x >= V) {
+                    st |= 1;
+                } else {
+                    double pv = orc_prob(prow[i][x], &st), qv = orc_prob(qrow[i][x], &st);
+                    if (qv == 0.0) st |= 2;
+                    accept = u * qv < pv;
+                }
+                if (accept) { tok[ne++] = x; continue; }
+                int64_t t = orc_draw(prow[i], qrow[i], V, u2, &st, &nr);
+                if (t >= 0) tok[ne++] = (int32_t)t;
+                break;
+            }
+            if (i == k) {
+                double u, u2;
+                if (uniforms) {
+                    u = uniforms[(w * (k + 1) + k) * 2];
+                    u2 = uniforms[(w * (k + 1) + k) * 2 + 1];
+                } else {
+                    orc_uniforms(seed, window_offset + (uint64_t)w, (uint32_t)k, &u, &u2);
+                }
+                (void)u;
+                int64_t t = orc_draw(prow[k], NULL, V, u2, &st, &nr);
+                if (t >= 0) tok[ne++] = (int32_t)t;
+            }
+        }
+        n_emitted[w] = ne;
+        status[w] = st;
+        if (near) near[w] = nr;
+    }
+}
+
+int orc_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
