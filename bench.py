@@ -1,0 +1,376 @@
+"""Benchmark: the 27B-shaped Q4 verify pass at K+1 = 4 on one GB300 (replicas on N GPUs).
+
+One step = one whole verify pass: 64 layers x 4 fused 4-bit verify-linear launches over the 4
+window columns, the lm_head (5120 x 151936) with the production sampler over the 4 positions, and
+the acceptance of the 3 drafts.  Inputs are synthetic (seeded), resident in HBM; the 11.9 GB of
+weights per step exceed the 129 MB L2, so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl svd|reference]
+
+Prints one JSON line on rank 0.  --impl reference times the fp64 CPU oracle on the host cores on
+a bounded sample of the same pass (one layer and 1/64 of the lm_head rows per step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "27B-shape Q4 verify passes/s at K+1=4"
+UNIT = "passes/s"
+WORKLOAD = ("27B-shaped dense Q4 verify pass, K+1=4: 64 layers x (qkv 5120x7168, o 5120x5120, "
+            "gate|up 5120x34816, down 17408x5120) + lm_head 5120x151936 + sampler "
+            "(T 0.6, top-p 0.95, min-p 0.05) + acceptance of 3 drafts")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        for key in ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs"):
+            if key in d:
+                return float(d[key]), "measured"
+    except Exception:
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_traffic():
+    """DRAM traffic per launch of the stack's verify-linear kernel from the committed ncu
+    summary, if it was taken on the current kernel source (else None)."""
+    src = os.path.join(ROOT, "speculative_decoding_verify_06_gb300", "csrc", "verify_linear.cu")
+    prof = os.path.join(ROOT, "profiles", "vl_mma_kernel_27b_stack_c4.txt")
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        txt = open(prof).read()
+        m_sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", txt)
+        m_tr = re.search(r"dram_bytes_per_stack_launch_avg:\s*([0-9.eE+]+)", txt)
+        if m_sha and m_tr and m_sha.group(1) == sha:
+            return float(m_tr.group(1))
+    except Exception:
+        pass
+    return None
+
+
+def _cpu_model() -> str:
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith(("model name", "cpu part", "hardware")):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine()
+
+
+class OracleSample:
+    """The oracle timed on the host on a bounded slice of the pass, scaled to passes/s.
+
+    A step runs, in fp64 on every host thread, the first `rows` rows of each of one layer's four
+    fused GEMMs and the matching share of the lm_head rows (1/64 of them per layer) at C = 4;
+    its time is scaled by (weights of a pass) / (weights sampled).  The sampler over the 4
+    positions and the acceptance of one window are timed once and added whole."""
+
+    def __init__(self, frac: float):
+        import numpy as np
+
+        import oracle
+        from speculative_decoding_verify_06_gb300 import synth
+        self.np, self.oracle, self.synth = np, oracle, synth
+        self.threads = oracle.max_threads()
+        C = 4
+        self.frac = frac
+        shapes = list(synth.LAYER_GEMMS) + [(synth.HIDDEN, synth.VOCAB // synth.LAYERS)]
+        self.mats, self.xs, self.sampled, self.full = [], [], 0, 0
+        for g, (i, o) in enumerate(shapes):
+            r = max(16, int(round(o * frac)))
+            self.mats.append(synth.qweight(r, i, seed=1000 + g))
+            self.xs.append(synth.activations(C, i, seed=2000 + g))
+            self.sampled += r * i
+            self.full += o * i
+        lg = synth.normal_logits(C, synth.VOCAB, seed=4, std=4.389)
+        t0 = time.perf_counter()
+        f32 = np.float32
+        p, *_ = oracle.sampler(lg, f32(0.6), f32(0.95), f32(0.05), nthreads=self.threads)
+        q, *_ = oracle.sampler(synth.perturb(lg[:3], 1.205, 5), f32(0.6), f32(0.95), f32(0.05),
+                               nthreads=self.threads)
+        d = synth.draw_from(q, 6).reshape(1, 3)
+        oracle.accept(p.astype(np.float32), d, q=q.astype(np.float32), seed=1, nthreads=self.threads)
+        self.t_tail = time.perf_counter() - t0
+
+    def step(self) -> float:
+        t0 = time.perf_counter()
+        for (c, s), x in zip(self.mats, self.xs):
+            self.oracle.verify_linear(c, s, x, nthreads=self.threads)
+        return time.perf_counter() - t0
+
+    def passes_per_s(self, step_times) -> float:
+        t_layer = statistics.mean(step_times) * self.full / self.sampled
+        return 1.0 / (self.synth.LAYERS * t_layer + self.t_tail)
+
+    def describe(self, n: int) -> str:
+        return (f"{n} step(s), each {self.sampled / 1e6:.1f}M of a layer's {self.full / 1e6:.1f}M "
+                f"weights (all four fused GEMMs and 1/64 of the lm_head, same fraction of rows) "
+                f"at C=4 in fp64, scaled to 64 layers; sampler (4+3 rows of 151936) and one "
+                f"acceptance window timed once ({self.t_tail:.2f} s) and added")
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    # size each step so that warm-up + timed steps stay near a minute of host time
+    probe = OracleSample(frac=1.0 / 64)
+    t_probe = probe.step()
+    budget_s = 60.0
+    frac = min(1.0, max(1.0 / 256, budget_s / max(1, args.steps + args.warmup) / (64 * t_probe)))
+    smp = OracleSample(frac=frac)
+    for _ in range(args.warmup):
+        smp.step()
+    times = [smp.step() for _ in range(args.steps)]
+    v = smp.passes_per_s(times)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / v,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "C": 4, "oracle": "fp64 C, OpenMP", "cpu": _cpu_model()},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": smp.threads, "kind": "oracle",
+                         "sample": smp.describe(args.steps)},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _gpu_id(dev) -> str:
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(dev.index or 0)
+
+
+def run_svd(args, rank, world, local_rank):
+    import torch
+
+    from speculative_decoding_verify_06_gb300 import build, roofline, stack, svd, synth
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    build.build_library()
+    vp = stack.VerifyPass(layers=args.layers, C=args.C, seed=rank, device=dev, pdl=not args.no_pdl)
+    vp.capture()
+    s = torch.cuda.current_stream(dev)
+    dist = world > 1
+    if dist:
+        import torch.distributed as td
+
+    for _ in range(args.warmup):
+        vp.launch(s)
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    if dist:
+        td.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(_gpu_id(dev)) as clk:
+        for i in range(K):
+            ev[i][0].record(s)
+            vp.launch(s, ev_mid=ev[i][1])
+            ev[i][2].record(s)
+        torch.cuda.synchronize(dev)
+    if dist:
+        td.barrier()
+    total_ms = ev[0][0].elapsed_time(ev[-1][2])
+    stack_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    tail_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    t_max = total_ms
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        td.all_reduce(t, op=td.ReduceOp.MAX)
+        t_max = float(t.item())
+    passes_per_s = world * K / (t_max / 1000.0)
+
+    # tokens per pass of this window's (p, q): 20k windows drawn from the same rows (untimed)
+    n_win = 20000
+    k, V = vp.k, vp.V
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4242 + rank)
+    drafts = torch.multinomial(vp.q, n_win, replacement=True, generator=gen).T.contiguous().to(torch.int32)
+    p_rows = torch.arange(k + 1, device=dev, dtype=torch.int64).repeat(n_win, 1)
+    q_rows = torch.arange(k, device=dev, dtype=torch.int64).repeat(n_win, 1)
+    tok = torch.empty((n_win, k + 1), dtype=torch.int32, device=dev)
+    ne = torch.empty(n_win, dtype=torch.int32, device=dev)
+    st = torch.empty(n_win, dtype=torch.int32, device=dev)
+    svd.svd_accept(vp.probs, drafts, n_win, k, V, tok, ne, st, q=vp.q, p_rows=p_rows,
+                   q_rows=q_rows, seed=rank + 17)
+    torch.cuda.synchronize(dev)
+    tokens_per_pass = float(ne.double().mean().item())
+
+    # end to end: inputs from pinned host memory and the result back, every step
+    host_in = [t.detach().cpu().pin_memory() for t in vp.inputs()]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in vp.outputs()]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    Ke = max(1, min(K, args.e2e_steps))
+    if dist:
+        td.barrier()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0 = time.perf_counter()
+    e0.record(s)
+    for _ in range(Ke):
+        for d_t, h_t in zip(vp.inputs(), host_in):
+            d_t.copy_(h_t, non_blocking=True)
+        vp.launch(s)
+        for h_t, d_t in zip(host_out, vp.outputs()):
+            h_t.copy_(d_t, non_blocking=True)
+    e1.record(s)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - w0
+    e2e_ms = max(e0.elapsed_time(e1), wall * 1000.0)
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        td.all_reduce(t, op=td.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * Ke / (e2e_ms / 1000.0)
+
+    stack_bytes = vp.stack_bytes()
+    achieved = stack_bytes / (stack_ms / 1000.0) / 1e9
+    peak, peak_kind = peaks()
+    traffic_pass = kernel_traffic()
+    n_launch = len(vp.linears)
+    line = {
+        "metric": METRIC, "value": passes_per_s, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": t_max / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "C": args.C, "layers": args.layers,
+                   "global_batch": world, "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2: 11.9 GB of weights streamed per step",
+                   "pdl": not args.no_pdl, "graph": "stack graph + tail graph per step"},
+        "stack": {"ms": stack_ms, "passes_per_s": 1000.0 / stack_ms, "bytes": stack_bytes,
+                  "gb_s": achieved, "tail_ms": tail_ms},
+        "tokens_per_pass": tokens_per_pass,
+        "effective_tokens_per_s": passes_per_s * tokens_per_pass,
+        "pass_bytes": vp.pass_bytes(),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_kind,
+                     "kernel": "vl_mma_kernel (256 launches of the stack, averaged)",
+                     "traffic": None if traffic_pass is None else traffic_pass},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": Ke},
+        "gpu_launches": K * (n_launch + (1 + 4 + 1 if vp.head else 0)),
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        smp = OracleSample(frac=0.25)
+        times = [smp.step() for _ in range(3)]
+        line["cpu_baseline"] = {"value": smp.passes_per_s(times), "unit": UNIT,
+                                "cores": smp.threads, "kind": "oracle", "sample": smp.describe(3),
+                                "cpu": _cpu_model()}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="svd", choices=["svd", "reference"])
+    ap.add_argument("--layers", type=int, default=64)
+    ap.add_argument("--C", type=int, default=4)
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-pdl", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as td
+        torch.cuda.set_device(local_rank)
+        td.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    run_svd(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as td
+        td.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,222 @@
+/*
+ * svd.h -- C ABI of the speculative-decoding verify pass for GB300 (sm_103a).
+ *
+ * The verify pass of speculative decoding scores K drafted tokens with one forward pass of the
+ * target model: every weight matrix is read from memory once and applied to the K+1 activation
+ * columns of the window; the target produces one distribution per window position; an
+ * acceptance rule keeps a prefix of the drafts and the target's own token caps the window.
+ * Sources:
+ *   "100 tokens per second from a 27B model on a 24 GB AMD card" (curriculo.me), sections
+ *     "The wall" and "How speculative decoding gets past a per-token wall";
+ *   "Decode is memory-bound: the ~59 tok/s ceiling on an RTX 4090, and how speculative decoding
+ *     gets past it" (trefon.com), sections "The ceiling", "Speculative decoding", "Two things
+ *     the math says to do";
+ *   the Hacker News thread on speculative decoding (hn.shard-db.dev, item 49596054): the
+ *     comments on parallel verification and on the [positions, vocabulary] output tensor.
+ *
+ * Conventions for every entry point:
+ *   - Buffers are DEVICE pointers unless stated; the caller allocates and owns all of them.
+ *     The library never allocates device memory, keeps no per-call state and never
+ *     synchronises the stream: every call only enqueues work on `stream` (cudaStream_t; NULL
+ *     is the legacy default stream) and returns.
+ *   - The return value is SVD_OK (0) or a negative SVD_ERR_* code; nothing is enqueued when a
+ *     call returns an error.  svd_error_string() names a code; svd_last_cuda_error() gives the
+ *     CUDA error behind the most recent SVD_ERR_CUDA of the calling thread.
+ *   - Errors in the CONTENT of device inputs (a draft id out of range, a NaN probability) are
+ *     not return codes: they are reported per window in a device status word (SVD_ST_*).
+ *   - Pointers handed to the vector loads must be 16-byte aligned where stated.
+ */
+#ifndef SVD_H_
+#define SVD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#pragma GCC visibility push(default) /* exported even when built with -fvisibility=hidden */
+#endif
+
+typedef struct CUstream_st *svd_stream_t; /* identical to cudaStream_t */
+
+/* Return codes. */
+enum {
+    SVD_OK = 0,
+    SVD_ERR_INVALID_ARG = -1, /* null pointer, bad size, misaligned pointer          */
+    SVD_ERR_UNSUPPORTED = -2, /* a valid request this build does not implement       */
+    SVD_ERR_CUDA = -3,        /* a CUDA call failed (see svd_last_cuda_error)        */
+    SVD_ERR_WORKSPACE = -4    /* workspace null or smaller than the query said       */
+};
+
+/* Per-window status bits written by svd_accept (0 = clean). */
+enum {
+    SVD_ST_BAD_TOKEN = 1,     /* a draft id outside [0, V): that position is rejected */
+    SVD_ST_Q_ZERO = 2,        /* q_i(x_i) == 0 for a drafted token                    */
+    SVD_ST_BAD_PROB = 4,      /* a probability read was NaN, infinite, < 0 or > 1;    */
+                              /* it was clamped into [0, 1]                           */
+    SVD_ST_ZERO_RESIDUAL = 8, /* (p - q)+ had zero mass; the draw used p instead      */
+    SVD_ST_EMPTY = 16         /* the distribution drawn from had zero mass: no token  */
+};
+
+/* Weight layouts. */
+enum {
+    SVD_LAYOUT_CANONICAL = 0, /* codes[out][in/2] bytes, input 2t in the low nibble,
+                                 input 2t+1 in the high nibble; scales[out][in/32] fp16 */
+    SVD_LAYOUT_NATIVE = 1     /* the tensor-core fragment order made by
+                                 svd_repack_weights (opaque; same byte count, rows
+                                 padded to 64, inputs padded to 64)                   */
+};
+
+/* Flags for svd_verify_linear. */
+enum {
+    SVD_F_PDL = 1 /* launch with programmatic dependent launch: the kernel may start while the
+                     previous kernel on the stream is still running and stream its weights
+                     early; it waits for that kernel before reading X or the workspace.  Set
+                     only when nothing in flight on the stream writes the weights. */
+};
+
+#define SVD_C_MAX 32 /* most activation columns (K+1 positions x sequences) per call */
+#define SVD_K_MAX 32 /* most drafted tokens per window                                */
+
+/* A block-quantised 4-bit weight matrix W (in_features x out_features): code c in 0..15
+ * stands for s * (c - 8) with one fp16 scale s per 32 consecutive inputs of an output row
+ * (4.5 bits per weight).  codes and scales are device pointers, 16-byte aligned. */
+typedef struct svd_qweight {
+    const void *codes;
+    const void *scales;
+    int64_t in_features;  /* multiple of 32 */
+    int64_t out_features; /* >= 1 */
+    int32_t layout;       /* SVD_LAYOUT_* */
+    int32_t reserved;     /* must be 0 */
+} svd_qweight;
+
+/* Sampler settings ("Decode is memory-bound ...", "Two things the math says to do":
+ * temperature 0.6, top-p 0.95, min-p 0.05).  greedy != 0 ignores the other fields. */
+typedef struct svd_sampler {
+    float temperature; /* > 0 */
+    float top_p;       /* (0, 1]; 1 disables the top-p filter */
+    float min_p;       /* [0, 1); 0 disables the min-p filter */
+    int32_t greedy;
+} svd_sampler;
+
+/* ---- errors ------------------------------------------------------------------------- */
+const char *svd_error_string(int code);
+int svd_last_cuda_error(void); /* cudaError_t of the thread's last SVD_ERR_CUDA */
+
+/* ---- load time: weight repack ------------------------------------------------------- */
+/* Byte sizes of the native layout of an in x out matrix (rows padded to 64, inputs padded to
+ * 64).  Returns SVD_ERR_INVALID_ARG for in % 32 != 0 or non-positive sizes. */
+int svd_native_sizes(int64_t in_features, int64_t out_features, size_t *codes_bytes,
+                     size_t *scales_bytes);
+
+/* Permute a CANONICAL matrix into the NATIVE layout the tensor-core kernel streams: for each
+ * 64-row block and each 64-input chunk, the 16-byte word every lane of a warp loads holds its
+ * A-fragment nibbles for four k16 MMA steps, and the scales follow in fragment order.  A pure
+ * bit permutation (padding codes are 8, padding scales 0); svd_unpack_weights is its inverse.
+ * dst buffers must hold svd_native_sizes() bytes and must not overlap src. */
+int svd_repack_weights(const svd_qweight *src_canonical, void *dst_codes, void *dst_scales,
+                       svd_stream_t stream);
+/* Inverse of svd_repack_weights (drops the padding). */
+int svd_unpack_weights(const svd_qweight *src_native, void *dst_codes, void *dst_scales,
+                       svd_stream_t stream);
+
+/* ---- (a) verify linear -------------------------------------------------------------- */
+/* Y[c][j] = sum_i s[j][i/32] * (code[j][i] - 8) * X[c][i]  for c < C, j < out, in fp32
+ * ("100 tokens per second ...", "How speculative decoding gets past a per-token wall": the
+ * weights are read once and applied to the K-wide batch of the window).
+ *   X: bf16 [C][in] row-major (token-major), 16-byte aligned.  Y: fp32 [C][out].
+ *   C in 1..SVD_C_MAX.
+ *   NATIVE weights run the tensor-core stream-K kernel (bf16 MMA, fp32 accumulate, one fresh
+ *   accumulator per 32-input block, scaled in fp32).  It needs a workspace of
+ *   svd_verify_linear_workspace_bytes() bytes that is ZERO-FILLED before its first use (it
+ *   holds per-row-block ticket counters, which every call returns to zero, and partial sums),
+ *   so one zeroed workspace serves any number of calls issued in stream order; calls that may
+ *   run concurrently need separate workspaces.
+ *   CANONICAL weights run the CUDA-core warp-shuffle kernel (no workspace; needs
+ *   C * in * 4 <= 196608 bytes, else SVD_ERR_UNSUPPORTED).
+ *   The result is deterministic: the same inputs give the same bits on every call. */
+size_t svd_verify_linear_workspace_bytes(int64_t in_features, int64_t out_features, int C);
+int svd_verify_linear(const svd_qweight *W, const void *X, int C, float *Y, void *workspace,
+                      size_t workspace_bytes, int flags, svd_stream_t stream);
+
+/* ---- (b) sampler and lm_head -------------------------------------------------------- */
+/* Per row of logits [rows][V] fp32: p = softmax(logits / T); keep v iff p[v] >= min_p *
+ * max p and v lies in the shortest prefix, in the order (p descending, id ascending), whose
+ * mass reaches top_p (the crossing token included); renormalise the kept mass to one.  Both
+ * filters read the same un-renormalised p ("Decode is memory-bound ...", "Two things the math
+ * says to do").  Writes probs [rows][V] fp32 and argmax [rows] (lowest id on ties; NaN
+ * logits never win).  greedy writes the one-hot distribution of the argmax.
+ *   probs must not alias logits.  rows in 1..SVD_C_MAX, V in 1..2^24. */
+size_t svd_sampler_workspace_bytes(int rows, int64_t V);
+int svd_sampler_probs(const float *logits, int rows, int64_t V, const svd_sampler *sampler,
+                      float *probs, int32_t *argmax, void *workspace, size_t workspace_bytes,
+                      svd_stream_t stream);
+
+/* lm_head projection of every window position followed by the sampler: logits = W_lm^T H
+ * ([positions][vocabulary], the HN thread's [4, vocabulary_size] tensor), then
+ * svd_sampler_probs.  W_lm must be NATIVE (hidden x vocabulary).  H: bf16 [C][hidden].
+ * logits: fp32 [C][V] (written).  The workspace (zero-filled before first use, as for
+ * svd_verify_linear) holds svd_lm_head_workspace_bytes() bytes. */
+size_t svd_lm_head_workspace_bytes(int64_t hidden, int64_t vocab, int C);
+int svd_lm_head_softmax(const svd_qweight *W_lm, const void *H, int C,
+                        const svd_sampler *sampler, float *logits, float *probs,
+                        int32_t *argmax, void *workspace, size_t workspace_bytes,
+                        svd_stream_t stream);
+
+/* ---- (c) acceptance ----------------------------------------------------------------- */
+/* One verify window per w in [0, n_windows) with k drafts x_0..x_{k-1} (draft [n][k]).
+ * Row i of the target distribution of window w is p + p_rows[w*(k+1)+i] * V when p_rows is
+ * given, else p + (w*(k+1)+i) * V (i = 0..k); the drafter's rows likewise through q_rows
+ * ([n][k]) or q + (w*k+i) * V.  Rows are fp32 probability vectors of length V.
+ * Greedy (q == NULL): emit x_i while x_i equals the target's argmax at position i (from
+ *   target_argmax [n][k+1] when given, else from p, lowest id on ties); at the first mismatch
+ *   j emit argmax_j; if all k match emit argmax_k ("100 tokens per second ...", "How
+ *   speculative decoding gets past a per-token wall"; the HN thread's "D E F" example).
+ * Sampled (q != NULL): for i = 0..k-1 accept x_i iff u_i * q_i(x_i) < p_i(x_i) (decided
+ *   exactly in double precision), i.e. with probability min(1, p/q); at the first rejection j
+ *   emit a draw from the normalised (p_j - q_j)+ with u'_j; if all k are accepted emit a
+ *   draw from p_k with u'_k, the target's own token capping the window ("Decode is
+ *   memory-bound ...", "Speculative decoding"; Leviathan et al. 2023, Chen et al. 2023).  A
+ *   draw from weights r emits the smallest v whose running sum exceeds u' * sum(r); the sums
+ *   are exact 128-bit fixed point (2^-62 per unit), so the draw does not depend on thread
+ *   order.
+ *   u_i, u'_i are words 0 and 1 of Philox4x32-10 (Salmon et al., SC'11) with key = seed and
+ *   counter = (window low 32 bits, window high 32 bits, i, 0), window = window_offset + w,
+ *   each mapped to (word >> 8) * 2^-24.  uniforms ([n][k+1][2] fp32, multiples of 2^-24 in
+ *   [0,1)) replaces them when non-NULL (a test hook).
+ * Outputs: out_tokens [n][k+1] (emitted tokens then -1), n_emitted [n] in [1, k+1] for a
+ *   clean window, status [n] (SVD_ST_* bits; 0 = clean).
+ * k in 1..SVD_K_MAX, V in 1..2^31-1, n_windows >= 0 (0 enqueues nothing). */
+int svd_accept(const float *p, const int64_t *p_rows, const float *q, const int64_t *q_rows,
+               const int32_t *target_argmax, const int32_t *draft, int64_t n_windows, int k,
+               int64_t V, uint64_t seed, uint64_t window_offset, const float *uniforms,
+               int32_t *out_tokens, int32_t *n_emitted, int32_t *status, svd_stream_t stream);
+
+/* ---- pass orchestration ------------------------------------------------------------- */
+/* Record every call the thread makes on `stream` between svd_graph_begin and svd_graph_end
+ * into one CUDA graph (stream capture), instantiate it and return an opaque handle; the
+ * verify pass of a whole model (256 verify-linear launches for 64 layers, the lm_head, the
+ * sampler and the acceptance) then replays with one svd_graph_launch.  Kernels recorded with
+ * SVD_F_PDL keep their programmatic dependencies inside the graph.  The handle owns host
+ * memory and the instantiated graph, no device buffers; free it with svd_graph_destroy. */
+typedef struct svd_graph svd_graph;
+int svd_graph_begin(svd_stream_t stream);
+int svd_graph_end(svd_stream_t stream, svd_graph **out);
+int svd_graph_launch(svd_graph *g, svd_stream_t stream);
+void svd_graph_destroy(svd_graph *g);
+
+/* Number of streaming multiprocessors of the current device (what the workspace queries
+ * size for); -1 on error. */
+int svd_device_sm_count(void);
+
+#if defined(__GNUC__)
+#pragma GCC visibility pop
+#endif
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SVD_H_ */

@@ -1,0 +1,606 @@
+// verify_linear.cu -- the weight-streaming dequant GEMM of the verify pass.
+//
+// "100 tokens per second from a 27B model on a 24 GB AMD card", section "How speculative
+// decoding gets past a per-token wall": the target scores K drafts in one forward pass because
+// every weight matrix is read once and applied to a K-wide batch of activations; the HN thread
+// on speculative decoding makes the same point layer by layer.  So the kernel here streams each
+// 4-bit matrix from HBM exactly once and multiplies it against the C = K+1 columns of a window:
+//
+//     Y[c][j] = sum_b s[j][b] * sum_{i in block b} (code[j][i] - 8) * X[c][i]
+//
+// Two kernels:
+//  * vl_mma_kernel (NATIVE layout) -- persistent stream-K over (64-row block, 64-input chunk)
+//    units.  Each warp owns a cp.async ring of its units in shared memory (codes + scales,
+//    2304 bytes per unit), dequantises nibbles straight into bf16 A fragments with one lop3 and
+//    one bf16x2 subtract per pair (value 128 + c built from the exponent pattern 0x4300, then
+//    minus 136 gives c - 8 exactly), and runs mma.sync m16n8k16 (bf16 in, fp32 accumulate)
+//    against the activations as the B operand.  Every 32-input block gets a fresh accumulator
+//    that is scaled by its fp16 scale in fp32, so the only rounding is fp32 accumulation.
+//    Warps of a CTA interleave the chunks of a row block; partial row blocks at the edges of a
+//    CTA's range are combined through a small workspace by the last CTA to arrive (an atomic
+//    ticket per row block, summed in CTA order: deterministic, no spinning).
+//  * vl_simt_kernel (CANONICAL layout) -- the plain CUDA-core version: one warp per output
+//    row, each lane one 32-input block at a time, fp32 FMAs, warp-shuffle reduction.
+#include "svd_common.cuh"
+
+namespace svd {
+
+// ---- native layout geometry ------------------------------------------------------------
+constexpr int kRowsPerBlock = 64;       // 4 MMA tiles of 16 rows
+constexpr int kTiles = 4;
+constexpr int kChunk = 64;              // inputs per unit (2 scale blocks, 4 k16 steps)
+constexpr int kUnitCodeBytes = 2048;    // 64 rows x 64 inputs x 4 bit
+constexpr int kUnitScaleBytes = 256;    // 64 rows x 2 blocks x fp16
+constexpr int kUnitBytes = kUnitCodeBytes + kUnitScaleBytes;
+
+struct NativeGeom {
+    int64_t n_rb, n_kc, n_units;
+};
+static NativeGeom native_geom(int64_t in_f, int64_t out_f) {
+    NativeGeom g;
+    g.n_rb = (out_f + kRowsPerBlock - 1) / kRowsPerBlock;
+    g.n_kc = (in_f + kChunk - 1) / kChunk;
+    g.n_units = g.n_rb * g.n_kc;
+    return g;
+}
+
+// Inside a unit, lane l = 4*g + t of a warp owns, for tile r and k16 step s (s = 0..3), one
+// 32-bit word whose nibble at bit 4p + 16h feeds A-fragment register p, half h:
+//   row   = 16 r + g + 8 (p & 1)
+//   input = 32 (s >> 1) + 8 t + 4 (s & 1) + 2 (p >> 1) + h        (relative to the chunk)
+// Steps 0,1 cover scale block 0 and steps 2,3 block 1; lane l's inputs of a block are the 8
+// consecutive ones at 32 b + 8 t, so its B fragments are one 16-byte load of X.
+__host__ __device__ inline void native_word_coords(int s, int p, int h, int g, int t,
+                                                   int *row_in_tile, int *input_in_chunk) {
+    *row_in_tile = g + 8 * (p & 1);
+    *input_in_chunk = 32 * (s >> 1) + 8 * t + 4 * (s & 1) + 2 * (p >> 1) + h;
+}
+
+__global__ void repack_codes_kernel(const uint8_t *__restrict__ src, uint32_t *__restrict__ dst,
+                                    int64_t in_f, int64_t out_f, int64_t n_kc, int64_t n_words) {
+    const int64_t wid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (wid >= n_words) return;
+    const int s = (int)(wid & 3), lane = (int)((wid >> 2) & 31), r = (int)((wid >> 7) & 3);
+    const int64_t unit = wid >> 9, rb = unit / n_kc, kc = unit % n_kc;
+    const int g = lane >> 2, t = lane & 3;
+    uint32_t word = 0;
+#pragma unroll
+    for (int p = 0; p < 4; ++p)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            int rt, ic;
+            native_word_coords(s, p, h, g, t, &rt, &ic);
+            const int64_t row = rb * kRowsPerBlock + 16 * r + rt, i = kc * kChunk + ic;
+            uint32_t nib = 8;  // code 8 is the value 0
+            if (row < out_f && i < in_f) {
+                const uint8_t byte = src[row * (in_f / 2) + i / 2];
+                nib = (i & 1) ? (byte >> 4) : (byte & 15);
+            }
+            word |= nib << (4 * p + 16 * h);
+        }
+    dst[wid] = word;
+}
+
+// Scales of a unit: tile r, group g: 8 bytes = fp16 s(g, blk0), s(g, blk1), s(g+8, blk0),
+// s(g+8, blk1), so lane 4g+t reads its four scales with one 8-byte load.
+__global__ void repack_scales_kernel(const uint16_t *__restrict__ src, uint16_t *__restrict__ dst,
+                                     int64_t in_f, int64_t out_f, int64_t n_kc, int64_t n_halves) {
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= n_halves) return;
+    const int q = (int)(idx & 3), g = (int)((idx >> 2) & 7), r = (int)((idx >> 5) & 3);
+    const int64_t unit = idx >> 7, rb = unit / n_kc, kc = unit % n_kc;
+    const int64_t row = rb * kRowsPerBlock + 16 * r + g + 8 * (q >> 1), blk = 2 * kc + (q & 1);
+    const int64_t nblk = in_f / 32;
+    dst[idx] = (row < out_f && blk < nblk) ? src[row * nblk + blk] : (uint16_t)0;
+}
+
+__global__ void unpack_codes_kernel(const uint32_t *__restrict__ src, uint8_t *__restrict__ dst,
+                                    int64_t in_f, int64_t out_f, int64_t n_kc) {
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t half_in = in_f / 2;
+    if (idx >= out_f * half_in) return;
+    const int64_t row = idx / half_in, byte = idx % half_in;
+    uint8_t outb = 0;
+    for (int h2 = 0; h2 < 2; ++h2) {
+        const int64_t i = 2 * byte + h2;
+        const int64_t rb = row / kRowsPerBlock, rr = row % kRowsPerBlock;
+        const int r = (int)(rr / 16), rt = (int)(rr % 16), g = rt % 8, prow = rt / 8;
+        const int64_t kc = i / kChunk;
+        const int ii = (int)(i % kChunk), sblk = ii / 32, iw = ii % 32, t = iw / 8;
+        const int slo = (iw % 8) / 4, e = iw % 4;
+        const int s = 2 * sblk + slo, p = 2 * (e >> 1) + prow, h = e & 1;
+        const int64_t wid = (((rb * n_kc + kc) * kTiles + r) * 32 + (4 * g + t)) * 4 + s;
+        const uint32_t nib = (src[wid] >> (4 * p + 16 * h)) & 15u;
+        outb |= (uint8_t)(nib << (4 * h2));
+    }
+    dst[idx] = outb;
+}
+
+__global__ void unpack_scales_kernel(const uint16_t *__restrict__ src, uint16_t *__restrict__ dst,
+                                     int64_t in_f, int64_t out_f, int64_t n_kc) {
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t nblk = in_f / 32;
+    if (idx >= out_f * nblk) return;
+    const int64_t row = idx / nblk, blk = idx % nblk;
+    const int64_t rb = row / kRowsPerBlock, rr = row % kRowsPerBlock;
+    const int r = (int)(rr / 16), rt = (int)(rr % 16), g = rt % 8, prow = rt / 8;
+    const int64_t kc = blk / 2;
+    const int q = 2 * prow + (int)(blk & 1);
+    dst[idx] = src[(((rb * n_kc + kc) * kTiles + r) * 8 + g) * 4 + q];
+}
+
+// ---- device building blocks -----------------------------------------------------------
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Four bf16x2 A registers from one native word: (bits >> 4p) & 0x000F000F | 0x43004300 is the
+// pair (128 + c_lo, 128 + c_hi) exactly; subtracting (136, 136) leaves (c - 8) exactly.
+__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t a[4]) {
+    const uint32_t magic = 0x43004300u, bias = 0x43084308u;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        uint32_t v;
+        const uint32_t sh = w >> (4 * p);
+        asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(v) : "r"(sh), "r"(0x000F000Fu), "r"(magic));
+        asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(a[p]) : "r"(v), "r"(bias));
+    }
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float d[4], const uint32_t a[4], uint32_t b0,
+                                               uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// CTA that owns unit n when n_units units are split into G contiguous ranges
+// [b*n/G, (b+1)*n/G).
+__device__ __forceinline__ int64_t owner_cta(int64_t n, int64_t G, int64_t n_units) {
+    return ((n + 1) * G - 1) / n_units;
+}
+
+// ---- the tensor-core stream-K kernel ---------------------------------------------------
+template <int NT, int NW, int D>
+struct MmaCfg {
+    static constexpr int kAcc = kTiles * NT * 4;              // fp32 accumulators per lane
+    static constexpr int kPartial = 32 * kAcc;                // floats per warp partial
+    static constexpr size_t kRing = (size_t)NW * D * kUnitBytes;
+    static constexpr size_t kSmem = kRing + (size_t)NW * kPartial * sizeof(float);
+};
+
+template <int NT, int NW, int D>
+__global__ void __launch_bounds__(NW * 32, (NT == 1 ? 2 : 1))
+vl_mma_kernel(const uint8_t *__restrict__ wcodes, const uint8_t *__restrict__ wscales,
+              const __nv_bfloat16 *__restrict__ X, float *__restrict__ Y, int64_t in_f,
+              int64_t out_f, int C, int64_t n_kc, int64_t n_units, float *__restrict__ ws_part,
+              unsigned int *__restrict__ ws_cnt) {
+    using Cfg = MmaCfg<NT, NW, D>;
+    constexpr int kAcc = Cfg::kAcc, kPartial = Cfg::kPartial;
+    extern __shared__ __align__(16) uint8_t smem[];
+    float *red = reinterpret_cast<float *>(smem + Cfg::kRing);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int64_t G = gridDim.x, b = blockIdx.x;
+    const int64_t start = b * n_units / G, end = (b + 1) * n_units / G;
+    const int64_t span = end - start;
+    const int J = span > warp ? (int)((span - warp + NW - 1) / NW) : 0;
+    uint8_t *ring = smem + (size_t)warp * D * kUnitBytes;
+
+    auto issue = [&](int j) {
+        const int64_t u = start + warp + (int64_t)NW * j;
+        uint8_t *slot = ring + (j % D) * kUnitBytes;
+        const uint8_t *src = wcodes + u * kUnitCodeBytes;
+#pragma unroll
+        for (int r = 0; r < kTiles; ++r) cp_async16(slot + r * 512 + lane * 16, src + r * 512 + lane * 16);
+        if (lane < 16)
+            cp_async16(slot + kUnitCodeBytes + lane * 16, wscales + u * kUnitScaleBytes + lane * 16);
+    };
+
+    // Weights do not depend on the upstream kernel: start streaming them before waiting on it.
+#pragma unroll
+    for (int s = 0; s < D - 1; ++s) {
+        if (s < J) issue(s);
+        cp_async_commit();
+    }
+    griddep_wait();
+    griddep_launch_dependents();
+
+    auto load_x = [&](int j, uint4 (&xr)[NT][2]) {
+        const int64_t u = start + warp + (int64_t)NW * j;
+        const int64_t kc = u % n_kc;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int col = nt * 8 + g;
+#pragma unroll
+            for (int blk = 0; blk < 2; ++blk) {
+                const int64_t i0 = kc * kChunk + blk * 32 + t * 8;
+                if (col < C && i0 < in_f)
+                    xr[nt][blk] = ldg_nc_v4(X + (int64_t)col * in_f + i0);
+                else
+                    xr[nt][blk] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+    };
+
+    float acc[kTiles][NT][4];
+#pragma unroll
+    for (int r = 0; r < kTiles; ++r)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[r][nt][q] = 0.f;
+
+    uint4 xr[NT][2];
+    if (J > 0) load_x(0, xr);
+
+    int j = 0;
+    const int64_t rb_first = start / n_kc, rb_last = (end - 1) / n_kc;
+    for (int64_t rb = rb_first; rb <= rb_last; ++rb) {
+        const int64_t seg_lo = max(start, rb * n_kc), seg_hi = min(end, (rb + 1) * n_kc);
+        while (j < J && start + warp + (int64_t)NW * j < seg_hi) {
+            if (j + D - 1 < J) issue(j + D - 1);
+            cp_async_commit();
+            cp_async_wait<D - 1>();
+            __syncwarp();
+            uint4 xc[NT][2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                xc[nt][0] = xr[nt][0];
+                xc[nt][1] = xr[nt][1];
+            }
+            if (j + 1 < J) load_x(j + 1, xr);
+            const uint8_t *slot = ring + (j % D) * kUnitBytes;
+#pragma unroll
+            for (int r = 0; r < kTiles; ++r) {
+                const uint4 cw = *reinterpret_cast<const uint4 *>(slot + r * 512 + lane * 16);
+                const uint2 sc =
+                    *reinterpret_cast<const uint2 *>(slot + kUnitCodeBytes + r * 64 + g * 8);
+                const float2 s_lo = __half22float2(*reinterpret_cast<const __half2 *>(&sc.x));
+                const float2 s_hi = __half22float2(*reinterpret_cast<const __half2 *>(&sc.y));
+#pragma unroll
+                for (int blk = 0; blk < 2; ++blk) {
+                    uint32_t a0[4], a1[4];
+                    dequant_word(blk ? cw.z : cw.x, a0);
+                    dequant_word(blk ? cw.w : cw.y, a1);
+                    const float sg = blk ? s_lo.y : s_lo.x, sh = blk ? s_hi.y : s_hi.x;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        float d[4] = {0.f, 0.f, 0.f, 0.f};
+                        mma_bf16_16816(d, a0, xc[nt][blk].x, xc[nt][blk].y);
+                        mma_bf16_16816(d, a1, xc[nt][blk].z, xc[nt][blk].w);
+                        acc[r][nt][0] = fmaf(sg, d[0], acc[r][nt][0]);
+                        acc[r][nt][1] = fmaf(sg, d[1], acc[r][nt][1]);
+                        acc[r][nt][2] = fmaf(sh, d[2], acc[r][nt][2]);
+                        acc[r][nt][3] = fmaf(sh, d[3], acc[r][nt][3]);
+                    }
+                }
+            }
+            __syncwarp();  // every lane is done with this slot before it is refilled
+            ++j;
+        }
+
+        // Row block rb is finished by this CTA: combine the warps' partials.
+        {
+            float4 *dst = reinterpret_cast<float4 *>(red + warp * kPartial + lane * kAcc);
+#pragma unroll
+            for (int r = 0; r < kTiles; ++r)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    dst[r * NT + nt] = make_float4(acc[r][nt][0], acc[r][nt][1], acc[r][nt][2],
+                                                   acc[r][nt][3]);
+                    acc[r][nt][0] = acc[r][nt][1] = acc[r][nt][2] = acc[r][nt][3] = 0.f;
+                }
+        }
+        __syncthreads();
+        const bool full = (seg_lo == rb * n_kc) && (seg_hi == (rb + 1) * n_kc);
+        const int slot_id = (rb == rb_first) ? 0 : 1;
+        float vals[kPartial / (NW * 32)];
+#pragma unroll
+        for (int m = 0; m < kPartial / (NW * 32); ++m) {
+            const int e = threadIdx.x + m * NW * 32;
+            float v = 0.f;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) v += red[w * kPartial + e];
+            vals[m] = v;
+        }
+        auto out_coords = [&](int e, int64_t *row, int *col) {
+            const int lsrc = e / kAcc, idx = e % kAcc, q = idx & 3, rn = idx >> 2;
+            const int r = rn / NT, nt = rn % NT;
+            *row = rb * kRowsPerBlock + 16 * r + (lsrc >> 2) + ((q >> 1) ? 8 : 0);
+            *col = nt * 8 + (lsrc & 3) * 2 + (q & 1);
+        };
+        if (full) {
+#pragma unroll
+            for (int m = 0; m < kPartial / (NW * 32); ++m) {
+                const int e = threadIdx.x + m * NW * 32;
+                int64_t row;
+                int col;
+                out_coords(e, &row, &col);
+                if (row < out_f && col < C) Y[(int64_t)col * out_f + row] = vals[m];
+            }
+            __syncthreads();  // red is free again
+        } else {
+            // Stream-K fix-up: publish this CTA's partial, take a ticket; the last CTA of the
+            // row block sums every partial in CTA order and resets the ticket.
+            float *mine = ws_part + (b * 2 + slot_id) * (int64_t)kPartial;
+#pragma unroll
+            for (int m = 0; m < kPartial / (NW * 32); ++m) mine[threadIdx.x + m * NW * 32] = vals[m];
+            __threadfence();
+            __shared__ int s_last;
+            __syncthreads();
+            const int64_t b_first = owner_cta(rb * n_kc, G, n_units);
+            const int64_t b_last = owner_cta((rb + 1) * n_kc - 1, G, n_units);
+            if (threadIdx.x == 0) {
+                const unsigned nseg = (unsigned)(b_last - b_first + 1);
+                const unsigned old = atomicAdd(ws_cnt + rb, 1u);
+                s_last = (old == nseg - 1) ? 1 : 0;
+            }
+            __syncthreads();
+            if (s_last) {
+                __threadfence();
+#pragma unroll
+                for (int m = 0; m < kPartial / (NW * 32); ++m) {
+                    const int e = threadIdx.x + m * NW * 32;
+                    float v = 0.f;
+                    for (int64_t bb = b_first; bb <= b_last; ++bb) {
+                        const int64_t bb_first_rb = (bb * n_units / G) / n_kc;
+                        const int sid = (rb == bb_first_rb) ? 0 : 1;
+                        v += __ldcg(ws_part + (bb * 2 + sid) * (int64_t)kPartial + e);
+                    }
+                    int64_t row;
+                    int col;
+                    out_coords(e, &row, &col);
+                    if (row < out_f && col < C) Y[(int64_t)col * out_f + row] = v;
+                }
+                if (threadIdx.x == 0) ws_cnt[rb] = 0u;
+            }
+        }
+    }
+    cp_async_wait<0>();
+}
+
+// ---- the CUDA-core kernel (canonical layout) -------------------------------------------
+// One warp per output row; lane l takes 32-input blocks l, l+32, ...: one 16-byte load of 32
+// nibbles, value (c - 8) built exactly as float(2^23 + c) - (2^23 + 8), C fp32 FMAs per
+// weight against activations held in shared memory as fp32 (one pad word every 32 to spread
+// the lanes over the banks), the block sum scaled by its fp16 scale, then a butterfly
+// reduction over the warp.
+template <int CC>
+__global__ void __launch_bounds__(256)
+vl_simt_kernel(const uint8_t *__restrict__ codes, const uint16_t *__restrict__ scales,
+               const __nv_bfloat16 *__restrict__ X, float *__restrict__ Y, int64_t in_f,
+               int64_t out_f) {
+    extern __shared__ float xs[];
+    const int64_t pitch = in_f + in_f / 32;
+    griddep_wait();
+    for (int64_t i = threadIdx.x; i < CC * in_f; i += blockDim.x) {
+        const int64_t c = i / in_f, k = i % in_f;
+        xs[c * pitch + k + k / 32] = __bfloat162float(X[i]);
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t nblk = in_f / 32;
+    for (int64_t row = (int64_t)blockIdx.x * 8 + warp; row < out_f; row += (int64_t)gridDim.x * 8) {
+        float acc[CC];
+#pragma unroll
+        for (int c = 0; c < CC; ++c) acc[c] = 0.f;
+        for (int64_t blk = lane; blk < nblk; blk += 32) {
+            const uint4 q = ldg_nc_v4(codes + row * (in_f / 2) + blk * 16);
+            const float s = __half2float(__ushort_as_half(scales[row * nblk + blk]));
+            const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+            float part[CC];
+#pragma unroll
+            for (int c = 0; c < CC; ++c) part[c] = 0.f;
+            const float *xb = xs + blk * 32 + blk;
+#pragma unroll
+            for (int wi = 0; wi < 4; ++wi)
+#pragma unroll
+                for (int n = 0; n < 8; ++n) {
+                    const uint32_t nib = (words[wi] >> (4 * n)) & 15u;
+                    const float wv = __uint_as_float(0x4B000000u | nib) - 8388616.0f;
+#pragma unroll
+                    for (int c = 0; c < CC; ++c) part[c] = fmaf(wv, xb[c * pitch + wi * 8 + n], part[c]);
+                }
+#pragma unroll
+            for (int c = 0; c < CC; ++c) acc[c] = fmaf(s, part[c], acc[c]);
+        }
+#pragma unroll
+        for (int c = 0; c < CC; ++c) {
+            float v = acc[c];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            acc[c] = v;
+        }
+        if (lane == 0)
+#pragma unroll
+            for (int c = 0; c < CC; ++c) Y[(int64_t)c * out_f + row] = acc[c];
+    }
+}
+
+// ---- host side ---------------------------------------------------------------------------
+constexpr int kNW = 8;   // consumer warps per CTA
+constexpr int kD1 = 5;   // ring depth, C <= 8
+constexpr int kD2 = 4;   // ring depth, C <= 16 / 32
+
+static int ntiles_for(int C) { return C <= 8 ? 1 : (C <= 16 ? 2 : 4); }
+
+static int ctas_for(int C) { return ntiles_for(C) == 1 ? 1 : 1; }
+
+static size_t part_floats(int C) { return (size_t)32 * kTiles * ntiles_for(C) * 4; }
+
+static int64_t grid_for(const NativeGeom &ng, int C) {
+    int64_t G = (int64_t)sm_count() * ctas_for(C);
+    if (G > ng.n_units) G = ng.n_units;
+    if (G < 1) G = 1;
+    return G;
+}
+
+size_t vl_workspace_bytes(int64_t in_f, int64_t out_f, int C) {
+    const NativeGeom ng = native_geom(in_f, out_f);
+    const int64_t G = grid_for(ng, C);
+    return align_up((size_t)G * 2 * part_floats(C) * sizeof(float), 256) +
+           align_up((size_t)ng.n_rb * sizeof(unsigned), 256);
+}
+
+template <int NT, int D>
+static cudaError_t launch_mma(const svd_qweight *W, const void *X, int C, float *Y, void *ws,
+                              bool pdl, cudaStream_t stream) {
+    using Cfg = MmaCfg<NT, kNW, D>;
+    auto kern = vl_mma_kernel<NT, kNW, D>;
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)Cfg::kSmem);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    const NativeGeom ng = native_geom(W->in_features, W->out_features);
+    const int64_t G = grid_for(ng, C);
+    float *part = reinterpret_cast<float *>(ws);
+    unsigned *cnt = reinterpret_cast<unsigned *>(
+        reinterpret_cast<uint8_t *>(ws) + align_up((size_t)G * 2 * part_floats(C) * sizeof(float), 256));
+    return launch(kern, dim3((unsigned)G), dim3(kNW * 32), Cfg::kSmem, stream, pdl,
+                  reinterpret_cast<const uint8_t *>(W->codes),
+                  reinterpret_cast<const uint8_t *>(W->scales),
+                  reinterpret_cast<const __nv_bfloat16 *>(X), Y, W->in_features,
+                  W->out_features, C, ng.n_kc, ng.n_units, part, cnt);
+}
+
+template <int CC>
+static cudaError_t launch_simt(const svd_qweight *W, const void *X, float *Y, bool pdl,
+                               cudaStream_t stream) {
+    auto kern = vl_simt_kernel<CC>;
+    const int64_t in_f = W->in_features;
+    const size_t smem = (size_t)CC * (in_f + in_f / 32) * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    int64_t grid = (int64_t)sm_count() * per_sm;
+    const int64_t need = (W->out_features + 7) / 8;
+    if (grid > need) grid = need;
+    return launch(kern, dim3((unsigned)grid), dim3(256), smem, stream, pdl,
+                  reinterpret_cast<const uint8_t *>(W->codes),
+                  reinterpret_cast<const uint16_t *>(W->scales),
+                  reinterpret_cast<const __nv_bfloat16 *>(X), Y, in_f, W->out_features);
+}
+
+static int check_qweight(const svd_qweight *W) {
+    if (!W || !W->codes || !W->scales) return SVD_ERR_INVALID_ARG;
+    if (W->in_features <= 0 || W->out_features <= 0 || W->in_features % 32 != 0)
+        return SVD_ERR_INVALID_ARG;
+    if (W->reserved != 0) return SVD_ERR_INVALID_ARG;
+    if (W->layout != SVD_LAYOUT_CANONICAL && W->layout != SVD_LAYOUT_NATIVE)
+        return SVD_ERR_INVALID_ARG;
+    if (!aligned16(W->codes) || !aligned16(W->scales)) return SVD_ERR_INVALID_ARG;
+    return SVD_OK;
+}
+
+int verify_linear(const svd_qweight *W, const void *X, int C, float *Y, void *ws,
+                  size_t ws_bytes, int flags, cudaStream_t stream) {
+    int rc = check_qweight(W);
+    if (rc != SVD_OK) return rc;
+    if (!X || !Y || C < 1 || C > SVD_C_MAX || !aligned16(X)) return SVD_ERR_INVALID_ARG;
+    if (flags & ~SVD_F_PDL) return SVD_ERR_INVALID_ARG;
+    const bool pdl = (flags & SVD_F_PDL) != 0;
+    if (sm_count() < 1) return SVD_ERR_CUDA;
+    if (W->layout == SVD_LAYOUT_NATIVE) {
+        if (!ws || ws_bytes < vl_workspace_bytes(W->in_features, W->out_features, C))
+            return SVD_ERR_WORKSPACE;
+        cudaError_t e;
+        switch (ntiles_for(C)) {
+            case 1: e = launch_mma<1, kD1>(W, X, C, Y, ws, pdl, stream); break;
+            case 2: e = launch_mma<2, kD2>(W, X, C, Y, ws, pdl, stream); break;
+            default: e = launch_mma<4, kD2>(W, X, C, Y, ws, pdl, stream); break;
+        }
+        SVD_CUDA_TRY(e);
+        return SVD_OK;
+    }
+    // canonical layout: CUDA-core kernel
+    if ((int64_t)C * W->in_features * 4 > 196608) return SVD_ERR_UNSUPPORTED;
+    cudaError_t e;
+    switch (C) {
+        case 1: e = launch_simt<1>(W, X, Y, pdl, stream); break;
+        case 2: e = launch_simt<2>(W, X, Y, pdl, stream); break;
+        case 3: e = launch_simt<3>(W, X, Y, pdl, stream); break;
+        case 4: e = launch_simt<4>(W, X, Y, pdl, stream); break;
+        case 5: e = launch_simt<5>(W, X, Y, pdl, stream); break;
+        case 6: e = launch_simt<6>(W, X, Y, pdl, stream); break;
+        case 7: e = launch_simt<7>(W, X, Y, pdl, stream); break;
+        case 8: e = launch_simt<8>(W, X, Y, pdl, stream); break;
+        default: return SVD_ERR_UNSUPPORTED;
+    }
+    SVD_CUDA_TRY(e);
+    return SVD_OK;
+}
+
+int native_sizes(int64_t in_f, int64_t out_f, size_t *cb, size_t *sb) {
+    if (in_f <= 0 || out_f <= 0 || in_f % 32 != 0) return SVD_ERR_INVALID_ARG;
+    const NativeGeom ng = native_geom(in_f, out_f);
+    if (cb) *cb = (size_t)ng.n_units * kUnitCodeBytes;
+    if (sb) *sb = (size_t)ng.n_units * kUnitScaleBytes;
+    return SVD_OK;
+}
+
+int repack(const svd_qweight *src, void *dc, void *ds, cudaStream_t stream) {
+    int rc = check_qweight(src);
+    if (rc != SVD_OK) return rc;
+    if (src->layout != SVD_LAYOUT_CANONICAL || !dc || !ds || !aligned16(dc) || !aligned16(ds))
+        return SVD_ERR_INVALID_ARG;
+    const NativeGeom ng = native_geom(src->in_features, src->out_features);
+    const int64_t n_words = ng.n_units * (kUnitCodeBytes / 4);
+    const int64_t n_halves = ng.n_units * (kUnitScaleBytes / 2);
+    repack_codes_kernel<<<(unsigned)((n_words + 255) / 256), 256, 0, stream>>>(
+        reinterpret_cast<const uint8_t *>(src->codes), reinterpret_cast<uint32_t *>(dc),
+        src->in_features, src->out_features, ng.n_kc, n_words);
+    SVD_CUDA_TRY(cudaGetLastError());
+    repack_scales_kernel<<<(unsigned)((n_halves + 255) / 256), 256, 0, stream>>>(
+        reinterpret_cast<const uint16_t *>(src->scales), reinterpret_cast<uint16_t *>(ds),
+        src->in_features, src->out_features, ng.n_kc, n_halves);
+    SVD_CUDA_TRY(cudaGetLastError());
+    return SVD_OK;
+}
+
+int unpack(const svd_qweight *src, void *dc, void *ds, cudaStream_t stream) {
+    int rc = check_qweight(src);
+    if (rc != SVD_OK) return rc;
+    if (src->layout != SVD_LAYOUT_NATIVE || !dc || !ds) return SVD_ERR_INVALID_ARG;
+    const NativeGeom ng = native_geom(src->in_features, src->out_features);
+    const int64_t nb = src->out_features * (src->in_features / 2);
+    const int64_t ns = src->out_features * (src->in_features / 32);
+    unpack_codes_kernel<<<(unsigned)((nb + 255) / 256), 256, 0, stream>>>(
+        reinterpret_cast<const uint32_t *>(src->codes), reinterpret_cast<uint8_t *>(dc),
+        src->in_features, src->out_features, ng.n_kc);
+    SVD_CUDA_TRY(cudaGetLastError());
+    unpack_scales_kernel<<<(unsigned)((ns + 255) / 256), 256, 0, stream>>>(
+        reinterpret_cast<const uint16_t *>(src->scales), reinterpret_cast<uint16_t *>(ds),
+        src->in_features, src->out_features, ng.n_kc);
+    SVD_CUDA_TRY(cudaGetLastError());
+    return SVD_OK;
+}
+
+}  // namespace svd

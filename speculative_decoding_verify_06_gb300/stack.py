@@ -1,0 +1,164 @@
+"""The verify pass of a 27B-shaped dense 4-bit model on one GPU, assembled from libsvd calls.
+
+A pass is 64 layers x 4 fused verify-linear launches (q|k|v, o, gate|up, down; every matrix read
+from HBM once and applied to the C = K+1 window columns), then the lm_head over all C positions
+with the production sampler, then the acceptance of the K drafts -- "100 tokens per second ..."
+(section "How speculative decoding gets past a per-token wall") and the HN thread's account of
+running every window position through each layer with one weight read.  The 256 linear launches
+carry programmatic dependent launch and are recorded once into a CUDA graph; a second graph
+holds lm_head, sampler and acceptance.
+
+The activations of every linear are independent synthetic N(0, 1) draws (there is no real model:
+attention, norms and activations between the GEMMs are out of scope), so each launch reads its
+own resident X and writes its own Y, in the stream order of the real dependency chain.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import roofline, svd, synth
+
+# Drafter noise giving alpha ~ 0.5 under the production sampler; computed by the oracle-only
+# script oracle/calibrate_sigma.py (stored in tests/golden/drafter_sigma.json).
+DRAFTER_SIGMA = 1.2053885962814093
+
+
+class Linear:
+    """One 4-bit matrix resident in the native layout, with its input and output buffers."""
+
+    def __init__(self, in_f: int, out_f: int, C: int, seed: int, device, keep_canonical=False):
+        codes, scales = synth.qweight_torch(out_f, in_f, seed, device)
+        cb, sb = svd.svd_native_sizes(in_f, out_f)
+        self.codes = torch.empty(cb, dtype=torch.uint8, device=device)
+        self.scales = torch.empty(sb, dtype=torch.uint8, device=device)
+        svd.svd_repack_weights(svd.QWeight(codes, scales, in_f, out_f, svd.SVD_LAYOUT_CANONICAL),
+                               self.codes, self.scales)
+        self.W = svd.QWeight(self.codes, self.scales, in_f, out_f, svd.SVD_LAYOUT_NATIVE)
+        self.canonical = (codes, scales) if keep_canonical else None
+        self.in_f, self.out_f, self.C = in_f, out_f, C
+        self.X = synth.activations_torch(C, in_f, seed + 7919, device)
+        self.Y = torch.empty((C, out_f), dtype=torch.float32, device=device)
+
+
+class VerifyPass:
+    def __init__(self, layers: int = synth.LAYERS, C: int = 4, seed: int = 0, device="cuda",
+                 head: bool = True, accept: bool = True, sampler: svd.Sampler | None = None,
+                 pdl: bool = True, keep_canonical: bool = False, gemms=synth.LAYER_GEMMS):
+        self.device = torch.device(device)
+        self.C, self.layers, self.pdl = C, layers, pdl
+        self.gemms = tuple(gemms)
+        self.sampler = sampler or svd.Sampler(0.6, 0.95, 0.05)
+        self.linears = []
+        for l in range(layers):
+            for g, (i, o) in enumerate(self.gemms):
+                self.linears.append(Linear(i, o, C, seed * 100003 + 1000 * l + g, self.device,
+                                           keep_canonical))
+        ws = max(svd.svd_verify_linear_workspace_bytes(i, o, C) for i, o in self.gemms)
+        self.ws = torch.zeros(ws, dtype=torch.uint8, device=self.device)
+        self.head = head
+        self.k = C - 1
+        if head:
+            self.lm = Linear(synth.HIDDEN, synth.VOCAB, C, seed * 100003 + 999_999, self.device,
+                             keep_canonical)
+            V = synth.VOCAB
+            self.V = V
+            self.probs = torch.empty((C, V), dtype=torch.float32, device=self.device)
+            self.argmax = torch.empty(C, dtype=torch.int32, device=self.device)
+            self.head_ws = torch.zeros(svd.svd_lm_head_workspace_bytes(synth.HIDDEN, V, C),
+                                       dtype=torch.uint8, device=self.device)
+        self.accept = accept and head and self.k >= 1
+        if self.accept:
+            self._setup_drafter(seed)
+        self.g_stack = self.g_tail = None
+        torch.cuda.synchronize()
+
+    # -- the drafter of the window (untimed set-up) -----------------------------------------
+    def _setup_drafter(self, seed: int):
+        k, V = self.k, self.V
+        self.enqueue_tail(with_accept=False)
+        gen = torch.Generator(device=self.device)
+        gen.manual_seed(seed + 31337)
+        noise = torch.empty((k, V), dtype=torch.float32, device=self.device)
+        noise.normal_(0.0, DRAFTER_SIGMA, generator=gen)
+        self.q_logits = (self.lm.Y[:k] + noise).contiguous()
+        self.q = torch.empty((k, V), dtype=torch.float32, device=self.device)
+        qam = torch.empty(k, dtype=torch.int32, device=self.device)
+        qws = torch.zeros(svd.svd_sampler_workspace_bytes(k, V), dtype=torch.uint8,
+                          device=self.device)
+        svd.svd_sampler_probs(self.q_logits, k, V, self.sampler, self.q, qam, qws)
+        self.draft = torch.multinomial(self.q, 1, generator=gen).to(torch.int32).view(1, k)
+        self.tokens = torch.empty((1, k + 1), dtype=torch.int32, device=self.device)
+        self.n_emitted = torch.empty(1, dtype=torch.int32, device=self.device)
+        self.status = torch.empty(1, dtype=torch.int32, device=self.device)
+        self.seed = seed
+
+    # -- enqueueing -------------------------------------------------------------------------
+    def enqueue_stack(self, stream=None):
+        flags = svd.SVD_F_PDL if self.pdl else 0
+        for lin in self.linears:
+            svd.svd_verify_linear(lin.W, lin.X, self.C, lin.Y, self.ws, flags=flags, stream=stream)
+
+    def enqueue_tail(self, stream=None, with_accept=True):
+        if not self.head:
+            return
+        svd.svd_lm_head_softmax(self.lm.W, self.lm.X, self.C, self.sampler, self.lm.Y, self.probs,
+                                self.argmax, self.head_ws, stream=stream)
+        if with_accept and self.accept:
+            svd.svd_accept(self.probs, self.draft, 1, self.k, self.V, self.tokens, self.n_emitted,
+                           self.status, q=self.q, seed=self.seed, stream=stream)
+
+    def capture(self):
+        """Record the stack and the tail into two CUDA graphs (after one eager warm-up)."""
+        s = torch.cuda.Stream(device=self.device)
+        s.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(s):
+            self.enqueue_stack(s)
+            self.enqueue_tail(s)
+            s.synchronize()
+            svd.svd_graph_begin(s)
+            self.enqueue_stack(s)
+            self.g_stack = svd.svd_graph_end(s)
+            if self.head:
+                svd.svd_graph_begin(s)
+                self.enqueue_tail(s)
+                self.g_tail = svd.svd_graph_end(s)
+        s.synchronize()
+        return self
+
+    def launch(self, stream=None, ev_mid=None):
+        self.g_stack.launch(stream)
+        if ev_mid is not None:
+            ev_mid.record(stream)
+        if self.g_tail is not None:
+            self.g_tail.launch(stream)
+
+    # -- accounting -------------------------------------------------------------------------
+    def stack_bytes(self) -> int:
+        return self.layers * sum(roofline.linear_bytes(i, o, self.C) for i, o in self.gemms)
+
+    def stack_flops(self) -> int:
+        return self.layers * sum(roofline.linear_flops(i, o, self.C) for i, o in self.gemms)
+
+    def pass_bytes(self) -> int:
+        b = self.stack_bytes()
+        if self.head:
+            b += roofline.head_bytes(self.C)
+        if self.accept:
+            b += roofline.accept_bytes_per_window(self.V, self.k, True)
+        return b
+
+    def inputs(self):
+        """The tensors a step consumes (copied host -> device in the end-to-end measurement)."""
+        t = [lin.X for lin in self.linears]
+        if self.head:
+            t.append(self.lm.X)
+        if self.accept:
+            t += [self.q, self.draft]
+        return t
+
+    def outputs(self):
+        if self.accept:
+            return [self.tokens, self.n_emitted, self.status]
+        if self.head:
+            return [self.argmax]
+        return [self.linears[-1].Y]

@@ -1,0 +1,262 @@
+"""Thin ctypes binding of ``libsvd.so`` (declared in ``include/svd.h``).
+
+Argument marshalling only: every function has the C entry point's name, turns torch tensors into
+device pointers and streams into ``cudaStream_t`` handles, calls the library and raises
+:class:`SvdError` on a non-zero return.  No arithmetic of the verify pass happens here, and
+there is no fallback: when the library is missing or cannot be loaded, every entry point raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libsvd.so")
+
+SVD_OK = 0
+SVD_ERR_INVALID_ARG = -1
+SVD_ERR_UNSUPPORTED = -2
+SVD_ERR_CUDA = -3
+SVD_ERR_WORKSPACE = -4
+
+SVD_ST_BAD_TOKEN = 1
+SVD_ST_Q_ZERO = 2
+SVD_ST_BAD_PROB = 4
+SVD_ST_ZERO_RESIDUAL = 8
+SVD_ST_EMPTY = 16
+
+SVD_LAYOUT_CANONICAL = 0
+SVD_LAYOUT_NATIVE = 1
+SVD_F_PDL = 1
+SVD_C_MAX = 32
+SVD_K_MAX = 32
+
+# Every symbol include/svd.h declares (checked by the CPU test suite).
+EXPORTS = (
+    "svd_error_string", "svd_last_cuda_error", "svd_native_sizes", "svd_repack_weights",
+    "svd_unpack_weights", "svd_verify_linear_workspace_bytes", "svd_verify_linear",
+    "svd_sampler_workspace_bytes", "svd_sampler_probs", "svd_lm_head_workspace_bytes",
+    "svd_lm_head_softmax", "svd_accept", "svd_graph_begin", "svd_graph_end", "svd_graph_launch",
+    "svd_graph_destroy", "svd_device_sm_count",
+)
+
+
+class SvdError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        detail = svd_error_string(code)
+        if code == SVD_ERR_CUDA:
+            detail += f" (cudaError {svd_last_cuda_error()})"
+        super().__init__(f"{fn}: {detail}")
+        self.code = code
+
+
+class _QWeight(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("in_features", ctypes.c_int64), ("out_features", ctypes.c_int64),
+                ("layout", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class _Sampler(ctypes.Structure):
+    _fields_ = [("temperature", ctypes.c_float), ("top_p", ctypes.c_float),
+                ("min_p", ctypes.c_float), ("greedy", ctypes.c_int32)]
+
+
+class QWeight:
+    """A 4-bit matrix on the device: codes and scales tensors plus its shape and layout."""
+
+    def __init__(self, codes, scales, in_features: int, out_features: int, layout: int):
+        self.codes, self.scales = codes, scales
+        self.in_features, self.out_features, self.layout = int(in_features), int(out_features), int(layout)
+
+    def _c(self) -> _QWeight:
+        return _QWeight(_ptr(self.codes), _ptr(self.scales), self.in_features, self.out_features,
+                        self.layout, 0)
+
+
+class Sampler:
+    def __init__(self, temperature=0.6, top_p=0.95, min_p=0.05, greedy=False):
+        self.temperature, self.top_p, self.min_p, self.greedy = temperature, top_p, min_p, greedy
+
+    def _c(self) -> _Sampler:
+        return _Sampler(float(self.temperature), float(self.top_p), float(self.min_p),
+                        int(bool(self.greedy)))
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Open libsvd.so (once).  Raises when it is missing: there is no fallback path."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"libsvd.so not built ({path}); run __graft_entry__.build()")
+        L = ctypes.CDLL(path)
+        P, i32, i64, u64, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64,
+                                ctypes.c_size_t)
+        sig = {
+            "svd_error_string": (ctypes.c_char_p, [i32]),
+            "svd_last_cuda_error": (i32, []),
+            "svd_device_sm_count": (i32, []),
+            "svd_native_sizes": (i32, [i64, i64, P, P]),
+            "svd_repack_weights": (i32, [P, P, P, P]),
+            "svd_unpack_weights": (i32, [P, P, P, P]),
+            "svd_verify_linear_workspace_bytes": (sz, [i64, i64, i32]),
+            "svd_verify_linear": (i32, [P, P, i32, P, P, sz, i32, P]),
+            "svd_sampler_workspace_bytes": (sz, [i32, i64]),
+            "svd_sampler_probs": (i32, [P, i32, i64, P, P, P, P, sz, P]),
+            "svd_lm_head_workspace_bytes": (sz, [i64, i64, i32]),
+            "svd_lm_head_softmax": (i32, [P, P, i32, P, P, P, P, P, sz, P]),
+            "svd_accept": (i32, [P, P, P, P, P, P, i64, i32, i64, u64, u64, P, P, P, P, P]),
+            "svd_graph_begin": (i32, [P]),
+            "svd_graph_end": (i32, [P, P]),
+            "svd_graph_launch": (i32, [P, P]),
+            "svd_graph_destroy": (None, [P]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+        return L
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn: str, rc: int):
+    if rc != SVD_OK:
+        raise SvdError(fn, rc)
+
+
+def svd_error_string(code: int) -> str:
+    return load().svd_error_string(int(code)).decode()
+
+
+def svd_last_cuda_error() -> int:
+    return int(load().svd_last_cuda_error())
+
+
+def svd_device_sm_count() -> int:
+    return int(load().svd_device_sm_count())
+
+
+def svd_native_sizes(in_features: int, out_features: int):
+    cb, sb = ctypes.c_size_t(), ctypes.c_size_t()
+    _check("svd_native_sizes",
+           load().svd_native_sizes(in_features, out_features, ctypes.byref(cb), ctypes.byref(sb)))
+    return cb.value, sb.value
+
+
+def svd_repack_weights(src: QWeight, dst_codes, dst_scales, stream=None):
+    w = src._c()
+    _check("svd_repack_weights", load().svd_repack_weights(
+        ctypes.byref(w), _ptr(dst_codes), _ptr(dst_scales), _stream(stream)))
+
+
+def svd_unpack_weights(src: QWeight, dst_codes, dst_scales, stream=None):
+    w = src._c()
+    _check("svd_unpack_weights", load().svd_unpack_weights(
+        ctypes.byref(w), _ptr(dst_codes), _ptr(dst_scales), _stream(stream)))
+
+
+def svd_verify_linear_workspace_bytes(in_features: int, out_features: int, C: int) -> int:
+    return int(load().svd_verify_linear_workspace_bytes(in_features, out_features, C))
+
+
+def svd_verify_linear(W: QWeight, X, C: int, Y, workspace=None, workspace_bytes: int = 0,
+                      flags: int = 0, stream=None):
+    w = W._c()
+    if workspace is not None and not workspace_bytes and not isinstance(workspace, int):
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check("svd_verify_linear", load().svd_verify_linear(
+        ctypes.byref(w), _ptr(X), int(C), _ptr(Y), _ptr(workspace), int(workspace_bytes),
+        int(flags), _stream(stream)))
+
+
+def svd_sampler_workspace_bytes(rows: int, V: int) -> int:
+    return int(load().svd_sampler_workspace_bytes(rows, V))
+
+
+def svd_sampler_probs(logits, rows: int, V: int, sampler: Sampler, probs, argmax, workspace,
+                      workspace_bytes: int = 0, stream=None):
+    s = sampler._c()
+    if not workspace_bytes:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check("svd_sampler_probs", load().svd_sampler_probs(
+        _ptr(logits), int(rows), int(V), ctypes.byref(s), _ptr(probs), _ptr(argmax),
+        _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def svd_lm_head_workspace_bytes(hidden: int, vocab: int, C: int) -> int:
+    return int(load().svd_lm_head_workspace_bytes(hidden, vocab, C))
+
+
+def svd_lm_head_softmax(W: QWeight, H, C: int, sampler: Sampler, logits, probs, argmax,
+                        workspace, workspace_bytes: int = 0, stream=None):
+    w = W._c()
+    s = sampler._c()
+    if not workspace_bytes:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check("svd_lm_head_softmax", load().svd_lm_head_softmax(
+        ctypes.byref(w), _ptr(H), int(C), ctypes.byref(s), _ptr(logits), _ptr(probs),
+        _ptr(argmax), _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def svd_accept(p, draft, n_windows: int, k: int, V: int, out_tokens, n_emitted, status,
+               q=None, p_rows=None, q_rows=None, target_argmax=None, seed: int = 0,
+               window_offset: int = 0, uniforms=None, stream=None):
+    _check("svd_accept", load().svd_accept(
+        _ptr(p), _ptr(p_rows), _ptr(q), _ptr(q_rows), _ptr(target_argmax), _ptr(draft),
+        int(n_windows), int(k), int(V), int(seed) & (2**64 - 1),
+        int(window_offset) & (2**64 - 1), _ptr(uniforms), _ptr(out_tokens), _ptr(n_emitted),
+        _ptr(status), _stream(stream)))
+
+
+class Graph:
+    """An instantiated CUDA graph of library calls (svd_graph_*)."""
+
+    def __init__(self, handle: int):
+        self.handle = handle
+
+    def launch(self, stream=None):
+        _check("svd_graph_launch", load().svd_graph_launch(self.handle, _stream(stream)))
+
+    def destroy(self):
+        if self.handle:
+            load().svd_graph_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+def svd_graph_begin(stream=None):
+    _check("svd_graph_begin", load().svd_graph_begin(_stream(stream)))
+
+
+def svd_graph_end(stream=None) -> Graph:
+    h = ctypes.c_void_p()
+    _check("svd_graph_end", load().svd_graph_end(_stream(stream), ctypes.byref(h)))
+    return Graph(h.value)

@@ -1,0 +1,168 @@
+"""GPU parity of the acceptance kernel (svd_accept) against the oracle on identical p, q, drafts
+and Philox uniforms: emitted tokens, counts and status bit-exact, except windows whose
+resampling uniform lies within 1e-6 of a token boundary (flagged by the oracle), which must be
+rare."""
+import numpy as np
+import pytest
+
+import oracle
+from speculative_decoding_verify_06_gb300 import synth
+from gpu_helpers import accept, lib
+
+pytestmark = pytest.mark.gpu
+
+
+def softmax_rows(l):
+    p, *_ = oracle.sampler(l, 1.0, 1.0, 0.0)
+    return p.astype(np.float32)
+
+
+def compare(p, draft, q=None, **kw):
+    lib()
+    tok_r, ne_r, st_r, near = oracle.accept(p, draft, q=q, seed=kw.get("seed", 0),
+                                            window_offset=kw.get("woff", 0),
+                                            uniforms=kw.get("uniforms"), p_rows=kw.get("p_rows"),
+                                            q_rows=kw.get("q_rows"),
+                                            target_argmax=kw.get("target_argmax"))
+    tok, ne, st = accept(p, draft, q=q, **kw)
+    clean = near == 0
+    assert np.array_equal(st, st_r)
+    assert np.array_equal(ne[clean], ne_r[clean]), np.nonzero(ne[clean] != ne_r[clean])
+    assert np.array_equal(tok[clean], tok_r[clean])
+    assert near.mean() <= max(1e-5, 3.0 / len(near)), near.sum()
+    k = draft.shape[1]
+    ok = st == 0
+    assert np.all((ne[ok] >= 1) & (ne[ok] <= k + 1))
+    return tok, ne, st, near
+
+
+def window_pq(n, k, V, seed, share=0.7, std=2.0):
+    lp = synth.normal_logits(n * (k + 1), V, seed=seed, std=std)
+    lq = synth.shared_logits(lp.reshape(n, k + 1, V)[:, :k].reshape(n * k, V), share, seed + 1, std)
+    return softmax_rows(lp), softmax_rows(lq)
+
+
+def test_tiny_window_workload_sampled_and_greedy():
+    """Vocabulary 4096, k = 3, 1000 windows, seed 0; p and q softmaxes of N(0, 2^2) logits that
+    share 70% of their variance."""
+    n, k, V = 1000, 3, 4096
+    p, q = window_pq(n, k, V, seed=0)
+    draft = synth.draw_from(q, seed=1).reshape(n, k)
+    compare(p, draft, q=q, seed=0)
+    # greedy: drafts from argmax q, argmax of p computed in the kernel or passed in
+    dg = np.argmax(q.reshape(n, k, V), axis=2).astype(np.int32)
+    compare(p, dg)
+    am = np.argmax(p.reshape(n, k + 1, V), axis=2).astype(np.int32)
+    compare(p, dg, target_argmax=am)
+
+
+@pytest.mark.parametrize("k", [1, 5, 32])
+def test_window_lengths(k):
+    n, V = 300, 2048
+    p, q = window_pq(n, k, V, seed=k, share=0.9)
+    draft = synth.draw_from(q, seed=k + 5).reshape(n, k)
+    compare(p, draft, q=q, seed=1234, woff=10_000_000_000)
+
+
+@pytest.mark.parametrize("V", [8, 20, 32, 33, 1001, 4097])
+def test_vocabulary_sizes_small_and_unaligned(V):
+    n, k = 400, 3
+    p, q = window_pq(n, k, V, seed=V)
+    draft = synth.draw_from(q, seed=V + 1).reshape(n, k)
+    compare(p, draft, q=q, seed=V)
+
+
+def test_lm_head_sized_vocabulary_sampler_truncated():
+    """Vocabulary 151936, k = 5: p and q after the production sampler (most entries zero)."""
+    n, k, V = 60, 5, synth.VOCAB
+    lp = synth.normal_logits(n * (k + 1), V, seed=21, std=4.389)
+    lq = synth.perturb(lp.reshape(n, k + 1, V)[:, :k].reshape(n * k, V), 1.205, seed=22)
+    p, *_ = oracle.sampler(lp, np.float32(0.6), np.float32(0.95), np.float32(0.05))
+    q, *_ = oracle.sampler(lq, np.float32(0.6), np.float32(0.95), np.float32(0.05))
+    p, q = p.astype(np.float32), q.astype(np.float32)
+    draft = synth.draw_from(q, seed=23).reshape(n, k)
+    compare(p, draft, q=q, seed=7)
+
+
+def _zipf_pool(n_pairs, V, alpha, seed):
+    """(p, q) pairs from Zipf(1.1)-ranked logits, l_q = l_p + tau * eps with tau bisected so
+    that sum min(p, q) = alpha within 1e-4."""
+    P, Q = [], []
+    for i in range(n_pairs):
+        lp = synth.zipf_logits(V, seed + i).astype(np.float64)
+        eps = synth.rng(seed + 1000 + i).normal(size=V)
+        p = np.exp(lp - lp.max())
+        p /= p.sum()
+        lo, hi = 0.0, 64.0
+        for _ in range(60):
+            tau = 0.5 * (lo + hi)
+            lq = lp + tau * eps
+            q = np.exp(lq - lq.max())
+            q /= q.sum()
+            a = np.minimum(p, q).sum()
+            if abs(a - alpha) < 1e-4:
+                break
+            if a > alpha:
+                lo = tau
+            else:
+                hi = tau
+        P.append(p.astype(np.float32))
+        Q.append(q.astype(np.float32))
+    return np.stack(P), np.stack(Q)
+
+
+@pytest.mark.parametrize("alpha,k", [(0.35, 3), (0.9, 5), (0.6, 1)])
+def test_acceptance_sweep_pool_indirection(alpha, k):
+    """The acceptance-sweep workload in miniature: a pool of (p, q) pairs at vocabulary 151936
+    addressed through p_rows / q_rows, stochastic and greedy drafters."""
+    V, n_pairs, n = synth.VOCAB, 8, 400
+    P, Q = _zipf_pool(n_pairs, V, alpha, seed=int(alpha * 100) + k)
+    g = synth.rng(k)
+    pair = g.integers(0, n_pairs, size=(n, k + 1))
+    p_rows = pair.astype(np.int64)
+    q_rows = pair[:, :k].astype(np.int64)
+    draft = np.empty((n, k), np.int32)
+    for i in range(k):
+        draft[:, i] = synth.draw_from(Q[pair[:, i]], seed=100 + i)
+    compare(P, draft, q=Q, p_rows=p_rows, q_rows=q_rows, seed=5)
+    # greedy drafter: the drafter's distribution is the one-hot of argmax q
+    Q1 = np.zeros_like(Q)
+    Q1[np.arange(n_pairs), np.argmax(Q, axis=1)] = 1.0
+    dg = np.argmax(Q, axis=1)[pair[:, :k]].astype(np.int32)
+    compare(P, dg, q=Q1, p_rows=p_rows, q_rows=q_rows, seed=6)
+
+
+def test_status_edge_cases_match_oracle():
+    V, k, n = 64, 3, 6
+    g = synth.rng(3)
+    p = g.dirichlet(np.ones(V), size=n * (k + 1)).astype(np.float32)
+    q = g.dirichlet(np.ones(V), size=n * k).astype(np.float32)
+    draft = g.integers(0, V, size=(n, k)).astype(np.int32)
+    draft[0, 0] = V + 5              # out of range
+    draft[1, 1] = -1                 # out of range (after an accept or not)
+    q[2 * k + 0, draft[2, 0]] = 0.0  # q(x) = 0 for a drafted token
+    p[3 * (k + 1) + 1, 7] = np.nan   # NaN in a row
+    p[4 * (k + 1) + 0] = q[4 * k + 0]  # p == q at position 0 of window 4 ...
+    p[5 * (k + 1) + 0] = 0.0         # ... and an empty p row
+    compare(p, draft, q=q, seed=3)
+    # zero residual: p <= q everywhere at a rejected position falls back to p
+    p2 = np.zeros((1 * (k + 1), V), np.float32)
+    p2[:, 5] = 1.0
+    q2 = np.zeros((k, V), np.float32)
+    q2[:, 5] = 1.0
+    uni = np.full((1, k + 1, 2), 0.25, np.float32)
+    d2 = np.array([[9, 5, 5]], np.int32)  # p(9) = q(9) = 0: rejected; (p - q)+ = 0
+    tok, ne, st, _ = compare(p2, d2, q=q2, uniforms=uni)
+    assert st[0] & 8 and tok[0, 0] == 5
+
+
+def test_uniform_hook_equals_philox():
+    n, k, V = 200, 3, 512
+    p, q = window_pq(n, k, V, seed=77)
+    draft = synth.draw_from(q, seed=78).reshape(n, k)
+    uni = np.array([[oracle.uniforms(99, 5 + w, i) for i in range(k + 1)] for w in range(n)],
+                   np.float32)
+    a = accept(p, draft, q=q, seed=99, woff=5)
+    b = accept(p, draft, q=q, uniforms=uni)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)

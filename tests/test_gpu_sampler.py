@@ -1,0 +1,109 @@
+"""GPU parity of the sampler (svd_sampler_probs) and of lm_head + sampler against the oracle on
+identical fp32 logits: argmax exact; the kept set exact wherever the oracle reports no decision
+within rounding of a filter boundary; kept probabilities within 1e-5 relative."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_decoding_verify_06_gb300 import svd, synth
+from gpu_helpers import DEV, assert_gemm_parity, lib, sampler, to_dev
+
+pytestmark = pytest.mark.gpu
+
+F32 = np.float32
+
+
+def check(logits, T, top_p, min_p, greedy=False):
+    lib()
+    smp = svd.Sampler(T, top_p, min_p, greedy)
+    pg, amg = sampler(logits, smp)
+    pr, amr, nk, fl = oracle.sampler(logits, F32(T), F32(top_p), F32(min_p), greedy)
+    assert np.array_equal(amg, amr)
+    for r in range(len(logits)):
+        kept_g, kept_r = pg[r] > 0, pr[r] > 0
+        assert kept_g[amr[r]]
+        assert abs(pg[r].astype(np.float64).sum() - 1.0) < 1e-5
+        if fl[r] == 0:
+            assert np.array_equal(kept_g, kept_r), (r, kept_g.sum(), kept_r.sum())
+            assert np.allclose(pg[r], pr[r], rtol=1e-5, atol=1e-12)
+    return pg, pr, fl
+
+
+def test_small_vocabulary_window():
+    check(synth.normal_logits(4, 4096, seed=0, std=2.0), 0.6, 0.95, 0.05)
+
+
+def test_lm_head_sized_rows():
+    check(synth.normal_logits(6, synth.VOCAB, seed=1, std=4.389), 0.6, 0.95, 0.05)
+
+
+def test_plain_softmax_special_case_general_path():
+    # min_p = 0 makes every token a survivor: the radix-select path; top_p = 1 keeps all
+    pg, pr, _ = check(synth.normal_logits(2, 20000, seed=2, std=1.0), 1.0, 1.0, 0.0)
+    assert np.all(pg > 0)
+
+
+def test_top_p_general_path_radix_select():
+    check(synth.normal_logits(3, synth.VOCAB, seed=3, std=1.5), 0.8, 0.9, 0.0)
+
+
+def test_top_p_general_path_with_heavy_ties():
+    g = synth.rng(4)
+    logits = g.integers(0, 4, size=(3, 30000)).astype(np.float32)
+    check(logits, 1.0, 0.7, 0.0)
+
+
+def test_flat_distribution_ties_resolved_by_id():
+    logits = np.zeros((2, 1000), np.float32)
+    pg, pr, _ = check(logits, 0.6, 0.95, 0.05)
+    assert (pg[0] > 0).sum() == 950 and np.all(pg[0, :950] > 0)
+
+
+def test_greedy_one_hot():
+    logits = synth.normal_logits(5, 5000, seed=6)
+    logits[0, 10] = logits[0, 20] = 50.0
+    pg, _, _ = check(logits, 0.6, 0.95, 0.05, greedy=True)
+    assert pg[0, 10] == 1.0 and pg[0].sum() == 1.0
+
+
+def test_hand_example_five_tokens():
+    p = np.array([0.5, 0.25, 0.15, 0.07, 0.03])
+    logits = np.log(p).astype(np.float32)[None]
+    pg, _, _ = check(logits, 1.0, 0.8, 0.0)
+    assert np.allclose(pg[0], np.r_[p[:3] / p[:3].sum(), 0, 0], rtol=1e-5)
+    pg, _, _ = check(logits, 1.0, 1.0, 0.2)
+    assert np.allclose(pg[0], np.r_[p[:3] / p[:3].sum(), 0, 0], rtol=1e-5)
+
+
+def test_lm_head_softmax_matches_oracle():
+    lib()
+    hidden, vocab, C = synth.HIDDEN, synth.VOCAB, 6
+    codes, scales = synth.qweight_torch(vocab, hidden, seed=99, device=DEV)
+    cb, sb = svd.svd_native_sizes(hidden, vocab)
+    nc = torch.empty(cb, dtype=torch.uint8, device=DEV)
+    ns = torch.empty(sb, dtype=torch.uint8, device=DEV)
+    svd.svd_repack_weights(svd.QWeight(codes, scales, hidden, vocab, svd.SVD_LAYOUT_CANONICAL), nc, ns)
+    W = svd.QWeight(nc, ns, hidden, vocab, svd.SVD_LAYOUT_NATIVE)
+    H = synth.activations_torch(C, hidden, seed=5, device=DEV)
+    logits = torch.empty((C, vocab), dtype=torch.float32, device=DEV)
+    probs = torch.empty_like(logits)
+    am = torch.empty(C, dtype=torch.int32, device=DEV)
+    ws = torch.zeros(svd.svd_lm_head_workspace_bytes(hidden, vocab, C), dtype=torch.uint8, device=DEV)
+    smp = svd.Sampler(0.6, 0.95, 0.05)
+    svd.svd_lm_head_softmax(W, H, C, smp, logits, probs, am, ws)
+    torch.cuda.synchronize()
+    lg = logits.cpu().numpy()
+    rows = np.unique(np.r_[synth.rng(1).choice(vocab, 100, replace=False), 0, vocab - 1,
+                           am.cpu().numpy()])
+    y_ref, a_ref = oracle.verify_linear(codes[rows].cpu().numpy(),
+                                        scales[rows].cpu().numpy().view(np.uint16),
+                                        H.view(torch.int16).cpu().numpy().view(np.uint16))
+    assert_gemm_parity(lg[:, rows], y_ref, a_ref)
+    pr, amr, nk, fl = oracle.sampler(lg, F32(0.6), F32(0.95), F32(0.05))
+    pg = probs.cpu().numpy()
+    assert np.array_equal(am.cpu().numpy(), amr)
+    for r in range(C):
+        if fl[r] == 0:
+            assert np.array_equal(pg[r] > 0, pr[r] > 0)
+            assert np.allclose(pg[r], pr[r], rtol=1e-5, atol=1e-12)

@@ -1,0 +1,60 @@
+"""The whole verify pass: layer stack + lm_head + sampler + acceptance recorded into CUDA graphs
+with programmatic dependent launch; replays must equal eager launches bit for bit and sampled
+outputs must match the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_decoding_verify_06_gb300 import stack, svd, synth
+from gpu_helpers import assert_gemm_parity, lib
+
+pytestmark = pytest.mark.gpu
+
+
+def test_graph_replay_equals_eager_and_oracle():
+    lib()
+    vp = stack.VerifyPass(layers=2, C=4, seed=3, keep_canonical=True)
+    vp.enqueue_stack()
+    vp.enqueue_tail()
+    torch.cuda.synchronize()
+    eager = [lin.Y.clone() for lin in vp.linears] + [vp.lm.Y.clone(), vp.probs.clone(),
+                                                     vp.tokens.clone(), vp.n_emitted.clone()]
+    for lin in vp.linears + [vp.lm]:
+        lin.Y.fill_(float("nan"))
+    vp.capture()
+    for _ in range(3):
+        vp.launch()
+    torch.cuda.synchronize()
+    replay = [lin.Y for lin in vp.linears] + [vp.lm.Y, vp.probs, vp.tokens, vp.n_emitted]
+    for a, b in zip(eager, replay):
+        assert torch.equal(a, b)
+    assert int(vp.status.item()) == 0 and 1 <= int(vp.n_emitted.item()) <= vp.k + 1
+    # sampled rows of every linear against the oracle
+    g = synth.rng(0)
+    for lin in vp.linears:
+        rows = np.unique(np.r_[g.choice(lin.out_f, 24, replace=False), 0, lin.out_f - 1])
+        codes, scales = lin.canonical
+        y_ref, a_ref = oracle.verify_linear(codes[rows].cpu().numpy(),
+                                            scales[rows].cpu().numpy().view(np.uint16),
+                                            lin.X.view(torch.int16).cpu().numpy().view(np.uint16))
+        assert_gemm_parity(lin.Y.cpu().numpy()[:, rows], y_ref, a_ref)
+    # the acceptance of the window against the oracle on the same p, q and drafts
+    tok_r, ne_r, st_r, near = oracle.accept(vp.probs.cpu().numpy(), vp.draft.cpu().numpy(),
+                                            q=vp.q.cpu().numpy(), seed=vp.seed)
+    if near[0] == 0:
+        assert np.array_equal(vp.tokens.cpu().numpy(), tok_r)
+        assert int(vp.n_emitted.item()) == ne_r[0] and int(vp.status.item()) == st_r[0]
+
+
+def test_pdl_and_plain_launches_agree():
+    lib()
+    a = stack.VerifyPass(layers=1, C=4, seed=5, head=False, pdl=True)
+    b = stack.VerifyPass(layers=1, C=4, seed=5, head=False, pdl=False)
+    a.capture()
+    b.capture()
+    a.launch()
+    b.launch()
+    torch.cuda.synchronize()
+    for x, y in zip(a.linears, b.linears):
+        assert torch.equal(x.Y, y.Y)
