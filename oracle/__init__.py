@@ -57,7 +57,8 @@ def lib():
             L.orc_uniforms.restype = None
             L.orc_uniforms.argtypes = [u64, u64, ctypes.c_uint32, P, P]
             L.orc_accept.restype = None
-            L.orc_accept.argtypes = [P, P, P, P, P, P, i64, i32, i64, u64, u64, P, P, P, P, P, i32]
+            L.orc_accept.argtypes = [P, P, P, P, P, P, i64, i32, i64, u64, u64, P, P, P, P, P, P,
+                                     i32]
             L.orc_max_threads.restype = i32
             L.orc_max_threads.argtypes = []
             _lib = L
@@ -146,13 +147,14 @@ def uniforms(seed: int, window: int, pos: int):
 
 
 def accept(p, draft, q=None, target_argmax=None, seed=0, window_offset=0, uniforms=None,
-           p_rows=None, q_rows=None, nthreads: int = 0):
+           p_rows=None, q_rows=None, nthreads: int = 0, return_margin: bool = False):
     """Greedy (q None) or sampled acceptance of every window.
 
     p: float32 [P, V] rows (indexed by p_rows [n, k+1] when given, else [n*(k+1), V]);
     q: float32 rows likewise with q_rows [n, k]; draft: int32 [n, k].
     Returns (tokens int32 [n, k+1] padded with -1, n_emitted int32 [n], status int32 [n],
-    near int32 [n]).  Follows "100 tokens per second ..." ("How speculative decoding gets past
+    near int32 [n]; with return_margin also margin float64 [n], the distance of each draw's
+    u' to the nearer edge of its token's interval, +inf without a draw).  Follows "100 tokens per second ..." ("How speculative decoding gets past
     a per-token wall"), "Decode is memory-bound ..." ("Speculative decoding") and the HN
     thread's "D E F" example.
     """
@@ -171,7 +173,10 @@ def accept(p, draft, q=None, target_argmax=None, seed=0, window_offset=0, unifor
     ne = np.empty(n, np.int32)
     st = np.empty(n, np.int32)
     nr = np.empty(n, np.int32)
+    mg = np.empty(n, np.float64)
     lib().orc_accept(_p(p), _p(pr), _p(q), _p(qr), _p(ta), _p(draft), n, k, V,
                      int(seed) & (2**64 - 1), int(window_offset) & (2**64 - 1), _p(un),
-                     _p(tok), _p(ne), _p(st), _p(nr), int(nthreads or max_threads()))
+                     _p(tok), _p(ne), _p(st), _p(nr), _p(mg), int(nthreads or max_threads()))
+    if return_margin:
+        return tok, ne, st, nr, mg
     return tok, ne, st, nr

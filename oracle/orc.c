@@ -266,7 +266,7 @@ void orc_uniforms(uint64_t seed, uint64_t window, uint32_t pos, double *u, doubl
 /*  16 the distribution drawn from has zero mass: no token is emitted there.            */
 /* near[w] is set when a draw's u' lies within 1e-6 of either edge of the chosen        */
 /* token's interval [C_{v-1}/R, C_v/R): there another summation order may pick a        */
-/* neighbour.                                                                           */
+/* neighbour.  margin[w] (optional) is that distance itself (+inf without a draw).      */
 /* ------------------------------------------------------------------------------------ */
 static double orc_prob(float f, int *st)
 {
@@ -280,7 +280,7 @@ static double orc_prob(float f, int *st)
 }
 
 static int64_t orc_draw(const float *pr, const float *qr, int64_t V, double u2, int *st,
-                        int *near)
+                        int *near, double *margin)
 {
     double *r = (double *)malloc(sizeof(double) * (size_t)V);
     double R = 0.0;
@@ -313,7 +313,9 @@ static int64_t orc_draw(const float *pr, const float *qr, int64_t V, double u2, 
             Cprev = R - r[tok];
             Cv = R;
         }
-        if (fabs(u2 - Cprev / R) < 1e-6 || fabs(u2 - Cv / R) < 1e-6) *near = 1;
+        double m = fmin(fabs(u2 - Cprev / R), fabs(u2 - Cv / R));
+        if (m < *margin) *margin = m;
+        if (m < 1e-6) *near = 1;
     } else {
         *st |= 16;
     }
@@ -336,12 +338,13 @@ void orc_accept(const float *p, const int64_t *p_rows, const float *q, const int
                 const int32_t *target_argmax, const int32_t *draft, int64_t n, int k,
                 int64_t V, uint64_t seed, uint64_t window_offset, const float *uniforms,
                 int32_t *out_tokens, int32_t *n_emitted, int32_t *status, int32_t *near,
-                int nthreads)
+                double *margin, int nthreads)
 {
     if (nthreads <= 0) nthreads = 1;
 #pragma omp parallel for num_threads(nthreads) schedule(dynamic, 16)
     for (int64_t w = 0; w < n; ++w) {
         int st = 0, nr = 0, ne = 0;
+        double mg = INFINITY;
         int32_t *tok = out_tokens + w * (k + 1);
         for (int i = 0; i <= k; ++i) tok[i] = -1;
         const float *prow[65], *qrow[65];
@@ -381,7 +384,7 @@ void orc_accept(const float *p, const int64_t *p_rows, const float *q, const int
                     accept = u * qv < pv;
                 }
                 if (accept) { tok[ne++] = x; continue; }
-                int64_t t = orc_draw(prow[i], qrow[i], V, u2, &st, &nr);
+                int64_t t = orc_draw(prow[i], qrow[i], V, u2, &st, &nr, &mg);
                 if (t >= 0) tok[ne++] = (int32_t)t;
                 break;
             }
@@ -394,13 +397,14 @@ void orc_accept(const float *p, const int64_t *p_rows, const float *q, const int
                     orc_uniforms(seed, window_offset + (uint64_t)w, (uint32_t)k, &u, &u2);
                 }
                 (void)u;
-                int64_t t = orc_draw(prow[k], NULL, V, u2, &st, &nr);
+                int64_t t = orc_draw(prow[k], NULL, V, u2, &st, &nr, &mg);
                 if (t >= 0) tok[ne++] = (int32_t)t;
             }
         }
         n_emitted[w] = ne;
         status[w] = st;
         if (near) near[w] = nr;
+        if (margin) margin[w] = mg;
     }
 }
 
