@@ -227,7 +227,8 @@ def run_svd(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     build.build_library()
-    vp = stack.VerifyPass(layers=args.layers, C=args.C, seed=rank, device=dev, pdl=not args.no_pdl)
+    vp = stack.VerifyPass(layers=args.layers, C=args.C, seed=rank, device=dev, pdl=not args.no_pdl,
+                          chain=not args.no_chain)
     vp.capture()
     s = torch.cuda.current_stream(dev)
     dist = world > 1
@@ -317,7 +318,9 @@ def run_svd(args, rank, world, local_rank):
         "config": {"workload": WORKLOAD, "C": args.C, "layers": args.layers,
                    "global_batch": world, "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2: 11.9 GB of weights streamed per step",
-                   "pdl": not args.no_pdl, "graph": "stack graph + tail graph per step"},
+                   "stack_launch": ("per-matrix launches, PDL" if args.no_chain else
+                                    "one persistent cooperative chain of 256 matrices"),
+                   "graph": "stack graph + tail graph per step"},
         "stack": {"ms": stack_ms, "passes_per_s": 1000.0 / stack_ms, "bytes": stack_bytes,
                   "gb_s": achieved, "tail_ms": tail_ms},
         "tokens_per_pass": tokens_per_pass,
@@ -325,11 +328,11 @@ def run_svd(args, rank, world, local_rank):
         "pass_bytes": vp.pass_bytes(),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind,
-                     "kernel": "vl_mma_kernel (256 launches of the stack, averaged)",
+                     "kernel": "vl_mma_kernel (the stack's 256 matrices, averaged)",
                      "traffic": None if traffic_pass is None else traffic_pass},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": Ke},
-        "gpu_launches": K * (n_launch + (1 + 4 + 1 if vp.head else 0)),
+        "gpu_launches": K * ((n_launch if args.no_chain else 1) + (1 + 4 + 1 if vp.head else 0)),
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -352,6 +355,8 @@ def main():
     ap.add_argument("--C", type=int, default=4)
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-pdl", action="store_true")
+    ap.add_argument("--no-chain", action="store_true",
+                    help="one launch per matrix (with PDL) instead of the persistent chain")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)

@@ -142,6 +142,26 @@ size_t svd_verify_linear_workspace_bytes(int64_t in_features, int64_t out_featur
 int svd_verify_linear(const svd_qweight *W, const void *X, int C, float *Y, void *workspace,
                       size_t workspace_bytes, int flags, svd_stream_t stream);
 
+/* A chain of verify-linear launches executed in order: op i+1 may read what op i wrote. */
+typedef struct svd_linear_op {
+    svd_qweight W;  /* NATIVE layout */
+    const void *X;  /* bf16 [C][W.in_features], 16-byte aligned */
+    float *Y;       /* fp32 [C][W.out_features] */
+} svd_linear_op;
+
+/* The verify linear of every op of a model's pass in ONE persistent cooperative launch per 256
+ * ops: each CTA streams its share of op 0, op 1, ... through the same shared-memory ring, so
+ * the weights of op i+1 are already in flight while op i finishes; a grid-wide barrier between
+ * ops orders op i's writes before op i+1 reads its activations ("100 tokens per second ...",
+ * "How speculative decoding gets past a per-token wall": every weight matrix of the pass read
+ * once for the whole window).  Results equal n_ops calls of svd_verify_linear bit for bit.
+ * ops is a HOST array; the weights must not change while the chain runs.  SVD_F_PDL applies
+ * to a chain of one op only.  The workspace is zero-filled before first use, as for
+ * svd_verify_linear. */
+size_t svd_verify_chain_workspace_bytes(const svd_linear_op *ops, int n_ops, int C);
+int svd_verify_chain(const svd_linear_op *ops, int n_ops, int C, void *workspace,
+                     size_t workspace_bytes, int flags, svd_stream_t stream);
+
 /* ---- (b) sampler and lm_head -------------------------------------------------------- */
 /* Per row of logits [rows][V] fp32: p = softmax(logits / T); keep v iff p[v] >= min_p *
  * max p and v lies in the shortest prefix, in the order (p descending, id ascending), whose

@@ -12,6 +12,9 @@ int verify_linear(const svd_qweight *W, const void *X, int C, float *Y, void *ws
 int native_sizes(int64_t in_f, int64_t out_f, size_t *cb, size_t *sb);
 int repack(const svd_qweight *src, void *dc, void *ds, cudaStream_t stream);
 int unpack(const svd_qweight *src, void *dc, void *ds, cudaStream_t stream);
+size_t chain_workspace_bytes(const svd_linear_op *ops, int n_ops, int C);
+int verify_chain(const svd_linear_op *ops, int n_ops, int C, void *ws, size_t ws_bytes, int flags,
+                 cudaStream_t stream);
 size_t sampler_ws_bytes(int rows, int64_t V);
 int sampler_probs(const float *logits, int rows, int64_t V, const svd_sampler *s, float *probs,
                   int32_t *argmax, void *ws, size_t ws_bytes, cudaStream_t stream);
@@ -80,6 +83,16 @@ size_t svd_verify_linear_workspace_bytes(int64_t in_f, int64_t out_f, int C) {
 int svd_verify_linear(const svd_qweight *W, const void *X, int C, float *Y, void *ws,
                       size_t ws_bytes, int flags, svd_stream_t stream) {
     return svd::verify_linear(W, X, C, Y, ws, ws_bytes, flags, (cudaStream_t)stream);
+}
+
+size_t svd_verify_chain_workspace_bytes(const svd_linear_op *ops, int n_ops, int C) {
+    if (!ops || n_ops < 1 || C < 1 || C > SVD_C_MAX || svd::sm_count() < 1) return 0;
+    return svd::chain_workspace_bytes(ops, n_ops, C);
+}
+
+int svd_verify_chain(const svd_linear_op *ops, int n_ops, int C, void *ws, size_t ws_bytes,
+                     int flags, svd_stream_t stream) {
+    return svd::verify_chain(ops, n_ops, C, ws, ws_bytes, flags, (cudaStream_t)stream);
 }
 
 size_t svd_sampler_workspace_bytes(int rows, int64_t V) {

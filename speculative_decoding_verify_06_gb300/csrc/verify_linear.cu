@@ -21,16 +21,23 @@
 //    ticket per row block, summed in CTA order: deterministic, no spinning).
 //  * vl_simt_kernel (CANONICAL layout) -- the plain CUDA-core version: one warp per output
 //    row, each lane one 32-input block at a time, fp32 FMAs, warp-shuffle reduction.
+#include <cooperative_groups.h>
+
+#include <memory>
+
 #include "svd_common.cuh"
 
 namespace svd {
 
 // ---- native layout geometry ------------------------------------------------------------
-constexpr int kRowsPerBlock = 64;       // 4 MMA tiles of 16 rows
-constexpr int kTiles = 4;
+#ifndef SVD_TILES
+#define SVD_TILES 4
+#endif
+constexpr int kTiles = SVD_TILES;                  // MMA tiles of 16 rows per unit
+constexpr int kRowsPerBlock = 16 * kTiles;
 constexpr int kChunk = 64;              // inputs per unit (2 scale blocks, 4 k16 steps)
-constexpr int kUnitCodeBytes = 2048;    // 64 rows x 64 inputs x 4 bit
-constexpr int kUnitScaleBytes = 256;    // 64 rows x 2 blocks x fp16
+constexpr int kUnitCodeBytes = 512 * kTiles;   // rows x 64 inputs x 4 bit
+constexpr int kUnitScaleBytes = 64 * kTiles;   // rows x 2 blocks x fp16
 constexpr int kUnitBytes = kUnitCodeBytes + kUnitScaleBytes;
 
 struct NativeGeom {
@@ -60,8 +67,8 @@ __global__ void repack_codes_kernel(const uint8_t *__restrict__ src, uint32_t *_
                                     int64_t in_f, int64_t out_f, int64_t n_kc, int64_t n_words) {
     const int64_t wid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (wid >= n_words) return;
-    const int s = (int)(wid & 3), lane = (int)((wid >> 2) & 31), r = (int)((wid >> 7) & 3);
-    const int64_t unit = wid >> 9, rb = unit / n_kc, kc = unit % n_kc;
+    const int s = (int)(wid & 3), lane = (int)((wid >> 2) & 31), r = (int)((wid >> 7) % kTiles);
+    const int64_t unit = wid / (128 * kTiles), rb = unit / n_kc, kc = unit % n_kc;
     const int g = lane >> 2, t = lane & 3;
     uint32_t word = 0;
 #pragma unroll
@@ -87,8 +94,8 @@ __global__ void repack_scales_kernel(const uint16_t *__restrict__ src, uint16_t 
                                      int64_t in_f, int64_t out_f, int64_t n_kc, int64_t n_halves) {
     const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= n_halves) return;
-    const int q = (int)(idx & 3), g = (int)((idx >> 2) & 7), r = (int)((idx >> 5) & 3);
-    const int64_t unit = idx >> 7, rb = unit / n_kc, kc = unit % n_kc;
+    const int q = (int)(idx & 3), g = (int)((idx >> 2) & 7), r = (int)((idx >> 5) % kTiles);
+    const int64_t unit = idx / (32 * kTiles), rb = unit / n_kc, kc = unit % n_kc;
     const int64_t row = rb * kRowsPerBlock + 16 * r + g + 8 * (q >> 1), blk = 2 * kc + (q & 1);
     const int64_t nblk = in_f / 32;
     dst[idx] = (row < out_f && blk < nblk) ? src[row * nblk + blk] : (uint16_t)0;
@@ -143,13 +150,21 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 // Four bf16x2 A registers from one native word: (bits >> 4p) & 0x000F000F | 0x43004300 is the
-// pair (128 + c_lo, 128 + c_hi) exactly; subtracting (136, 136) leaves (c - 8) exactly.
-__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t a[4]) {
+// pair (128 + c_lo, 128 + c_hi) exactly; subtracting (136, 136) leaves (c - 8) exactly.  With
+// MULHI the three right shifts are taken as mul.hi by 2^28, 2^24, 2^20 held in registers (the
+// integer-multiply unit), which leaves only the lop3s on the integer ALU.
+template <bool MULHI>
+__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t a[4], uint32_t m4, uint32_t m8,
+                                             uint32_t m12) {
     const uint32_t magic = 0x43004300u, bias = 0x43084308u;
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
-        uint32_t v;
-        const uint32_t sh = w >> (4 * p);
+        uint32_t v, sh;
+        if (MULHI) {
+            sh = (p == 0) ? w : __umulhi(w, p == 1 ? m4 : (p == 2 ? m8 : m12));
+        } else {
+            sh = w >> (4 * p);
+        }
         asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(v) : "r"(sh), "r"(0x000F000Fu), "r"(magic));
         asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(a[p]) : "r"(v), "r"(bias));
     }
@@ -172,13 +187,33 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void *p) {
     return v;
 }
 
-// CTA that owns unit n when n_units units are split into G contiguous ranges
-// [b*n/G, (b+1)*n/G).
-__device__ __forceinline__ int64_t owner_cta(int64_t n, int64_t G, int64_t n_units) {
-    return ((n + 1) * G - 1) / n_units;
+// One verify-linear launch in the native layout (a link of a chain).
+struct VlOp {
+    const uint8_t *codes;
+    const uint8_t *scales;
+    const __nv_bfloat16 *X;
+    float *Y;
+    int64_t in_f, out_f, n_kc, n_units;
+};
+
+template <int MAXOPS>
+struct VlOps {
+    int n;
+    int C;
+    uint32_t m4, m8, m12;  // 2^28, 2^24, 2^20: shift multipliers kept opaque to the compiler
+    VlOp op[MAXOPS];
+};
+
+// The units of an op are split into G_op = min(G, n_units) contiguous CTA ranges
+// [b n / G_op, (b+1) n / G_op); every CTA below G_op owns at least one unit.
+// owner_cta(n) is the CTA whose range holds unit n.
+__device__ __forceinline__ int64_t owner_cta(int64_t n, int64_t Gop, int64_t n_units) {
+    return ((n + 1) * Gop - 1) / n_units;
 }
 
 // ---- the tensor-core stream-K kernel ---------------------------------------------------
+constexpr int kPartialSlotFloats = 32 * kTiles * 4 * 4;  // largest warp partial (4 n-tiles)
+
 template <int NT, int NW, int D>
 struct MmaCfg {
     static constexpr int kAcc = kTiles * NT * 4;              // fp32 accumulators per lane
@@ -187,192 +222,233 @@ struct MmaCfg {
     static constexpr size_t kSmem = kRing + (size_t)NW * kPartial * sizeof(float);
 };
 
-template <int NT, int NW, int D>
-__global__ void __launch_bounds__(NW * 32, (NT == 1 ? 2 : 1))
-vl_mma_kernel(const uint8_t *__restrict__ wcodes, const uint8_t *__restrict__ wscales,
-              const __nv_bfloat16 *__restrict__ X, float *__restrict__ Y, int64_t in_f,
-              int64_t out_f, int C, int64_t n_kc, int64_t n_units, float *__restrict__ ws_part,
+// Runs every op of P in order on a persistent grid.  Each warp keeps a ring of D unit slots
+// in shared memory filled by cp.async; the issue cursor walks the warp's units op after op,
+// so the weights of op g+1 stream in while op g finishes.  Activations of op g+1 are read
+// only after the grid barrier that ends op g (a chain of more than one op is launched
+// cooperatively), or, for op 0, after griddepcontrol.wait.
+template <int NT, int NW, int D, int MAXOPS, int MINB, bool MULHI>
+__global__ void __launch_bounds__(NW * 32, MINB)
+vl_mma_kernel(const __grid_constant__ VlOps<MAXOPS> P, float *__restrict__ ws_part,
               unsigned int *__restrict__ ws_cnt) {
     using Cfg = MmaCfg<NT, NW, D>;
     constexpr int kAcc = Cfg::kAcc, kPartial = Cfg::kPartial;
+    constexpr int kPer = kPartial / (NW * 32);  // reduced elements per thread
     extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ int s_last;
     float *red = reinterpret_cast<float *>(smem + Cfg::kRing);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, t = lane & 3;
+    const int g4 = lane >> 2, t4 = lane & 3;
     const int64_t G = gridDim.x, b = blockIdx.x;
-    const int64_t start = b * n_units / G, end = (b + 1) * n_units / G;
-    const int64_t span = end - start;
-    const int J = span > warp ? (int)((span - warp + NW - 1) / NW) : 0;
+    const int C = P.C;
     uint8_t *ring = smem + (size_t)warp * D * kUnitBytes;
 
-    auto issue = [&](int j) {
-        const int64_t u = start + warp + (int64_t)NW * j;
-        uint8_t *slot = ring + (j % D) * kUnitBytes;
-        const uint8_t *src = wcodes + u * kUnitCodeBytes;
-#pragma unroll
-        for (int r = 0; r < kTiles; ++r) cp_async16(slot + r * 512 + lane * 16, src + r * 512 + lane * 16);
-        if (lane < 16)
-            cp_async16(slot + kUnitCodeBytes + lane * 16, wscales + u * kUnitScaleBytes + lane * 16);
-    };
-
-    // Weights do not depend on the upstream kernel: start streaming them before waiting on it.
-#pragma unroll
-    for (int s = 0; s < D - 1; ++s) {
-        if (s < J) issue(s);
-        cp_async_commit();
-    }
-    griddep_wait();
-    griddep_launch_dependents();
-
-    auto load_x = [&](int j, uint4 (&xr)[NT][2]) {
-        const int64_t u = start + warp + (int64_t)NW * j;
-        const int64_t kc = u % n_kc;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int col = nt * 8 + g;
-#pragma unroll
-            for (int blk = 0; blk < 2; ++blk) {
-                const int64_t i0 = kc * kChunk + blk * 32 + t * 8;
-                if (col < C && i0 < in_f)
-                    xr[nt][blk] = ldg_nc_v4(X + (int64_t)col * in_f + i0);
-                else
-                    xr[nt][blk] = make_uint4(0u, 0u, 0u, 0u);
-            }
+    // ---- issue cursor: (op ig, unit ij of iJ), source pointers, ring slot ------------------
+    int ig = -1, ij = 0, iJ = 0, islot = 0;
+    const uint8_t *pc = nullptr, *ps = nullptr;
+    auto iseek = [&]() {
+        while (ij >= iJ) {
+            if (++ig >= P.n) return;
+            const VlOp &o = P.op[ig];
+            const int64_t Gop = min(G, o.n_units);
+            ij = 0;
+            iJ = 0;
+            if (b >= Gop) continue;
+            const int64_t st = b * o.n_units / Gop, en = (b + 1) * o.n_units / Gop;
+            const int64_t span = en - st;
+            iJ = span > warp ? (int)((span - warp + NW - 1) / NW) : 0;
+            pc = o.codes + (st + warp) * kUnitCodeBytes + lane * 16;
+            ps = o.scales + (st + warp) * kUnitScaleBytes + lane * 16;
         }
     };
-
-    float acc[kTiles][NT][4];
+    auto issue_one = [&]() {
+        if (ig < P.n) {
+            uint8_t *slot = ring + islot * kUnitBytes;
 #pragma unroll
-    for (int r = 0; r < kTiles; ++r)
+            for (int r = 0; r < kTiles; ++r) cp_async16(slot + r * 512 + lane * 16, pc + r * 512);
+            if (lane < kUnitScaleBytes / 16) cp_async16(slot + kUnitCodeBytes + lane * 16, ps);
+            pc += NW * kUnitCodeBytes;
+            ps += NW * kUnitScaleBytes;
+            ++ij;
+            islot = (islot + 1 == D) ? 0 : islot + 1;
+            iseek();
+        }
+        cp_async_commit();
+    };
+    iseek();
+    // Weights never depend on earlier kernels or ops: start streaming before any wait.
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) acc[r][nt][q] = 0.f;
+    for (int s = 0; s < D - 1; ++s) issue_one();
 
-    uint4 xr[NT][2];
-    if (J > 0) load_x(0, xr);
+    int cslot = 0;
+    for (int gi = 0; gi < P.n; ++gi) {
+        const VlOp &o = P.op[gi];
+        if (gi == 0) {
+            griddep_wait();
+            griddep_launch_dependents();
+        } else {
+            cooperative_groups::this_grid().sync();
+        }
+        const int64_t Gop = min(G, o.n_units);
+        if (b >= Gop) continue;
+        const int64_t n_kc = o.n_kc, n_units = o.n_units, in_f = o.in_f, out_f = o.out_f;
+        const int64_t start = b * n_units / Gop, end = (b + 1) * n_units / Gop;
+        const int64_t span = end - start;
+        const int J = span > warp ? (int)((span - warp + NW - 1) / NW) : 0;
+        const __nv_bfloat16 *X = o.X;
 
-    int j = 0;
-    const int64_t rb_first = start / n_kc, rb_last = (end - 1) / n_kc;
-    for (int64_t rb = rb_first; rb <= rb_last; ++rb) {
-        const int64_t seg_lo = max(start, rb * n_kc), seg_hi = min(end, (rb + 1) * n_kc);
-        while (j < J && start + warp + (int64_t)NW * j < seg_hi) {
-            if (j + D - 1 < J) issue(j + D - 1);
-            cp_async_commit();
-            cp_async_wait<D - 1>();
-            __syncwarp();
-            uint4 xc[NT][2];
+        auto load_x = [&](int64_t kc, uint4 (&xr)[NT][2]) {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                xc[nt][0] = xr[nt][0];
-                xc[nt][1] = xr[nt][1];
-            }
-            if (j + 1 < J) load_x(j + 1, xr);
-            const uint8_t *slot = ring + (j % D) * kUnitBytes;
-#pragma unroll
-            for (int r = 0; r < kTiles; ++r) {
-                const uint4 cw = *reinterpret_cast<const uint4 *>(slot + r * 512 + lane * 16);
-                const uint2 sc =
-                    *reinterpret_cast<const uint2 *>(slot + kUnitCodeBytes + r * 64 + g * 8);
-                const float2 s_lo = __half22float2(*reinterpret_cast<const __half2 *>(&sc.x));
-                const float2 s_hi = __half22float2(*reinterpret_cast<const __half2 *>(&sc.y));
+                const int col = nt * 8 + g4;
 #pragma unroll
                 for (int blk = 0; blk < 2; ++blk) {
-                    uint32_t a0[4], a1[4];
-                    dequant_word(blk ? cw.z : cw.x, a0);
-                    dequant_word(blk ? cw.w : cw.y, a1);
-                    const float sg = blk ? s_lo.y : s_lo.x, sh = blk ? s_hi.y : s_hi.x;
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        float d[4] = {0.f, 0.f, 0.f, 0.f};
-                        mma_bf16_16816(d, a0, xc[nt][blk].x, xc[nt][blk].y);
-                        mma_bf16_16816(d, a1, xc[nt][blk].z, xc[nt][blk].w);
-                        acc[r][nt][0] = fmaf(sg, d[0], acc[r][nt][0]);
-                        acc[r][nt][1] = fmaf(sg, d[1], acc[r][nt][1]);
-                        acc[r][nt][2] = fmaf(sh, d[2], acc[r][nt][2]);
-                        acc[r][nt][3] = fmaf(sh, d[3], acc[r][nt][3]);
-                    }
+                    const int64_t i0 = kc * kChunk + blk * 32 + t4 * 8;
+                    if (col < C && i0 < in_f)
+                        xr[nt][blk] = ldg_nc_v4(X + (int64_t)col * in_f + i0);
+                    else
+                        xr[nt][blk] = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
-            __syncwarp();  // every lane is done with this slot before it is refilled
-            ++j;
-        }
+        };
 
-        // Row block rb is finished by this CTA: combine the warps' partials.
-        {
-            float4 *dst = reinterpret_cast<float4 *>(red + warp * kPartial + lane * kAcc);
+        float acc[kTiles][NT][4];
 #pragma unroll
-            for (int r = 0; r < kTiles; ++r)
+        for (int r = 0; r < kTiles; ++r)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[r][nt][q] = 0.f;
+
+        int64_t u = start + warp;
+        int64_t kc = u % n_kc;
+        uint4 xr[NT][2];
+        if (J > 0) load_x(kc, xr);
+        int j = 0;
+        const int64_t rb_first = start / n_kc, rb_last = (end - 1) / n_kc;
+        for (int64_t rb = rb_first; rb <= rb_last; ++rb) {
+            const int64_t seg_lo = max(start, rb * n_kc), seg_hi = min(end, (rb + 1) * n_kc);
+            while (j < J && u < seg_hi) {
+                issue_one();
+                cp_async_wait<D - 1>();
+                __syncwarp();
+                uint4 xc[NT][2];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    dst[r * NT + nt] = make_float4(acc[r][nt][0], acc[r][nt][1], acc[r][nt][2],
-                                                   acc[r][nt][3]);
-                    acc[r][nt][0] = acc[r][nt][1] = acc[r][nt][2] = acc[r][nt][3] = 0.f;
+                    xc[nt][0] = xr[nt][0];
+                    xc[nt][1] = xr[nt][1];
                 }
-        }
-        __syncthreads();
-        const bool full = (seg_lo == rb * n_kc) && (seg_hi == (rb + 1) * n_kc);
-        const int slot_id = (rb == rb_first) ? 0 : 1;
-        float vals[kPartial / (NW * 32)];
+                int64_t kn = kc + NW;
+                while (kn >= n_kc) kn -= n_kc;
+                if (j + 1 < J) load_x(kn, xr);
+                const uint8_t *slot = ring + cslot * kUnitBytes;
 #pragma unroll
-        for (int m = 0; m < kPartial / (NW * 32); ++m) {
-            const int e = threadIdx.x + m * NW * 32;
-            float v = 0.f;
+                for (int r = 0; r < kTiles; ++r) {
+                    const uint4 cw = *reinterpret_cast<const uint4 *>(slot + r * 512 + lane * 16);
+                    const uint2 sc =
+                        *reinterpret_cast<const uint2 *>(slot + kUnitCodeBytes + r * 64 + g4 * 8);
+                    const float2 s_lo = __half22float2(*reinterpret_cast<const __half2 *>(&sc.x));
+                    const float2 s_hi = __half22float2(*reinterpret_cast<const __half2 *>(&sc.y));
 #pragma unroll
-            for (int w = 0; w < NW; ++w) v += red[w * kPartial + e];
-            vals[m] = v;
-        }
-        auto out_coords = [&](int e, int64_t *row, int *col) {
-            const int lsrc = e / kAcc, idx = e % kAcc, q = idx & 3, rn = idx >> 2;
-            const int r = rn / NT, nt = rn % NT;
-            *row = rb * kRowsPerBlock + 16 * r + (lsrc >> 2) + ((q >> 1) ? 8 : 0);
-            *col = nt * 8 + (lsrc & 3) * 2 + (q & 1);
-        };
-        if (full) {
+                    for (int blk = 0; blk < 2; ++blk) {
+                        uint32_t a0[4], a1[4];
+                        dequant_word<MULHI>(blk ? cw.z : cw.x, a0, P.m4, P.m8, P.m12);
+                        dequant_word<MULHI>(blk ? cw.w : cw.y, a1, P.m4, P.m8, P.m12);
+                        const float sg = blk ? s_lo.y : s_lo.x, sh = blk ? s_hi.y : s_hi.x;
 #pragma unroll
-            for (int m = 0; m < kPartial / (NW * 32); ++m) {
-                const int e = threadIdx.x + m * NW * 32;
-                int64_t row;
-                int col;
-                out_coords(e, &row, &col);
-                if (row < out_f && col < C) Y[(int64_t)col * out_f + row] = vals[m];
-            }
-            __syncthreads();  // red is free again
-        } else {
-            // Stream-K fix-up: publish this CTA's partial, take a ticket; the last CTA of the
-            // row block sums every partial in CTA order and resets the ticket.
-            float *mine = ws_part + (b * 2 + slot_id) * (int64_t)kPartial;
-#pragma unroll
-            for (int m = 0; m < kPartial / (NW * 32); ++m) mine[threadIdx.x + m * NW * 32] = vals[m];
-            __threadfence();
-            __shared__ int s_last;
-            __syncthreads();
-            const int64_t b_first = owner_cta(rb * n_kc, G, n_units);
-            const int64_t b_last = owner_cta((rb + 1) * n_kc - 1, G, n_units);
-            if (threadIdx.x == 0) {
-                const unsigned nseg = (unsigned)(b_last - b_first + 1);
-                const unsigned old = atomicAdd(ws_cnt + rb, 1u);
-                s_last = (old == nseg - 1) ? 1 : 0;
-            }
-            __syncthreads();
-            if (s_last) {
-                __threadfence();
-#pragma unroll
-                for (int m = 0; m < kPartial / (NW * 32); ++m) {
-                    const int e = threadIdx.x + m * NW * 32;
-                    float v = 0.f;
-                    for (int64_t bb = b_first; bb <= b_last; ++bb) {
-                        const int64_t bb_first_rb = (bb * n_units / G) / n_kc;
-                        const int sid = (rb == bb_first_rb) ? 0 : 1;
-                        v += __ldcg(ws_part + (bb * 2 + sid) * (int64_t)kPartial + e);
+                        for (int nt = 0; nt < NT; ++nt) {
+                            float d[4] = {0.f, 0.f, 0.f, 0.f};
+                            mma_bf16_16816(d, a0, xc[nt][blk].x, xc[nt][blk].y);
+                            mma_bf16_16816(d, a1, xc[nt][blk].z, xc[nt][blk].w);
+                            acc[r][nt][0] = fmaf(sg, d[0], acc[r][nt][0]);
+                            acc[r][nt][1] = fmaf(sg, d[1], acc[r][nt][1]);
+                            acc[r][nt][2] = fmaf(sh, d[2], acc[r][nt][2]);
+                            acc[r][nt][3] = fmaf(sh, d[3], acc[r][nt][3]);
+                        }
                     }
+                }
+                __syncwarp();  // every lane is done with this slot before it is refilled
+                cslot = (cslot + 1 == D) ? 0 : cslot + 1;
+                ++j;
+                u += NW;
+                kc = kn;
+            }
+
+            // Row block rb is finished by this CTA: combine the warps' partials.
+            {
+                float4 *dst = reinterpret_cast<float4 *>(red + warp * kPartial + lane * kAcc);
+#pragma unroll
+                for (int r = 0; r < kTiles; ++r)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        dst[r * NT + nt] = make_float4(acc[r][nt][0], acc[r][nt][1],
+                                                       acc[r][nt][2], acc[r][nt][3]);
+                        acc[r][nt][0] = acc[r][nt][1] = acc[r][nt][2] = acc[r][nt][3] = 0.f;
+                    }
+            }
+            __syncthreads();
+            const bool full = (seg_lo == rb * n_kc) && (seg_hi == (rb + 1) * n_kc);
+            const int slot_id = (rb == rb_first) ? 0 : 1;
+            float vals[kPer];
+#pragma unroll
+            for (int m = 0; m < kPer; ++m) {
+                const int e = threadIdx.x + m * NW * 32;
+                float v = 0.f;
+#pragma unroll
+                for (int w = 0; w < NW; ++w) v += red[w * kPartial + e];
+                vals[m] = v;
+            }
+            auto out_coords = [&](int e, int64_t *row, int *col) {
+                const int lsrc = e / kAcc, idx = e % kAcc, q = idx & 3, rn = idx >> 2;
+                const int r = rn / NT, nt = rn % NT;
+                *row = rb * kRowsPerBlock + 16 * r + (lsrc >> 2) + ((q >> 1) ? 8 : 0);
+                *col = nt * 8 + (lsrc & 3) * 2 + (q & 1);
+            };
+            if (full) {
+#pragma unroll
+                for (int m = 0; m < kPer; ++m) {
                     int64_t row;
                     int col;
-                    out_coords(e, &row, &col);
-                    if (row < out_f && col < C) Y[(int64_t)col * out_f + row] = v;
+                    out_coords(threadIdx.x + m * NW * 32, &row, &col);
+                    if (row < out_f && col < C) o.Y[(int64_t)col * out_f + row] = vals[m];
                 }
-                if (threadIdx.x == 0) ws_cnt[rb] = 0u;
+                __syncthreads();  // red is free again
+            } else {
+                // Stream-K fix-up: publish this CTA's partial, take a ticket; the last CTA of
+                // the row block sums every partial in CTA order and resets the ticket.
+                float *mine = ws_part + (b * 2 + slot_id) * (int64_t)kPartialSlotFloats;
+#pragma unroll
+                for (int m = 0; m < kPer; ++m) mine[threadIdx.x + m * NW * 32] = vals[m];
+                __threadfence();
+                __syncthreads();
+                const int64_t b_first = owner_cta(rb * n_kc, Gop, n_units);
+                const int64_t b_last = owner_cta((rb + 1) * n_kc - 1, Gop, n_units);
+                if (threadIdx.x == 0) {
+                    const unsigned nseg = (unsigned)(b_last - b_first + 1);
+                    const unsigned old = atomicAdd(ws_cnt + rb, 1u);
+                    s_last = (old == nseg - 1) ? 1 : 0;
+                }
+                __syncthreads();
+                if (s_last) {
+                    __threadfence();
+#pragma unroll
+                    for (int m = 0; m < kPer; ++m) {
+                        const int e = threadIdx.x + m * NW * 32;
+                        float v = 0.f;
+                        for (int64_t bb = b_first; bb <= b_last; ++bb) {
+                            const int64_t bb_first_rb = (bb * n_units / Gop) / n_kc;
+                            const int sid = (rb == bb_first_rb) ? 0 : 1;
+                            v += __ldcg(ws_part + (bb * 2 + sid) * (int64_t)kPartialSlotFloats + e);
+                        }
+                        int64_t row;
+                        int col;
+                        out_coords(e, &row, &col);
+                        if (row < out_f && col < C) o.Y[(int64_t)col * out_f + row] = v;
+                    }
+                    if (threadIdx.x == 0) ws_cnt[rb] = 0u;
+                }
+                __syncthreads();  // s_last and red are free again
             }
         }
     }
@@ -438,54 +514,117 @@ vl_simt_kernel(const uint8_t *__restrict__ codes, const uint16_t *__restrict__ s
 }
 
 // ---- host side ---------------------------------------------------------------------------
-constexpr int kNW = 8;   // consumer warps per CTA
-constexpr int kD1 = 5;   // ring depth, C <= 8
-constexpr int kD2 = 4;   // ring depth, C <= 16 / 32
+#ifndef SVD_NW
+#define SVD_NW 8
+#endif
+#ifndef SVD_D1
+#define SVD_D1 5
+#endif
+#ifndef SVD_MINB1
+#define SVD_MINB1 2
+#endif
+#ifndef SVD_MULHI
+#define SVD_MULHI true
+#endif
+constexpr int kNW = SVD_NW;        // warps per CTA
+constexpr int kD1 = SVD_D1;        // ring depth, C <= 8
+constexpr int kD2 = 4;             // ring depth, C <= 16 / 32
+constexpr int kMinB1 = SVD_MINB1;  // CTAs per SM the C <= 8 kernel is compiled for
+constexpr bool kMulHi = SVD_MULHI;
+constexpr int kMaxCtasPerSm = 4;   // the workspace holds partial slots for this many
+constexpr int kChainMax = 256;     // ops per chain launch (kernel parameters, ~16 KB)
 
 static int ntiles_for(int C) { return C <= 8 ? 1 : (C <= 16 ? 2 : 4); }
 
-static int ctas_for(int C) { return ntiles_for(C) == 1 ? 1 : 1; }
-
-static size_t part_floats(int C) { return (size_t)32 * kTiles * ntiles_for(C) * 4; }
-
-static int64_t grid_for(const NativeGeom &ng, int C) {
-    int64_t G = (int64_t)sm_count() * ctas_for(C);
-    if (G > ng.n_units) G = ng.n_units;
-    if (G < 1) G = 1;
-    return G;
+// Workspace: [partial slots: SMs x kMaxCtasPerSm CTAs x 2 x kPartialSlotFloats][tickets].  The
+// partial region has the same size and place for every matrix and C, so calls of any shape
+// can share one zero-filled workspace; the tickets after it are per 64-row block.
+static size_t partial_region_bytes() {
+    return align_up((size_t)sm_count() * kMaxCtasPerSm * 2 * kPartialSlotFloats * sizeof(float),
+                    256);
 }
 
 size_t vl_workspace_bytes(int64_t in_f, int64_t out_f, int C) {
+    (void)C;
     const NativeGeom ng = native_geom(in_f, out_f);
-    const int64_t G = grid_for(ng, C);
-    return align_up((size_t)G * 2 * part_floats(C) * sizeof(float), 256) +
-           align_up((size_t)ng.n_rb * sizeof(unsigned), 256);
+    return partial_region_bytes() + align_up((size_t)ng.n_rb * sizeof(unsigned), 256);
 }
 
-template <int NT, int D>
-static cudaError_t launch_mma(const svd_qweight *W, const void *X, int C, float *Y, void *ws,
-                              bool pdl, cudaStream_t stream) {
+template <int NT, int D, int MAXOPS>
+static cudaError_t launch_mma(const VlOps<MAXOPS> &P, void *ws, bool pdl, bool coop,
+                              int64_t max_units, cudaStream_t stream) {
     using Cfg = MmaCfg<NT, kNW, D>;
-    auto kern = vl_mma_kernel<NT, kNW, D>;
-    static bool attr_set[64] = {false};
+    auto kern = vl_mma_kernel<NT, kNW, D, MAXOPS, (NT == 1 ? kMinB1 : 1), kMulHi>;
+    static int per_sm_cache[64] = {0};
     int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)Cfg::kSmem);
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    int per_sm = (dev >= 0 && dev < 64) ? per_sm_cache[dev] : 0;
+    if (per_sm == 0) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kNW * 32, Cfg::kSmem);
+        if (e != cudaSuccess) return e;
+        per_sm = per_sm < 1 ? 1 : (per_sm > kMaxCtasPerSm ? kMaxCtasPerSm : per_sm);
+        if (dev >= 0 && dev < 64) per_sm_cache[dev] = per_sm;
     }
-    const NativeGeom ng = native_geom(W->in_features, W->out_features);
-    const int64_t G = grid_for(ng, C);
+    int64_t G = (int64_t)sm_count() * per_sm;
+    if (!coop && G > max_units) G = max_units;  // a lone op never needs idle CTAs
+    if (G < 1) G = 1;
     float *part = reinterpret_cast<float *>(ws);
-    unsigned *cnt = reinterpret_cast<unsigned *>(
-        reinterpret_cast<uint8_t *>(ws) + align_up((size_t)G * 2 * part_floats(C) * sizeof(float), 256));
-    return launch(kern, dim3((unsigned)G), dim3(kNW * 32), Cfg::kSmem, stream, pdl,
-                  reinterpret_cast<const uint8_t *>(W->codes),
-                  reinterpret_cast<const uint8_t *>(W->scales),
-                  reinterpret_cast<const __nv_bfloat16 *>(X), Y, W->in_features,
-                  W->out_features, C, ng.n_kc, ng.n_units, part, cnt);
+    unsigned *cnt = reinterpret_cast<unsigned *>(reinterpret_cast<uint8_t *>(ws) +
+                                                 partial_region_bytes());
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)G);
+    cfg.blockDim = dim3(kNW * 32);
+    cfg.dynamicSmemBytes = Cfg::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (coop) {
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    } else if (pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kern, P, part, cnt);
+}
+
+template <int MAXOPS>
+static void set_shift_multipliers(VlOps<MAXOPS> &P) {
+    P.m4 = 1u << 28;
+    P.m8 = 1u << 24;
+    P.m12 = 1u << 20;
+}
+
+static VlOp make_op(const svd_qweight *W, const void *X, float *Y) {
+    const NativeGeom ng = native_geom(W->in_features, W->out_features);
+    VlOp o;
+    o.codes = reinterpret_cast<const uint8_t *>(W->codes);
+    o.scales = reinterpret_cast<const uint8_t *>(W->scales);
+    o.X = reinterpret_cast<const __nv_bfloat16 *>(X);
+    o.Y = Y;
+    o.in_f = W->in_features;
+    o.out_f = W->out_features;
+    o.n_kc = ng.n_kc;
+    o.n_units = ng.n_units;
+    return o;
+}
+
+template <int MAXOPS>
+static cudaError_t launch_ops(const VlOps<MAXOPS> &P, void *ws, bool pdl, cudaStream_t stream) {
+    int64_t max_units = 0;
+    for (int i = 0; i < P.n; ++i) max_units = P.op[i].n_units > max_units ? P.op[i].n_units : max_units;
+    const bool coop = P.n > 1;
+    switch (ntiles_for(P.C)) {
+        case 1: return launch_mma<1, kD1, MAXOPS>(P, ws, pdl, coop, max_units, stream);
+        case 2: return launch_mma<2, kD2, MAXOPS>(P, ws, pdl, coop, max_units, stream);
+        default: return launch_mma<4, kD2, MAXOPS>(P, ws, pdl, coop, max_units, stream);
+    }
 }
 
 template <int CC>
@@ -531,13 +670,12 @@ int verify_linear(const svd_qweight *W, const void *X, int C, float *Y, void *ws
     if (W->layout == SVD_LAYOUT_NATIVE) {
         if (!ws || ws_bytes < vl_workspace_bytes(W->in_features, W->out_features, C))
             return SVD_ERR_WORKSPACE;
-        cudaError_t e;
-        switch (ntiles_for(C)) {
-            case 1: e = launch_mma<1, kD1>(W, X, C, Y, ws, pdl, stream); break;
-            case 2: e = launch_mma<2, kD2>(W, X, C, Y, ws, pdl, stream); break;
-            default: e = launch_mma<4, kD2>(W, X, C, Y, ws, pdl, stream); break;
-        }
-        SVD_CUDA_TRY(e);
+        VlOps<1> P;
+        P.n = 1;
+        P.C = C;
+        set_shift_multipliers(P);
+        P.op[0] = make_op(W, X, Y);
+        SVD_CUDA_TRY(launch_ops(P, ws, pdl, stream));
         return SVD_OK;
     }
     // canonical layout: CUDA-core kernel
@@ -555,6 +693,51 @@ int verify_linear(const svd_qweight *W, const void *X, int C, float *Y, void *ws
         default: return SVD_ERR_UNSUPPORTED;
     }
     SVD_CUDA_TRY(e);
+    return SVD_OK;
+}
+
+size_t chain_workspace_bytes(const svd_linear_op *ops, int n_ops, int C) {
+    int64_t n_rb = 1;
+    for (int i = 0; i < n_ops; ++i) {
+        const NativeGeom ng = native_geom(ops[i].W.in_features, ops[i].W.out_features);
+        n_rb = ng.n_rb > n_rb ? ng.n_rb : n_rb;
+    }
+    (void)C;
+    return partial_region_bytes() + align_up((size_t)n_rb * sizeof(unsigned), 256);
+}
+
+int verify_chain(const svd_linear_op *ops, int n_ops, int C, void *ws, size_t ws_bytes, int flags,
+                 cudaStream_t stream) {
+    if (!ops || n_ops < 1 || C < 1 || C > SVD_C_MAX) return SVD_ERR_INVALID_ARG;
+    if (flags & ~SVD_F_PDL) return SVD_ERR_INVALID_ARG;
+    for (int i = 0; i < n_ops; ++i) {
+        const int rc = check_qweight(&ops[i].W);
+        if (rc != SVD_OK) return rc;
+        if (ops[i].W.layout != SVD_LAYOUT_NATIVE) return SVD_ERR_INVALID_ARG;
+        if (!ops[i].X || !ops[i].Y || !aligned16(ops[i].X)) return SVD_ERR_INVALID_ARG;
+    }
+    if (sm_count() < 1) return SVD_ERR_CUDA;
+    if (!ws || ws_bytes < chain_workspace_bytes(ops, n_ops, C)) return SVD_ERR_WORKSPACE;
+    // host staging of the kernel parameters (copied into the launch)
+    std::unique_ptr<VlOps<kChainMax>> Pp(new VlOps<kChainMax>);
+    VlOps<kChainMax> &P = *Pp;
+    for (int first = 0; first < n_ops; first += kChainMax) {
+        const int n = (n_ops - first) < kChainMax ? (n_ops - first) : kChainMax;
+        if (n == 1) {
+            VlOps<1> P1;
+            P1.n = 1;
+            P1.C = C;
+            set_shift_multipliers(P1);
+            P1.op[0] = make_op(&ops[first].W, ops[first].X, ops[first].Y);
+            SVD_CUDA_TRY(launch_ops(P1, ws, first == 0 && (flags & SVD_F_PDL), stream));
+            continue;
+        }
+        P.n = n;
+        P.C = C;
+        set_shift_multipliers(P);
+        for (int i = 0; i < n; ++i) P.op[i] = make_op(&ops[first + i].W, ops[first + i].X, ops[first + i].Y);
+        SVD_CUDA_TRY(launch_ops(P, ws, false, stream));
+    }
     return SVD_OK;
 }
 

@@ -1,12 +1,11 @@
 """The verify pass of a 27B-shaped dense 4-bit model on one GPU, assembled from libsvd calls.
 
-A pass is 64 layers x 4 fused verify-linear launches (q|k|v, o, gate|up, down; every matrix read
-from HBM once and applied to the C = K+1 window columns), then the lm_head over all C positions
+A pass is 64 layers x 4 fused verify-linear products (q|k|v, o, gate|up, down; every matrix read
+from HBM once and applied to the C = K+1 window columns), run as one persistent chain launch, then the lm_head over all C positions
 with the production sampler, then the acceptance of the K drafts -- "100 tokens per second ..."
 (section "How speculative decoding gets past a per-token wall") and the HN thread's account of
-running every window position through each layer with one weight read.  The 256 linear launches
-carry programmatic dependent launch and are recorded once into a CUDA graph; a second graph
-holds lm_head, sampler and acceptance.
+running every window position through each layer with one weight read.  The stack is recorded
+once into a CUDA graph; a second graph holds lm_head, sampler and acceptance.
 
 The activations of every linear are independent synthetic N(0, 1) draws (there is no real model:
 attention, norms and activations between the GEMMs are out of scope), so each launch reads its
@@ -43,9 +42,10 @@ class Linear:
 class VerifyPass:
     def __init__(self, layers: int = synth.LAYERS, C: int = 4, seed: int = 0, device="cuda",
                  head: bool = True, accept: bool = True, sampler: svd.Sampler | None = None,
-                 pdl: bool = True, keep_canonical: bool = False, gemms=synth.LAYER_GEMMS):
+                 pdl: bool = True, keep_canonical: bool = False, gemms=synth.LAYER_GEMMS,
+                 chain: bool = True):
         self.device = torch.device(device)
-        self.C, self.layers, self.pdl = C, layers, pdl
+        self.C, self.layers, self.pdl, self.chain = C, layers, pdl, chain
         self.gemms = tuple(gemms)
         self.sampler = sampler or svd.Sampler(0.6, 0.95, 0.05)
         self.linears = []
@@ -53,7 +53,9 @@ class VerifyPass:
             for g, (i, o) in enumerate(self.gemms):
                 self.linears.append(Linear(i, o, C, seed * 100003 + 1000 * l + g, self.device,
                                            keep_canonical))
-        ws = max(svd.svd_verify_linear_workspace_bytes(i, o, C) for i, o in self.gemms)
+        self.ops = [(lin.W, lin.X, lin.Y) for lin in self.linears]
+        ws = max(max(svd.svd_verify_linear_workspace_bytes(i, o, C) for i, o in self.gemms),
+                 svd.svd_verify_chain_workspace_bytes(self.ops, C))
         self.ws = torch.zeros(ws, dtype=torch.uint8, device=self.device)
         self.head = head
         self.k = C - 1
@@ -94,6 +96,11 @@ class VerifyPass:
 
     # -- enqueueing -------------------------------------------------------------------------
     def enqueue_stack(self, stream=None):
+        """The layer stack: one persistent cooperative chain launch (default), or one launch per
+        matrix with programmatic dependent launch."""
+        if self.chain:
+            svd.svd_verify_chain(self.ops, self.C, self.ws, stream=stream)
+            return
         flags = svd.SVD_F_PDL if self.pdl else 0
         for lin in self.linears:
             svd.svd_verify_linear(lin.W, lin.X, self.C, lin.Y, self.ws, flags=flags, stream=stream)

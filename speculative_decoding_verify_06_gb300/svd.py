@@ -36,6 +36,7 @@ SVD_K_MAX = 32
 EXPORTS = (
     "svd_error_string", "svd_last_cuda_error", "svd_native_sizes", "svd_repack_weights",
     "svd_unpack_weights", "svd_verify_linear_workspace_bytes", "svd_verify_linear",
+    "svd_verify_chain_workspace_bytes", "svd_verify_chain",
     "svd_sampler_workspace_bytes", "svd_sampler_probs", "svd_lm_head_workspace_bytes",
     "svd_lm_head_softmax", "svd_accept", "svd_graph_begin", "svd_graph_end", "svd_graph_launch",
     "svd_graph_destroy", "svd_device_sm_count",
@@ -74,6 +75,10 @@ class QWeight:
                         self.layout, 0)
 
 
+class _LinearOp(ctypes.Structure):
+    _fields_ = [("W", _QWeight), ("X", ctypes.c_void_p), ("Y", ctypes.c_void_p)]
+
+
 class Sampler:
     def __init__(self, temperature=0.6, top_p=0.95, min_p=0.05, greedy=False):
         self.temperature, self.top_p, self.min_p, self.greedy = temperature, top_p, min_p, greedy
@@ -107,6 +112,8 @@ def load(path: str = LIB_PATH):
             "svd_unpack_weights": (i32, [P, P, P, P]),
             "svd_verify_linear_workspace_bytes": (sz, [i64, i64, i32]),
             "svd_verify_linear": (i32, [P, P, i32, P, P, sz, i32, P]),
+            "svd_verify_chain_workspace_bytes": (sz, [P, i32, i32]),
+            "svd_verify_chain": (i32, [P, i32, i32, P, sz, i32, P]),
             "svd_sampler_workspace_bytes": (sz, [i32, i64]),
             "svd_sampler_probs": (i32, [P, i32, i64, P, P, P, P, sz, P]),
             "svd_lm_head_workspace_bytes": (sz, [i64, i64, i32]),
@@ -190,6 +197,30 @@ def svd_verify_linear(W: QWeight, X, C: int, Y, workspace=None, workspace_bytes:
     _check("svd_verify_linear", load().svd_verify_linear(
         ctypes.byref(w), _ptr(X), int(C), _ptr(Y), _ptr(workspace), int(workspace_bytes),
         int(flags), _stream(stream)))
+
+
+def _ops_array(ops):
+    """ops: sequence of (QWeight, X, Y) -> ctypes array of svd_linear_op."""
+    arr = (_LinearOp * len(ops))()
+    for i, (W, X, Y) in enumerate(ops):
+        arr[i].W = W._c()
+        arr[i].X = _ptr(X)
+        arr[i].Y = _ptr(Y)
+    return arr
+
+
+def svd_verify_chain_workspace_bytes(ops, C: int) -> int:
+    arr = _ops_array(ops)
+    return int(load().svd_verify_chain_workspace_bytes(arr, len(ops), int(C)))
+
+
+def svd_verify_chain(ops, C: int, workspace, workspace_bytes: int = 0, flags: int = 0,
+                     stream=None):
+    arr = _ops_array(ops)
+    if not workspace_bytes:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check("svd_verify_chain", load().svd_verify_chain(
+        arr, len(ops), int(C), _ptr(workspace), int(workspace_bytes), int(flags), _stream(stream)))
 
 
 def svd_sampler_workspace_bytes(rows: int, V: int) -> int:

@@ -47,14 +47,14 @@ def test_graph_replay_equals_eager_and_oracle():
         assert int(vp.n_emitted.item()) == ne_r[0] and int(vp.status.item()) == st_r[0]
 
 
-def test_pdl_and_plain_launches_agree():
+def test_chain_pdl_and_plain_launches_agree():
     lib()
-    a = stack.VerifyPass(layers=1, C=4, seed=5, head=False, pdl=True)
-    b = stack.VerifyPass(layers=1, C=4, seed=5, head=False, pdl=False)
-    a.capture()
-    b.capture()
-    a.launch()
-    b.launch()
+    a = stack.VerifyPass(layers=2, C=4, seed=5, head=False, chain=True)
+    b = stack.VerifyPass(layers=2, C=4, seed=5, head=False, chain=False, pdl=True)
+    c = stack.VerifyPass(layers=2, C=4, seed=5, head=False, chain=False, pdl=False)
+    for v in (a, b, c):
+        v.capture()
+        v.launch()
     torch.cuda.synchronize()
-    for x, y in zip(a.linears, b.linears):
-        assert torch.equal(x.Y, y.Y)
+    for x, y, z in zip(a.linears, b.linears, c.linears):
+        assert torch.equal(x.Y, y.Y) and torch.equal(x.Y, z.Y)
