@@ -24,6 +24,7 @@
 #include <cooperative_groups.h>
 
 #include <memory>
+#include <mutex>
 
 #include "svd_common.cuh"
 
@@ -149,6 +150,39 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Bulk (TMA-engine) copies into shared memory completing on an mbarrier.
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(mbar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t mbar) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(mbar)
+        : "memory");
+}
+// Waits for phase `parity` of an mbarrier; gives up after a bounded number of polls (each poll
+// may suspend the thread briefly), so a broken pipeline cannot hang the GPU.
+__device__ __forceinline__ void mbar_wait(uint32_t mbar, uint32_t parity) {
+    for (int it = 0; it < (1 << 22); ++it) {
+        uint32_t ok;
+        asm volatile(
+            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; "
+            "selp.u32 %0, 1, 0, p; }"
+            : "=r"(ok)
+            : "r"(mbar), "r"(parity)
+            : "memory");
+        if (ok) return;
+    }
+}
+
 // Four bf16x2 A registers from one native word: (bits >> 4p) & 0x000F000F | 0x43004300 is the
 // pair (128 + c_lo, 128 + c_hi) exactly; subtracting (136, 136) leaves (c - 8) exactly.  With
 // MULHI the three right shifts are taken as mul.hi by 2^28, 2^24, 2^20 held in registers (the
@@ -214,12 +248,13 @@ __device__ __forceinline__ int64_t owner_cta(int64_t n, int64_t Gop, int64_t n_u
 // ---- the tensor-core stream-K kernel ---------------------------------------------------
 constexpr int kPartialSlotFloats = 32 * kTiles * 4 * 4;  // largest warp partial (4 n-tiles)
 
-template <int NT, int NW, int D>
+template <int NT, int NW, int D, bool ASYNC>
 struct MmaCfg {
     static constexpr int kAcc = kTiles * NT * 4;              // fp32 accumulators per lane
     static constexpr int kPartial = 32 * kAcc;                // floats per warp partial
     static constexpr size_t kRing = (size_t)NW * D * kUnitBytes;
-    static constexpr size_t kSmem = kRing + (size_t)NW * kPartial * sizeof(float);
+    static constexpr size_t kSmem =
+        kRing + (size_t)(ASYNC ? 2 : 1) * NW * kPartial * sizeof(float);
 };
 
 // Runs every op of P in order on a persistent grid.  Each warp keeps a ring of D unit slots
@@ -227,22 +262,38 @@ struct MmaCfg {
 // so the weights of op g+1 stream in while op g finishes.  Activations of op g+1 are read
 // only after the grid barrier that ends op g (a chain of more than one op is launched
 // cooperatively), or, for op 0, after griddepcontrol.wait.
-template <int NT, int NW, int D, int MAXOPS, int MINB, bool MULHI>
+//
+// A row block ends asynchronously: each warp drops its partial sums into one of two shared
+// buffers and takes a shared ticket; the last warp to arrive sums the eight partials (in warp
+// order) and writes the rows or the CTA's stream-K partial, while the other warps go on
+// streaming.  A buffer is reused two row blocks later, after its reducer has released it.
+template <int NT, int NW, int D, int MAXOPS, int MINB, bool MULHI, bool ASYNC, bool BULK>
 __global__ void __launch_bounds__(NW * 32, MINB)
 vl_mma_kernel(const __grid_constant__ VlOps<MAXOPS> P, float *__restrict__ ws_part,
               unsigned int *__restrict__ ws_cnt) {
-    using Cfg = MmaCfg<NT, NW, D>;
+    using Cfg = MmaCfg<NT, NW, D, ASYNC>;
     constexpr int kAcc = Cfg::kAcc, kPartial = Cfg::kPartial;
-    constexpr int kPer = kPartial / (NW * 32);  // reduced elements per thread
+    constexpr int kPerLane = kPartial / 32;  // reduced elements per lane of the reducer warp
     extern __shared__ __align__(16) uint8_t smem[];
-    __shared__ int s_last;
-    float *red = reinterpret_cast<float *>(smem + Cfg::kRing);
+    __shared__ unsigned s_tick[2], s_free[2];
+    __shared__ __align__(8) uint64_t s_mbar[BULK ? NW * D : 1];
+    float *red = reinterpret_cast<float *>(smem + Cfg::kRing);  // [2][NW][kPartial]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g4 = lane >> 2, t4 = lane & 3;
     const int64_t G = gridDim.x, b = blockIdx.x;
     const int C = P.C;
     uint8_t *ring = smem + (size_t)warp * D * kUnitBytes;
+    if (threadIdx.x < 2) {
+        s_tick[threadIdx.x] = 0u;
+        s_free[threadIdx.x] = 0u;
+    }
+    const uint32_t mbar0 = smem_u32(&s_mbar[0]) + (BULK ? warp * D * 8 : 0);
+    if (BULK && lane == 0) {
+        for (int i = 0; i < D; ++i) mbar_init(mbar0 + 8 * i, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
 
     // ---- issue cursor: (op ig, unit ij of iJ), source pointers, ring slot ------------------
     int ig = -1, ij = 0, iJ = 0, islot = 0;
@@ -264,24 +315,48 @@ vl_mma_kernel(const __grid_constant__ VlOps<MAXOPS> P, float *__restrict__ ws_pa
     };
     auto issue_one = [&]() {
         if (ig < P.n) {
-            uint8_t *slot = ring + islot * kUnitBytes;
+            if constexpr (BULK) {
+                if (lane == 0) {
+                    const uint32_t slot = smem_u32(ring + islot * kUnitBytes);
+                    const uint32_t mb = mbar0 + 8 * islot;
+                    // the slot was last read through the generic proxy: order those reads
+                    // before the bulk copy (async proxy) overwrites it
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    mbar_expect_tx(mb, kUnitBytes);
+                    bulk_g2s(slot, pc - lane * 16, kUnitCodeBytes, mb);
+                    bulk_g2s(slot + kUnitCodeBytes, ps - lane * 16, kUnitScaleBytes, mb);
+                }
+            } else {
+                uint8_t *slot = ring + islot * kUnitBytes + lane * 16;
 #pragma unroll
-            for (int r = 0; r < kTiles; ++r) cp_async16(slot + r * 512 + lane * 16, pc + r * 512);
-            if (lane < kUnitScaleBytes / 16) cp_async16(slot + kUnitCodeBytes + lane * 16, ps);
+                for (int r = 0; r < kTiles; ++r) cp_async16(slot + r * 512, pc + r * 512);
+                if (lane < kUnitScaleBytes / 16) cp_async16(slot + kUnitCodeBytes, ps);
+            }
             pc += NW * kUnitCodeBytes;
             ps += NW * kUnitScaleBytes;
             ++ij;
             islot = (islot + 1 == D) ? 0 : islot + 1;
             iseek();
         }
-        cp_async_commit();
+        if constexpr (!BULK) cp_async_commit();
     };
     iseek();
     // Weights never depend on earlier kernels or ops: start streaming before any wait.
 #pragma unroll
     for (int s = 0; s < D - 1; ++s) issue_one();
+    __syncthreads();  // s_tick / s_free initialised
+
+    float acc[kTiles][NT][4];
+#pragma unroll
+    for (int r = 0; r < kTiles; ++r)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[r][nt][q] = 0.f;
 
     int cslot = 0;
+    uint32_t cphase = 0;  // parity of the slot's current use (bulk copies)
+    unsigned seg = 0;  // row-block segments this CTA has finished (all ops)
     for (int gi = 0; gi < P.n; ++gi) {
         const VlOp &o = P.op[gi];
         if (gi == 0) {
@@ -296,30 +371,26 @@ vl_mma_kernel(const __grid_constant__ VlOps<MAXOPS> P, float *__restrict__ ws_pa
         const int64_t start = b * n_units / Gop, end = (b + 1) * n_units / Gop;
         const int64_t span = end - start;
         const int J = span > warp ? (int)((span - warp + NW - 1) / NW) : 0;
-        const __nv_bfloat16 *X = o.X;
 
+        // this lane's activation rows (B operand: column nt*8 + g4, inputs from t4*8)
+        const __nv_bfloat16 *xrow[NT];
+        bool xok[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int col = nt * 8 + g4;
+            xok[nt] = col < C;
+            xrow[nt] = o.X + (int64_t)(xok[nt] ? col : 0) * in_f + t4 * 8;
+        }
+        const bool tail32 = (in_f & 63) != 0;  // the last chunk holds a single 32-input block
         auto load_x = [&](int64_t kc, uint4 (&xr)[NT][2]) {
+            const bool lastc = tail32 && (kc == n_kc - 1);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                const int col = nt * 8 + g4;
-#pragma unroll
-                for (int blk = 0; blk < 2; ++blk) {
-                    const int64_t i0 = kc * kChunk + blk * 32 + t4 * 8;
-                    if (col < C && i0 < in_f)
-                        xr[nt][blk] = ldg_nc_v4(X + (int64_t)col * in_f + i0);
-                    else
-                        xr[nt][blk] = make_uint4(0u, 0u, 0u, 0u);
-                }
+                const __nv_bfloat16 *src = xrow[nt] + kc * kChunk;
+                xr[nt][0] = xok[nt] ? ldg_nc_v4(src) : make_uint4(0u, 0u, 0u, 0u);
+                xr[nt][1] = (xok[nt] && !lastc) ? ldg_nc_v4(src + 32) : make_uint4(0u, 0u, 0u, 0u);
             }
         };
-
-        float acc[kTiles][NT][4];
-#pragma unroll
-        for (int r = 0; r < kTiles; ++r)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) acc[r][nt][q] = 0.f;
 
         int64_t u = start + warp;
         int64_t kc = u % n_kc;
@@ -327,12 +398,16 @@ vl_mma_kernel(const __grid_constant__ VlOps<MAXOPS> P, float *__restrict__ ws_pa
         if (J > 0) load_x(kc, xr);
         int j = 0;
         const int64_t rb_first = start / n_kc, rb_last = (end - 1) / n_kc;
-        for (int64_t rb = rb_first; rb <= rb_last; ++rb) {
+        for (int64_t rb = rb_first; rb <= rb_last; ++rb, ++seg) {
             const int64_t seg_lo = max(start, rb * n_kc), seg_hi = min(end, (rb + 1) * n_kc);
             while (j < J && u < seg_hi) {
                 issue_one();
-                cp_async_wait<D - 1>();
-                __syncwarp();
+                if constexpr (BULK) {
+                    mbar_wait(mbar0 + 8 * cslot, cphase);
+                } else {
+                    cp_async_wait<D - 1>();
+                    __syncwarp();
+                }
                 uint4 xc[NT][2];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
@@ -343,18 +418,22 @@ vl_mma_kernel(const __grid_constant__ VlOps<MAXOPS> P, float *__restrict__ ws_pa
                 while (kn >= n_kc) kn -= n_kc;
                 if (j + 1 < J) load_x(kn, xr);
                 const uint8_t *slot = ring + cslot * kUnitBytes;
+                uint4 cw[kTiles];
+                uint2 sc[kTiles];
 #pragma unroll
                 for (int r = 0; r < kTiles; ++r) {
-                    const uint4 cw = *reinterpret_cast<const uint4 *>(slot + r * 512 + lane * 16);
-                    const uint2 sc =
-                        *reinterpret_cast<const uint2 *>(slot + kUnitCodeBytes + r * 64 + g4 * 8);
-                    const float2 s_lo = __half22float2(*reinterpret_cast<const __half2 *>(&sc.x));
-                    const float2 s_hi = __half22float2(*reinterpret_cast<const __half2 *>(&sc.y));
+                    cw[r] = *reinterpret_cast<const uint4 *>(slot + r * 512 + lane * 16);
+                    sc[r] = *reinterpret_cast<const uint2 *>(slot + kUnitCodeBytes + r * 64 + g4 * 8);
+                }
+#pragma unroll
+                for (int r = 0; r < kTiles; ++r) {
+                    const float2 s_lo = __half22float2(*reinterpret_cast<const __half2 *>(&sc[r].x));
+                    const float2 s_hi = __half22float2(*reinterpret_cast<const __half2 *>(&sc[r].y));
 #pragma unroll
                     for (int blk = 0; blk < 2; ++blk) {
                         uint32_t a0[4], a1[4];
-                        dequant_word<MULHI>(blk ? cw.z : cw.x, a0, P.m4, P.m8, P.m12);
-                        dequant_word<MULHI>(blk ? cw.w : cw.y, a1, P.m4, P.m8, P.m12);
+                        dequant_word<MULHI>(blk ? cw[r].z : cw[r].x, a0, P.m4, P.m8, P.m12);
+                        dequant_word<MULHI>(blk ? cw[r].w : cw[r].y, a1, P.m4, P.m8, P.m12);
                         const float sg = blk ? s_lo.y : s_lo.x, sh = blk ? s_hi.y : s_hi.x;
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
@@ -369,15 +448,106 @@ vl_mma_kernel(const __grid_constant__ VlOps<MAXOPS> P, float *__restrict__ ws_pa
                     }
                 }
                 __syncwarp();  // every lane is done with this slot before it is refilled
-                cslot = (cslot + 1 == D) ? 0 : cslot + 1;
+                if (++cslot == D) {
+                    cslot = 0;
+                    cphase ^= 1u;
+                }
                 ++j;
                 u += NW;
                 kc = kn;
             }
 
-            // Row block rb is finished by this CTA: combine the warps' partials.
+            // ---- end of row block rb ---------------------------------------------------------
+            if constexpr (!ASYNC) {
+                // All threads of the CTA combine the warps' partials, two elements each.
+                {
+                    float4 *dst = reinterpret_cast<float4 *>(red + warp * kPartial + lane * kAcc);
+#pragma unroll
+                    for (int r = 0; r < kTiles; ++r)
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            dst[r * NT + nt] = make_float4(acc[r][nt][0], acc[r][nt][1],
+                                                           acc[r][nt][2], acc[r][nt][3]);
+                            acc[r][nt][0] = acc[r][nt][1] = acc[r][nt][2] = acc[r][nt][3] = 0.f;
+                        }
+                }
+                __syncthreads();
+                constexpr int kPer = kPartial / (NW * 32);
+                float vals[kPer];
+#pragma unroll
+                for (int m = 0; m < kPer; ++m) {
+                    const int e = threadIdx.x + m * NW * 32;
+                    float v = 0.f;
+#pragma unroll
+                    for (int w = 0; w < NW; ++w) v += red[w * kPartial + e];
+                    vals[m] = v;
+                }
+                auto coords = [&](int e, int64_t *row, int *col) {
+                    const int lsrc = e / kAcc, idx = e % kAcc, q = idx & 3, rn = idx >> 2;
+                    const int r = rn / NT, nt = rn % NT;
+                    *row = rb * kRowsPerBlock + 16 * r + (lsrc >> 2) + ((q >> 1) ? 8 : 0);
+                    *col = nt * 8 + (lsrc & 3) * 2 + (q & 1);
+                };
+                const bool full = (seg_lo == rb * n_kc) && (seg_hi == (rb + 1) * n_kc);
+                if (full) {
+#pragma unroll
+                    for (int m = 0; m < kPer; ++m) {
+                        int64_t row;
+                        int col;
+                        coords(threadIdx.x + m * NW * 32, &row, &col);
+                        if (row < out_f && col < C) o.Y[(int64_t)col * out_f + row] = vals[m];
+                    }
+                } else {
+                    // Stream-K fix-up: publish this CTA's partial, take a ticket (one thread,
+                    // release); the last CTA of the row block sums every partial in CTA order.
+                    const int slot_id = (rb == rb_first) ? 0 : 1;
+                    float *mine = ws_part + (b * 2 + slot_id) * (int64_t)kPartialSlotFloats;
+#pragma unroll
+                    for (int m = 0; m < kPer; ++m) mine[threadIdx.x + m * NW * 32] = vals[m];
+                    __threadfence();
+                    __syncthreads();
+                    const int64_t b_first = owner_cta(rb * n_kc, Gop, n_units);
+                    const int64_t b_last = owner_cta((rb + 1) * n_kc - 1, Gop, n_units);
+                    if (threadIdx.x == 0) {
+                        __threadfence();
+                        const unsigned old = atomicAdd(ws_cnt + rb, 1u);
+                        s_tick[0] = (old == (unsigned)(b_last - b_first)) ? 1u : 0u;
+                    }
+                    __syncthreads();
+                    if (s_tick[0]) {
+                        __threadfence();
+#pragma unroll
+                        for (int m = 0; m < kPer; ++m) {
+                            const int e = threadIdx.x + m * NW * 32;
+                            float v = 0.f;
+                            for (int64_t bb = b_first; bb <= b_last; ++bb) {
+                                const int64_t bb_first_rb = (bb * n_units / Gop) / n_kc;
+                                const int sid = (rb == bb_first_rb) ? 0 : 1;
+                                v += __ldcg(ws_part + (bb * 2 + sid) * (int64_t)kPartialSlotFloats + e);
+                            }
+                            int64_t row;
+                            int col;
+                            coords(e, &row, &col);
+                            if (row < out_f && col < C) o.Y[(int64_t)col * out_f + row] = v;
+                        }
+                        if (threadIdx.x == 0) ws_cnt[rb] = 0u;
+                    }
+                }
+                __syncthreads();  // red and s_tick are free again
+                continue;
+            }
+
+            // ---- asynchronous variant: the last warp of the row block reduces ----------------
+            const int buf = seg & 1;
+            if (seg >= 2) {  // the reducer of segment seg - 2 must have released the buffer
+                const unsigned need = seg >> 1;
+                for (int spin = 0; spin < (1 << 24); ++spin) {
+                    if (*reinterpret_cast<volatile unsigned *>(&s_free[buf]) >= need) break;
+                    __nanosleep(32);
+                }
+            }
             {
-                float4 *dst = reinterpret_cast<float4 *>(red + warp * kPartial + lane * kAcc);
+                float4 *dst = reinterpret_cast<float4 *>(red + (buf * NW + warp) * kPartial + lane * kAcc);
 #pragma unroll
                 for (int r = 0; r < kTiles; ++r)
 #pragma unroll
@@ -387,16 +557,25 @@ vl_mma_kernel(const __grid_constant__ VlOps<MAXOPS> P, float *__restrict__ ws_pa
                         acc[r][nt][0] = acc[r][nt][1] = acc[r][nt][2] = acc[r][nt][3] = 0.f;
                     }
             }
-            __syncthreads();
-            const bool full = (seg_lo == rb * n_kc) && (seg_hi == (rb + 1) * n_kc);
-            const int slot_id = (rb == rb_first) ? 0 : 1;
-            float vals[kPer];
+            __syncwarp();
+            unsigned ticket = 0;
+            if (lane == 0) {
+                __threadfence_block();
+                ticket = atomicAdd(&s_tick[buf], 1u);
+            }
+            ticket = __shfl_sync(0xffffffffu, ticket, 0);
+            if (ticket != NW - 1) continue;  // another warp reduces this row block
+
+            // ---- the reducer: the last warp of the CTA to finish row block rb ----------------
+            __threadfence_block();
+            const float *rbuf = red + buf * NW * kPartial;
+            float vals[kPerLane];
 #pragma unroll
-            for (int m = 0; m < kPer; ++m) {
-                const int e = threadIdx.x + m * NW * 32;
+            for (int m = 0; m < kPerLane; ++m) {
+                const int e = lane + 32 * m;
                 float v = 0.f;
 #pragma unroll
-                for (int w = 0; w < NW; ++w) v += red[w * kPartial + e];
+                for (int w = 0; w < NW; ++w) v += rbuf[w * kPartial + e];
                 vals[m] = v;
             }
             auto out_coords = [&](int e, int64_t *row, int *col) {
@@ -405,36 +584,34 @@ vl_mma_kernel(const __grid_constant__ VlOps<MAXOPS> P, float *__restrict__ ws_pa
                 *row = rb * kRowsPerBlock + 16 * r + (lsrc >> 2) + ((q >> 1) ? 8 : 0);
                 *col = nt * 8 + (lsrc & 3) * 2 + (q & 1);
             };
+            const bool full = (seg_lo == rb * n_kc) && (seg_hi == (rb + 1) * n_kc);
             if (full) {
 #pragma unroll
-                for (int m = 0; m < kPer; ++m) {
+                for (int m = 0; m < kPerLane; ++m) {
                     int64_t row;
                     int col;
-                    out_coords(threadIdx.x + m * NW * 32, &row, &col);
+                    out_coords(lane + 32 * m, &row, &col);
                     if (row < out_f && col < C) o.Y[(int64_t)col * out_f + row] = vals[m];
                 }
-                __syncthreads();  // red is free again
             } else {
                 // Stream-K fix-up: publish this CTA's partial, take a ticket; the last CTA of
                 // the row block sums every partial in CTA order and resets the ticket.
+                const int slot_id = (rb == rb_first) ? 0 : 1;
                 float *mine = ws_part + (b * 2 + slot_id) * (int64_t)kPartialSlotFloats;
 #pragma unroll
-                for (int m = 0; m < kPer; ++m) mine[threadIdx.x + m * NW * 32] = vals[m];
+                for (int m = 0; m < kPerLane; ++m) mine[lane + 32 * m] = vals[m];
                 __threadfence();
-                __syncthreads();
+                __syncwarp();
                 const int64_t b_first = owner_cta(rb * n_kc, Gop, n_units);
                 const int64_t b_last = owner_cta((rb + 1) * n_kc - 1, Gop, n_units);
-                if (threadIdx.x == 0) {
-                    const unsigned nseg = (unsigned)(b_last - b_first + 1);
-                    const unsigned old = atomicAdd(ws_cnt + rb, 1u);
-                    s_last = (old == nseg - 1) ? 1 : 0;
-                }
-                __syncthreads();
-                if (s_last) {
+                unsigned old = 0;
+                if (lane == 0) old = atomicAdd(ws_cnt + rb, 1u);
+                old = __shfl_sync(0xffffffffu, old, 0);
+                if (old == (unsigned)(b_last - b_first)) {
                     __threadfence();
 #pragma unroll
-                    for (int m = 0; m < kPer; ++m) {
-                        const int e = threadIdx.x + m * NW * 32;
+                    for (int m = 0; m < kPerLane; ++m) {
+                        const int e = lane + 32 * m;
                         float v = 0.f;
                         for (int64_t bb = b_first; bb <= b_last; ++bb) {
                             const int64_t bb_first_rb = (bb * n_units / Gop) / n_kc;
@@ -446,13 +623,18 @@ vl_mma_kernel(const __grid_constant__ VlOps<MAXOPS> P, float *__restrict__ ws_pa
                         out_coords(e, &row, &col);
                         if (row < out_f && col < C) o.Y[(int64_t)col * out_f + row] = v;
                     }
-                    if (threadIdx.x == 0) ws_cnt[rb] = 0u;
+                    if (lane == 0) ws_cnt[rb] = 0u;
                 }
-                __syncthreads();  // s_last and red are free again
+            }
+            __syncwarp();
+            if (lane == 0) {
+                s_tick[buf] = 0u;
+                __threadfence_block();
+                atomicAdd(&s_free[buf], 1u);
             }
         }
     }
-    cp_async_wait<0>();
+    if constexpr (!BULK) cp_async_wait<0>();
 }
 
 // ---- the CUDA-core kernel (canonical layout) -------------------------------------------
@@ -515,23 +697,31 @@ vl_simt_kernel(const uint8_t *__restrict__ codes, const uint16_t *__restrict__ s
 
 // ---- host side ---------------------------------------------------------------------------
 #ifndef SVD_NW
-#define SVD_NW 8
+#define SVD_NW 16
 #endif
 #ifndef SVD_D1
 #define SVD_D1 5
 #endif
 #ifndef SVD_MINB1
-#define SVD_MINB1 2
+#define SVD_MINB1 1
 #endif
 #ifndef SVD_MULHI
-#define SVD_MULHI true
+#define SVD_MULHI false
+#endif
+#ifndef SVD_ASYNC
+#define SVD_ASYNC false
+#endif
+#ifndef SVD_BULK
+#define SVD_BULK true
 #endif
 constexpr int kNW = SVD_NW;        // warps per CTA
 constexpr int kD1 = SVD_D1;        // ring depth, C <= 8
 constexpr int kD2 = 4;             // ring depth, C <= 16 / 32
 constexpr int kMinB1 = SVD_MINB1;  // CTAs per SM the C <= 8 kernel is compiled for
 constexpr bool kMulHi = SVD_MULHI;
-constexpr int kMaxCtasPerSm = 4;   // the workspace holds partial slots for this many
+constexpr bool kAsyncRed = SVD_ASYNC;  // row-block reduction by the last warp (else all threads)
+constexpr bool kBulk = SVD_BULK;       // weights by bulk copies (else per-lane cp.async)
+constexpr int kMaxCtasPerSm = 2;   // the workspace holds partial slots for this many
 constexpr int kChainMax = 256;     // ops per chain launch (kernel parameters, ~16 KB)
 
 static int ntiles_for(int C) { return C <= 8 ? 1 : (C <= 16 ? 2 : 4); }
@@ -553,8 +743,9 @@ size_t vl_workspace_bytes(int64_t in_f, int64_t out_f, int C) {
 template <int NT, int D, int MAXOPS>
 static cudaError_t launch_mma(const VlOps<MAXOPS> &P, void *ws, bool pdl, bool coop,
                               int64_t max_units, cudaStream_t stream) {
-    using Cfg = MmaCfg<NT, kNW, D>;
-    auto kern = vl_mma_kernel<NT, kNW, D, MAXOPS, (NT == 1 ? kMinB1 : 1), kMulHi>;
+    constexpr int NW = (NT == 4 && kNW > 8) ? 8 : kNW;  // four n-tiles: partials fill smem
+    using Cfg = MmaCfg<NT, NW, D, kAsyncRed>;
+    auto kern = vl_mma_kernel<NT, NW, D, MAXOPS, (NT == 1 ? kMinB1 : 1), kMulHi, kAsyncRed, kBulk>;
     static int per_sm_cache[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -563,7 +754,7 @@ static cudaError_t launch_mma(const VlOps<MAXOPS> &P, void *ws, bool pdl, bool c
     if (per_sm == 0) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
         if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kNW * 32, Cfg::kSmem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NW * 32, Cfg::kSmem);
         if (e != cudaSuccess) return e;
         per_sm = per_sm < 1 ? 1 : (per_sm > kMaxCtasPerSm ? kMaxCtasPerSm : per_sm);
         if (dev >= 0 && dev < 64) per_sm_cache[dev] = per_sm;
@@ -576,7 +767,7 @@ static cudaError_t launch_mma(const VlOps<MAXOPS> &P, void *ws, bool pdl, bool c
                                                  partial_region_bytes());
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)G);
-    cfg.blockDim = dim3(kNW * 32);
+    cfg.blockDim = dim3(NW * 32);
     cfg.dynamicSmemBytes = Cfg::kSmem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
