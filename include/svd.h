@@ -162,6 +162,30 @@ size_t svd_verify_chain_workspace_bytes(const svd_linear_op *ops, int n_ops, int
 int svd_verify_chain(const svd_linear_op *ops, int n_ops, int C, void *workspace,
                      size_t workspace_bytes, int flags, svd_stream_t stream);
 
+/* ---- verify linear without caller scratch -------------------------------------------- */
+/* (This entry point has no counterpart on the source pages; it is a deployment convenience.)
+ * Some callers cannot allocate device memory at the point where they run the verify pass:
+ * code that executes while another component owns every allocation (a host framework's
+ * memory pool, a pre-reserved arena), inside callbacks or real-time threads where cudaMalloc's
+ * implicit synchronisation is not allowed, or in plugins that are handed only the tensors they
+ * read and write.  svd_verify_linear_noalloc computes exactly what svd_verify_linear computes
+ * for a NATIVE matrix, with the same arguments minus the workspace: its scratch (stream-K
+ * partial sums and per-row-block tickets) is a fixed array of SVD_NOALLOC_SCRATCH_BYTES in the
+ * library's own device memory, reserved on every GPU that loads the library until the
+ * process exits.  It calls no allocator of any kind.
+ *   - out_features <= SVD_NOALLOC_MAX_OUT_FEATURES and at most 160 SMs, else
+ *     SVD_ERR_UNSUPPORTED (other limits as for svd_verify_linear).
+ *   - The first call on each device looks up the array's device address (with that device
+ *     current); make that first call before any stream capture.
+ *   - Every call clears the tickets with a memset on `stream` and then launches the kernel.
+ *     All calls share the one array, so calls that may overlap on the GPU (different streams
+ *     without ordering between them) race and give wrong results; issue them in one stream or
+ *     order them with events. */
+#define SVD_NOALLOC_MAX_OUT_FEATURES 262144
+#define SVD_NOALLOC_SCRATCH_BYTES (5u * 1024u * 1024u + 32u * 1024u)
+int svd_verify_linear_noalloc(const svd_qweight *W, const void *X, int C, float *Y, int flags,
+                              svd_stream_t stream);
+
 /* ---- (b) sampler and lm_head -------------------------------------------------------- */
 /* Per row of logits [rows][V] fp32: p = softmax(logits / T); keep v iff p[v] >= min_p *
  * max p and v lies in the shortest prefix, in the order (p descending, id ascending), whose

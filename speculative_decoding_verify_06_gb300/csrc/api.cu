@@ -12,6 +12,8 @@ int verify_linear(const svd_qweight *W, const void *X, int C, float *Y, void *ws
 int native_sizes(int64_t in_f, int64_t out_f, size_t *cb, size_t *sb);
 int repack(const svd_qweight *src, void *dc, void *ds, cudaStream_t stream);
 int unpack(const svd_qweight *src, void *dc, void *ds, cudaStream_t stream);
+int verify_linear_noalloc(const svd_qweight *W, const void *X, int C, float *Y, int flags,
+                          cudaStream_t stream);
 size_t chain_workspace_bytes(const svd_linear_op *ops, int n_ops, int C);
 int verify_chain(const svd_linear_op *ops, int n_ops, int C, void *ws, size_t ws_bytes, int flags,
                  cudaStream_t stream);
@@ -83,6 +85,11 @@ size_t svd_verify_linear_workspace_bytes(int64_t in_f, int64_t out_f, int C) {
 int svd_verify_linear(const svd_qweight *W, const void *X, int C, float *Y, void *ws,
                       size_t ws_bytes, int flags, svd_stream_t stream) {
     return svd::verify_linear(W, X, C, Y, ws, ws_bytes, flags, (cudaStream_t)stream);
+}
+
+int svd_verify_linear_noalloc(const svd_qweight *W, const void *X, int C, float *Y, int flags,
+                              svd_stream_t stream) {
+    return svd::verify_linear_noalloc(W, X, C, Y, flags, (cudaStream_t)stream);
 }
 
 size_t svd_verify_chain_workspace_bytes(const svd_linear_op *ops, int n_ops, int C) {

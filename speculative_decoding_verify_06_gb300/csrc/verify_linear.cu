@@ -977,4 +977,64 @@ int unpack(const svd_qweight *src, void *dc, void *ds, cudaStream_t stream) {
     return SVD_OK;
 }
 
+// ---- verify linear without caller scratch ----------------------------------------------
+// The stream-K kernel needs a small scratch area (partial sums of row blocks split between
+// CTAs, and one ticket counter per 64-row block).  svd_verify_linear takes it from the caller;
+// this variant takes it from a fixed array in the library's own device memory instead, for
+// callers that cannot allocate device memory.  The array is reserved when the library's
+// module is loaded on a device and stays there until the process exits.
+constexpr int kNoAllocMaxSms = 160;
+constexpr int64_t kNoAllocMaxRowBlocks = SVD_NOALLOC_MAX_OUT_FEATURES / kRowsPerBlock;
+constexpr size_t kNoAllocPartialBytes =
+    (size_t)kNoAllocMaxSms * kMaxCtasPerSm * 2 * kPartialSlotFloats * sizeof(float);
+constexpr size_t kNoAllocBytes = kNoAllocPartialBytes + kNoAllocMaxRowBlocks * sizeof(unsigned);
+static_assert(kNoAllocBytes <= SVD_NOALLOC_SCRATCH_BYTES, "scratch bound in svd.h");
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+// Device address of g_noalloc_scratch, looked up once per device with that device current
+// (in host code the symbol is only a host-side handle and must never reach a kernel).
+static std::mutex g_noalloc_mu;
+static void *g_noalloc_ptr[64] = {nullptr};
+
+int verify_linear_noalloc(const svd_qweight *W, const void *X, int C, float *Y, int flags,
+                          cudaStream_t stream) {
+    int rc = check_qweight(W);
+    if (rc != SVD_OK) return rc;
+    if (W->layout != SVD_LAYOUT_NATIVE) return SVD_ERR_INVALID_ARG;
+    if (!X || !Y || C < 1 || C > SVD_C_MAX || !aligned16(X)) return SVD_ERR_INVALID_ARG;
+    if (flags & ~SVD_F_PDL) return SVD_ERR_INVALID_ARG;
+    if (W->out_features > SVD_NOALLOC_MAX_OUT_FEATURES) return SVD_ERR_UNSUPPORTED;
+    const int sms = sm_count();
+    if (sms < 1) return SVD_ERR_CUDA;
+    if (sms > kNoAllocMaxSms) return SVD_ERR_UNSUPPORTED;
+    int dev = 0;
+    SVD_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return SVD_ERR_UNSUPPORTED;
+    void *base = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mu);
+        if (!g_noalloc_ptr[dev]) {
+            void *p = nullptr;
+            SVD_CUDA_TRY(cudaGetSymbolAddress(&p, g_noalloc_scratch));
+            g_noalloc_ptr[dev] = p;
+        }
+        base = g_noalloc_ptr[dev];
+    }
+    // Same layout as a caller workspace: partial slots, then the tickets, which must start at
+    // zero.  Every call clears them again on the stream before its kernel, so a call never
+    // depends on what the previous one left behind.
+    const NativeGeom ng = native_geom(W->in_features, W->out_features);
+    unsigned char *tickets = reinterpret_cast<unsigned char *>(base) + partial_region_bytes();
+    SVD_CUDA_TRY(cudaMemsetAsync(tickets, 0, (size_t)ng.n_rb * sizeof(unsigned), stream));
+    VlOps<1> P;
+    P.n = 1;
+    P.C = C;
+    set_shift_multipliers(P);
+    P.op[0] = make_op(W, X, Y);
+    SVD_CUDA_TRY(launch_ops(P, base, (flags & SVD_F_PDL) != 0, stream));
+    return SVD_OK;
+}
+
 }  // namespace svd
+

@@ -36,7 +36,7 @@ SVD_K_MAX = 32
 EXPORTS = (
     "svd_error_string", "svd_last_cuda_error", "svd_native_sizes", "svd_repack_weights",
     "svd_unpack_weights", "svd_verify_linear_workspace_bytes", "svd_verify_linear",
-    "svd_verify_chain_workspace_bytes", "svd_verify_chain",
+    "svd_verify_linear_noalloc", "svd_verify_chain_workspace_bytes", "svd_verify_chain",
     "svd_sampler_workspace_bytes", "svd_sampler_probs", "svd_lm_head_workspace_bytes",
     "svd_lm_head_softmax", "svd_accept", "svd_graph_begin", "svd_graph_end", "svd_graph_launch",
     "svd_graph_destroy", "svd_device_sm_count",
@@ -112,6 +112,7 @@ def load(path: str = LIB_PATH):
             "svd_unpack_weights": (i32, [P, P, P, P]),
             "svd_verify_linear_workspace_bytes": (sz, [i64, i64, i32]),
             "svd_verify_linear": (i32, [P, P, i32, P, P, sz, i32, P]),
+            "svd_verify_linear_noalloc": (i32, [P, P, i32, P, i32, P]),
             "svd_verify_chain_workspace_bytes": (sz, [P, i32, i32]),
             "svd_verify_chain": (i32, [P, i32, i32, P, sz, i32, P]),
             "svd_sampler_workspace_bytes": (sz, [i32, i64]),
@@ -197,6 +198,14 @@ def svd_verify_linear(W: QWeight, X, C: int, Y, workspace=None, workspace_bytes:
     _check("svd_verify_linear", load().svd_verify_linear(
         ctypes.byref(w), _ptr(X), int(C), _ptr(Y), _ptr(workspace), int(workspace_bytes),
         int(flags), _stream(stream)))
+
+
+def svd_verify_linear_noalloc(W: QWeight, X, C: int, Y, flags: int = 0, stream=None):
+    """svd_verify_linear without a workspace argument: the scratch lives in the library's own
+    device memory (for callers that cannot allocate)."""
+    w = W._c()
+    _check("svd_verify_linear_noalloc", load().svd_verify_linear_noalloc(
+        ctypes.byref(w), _ptr(X), int(C), _ptr(Y), int(flags), _stream(stream)))
 
 
 def _ops_array(ops):
