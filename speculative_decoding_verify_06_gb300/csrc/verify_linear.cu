@@ -9,16 +9,20 @@
 //     Y[c][j] = sum_b s[j][b] * sum_{i in block b} (code[j][i] - 8) * X[c][i]
 //
 // Two kernels:
-//  * vl_mma_kernel (NATIVE layout) -- persistent stream-K over (64-row block, 64-input chunk)
-//    units.  Each warp owns a cp.async ring of its units in shared memory (codes + scales,
-//    2304 bytes per unit), dequantises nibbles straight into bf16 A fragments with one lop3 and
-//    one bf16x2 subtract per pair (value 128 + c built from the exponent pattern 0x4300, then
-//    minus 136 gives c - 8 exactly), and runs mma.sync m16n8k16 (bf16 in, fp32 accumulate)
-//    against the activations as the B operand.  Every 32-input block gets a fresh accumulator
-//    that is scaled by its fp16 scale in fp32, so the only rounding is fp32 accumulation.
-//    Warps of a CTA interleave the chunks of a row block; partial row blocks at the edges of a
-//    CTA's range are combined through a small workspace by the last CTA to arrive (an atomic
-//    ticket per row block, summed in CTA order: deterministic, no spinning).
+//  * vl_ws_kernel (NATIVE layout) -- a persistent, warp-specialised stream-K kernel over
+//    (64-row block, 64-input chunk) units.  A producer warp moves each CTA's units, stage by
+//    stage (codes and scales of 15 consecutive units, two bulk copies completing on an
+//    mbarrier), into a ring in shared memory and never waits on anything but a free stage.
+//    Fifteen consumer warps dequantise nibbles straight into bf16 A fragments with one lop3
+//    and one bf16x2 subtract per pair (value 128 + c built from the exponent pattern 0x4300,
+//    then minus 136 gives c - 8 exactly), and run mma.sync m16n8k16 (bf16 in, fp32
+//    accumulate) against the activations as the B operand.  Every 32-input block gets a
+//    fresh accumulator that is scaled by its fp16 scale in fp32, so the only rounding is fp32
+//    accumulation.  Partial row blocks at the edges of a CTA's range are finished by the last
+//    CTA to arrive (an atomic ticket per row block, partials summed in CTA order:
+//    deterministic, no spinning).  A chain of matrices runs in one cooperative launch with a
+//    barrier among the consumer warps between matrices; the producer keeps streaming the
+//    next matrix's weights through it.
 //  * vl_simt_kernel (CANONICAL layout) -- the plain CUDA-core version: one warp per output
 //    row, each lane one 32-input block at a time, fp32 FMAs, warp-shuffle reduction.
 #include <cooperative_groups.h>
@@ -138,18 +142,6 @@ __global__ void unpack_scales_kernel(const uint16_t *__restrict__ src, uint16_t 
 }
 
 // ---- device building blocks -----------------------------------------------------------
-__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
-    const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem_src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 // Bulk (TMA-engine) copies into shared memory completing on an mbarrier.
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -168,6 +160,15 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         "l"(src), "r"(bytes), "r"(mbar)
         : "memory");
 }
+// Activations read through L2 only: in a chain, op i+1 may read what op i wrote in the same
+// kernel, so the non-coherent path must not be used there.
+__device__ __forceinline__ uint4 ldg_cg_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
 // Waits for phase `parity` of an mbarrier; gives up after a bounded number of polls (each poll
 // may suspend the thread briefly), so a broken pipeline cannot hang the GPU.
 __device__ __forceinline__ void mbar_wait(uint32_t mbar, uint32_t parity) {
@@ -184,21 +185,13 @@ __device__ __forceinline__ void mbar_wait(uint32_t mbar, uint32_t parity) {
 }
 
 // Four bf16x2 A registers from one native word: (bits >> 4p) & 0x000F000F | 0x43004300 is the
-// pair (128 + c_lo, 128 + c_hi) exactly; subtracting (136, 136) leaves (c - 8) exactly.  With
-// MULHI the three right shifts are taken as mul.hi by 2^28, 2^24, 2^20 held in registers (the
-// integer-multiply unit), which leaves only the lop3s on the integer ALU.
-template <bool MULHI>
-__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t a[4], uint32_t m4, uint32_t m8,
-                                             uint32_t m12) {
+// pair (128 + c_lo, 128 + c_hi) exactly; subtracting (136, 136) leaves (c - 8) exactly.
+__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t a[4]) {
     const uint32_t magic = 0x43004300u, bias = 0x43084308u;
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
-        uint32_t v, sh;
-        if (MULHI) {
-            sh = (p == 0) ? w : __umulhi(w, p == 1 ? m4 : (p == 2 ? m8 : m12));
-        } else {
-            sh = w >> (4 * p);
-        }
+        uint32_t v;
+        const uint32_t sh = w >> (4 * p);
         asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(v) : "r"(sh), "r"(0x000F000Fu), "r"(magic));
         asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(a[p]) : "r"(v), "r"(bias));
     }
@@ -234,7 +227,6 @@ template <int MAXOPS>
 struct VlOps {
     int n;
     int C;
-    uint32_t m4, m8, m12;  // 2^28, 2^24, 2^20: shift multipliers kept opaque to the compiler
     VlOp op[MAXOPS];
 };
 
@@ -248,103 +240,111 @@ __device__ __forceinline__ int64_t owner_cta(int64_t n, int64_t Gop, int64_t n_u
 // ---- the tensor-core stream-K kernel ---------------------------------------------------
 constexpr int kPartialSlotFloats = 32 * kTiles * 4 * 4;  // largest warp partial (4 n-tiles)
 
-template <int NT, int NW, int D, bool ASYNC>
-struct MmaCfg {
-    static constexpr int kAcc = kTiles * NT * 4;              // fp32 accumulators per lane
-    static constexpr int kPartial = 32 * kAcc;                // floats per warp partial
-    static constexpr size_t kRing = (size_t)NW * D * kUnitBytes;
-    static constexpr size_t kSmem =
-        kRing + (size_t)(ASYNC ? 2 : 1) * NW * kPartial * sizeof(float);
+// ---- the warp-specialised tensor-core stream-K kernel ------------------------------------
+// CTA = NWC consumer warps + 1 producer warp.  The producer's lane 0 walks the CTA's units of
+// every op (in op order) in stages of NWC consecutive units -- one contiguous byte range of
+// codes and one of scales, moved by two bulk copies -- into a ring of S stages, waiting only
+// for a stage to be released.  It never takes part in a barrier, so weights keep streaming
+// while the consumers synchronise.  Consumer warp w takes unit w of every stage: warps
+// interleave the chunks of a 64-row block; at the end of a block the CTA's consumers combine
+// their partials in shared memory (named barrier), and a block split between CTAs is finished
+// by the last CTA to arrive (a ticket per block; partials summed in CTA order).  Ops of a
+// chain are separated by a barrier among the consumer warps of all CTAs (cooperative launch);
+// op 0 waits for the preceding kernel with griddepcontrol.wait before touching activations.
+template <int NT, int NWC, int S>
+struct WsCfg {
+    static constexpr int kAcc = kTiles * NT * 4;    // fp32 accumulators per lane
+    static constexpr int kPartial = 32 * kAcc;      // floats per warp partial
+    static constexpr int kPer = (kPartial + NWC * 32 - 1) / (NWC * 32);
+    static constexpr int kStage = NWC * kUnitBytes;
+    static constexpr size_t kRing = (size_t)S * kStage;
+    static constexpr size_t kSmem = kRing + (size_t)NWC * kPartial * sizeof(float);
+    static constexpr int kThreads = (NWC + 1) * 32;
 };
 
-// Runs every op of P in order on a persistent grid.  Each warp keeps a ring of D unit slots
-// in shared memory filled by cp.async; the issue cursor walks the warp's units op after op,
-// so the weights of op g+1 stream in while op g finishes.  Activations of op g+1 are read
-// only after the grid barrier that ends op g (a chain of more than one op is launched
-// cooperatively), or, for op 0, after griddepcontrol.wait.
-//
-// A row block ends asynchronously: each warp drops its partial sums into one of two shared
-// buffers and takes a shared ticket; the last warp to arrive sums the eight partials (in warp
-// order) and writes the rows or the CTA's stream-K partial, while the other warps go on
-// streaming.  A buffer is reused two row blocks later, after its reducer has released it.
-template <int NT, int NW, int D, int MAXOPS, int MINB, bool MULHI, bool ASYNC, bool BULK>
-__global__ void __launch_bounds__(NW * 32, MINB)
-vl_mma_kernel(const __grid_constant__ VlOps<MAXOPS> P, float *__restrict__ ws_part,
-              unsigned int *__restrict__ ws_cnt) {
-    using Cfg = MmaCfg<NT, NW, D, ASYNC>;
-    constexpr int kAcc = Cfg::kAcc, kPartial = Cfg::kPartial;
-    constexpr int kPerLane = kPartial / 32;  // reduced elements per lane of the reducer warp
-    extern __shared__ __align__(16) uint8_t smem[];
-    __shared__ unsigned s_tick[2], s_free[2];
-    __shared__ __align__(8) uint64_t s_mbar[BULK ? NW * D : 1];
-    float *red = reinterpret_cast<float *>(smem + Cfg::kRing);  // [2][NW][kPartial]
+__device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mbar) : "memory");
+}
+__device__ __forceinline__ void consumers_sync(int nthreads) {
+    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+// The gi-th barrier of a launch among the consumers of all G CTAs: one release-add per CTA
+// (after a CTA barrier, so it publishes every consumer's writes) on a counter in the
+// workspace, then acquire polling until the counter reaches gi * G.  Polling is bounded.
+__device__ __forceinline__ void consumer_grid_barrier(unsigned *gbar, unsigned target) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(gbar) : "memory");
+    for (int it = 0; it < (1 << 26); ++it) {
+        unsigned v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(gbar) : "memory");
+        if (v >= target) return;
+        if (it > 512) __nanosleep(32);
+    }
+}
+
+// Ticket of a split row block: release this CTA's partial (written by all consumers before a
+// CTA barrier), take the ticket with acquire so that the last CTA sees every other partial.
+__device__ __forceinline__ unsigned take_ticket(unsigned *cnt) {
+    unsigned old;
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(cnt) : "memory");
+    return old;
+}
+
+template <int NT, int NWC, int S, int MAXOPS, int MINB>
+__global__ void __launch_bounds__((NWC + 1) * 32, MINB)
+vl_ws_kernel(const __grid_constant__ VlOps<MAXOPS> P, float *__restrict__ ws_part,
+             unsigned int *__restrict__ ws_cnt, unsigned int *__restrict__ gbar) {
+    using Cfg = WsCfg<NT, NWC, S>;
+    constexpr int kAcc = Cfg::kAcc, kPartial = Cfg::kPartial, kPer = Cfg::kPer;
+    constexpr int kCons = NWC * 32;
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t s_full[S], s_empty[S];
+    __shared__ unsigned s_flag;
+    float *red = reinterpret_cast<float *>(smem + Cfg::kRing);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g4 = lane >> 2, t4 = lane & 3;
     const int64_t G = gridDim.x, b = blockIdx.x;
-    const int C = P.C;
-    uint8_t *ring = smem + (size_t)warp * D * kUnitBytes;
-    if (threadIdx.x < 2) {
-        s_tick[threadIdx.x] = 0u;
-        s_free[threadIdx.x] = 0u;
-    }
-    const uint32_t mbar0 = smem_u32(&s_mbar[0]) + (BULK ? warp * D * 8 : 0);
-    if (BULK && lane == 0) {
-        for (int i = 0; i < D; ++i) mbar_init(mbar0 + 8 * i, 1);
+    const uint32_t full0 = smem_u32(&s_full[0]), empty0 = smem_u32(&s_empty[0]);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(full0 + 8 * i, 1);
+            mbar_init(empty0 + 8 * i, NWC);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    __syncwarp();
+    __syncthreads();
 
-    // ---- issue cursor: (op ig, unit ij of iJ), source pointers, ring slot ------------------
-    int ig = -1, ij = 0, iJ = 0, islot = 0;
-    const uint8_t *pc = nullptr, *ps = nullptr;
-    auto iseek = [&]() {
-        while (ij >= iJ) {
-            if (++ig >= P.n) return;
-            const VlOp &o = P.op[ig];
-            const int64_t Gop = min(G, o.n_units);
-            ij = 0;
-            iJ = 0;
-            if (b >= Gop) continue;
-            const int64_t st = b * o.n_units / Gop, en = (b + 1) * o.n_units / Gop;
-            const int64_t span = en - st;
-            iJ = span > warp ? (int)((span - warp + NW - 1) / NW) : 0;
-            pc = o.codes + (st + warp) * kUnitCodeBytes + lane * 16;
-            ps = o.scales + (st + warp) * kUnitScaleBytes + lane * 16;
-        }
-    };
-    auto issue_one = [&]() {
-        if (ig < P.n) {
-            if constexpr (BULK) {
-                if (lane == 0) {
-                    const uint32_t slot = smem_u32(ring + islot * kUnitBytes);
-                    const uint32_t mb = mbar0 + 8 * islot;
-                    // the slot was last read through the generic proxy: order those reads
-                    // before the bulk copy (async proxy) overwrites it
+    if (warp == NWC) {
+        // ---- producer: weights never depend on earlier kernels or ops -----------------------
+        if (lane == 0) {
+            uint32_t sc = 0;
+            for (int gi = 0; gi < P.n; ++gi) {
+                const VlOp &o = P.op[gi];
+                const int64_t Gop = min(G, o.n_units);
+                if (b >= Gop) continue;
+                const int64_t st = b * o.n_units / Gop, en = (b + 1) * o.n_units / Gop;
+                for (int64_t u0 = st; u0 < en; u0 += NWC, ++sc) {
+                    const uint32_t slot = sc % S, round = sc / S;
+                    if (round > 0) mbar_wait(empty0 + 8 * slot, (round - 1) & 1u);
+                    const uint32_t n = (uint32_t)min((int64_t)NWC, en - u0);
+                    const uint32_t dst = smem_u32(smem + (size_t)slot * Cfg::kStage);
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    mbar_expect_tx(mb, kUnitBytes);
-                    bulk_g2s(slot, pc - lane * 16, kUnitCodeBytes, mb);
-                    bulk_g2s(slot + kUnitCodeBytes, ps - lane * 16, kUnitScaleBytes, mb);
+                    mbar_expect_tx(full0 + 8 * slot, n * kUnitBytes);
+                    bulk_g2s(dst, o.codes + u0 * kUnitCodeBytes, n * kUnitCodeBytes, full0 + 8 * slot);
+                    bulk_g2s(dst + NWC * kUnitCodeBytes, o.scales + u0 * kUnitScaleBytes,
+                             n * kUnitScaleBytes, full0 + 8 * slot);
                 }
-            } else {
-                uint8_t *slot = ring + islot * kUnitBytes + lane * 16;
-#pragma unroll
-                for (int r = 0; r < kTiles; ++r) cp_async16(slot + r * 512, pc + r * 512);
-                if (lane < kUnitScaleBytes / 16) cp_async16(slot + kUnitCodeBytes, ps);
             }
-            pc += NW * kUnitCodeBytes;
-            ps += NW * kUnitScaleBytes;
-            ++ij;
-            islot = (islot + 1 == D) ? 0 : islot + 1;
-            iseek();
         }
-        if constexpr (!BULK) cp_async_commit();
-    };
-    iseek();
-    // Weights never depend on earlier kernels or ops: start streaming before any wait.
-#pragma unroll
-    for (int s = 0; s < D - 1; ++s) issue_one();
-    __syncthreads();  // s_tick / s_free initialised
+        return;
+    }
+
+    // ---- consumers -------------------------------------------------------------------------
+    const int g4 = lane >> 2, t4 = lane & 3;
+    const int C = P.C;
+    griddep_wait();
+    griddep_launch_dependents();
 
     float acc[kTiles][NT][4];
 #pragma unroll
@@ -354,25 +354,22 @@ vl_mma_kernel(const __grid_constant__ VlOps<MAXOPS> P, float *__restrict__ ws_pa
 #pragma unroll
             for (int q = 0; q < 4; ++q) acc[r][nt][q] = 0.f;
 
-    int cslot = 0;
-    uint32_t cphase = 0;  // parity of the slot's current use (bulk copies)
-    unsigned seg = 0;  // row-block segments this CTA has finished (all ops)
+    uint32_t sc = 0;  // stage counter, in step with the producer's
     for (int gi = 0; gi < P.n; ++gi) {
         const VlOp &o = P.op[gi];
-        if (gi == 0) {
-            griddep_wait();
-            griddep_launch_dependents();
-        } else {
-            cooperative_groups::this_grid().sync();
+        if (gi > 0) {
+            consumers_sync(kCons);
+            if (threadIdx.x == 0) consumer_grid_barrier(gbar, (unsigned)gi * (unsigned)G);
+            consumers_sync(kCons);
         }
         const int64_t Gop = min(G, o.n_units);
         if (b >= Gop) continue;
         const int64_t n_kc = o.n_kc, n_units = o.n_units, in_f = o.in_f, out_f = o.out_f;
         const int64_t start = b * n_units / Gop, end = (b + 1) * n_units / Gop;
         const int64_t span = end - start;
-        const int J = span > warp ? (int)((span - warp + NW - 1) / NW) : 0;
+        const int J = span > warp ? (int)((span - warp + NWC - 1) / NWC) : 0;
+        const int nstages = (int)((span + NWC - 1) / NWC);
 
-        // this lane's activation rows (B operand: column nt*8 + g4, inputs from t4*8)
         const __nv_bfloat16 *xrow[NT];
         bool xok[NT];
 #pragma unroll
@@ -387,8 +384,13 @@ vl_mma_kernel(const __grid_constant__ VlOps<MAXOPS> P, float *__restrict__ ws_pa
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 const __nv_bfloat16 *src = xrow[nt] + kc * kChunk;
-                xr[nt][0] = xok[nt] ? ldg_nc_v4(src) : make_uint4(0u, 0u, 0u, 0u);
-                xr[nt][1] = (xok[nt] && !lastc) ? ldg_nc_v4(src + 32) : make_uint4(0u, 0u, 0u, 0u);
+                if constexpr (MAXOPS > 1) {
+                    xr[nt][0] = xok[nt] ? ldg_cg_v4(src) : make_uint4(0u, 0u, 0u, 0u);
+                    xr[nt][1] = (xok[nt] && !lastc) ? ldg_cg_v4(src + 32) : make_uint4(0u, 0u, 0u, 0u);
+                } else {
+                    xr[nt][0] = xok[nt] ? ldg_nc_v4(src) : make_uint4(0u, 0u, 0u, 0u);
+                    xr[nt][1] = (xok[nt] && !lastc) ? ldg_nc_v4(src + 32) : make_uint4(0u, 0u, 0u, 0u);
+                }
             }
         };
 
@@ -398,42 +400,34 @@ vl_mma_kernel(const __grid_constant__ VlOps<MAXOPS> P, float *__restrict__ ws_pa
         if (J > 0) load_x(kc, xr);
         int j = 0;
         const int64_t rb_first = start / n_kc, rb_last = (end - 1) / n_kc;
-        for (int64_t rb = rb_first; rb <= rb_last; ++rb, ++seg) {
+        for (int64_t rb = rb_first; rb <= rb_last; ++rb) {
             const int64_t seg_lo = max(start, rb * n_kc), seg_hi = min(end, (rb + 1) * n_kc);
             while (j < J && u < seg_hi) {
-                issue_one();
-                if constexpr (BULK) {
-                    mbar_wait(mbar0 + 8 * cslot, cphase);
-                } else {
-                    cp_async_wait<D - 1>();
-                    __syncwarp();
-                }
+                const uint32_t slot = sc % S;
+                mbar_wait(full0 + 8 * slot, (sc / S) & 1u);
                 uint4 xc[NT][2];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     xc[nt][0] = xr[nt][0];
                     xc[nt][1] = xr[nt][1];
                 }
-                int64_t kn = kc + NW;
+                int64_t kn = kc + NWC;
                 while (kn >= n_kc) kn -= n_kc;
                 if (j + 1 < J) load_x(kn, xr);
-                const uint8_t *slot = ring + cslot * kUnitBytes;
-                uint4 cw[kTiles];
-                uint2 sc[kTiles];
+                const uint8_t *cbase = smem + (size_t)slot * Cfg::kStage + warp * kUnitCodeBytes;
+                const uint8_t *sbase =
+                    smem + (size_t)slot * Cfg::kStage + NWC * kUnitCodeBytes + warp * kUnitScaleBytes;
 #pragma unroll
                 for (int r = 0; r < kTiles; ++r) {
-                    cw[r] = *reinterpret_cast<const uint4 *>(slot + r * 512 + lane * 16);
-                    sc[r] = *reinterpret_cast<const uint2 *>(slot + kUnitCodeBytes + r * 64 + g4 * 8);
-                }
-#pragma unroll
-                for (int r = 0; r < kTiles; ++r) {
-                    const float2 s_lo = __half22float2(*reinterpret_cast<const __half2 *>(&sc[r].x));
-                    const float2 s_hi = __half22float2(*reinterpret_cast<const __half2 *>(&sc[r].y));
+                    const uint4 cw = *reinterpret_cast<const uint4 *>(cbase + r * 512 + lane * 16);
+                    const uint2 scw = *reinterpret_cast<const uint2 *>(sbase + r * 64 + g4 * 8);
+                    const float2 s_lo = __half22float2(*reinterpret_cast<const __half2 *>(&scw.x));
+                    const float2 s_hi = __half22float2(*reinterpret_cast<const __half2 *>(&scw.y));
 #pragma unroll
                     for (int blk = 0; blk < 2; ++blk) {
                         uint32_t a0[4], a1[4];
-                        dequant_word<MULHI>(blk ? cw[r].z : cw[r].x, a0, P.m4, P.m8, P.m12);
-                        dequant_word<MULHI>(blk ? cw[r].w : cw[r].y, a1, P.m4, P.m8, P.m12);
+                        dequant_word(blk ? cw.z : cw.x, a0);
+                        dequant_word(blk ? cw.w : cw.y, a1);
                         const float sg = blk ? s_lo.y : s_lo.x, sh = blk ? s_hi.y : s_hi.x;
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
@@ -447,107 +441,17 @@ vl_mma_kernel(const __grid_constant__ VlOps<MAXOPS> P, float *__restrict__ ws_pa
                         }
                     }
                 }
-                __syncwarp();  // every lane is done with this slot before it is refilled
-                if (++cslot == D) {
-                    cslot = 0;
-                    cphase ^= 1u;
-                }
+                __syncwarp();  // every lane has read the stage
+                if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+                ++sc;
                 ++j;
-                u += NW;
+                u += NWC;
                 kc = kn;
             }
 
-            // ---- end of row block rb ---------------------------------------------------------
-            if constexpr (!ASYNC) {
-                // All threads of the CTA combine the warps' partials, two elements each.
-                {
-                    float4 *dst = reinterpret_cast<float4 *>(red + warp * kPartial + lane * kAcc);
-#pragma unroll
-                    for (int r = 0; r < kTiles; ++r)
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            dst[r * NT + nt] = make_float4(acc[r][nt][0], acc[r][nt][1],
-                                                           acc[r][nt][2], acc[r][nt][3]);
-                            acc[r][nt][0] = acc[r][nt][1] = acc[r][nt][2] = acc[r][nt][3] = 0.f;
-                        }
-                }
-                __syncthreads();
-                constexpr int kPer = kPartial / (NW * 32);
-                float vals[kPer];
-#pragma unroll
-                for (int m = 0; m < kPer; ++m) {
-                    const int e = threadIdx.x + m * NW * 32;
-                    float v = 0.f;
-#pragma unroll
-                    for (int w = 0; w < NW; ++w) v += red[w * kPartial + e];
-                    vals[m] = v;
-                }
-                auto coords = [&](int e, int64_t *row, int *col) {
-                    const int lsrc = e / kAcc, idx = e % kAcc, q = idx & 3, rn = idx >> 2;
-                    const int r = rn / NT, nt = rn % NT;
-                    *row = rb * kRowsPerBlock + 16 * r + (lsrc >> 2) + ((q >> 1) ? 8 : 0);
-                    *col = nt * 8 + (lsrc & 3) * 2 + (q & 1);
-                };
-                const bool full = (seg_lo == rb * n_kc) && (seg_hi == (rb + 1) * n_kc);
-                if (full) {
-#pragma unroll
-                    for (int m = 0; m < kPer; ++m) {
-                        int64_t row;
-                        int col;
-                        coords(threadIdx.x + m * NW * 32, &row, &col);
-                        if (row < out_f && col < C) o.Y[(int64_t)col * out_f + row] = vals[m];
-                    }
-                } else {
-                    // Stream-K fix-up: publish this CTA's partial, take a ticket (one thread,
-                    // release); the last CTA of the row block sums every partial in CTA order.
-                    const int slot_id = (rb == rb_first) ? 0 : 1;
-                    float *mine = ws_part + (b * 2 + slot_id) * (int64_t)kPartialSlotFloats;
-#pragma unroll
-                    for (int m = 0; m < kPer; ++m) mine[threadIdx.x + m * NW * 32] = vals[m];
-                    __threadfence();
-                    __syncthreads();
-                    const int64_t b_first = owner_cta(rb * n_kc, Gop, n_units);
-                    const int64_t b_last = owner_cta((rb + 1) * n_kc - 1, Gop, n_units);
-                    if (threadIdx.x == 0) {
-                        __threadfence();
-                        const unsigned old = atomicAdd(ws_cnt + rb, 1u);
-                        s_tick[0] = (old == (unsigned)(b_last - b_first)) ? 1u : 0u;
-                    }
-                    __syncthreads();
-                    if (s_tick[0]) {
-                        __threadfence();
-#pragma unroll
-                        for (int m = 0; m < kPer; ++m) {
-                            const int e = threadIdx.x + m * NW * 32;
-                            float v = 0.f;
-                            for (int64_t bb = b_first; bb <= b_last; ++bb) {
-                                const int64_t bb_first_rb = (bb * n_units / Gop) / n_kc;
-                                const int sid = (rb == bb_first_rb) ? 0 : 1;
-                                v += __ldcg(ws_part + (bb * 2 + sid) * (int64_t)kPartialSlotFloats + e);
-                            }
-                            int64_t row;
-                            int col;
-                            coords(e, &row, &col);
-                            if (row < out_f && col < C) o.Y[(int64_t)col * out_f + row] = v;
-                        }
-                        if (threadIdx.x == 0) ws_cnt[rb] = 0u;
-                    }
-                }
-                __syncthreads();  // red and s_tick are free again
-                continue;
-            }
-
-            // ---- asynchronous variant: the last warp of the row block reduces ----------------
-            const int buf = seg & 1;
-            if (seg >= 2) {  // the reducer of segment seg - 2 must have released the buffer
-                const unsigned need = seg >> 1;
-                for (int spin = 0; spin < (1 << 24); ++spin) {
-                    if (*reinterpret_cast<volatile unsigned *>(&s_free[buf]) >= need) break;
-                    __nanosleep(32);
-                }
-            }
+            // ---- row block rb is finished by this CTA: combine the consumer warps' partials
             {
-                float4 *dst = reinterpret_cast<float4 *>(red + (buf * NW + warp) * kPartial + lane * kAcc);
+                float4 *dst = reinterpret_cast<float4 *>(red + warp * kPartial + lane * kAcc);
 #pragma unroll
                 for (int r = 0; r < kTiles; ++r)
 #pragma unroll
@@ -557,28 +461,19 @@ vl_mma_kernel(const __grid_constant__ VlOps<MAXOPS> P, float *__restrict__ ws_pa
                         acc[r][nt][0] = acc[r][nt][1] = acc[r][nt][2] = acc[r][nt][3] = 0.f;
                     }
             }
-            __syncwarp();
-            unsigned ticket = 0;
-            if (lane == 0) {
-                __threadfence_block();
-                ticket = atomicAdd(&s_tick[buf], 1u);
-            }
-            ticket = __shfl_sync(0xffffffffu, ticket, 0);
-            if (ticket != NW - 1) continue;  // another warp reduces this row block
-
-            // ---- the reducer: the last warp of the CTA to finish row block rb ----------------
-            __threadfence_block();
-            const float *rbuf = red + buf * NW * kPartial;
-            float vals[kPerLane];
+            consumers_sync(kCons);
+            float vals[kPer];
 #pragma unroll
-            for (int m = 0; m < kPerLane; ++m) {
-                const int e = lane + 32 * m;
+            for (int m = 0; m < kPer; ++m) {
+                const int e = threadIdx.x + m * kCons;
                 float v = 0.f;
+                if (e < kPartial) {
 #pragma unroll
-                for (int w = 0; w < NW; ++w) v += rbuf[w * kPartial + e];
+                    for (int w = 0; w < NWC; ++w) v += red[w * kPartial + e];
+                }
                 vals[m] = v;
             }
-            auto out_coords = [&](int e, int64_t *row, int *col) {
+            auto coords = [&](int e, int64_t *row, int *col) {
                 const int lsrc = e / kAcc, idx = e % kAcc, q = idx & 3, rn = idx >> 2;
                 const int r = rn / NT, nt = rn % NT;
                 *row = rb * kRowsPerBlock + 16 * r + (lsrc >> 2) + ((q >> 1) ? 8 : 0);
@@ -587,10 +482,12 @@ vl_mma_kernel(const __grid_constant__ VlOps<MAXOPS> P, float *__restrict__ ws_pa
             const bool full = (seg_lo == rb * n_kc) && (seg_hi == (rb + 1) * n_kc);
             if (full) {
 #pragma unroll
-                for (int m = 0; m < kPerLane; ++m) {
+                for (int m = 0; m < kPer; ++m) {
+                    const int e = threadIdx.x + m * kCons;
+                    if (e >= kPartial) break;
                     int64_t row;
                     int col;
-                    out_coords(lane + 32 * m, &row, &col);
+                    coords(e, &row, &col);
                     if (row < out_f && col < C) o.Y[(int64_t)col * out_f + row] = vals[m];
                 }
             } else {
@@ -599,42 +496,63 @@ vl_mma_kernel(const __grid_constant__ VlOps<MAXOPS> P, float *__restrict__ ws_pa
                 const int slot_id = (rb == rb_first) ? 0 : 1;
                 float *mine = ws_part + (b * 2 + slot_id) * (int64_t)kPartialSlotFloats;
 #pragma unroll
-                for (int m = 0; m < kPerLane; ++m) mine[lane + 32 * m] = vals[m];
-                __threadfence();
-                __syncwarp();
+                for (int m = 0; m < kPer; ++m)
+                    if (threadIdx.x + m * kCons < kPartial) mine[threadIdx.x + m * kCons] = vals[m];
+                consumers_sync(kCons);
                 const int64_t b_first = owner_cta(rb * n_kc, Gop, n_units);
                 const int64_t b_last = owner_cta((rb + 1) * n_kc - 1, Gop, n_units);
-                unsigned old = 0;
-                if (lane == 0) old = atomicAdd(ws_cnt + rb, 1u);
-                old = __shfl_sync(0xffffffffu, old, 0);
-                if (old == (unsigned)(b_last - b_first)) {
-                    __threadfence();
+                if (threadIdx.x == 0) {
+                    const unsigned old = take_ticket(ws_cnt + rb);
+                    s_flag = (old == (unsigned)(b_last - b_first)) ? 1u : 0u;
+                }
+                consumers_sync(kCons);
+                if (s_flag) {
+                    auto part = [&](int64_t bb, int e) {
+                        const int64_t bb_first_rb = (bb * n_units / Gop) / n_kc;
+                        const int sid = (rb == bb_first_rb) ? 0 : 1;
+                        return __ldcg(ws_part + (bb * 2 + sid) * (int64_t)kPartialSlotFloats + e);
+                    };
 #pragma unroll
-                    for (int m = 0; m < kPerLane; ++m) {
-                        const int e = lane + 32 * m;
+                    for (int m = 0; m < kPer; ++m) {
+                        const int e = threadIdx.x + m * kCons;
+                        if (e >= kPartial) break;
                         float v = 0.f;
-                        for (int64_t bb = b_first; bb <= b_last; ++bb) {
-                            const int64_t bb_first_rb = (bb * n_units / Gop) / n_kc;
-                            const int sid = (rb == bb_first_rb) ? 0 : 1;
-                            v += __ldcg(ws_part + (bb * 2 + sid) * (int64_t)kPartialSlotFloats + e);
+                        int64_t bb = b_first;
+                        for (; bb + 3 <= b_last; bb += 4) {  // four loads in flight, summed in order
+                            const float p0 = part(bb, e), p1 = part(bb + 1, e);
+                            const float p2 = part(bb + 2, e), p3 = part(bb + 3, e);
+                            v += p0;
+                            v += p1;
+                            v += p2;
+                            v += p3;
                         }
+                        for (; bb <= b_last; ++bb) v += part(bb, e);
                         int64_t row;
                         int col;
-                        out_coords(e, &row, &col);
+                        coords(e, &row, &col);
                         if (row < out_f && col < C) o.Y[(int64_t)col * out_f + row] = v;
                     }
-                    if (lane == 0) ws_cnt[rb] = 0u;
+                    if (threadIdx.x == 0) ws_cnt[rb] = 0u;
                 }
             }
+            consumers_sync(kCons);  // red and s_flag are free again
+        }
+        // stages of this op that hold no unit of this warp: release them in order
+        for (int k = J; k < nstages; ++k) {
+            const uint32_t slot = sc % S;
+            mbar_wait(full0 + 8 * slot, (sc / S) & 1u);
             __syncwarp();
-            if (lane == 0) {
-                s_tick[buf] = 0u;
-                __threadfence_block();
-                atomicAdd(&s_free[buf], 1u);
-            }
+            if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+            ++sc;
         }
     }
-    if constexpr (!BULK) cp_async_wait<0>();
+    // the last CTA out returns the barrier counters to zero for the next launch
+    if (threadIdx.x == 0) {
+        if (take_ticket(gbar + 1) == (unsigned)G - 1u) {
+            gbar[0] = 0u;
+            gbar[1] = 0u;
+        }
+    }
 }
 
 // ---- the CUDA-core kernel (canonical layout) -------------------------------------------
@@ -696,56 +614,48 @@ vl_simt_kernel(const uint8_t *__restrict__ codes, const uint16_t *__restrict__ s
 }
 
 // ---- host side ---------------------------------------------------------------------------
-#ifndef SVD_NW
-#define SVD_NW 16
+#ifndef SVD_NWC
+#define SVD_NWC 15
 #endif
-#ifndef SVD_D1
-#define SVD_D1 5
+#ifndef SVD_MINB
+#define SVD_MINB 1
 #endif
-#ifndef SVD_MINB1
-#define SVD_MINB1 1
+#ifndef SVD_S1
+#define SVD_S1 5
 #endif
-#ifndef SVD_MULHI
-#define SVD_MULHI false
-#endif
-#ifndef SVD_ASYNC
-#define SVD_ASYNC false
-#endif
-#ifndef SVD_BULK
-#define SVD_BULK true
-#endif
-constexpr int kNW = SVD_NW;        // warps per CTA
-constexpr int kD1 = SVD_D1;        // ring depth, C <= 8
-constexpr int kD2 = 4;             // ring depth, C <= 16 / 32
-constexpr int kMinB1 = SVD_MINB1;  // CTAs per SM the C <= 8 kernel is compiled for
-constexpr bool kMulHi = SVD_MULHI;
-constexpr bool kAsyncRed = SVD_ASYNC;  // row-block reduction by the last warp (else all threads)
-constexpr bool kBulk = SVD_BULK;       // weights by bulk copies (else per-lane cp.async)
-constexpr int kMaxCtasPerSm = 2;   // the workspace holds partial slots for this many
-constexpr int kChainMax = 256;     // ops per chain launch (kernel parameters, ~16 KB)
+constexpr int kNWC1 = SVD_NWC;    // consumer warps per CTA, C <= 8 (plus one producer warp)
+constexpr int kMinB1 = SVD_MINB;  // CTAs per SM the C <= 8 kernel is compiled for
+constexpr int kS1 = SVD_S1;       // ring stages, C <= 8
+constexpr int kNWC2 = 8;          // consumer warps per CTA, C <= 16 / 32
+constexpr int kS2 = 8;            // ring stages, C <= 16
+constexpr int kS4 = 6;            // ring stages, C <= 32
+constexpr int kMaxCtasPerSm = 2;  // the workspace holds partial slots for this many
+constexpr int kChainMax = 256;    // ops per chain launch (kernel parameters, ~16 KB)
 
 static int ntiles_for(int C) { return C <= 8 ? 1 : (C <= 16 ? 2 : 4); }
 
-// Workspace: [partial slots: SMs x kMaxCtasPerSm CTAs x 2 x kPartialSlotFloats][tickets].  The
-// partial region has the same size and place for every matrix and C, so calls of any shape
-// can share one zero-filled workspace; the tickets after it are per 64-row block.
+// Workspace: [partial slots: SMs x kMaxCtasPerSm CTAs x 2 x kPartialSlotFloats]
+//            [grid-barrier counters, 256 bytes][tickets, one per 64-row block].
+// The partial region has the same size and place for every matrix and C, so calls of any
+// shape can share one zero-filled workspace; every launch returns the counters and tickets
+// to zero.
 static size_t partial_region_bytes() {
     return align_up((size_t)sm_count() * kMaxCtasPerSm * 2 * kPartialSlotFloats * sizeof(float),
                     256);
 }
+constexpr size_t kBarrierBytes = 256;
 
 size_t vl_workspace_bytes(int64_t in_f, int64_t out_f, int C) {
     (void)C;
     const NativeGeom ng = native_geom(in_f, out_f);
-    return partial_region_bytes() + align_up((size_t)ng.n_rb * sizeof(unsigned), 256);
+    return partial_region_bytes() + kBarrierBytes + align_up((size_t)ng.n_rb * sizeof(unsigned), 256);
 }
 
-template <int NT, int D, int MAXOPS>
-static cudaError_t launch_mma(const VlOps<MAXOPS> &P, void *ws, bool pdl, bool coop,
-                              int64_t max_units, cudaStream_t stream) {
-    constexpr int NW = (NT == 4 && kNW > 8) ? 8 : kNW;  // four n-tiles: partials fill smem
-    using Cfg = MmaCfg<NT, NW, D, kAsyncRed>;
-    auto kern = vl_mma_kernel<NT, NW, D, MAXOPS, (NT == 1 ? kMinB1 : 1), kMulHi, kAsyncRed, kBulk>;
+template <int NT, int NWC, int S, int MINB, int MAXOPS>
+static cudaError_t launch_ws(const VlOps<MAXOPS> &P, void *ws, bool pdl, bool coop,
+                             int64_t max_units, cudaStream_t stream) {
+    using Cfg = WsCfg<NT, NWC, S>;
+    auto kern = vl_ws_kernel<NT, NWC, S, MAXOPS, MINB>;
     static int per_sm_cache[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -754,7 +664,7 @@ static cudaError_t launch_mma(const VlOps<MAXOPS> &P, void *ws, bool pdl, bool c
     if (per_sm == 0) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
         if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NW * 32, Cfg::kSmem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, Cfg::kThreads, Cfg::kSmem);
         if (e != cudaSuccess) return e;
         per_sm = per_sm < 1 ? 1 : (per_sm > kMaxCtasPerSm ? kMaxCtasPerSm : per_sm);
         if (dev >= 0 && dev < 64) per_sm_cache[dev] = per_sm;
@@ -762,12 +672,13 @@ static cudaError_t launch_mma(const VlOps<MAXOPS> &P, void *ws, bool pdl, bool c
     int64_t G = (int64_t)sm_count() * per_sm;
     if (!coop && G > max_units) G = max_units;  // a lone op never needs idle CTAs
     if (G < 1) G = 1;
-    float *part = reinterpret_cast<float *>(ws);
-    unsigned *cnt = reinterpret_cast<unsigned *>(reinterpret_cast<uint8_t *>(ws) +
-                                                 partial_region_bytes());
+    uint8_t *base = reinterpret_cast<uint8_t *>(ws);
+    float *part = reinterpret_cast<float *>(base);
+    unsigned *gbar = reinterpret_cast<unsigned *>(base + partial_region_bytes());
+    unsigned *cnt = reinterpret_cast<unsigned *>(base + partial_region_bytes() + kBarrierBytes);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)G);
-    cfg.blockDim = dim3(NW * 32);
+    cfg.blockDim = dim3(Cfg::kThreads);
     cfg.dynamicSmemBytes = Cfg::kSmem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -782,14 +693,7 @@ static cudaError_t launch_mma(const VlOps<MAXOPS> &P, void *ws, bool pdl, bool c
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, kern, P, part, cnt);
-}
-
-template <int MAXOPS>
-static void set_shift_multipliers(VlOps<MAXOPS> &P) {
-    P.m4 = 1u << 28;
-    P.m8 = 1u << 24;
-    P.m12 = 1u << 20;
+    return cudaLaunchKernelEx(&cfg, kern, P, part, cnt, gbar);
 }
 
 static VlOp make_op(const svd_qweight *W, const void *X, float *Y) {
@@ -812,9 +716,9 @@ static cudaError_t launch_ops(const VlOps<MAXOPS> &P, void *ws, bool pdl, cudaSt
     for (int i = 0; i < P.n; ++i) max_units = P.op[i].n_units > max_units ? P.op[i].n_units : max_units;
     const bool coop = P.n > 1;
     switch (ntiles_for(P.C)) {
-        case 1: return launch_mma<1, kD1, MAXOPS>(P, ws, pdl, coop, max_units, stream);
-        case 2: return launch_mma<2, kD2, MAXOPS>(P, ws, pdl, coop, max_units, stream);
-        default: return launch_mma<4, kD2, MAXOPS>(P, ws, pdl, coop, max_units, stream);
+        case 1: return launch_ws<1, kNWC1, kS1, kMinB1, MAXOPS>(P, ws, pdl, coop, max_units, stream);
+        case 2: return launch_ws<2, kNWC2, kS2, 1, MAXOPS>(P, ws, pdl, coop, max_units, stream);
+        default: return launch_ws<4, kNWC2, kS4, 1, MAXOPS>(P, ws, pdl, coop, max_units, stream);
     }
 }
 
@@ -864,7 +768,6 @@ int verify_linear(const svd_qweight *W, const void *X, int C, float *Y, void *ws
         VlOps<1> P;
         P.n = 1;
         P.C = C;
-        set_shift_multipliers(P);
         P.op[0] = make_op(W, X, Y);
         SVD_CUDA_TRY(launch_ops(P, ws, pdl, stream));
         return SVD_OK;
@@ -894,7 +797,7 @@ size_t chain_workspace_bytes(const svd_linear_op *ops, int n_ops, int C) {
         n_rb = ng.n_rb > n_rb ? ng.n_rb : n_rb;
     }
     (void)C;
-    return partial_region_bytes() + align_up((size_t)n_rb * sizeof(unsigned), 256);
+    return partial_region_bytes() + kBarrierBytes + align_up((size_t)n_rb * sizeof(unsigned), 256);
 }
 
 int verify_chain(const svd_linear_op *ops, int n_ops, int C, void *ws, size_t ws_bytes, int flags,
@@ -918,14 +821,12 @@ int verify_chain(const svd_linear_op *ops, int n_ops, int C, void *ws, size_t ws
             VlOps<1> P1;
             P1.n = 1;
             P1.C = C;
-            set_shift_multipliers(P1);
             P1.op[0] = make_op(&ops[first].W, ops[first].X, ops[first].Y);
             SVD_CUDA_TRY(launch_ops(P1, ws, first == 0 && (flags & SVD_F_PDL), stream));
             continue;
         }
         P.n = n;
         P.C = C;
-        set_shift_multipliers(P);
         for (int i = 0; i < n; ++i) P.op[i] = make_op(&ops[first + i].W, ops[first + i].X, ops[first + i].Y);
         SVD_CUDA_TRY(launch_ops(P, ws, false, stream));
     }
@@ -987,7 +888,8 @@ constexpr int kNoAllocMaxSms = 160;
 constexpr int64_t kNoAllocMaxRowBlocks = SVD_NOALLOC_MAX_OUT_FEATURES / kRowsPerBlock;
 constexpr size_t kNoAllocPartialBytes =
     (size_t)kNoAllocMaxSms * kMaxCtasPerSm * 2 * kPartialSlotFloats * sizeof(float);
-constexpr size_t kNoAllocBytes = kNoAllocPartialBytes + kNoAllocMaxRowBlocks * sizeof(unsigned);
+constexpr size_t kNoAllocBytes =
+    kNoAllocPartialBytes + kBarrierBytes + kNoAllocMaxRowBlocks * sizeof(unsigned);
 static_assert(kNoAllocBytes <= SVD_NOALLOC_SCRATCH_BYTES, "scratch bound in svd.h");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
@@ -1021,16 +923,16 @@ int verify_linear_noalloc(const svd_qweight *W, const void *X, int C, float *Y, 
         }
         base = g_noalloc_ptr[dev];
     }
-    // Same layout as a caller workspace: partial slots, then the tickets, which must start at
-    // zero.  Every call clears them again on the stream before its kernel, so a call never
-    // depends on what the previous one left behind.
+    // Same layout as a caller workspace: partial slots, then the barrier counters and the
+    // tickets, which must start at zero.  Every call clears them again on the stream before
+    // its kernel, so a call never depends on what the previous one left behind.
     const NativeGeom ng = native_geom(W->in_features, W->out_features);
-    unsigned char *tickets = reinterpret_cast<unsigned char *>(base) + partial_region_bytes();
-    SVD_CUDA_TRY(cudaMemsetAsync(tickets, 0, (size_t)ng.n_rb * sizeof(unsigned), stream));
+    unsigned char *counters = reinterpret_cast<unsigned char *>(base) + partial_region_bytes();
+    SVD_CUDA_TRY(cudaMemsetAsync(counters, 0, kBarrierBytes + (size_t)ng.n_rb * sizeof(unsigned),
+                                 stream));
     VlOps<1> P;
     P.n = 1;
     P.C = C;
-    set_shift_multipliers(P);
     P.op[0] = make_op(W, X, Y);
     SVD_CUDA_TRY(launch_ops(P, base, (flags & SVD_F_PDL) != 0, stream));
     return SVD_OK;
