@@ -108,7 +108,7 @@ def kernel_traffic():
     """DRAM traffic per launch of the stack's verify-linear kernel from the committed ncu
     summary, if it was taken on the current kernel source (else None)."""
     src = os.path.join(ROOT, "speculative_decoding_verify_06_gb300", "csrc", "verify_linear.cu")
-    prof = os.path.join(ROOT, "profiles", "vl_mma_kernel_27b_stack_c4.txt")
+    prof = os.path.join(ROOT, "profiles", "vl_ws_kernel_27b_stack_c4.txt")
     try:
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         txt = open(prof).read()
@@ -228,7 +228,7 @@ def run_svd(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     build.build_library()
     vp = stack.VerifyPass(layers=args.layers, C=args.C, seed=rank, device=dev, pdl=not args.no_pdl,
-                          chain=not args.no_chain)
+                          chain=not args.no_chain, head=not args.stack_only)
     vp.capture()
     s = torch.cuda.current_stream(dev)
     dist = world > 1
@@ -263,20 +263,22 @@ def run_svd(args, rank, world, local_rank):
     passes_per_s = world * K / (t_max / 1000.0)
 
     # tokens per pass of this window's (p, q): 20k windows drawn from the same rows (untimed)
-    n_win = 20000
-    k, V = vp.k, vp.V
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(4242 + rank)
-    drafts = torch.multinomial(vp.q, n_win, replacement=True, generator=gen).T.contiguous().to(torch.int32)
-    p_rows = torch.arange(k + 1, device=dev, dtype=torch.int64).repeat(n_win, 1)
-    q_rows = torch.arange(k, device=dev, dtype=torch.int64).repeat(n_win, 1)
-    tok = torch.empty((n_win, k + 1), dtype=torch.int32, device=dev)
-    ne = torch.empty(n_win, dtype=torch.int32, device=dev)
-    st = torch.empty(n_win, dtype=torch.int32, device=dev)
-    svd.svd_accept(vp.probs, drafts, n_win, k, V, tok, ne, st, q=vp.q, p_rows=p_rows,
-                   q_rows=q_rows, seed=rank + 17)
-    torch.cuda.synchronize(dev)
-    tokens_per_pass = float(ne.double().mean().item())
+    tokens_per_pass = None
+    if vp.accept:
+        n_win = 20000
+        k, V = vp.k, vp.V
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(4242 + rank)
+        drafts = torch.multinomial(vp.q, n_win, replacement=True, generator=gen).T.contiguous().to(torch.int32)
+        p_rows = torch.arange(k + 1, device=dev, dtype=torch.int64).repeat(n_win, 1)
+        q_rows = torch.arange(k, device=dev, dtype=torch.int64).repeat(n_win, 1)
+        tok = torch.empty((n_win, k + 1), dtype=torch.int32, device=dev)
+        ne = torch.empty(n_win, dtype=torch.int32, device=dev)
+        st = torch.empty(n_win, dtype=torch.int32, device=dev)
+        svd.svd_accept(vp.probs, drafts, n_win, k, V, tok, ne, st, q=vp.q, p_rows=p_rows,
+                       q_rows=q_rows, seed=rank + 17)
+        torch.cuda.synchronize(dev)
+        tokens_per_pass = float(ne.double().mean().item())
 
     # end to end: inputs from pinned host memory and the result back, every step
     host_in = [t.detach().cpu().pin_memory() for t in vp.inputs()]
@@ -320,15 +322,17 @@ def run_svd(args, rank, world, local_rank):
                    "l2": "inputs larger than L2: 11.9 GB of weights streamed per step",
                    "stack_launch": ("per-matrix launches, PDL" if args.no_chain else
                                     "one persistent cooperative chain of 256 matrices"),
-                   "graph": "stack graph + tail graph per step"},
+                   "graph": "stack graph + tail graph per step",
+                   "stack_only": bool(args.stack_only)},
         "stack": {"ms": stack_ms, "passes_per_s": 1000.0 / stack_ms, "bytes": stack_bytes,
                   "gb_s": achieved, "tail_ms": tail_ms},
         "tokens_per_pass": tokens_per_pass,
-        "effective_tokens_per_s": passes_per_s * tokens_per_pass,
+        "effective_tokens_per_s": (None if tokens_per_pass is None else
+                                   passes_per_s * tokens_per_pass),
         "pass_bytes": vp.pass_bytes(),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind,
-                     "kernel": "vl_mma_kernel (the stack's 256 matrices, averaged)",
+                     "kernel": "vl_ws_kernel (one chain launch: the stack's 256 matrices)",
                      "traffic": None if traffic_pass is None else traffic_pass},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": Ke},
@@ -358,6 +362,9 @@ def main():
     ap.add_argument("--no-chain", action="store_true",
                     help="one launch per matrix (with PDL) instead of the persistent chain")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--stack-only", action="store_true",
+                    help="time the layer stack alone (no lm_head, sampler or acceptance); for "
+                         "profiling small stacks")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world = int(os.environ.get("WORLD_SIZE", "1"))
