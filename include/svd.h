@@ -132,9 +132,10 @@ int svd_unpack_weights(const svd_qweight *src_native, void *dst_codes, void *dst
  *   NATIVE weights run the tensor-core stream-K kernel (bf16 MMA, fp32 accumulate, one fresh
  *   accumulator per 32-input block, scaled in fp32).  It needs a workspace of
  *   svd_verify_linear_workspace_bytes() bytes that is ZERO-FILLED before its first use (it
- *   holds per-row-block ticket counters, which every call returns to zero, and partial sums),
- *   so one zeroed workspace serves any number of calls issued in stream order; calls that may
- *   run concurrently need separate workspaces.
+ *   holds barrier counters, which every call returns to zero, a launch counter, and partial
+ *   sums of row blocks split between CTAs, tagged with the launch that wrote them), so one
+ *   zeroed workspace serves any number of calls issued in stream order, for any matrix shape
+ *   and C; calls that may run concurrently need separate workspaces.
  *   CANONICAL weights run the CUDA-core warp-shuffle kernel (no workspace; needs
  *   C * in * 4 <= 196608 bytes, else SVD_ERR_UNSUPPORTED).
  *   The result is deterministic: the same inputs give the same bits on every call. */
@@ -170,14 +171,15 @@ int svd_verify_chain(const svd_linear_op *ops, int n_ops, int C, void *workspace
  * implicit synchronisation is not allowed, or in plugins that are handed only the tensors they
  * read and write.  svd_verify_linear_noalloc computes exactly what svd_verify_linear computes
  * for a NATIVE matrix, with the same arguments minus the workspace: its scratch (stream-K
- * partial sums and per-row-block tickets) is a fixed array of SVD_NOALLOC_SCRATCH_BYTES in the
+ * partial sums and barrier words) is a fixed array of SVD_NOALLOC_SCRATCH_BYTES in the
  * library's own device memory, reserved on every GPU that loads the library until the
  * process exits.  It calls no allocator of any kind.
  *   - out_features <= SVD_NOALLOC_MAX_OUT_FEATURES and at most 160 SMs, else
  *     SVD_ERR_UNSUPPORTED (other limits as for svd_verify_linear).
  *   - The first call on each device looks up the array's device address (with that device
  *     current); make that first call before any stream capture.
- *   - Every call clears the tickets with a memset on `stream` and then launches the kernel.
+ *   - Every call clears the barrier counters with a memset on `stream` and then launches the
+ *     kernel.
  *     All calls share the one array, so calls that may overlap on the GPU (different streams
  *     without ordering between them) race and give wrong results; issue them in one stream or
  *     order them with events. */

@@ -9,20 +9,19 @@
 //     Y[c][j] = sum_b s[j][b] * sum_{i in block b} (code[j][i] - 8) * X[c][i]
 //
 // Two kernels:
-//  * vl_ws_kernel (NATIVE layout) -- a persistent, warp-specialised stream-K kernel over
-//    (64-row block, 64-input chunk) units.  A producer warp moves each CTA's units, stage by
-//    stage (codes and scales of 15 consecutive units, two bulk copies completing on an
-//    mbarrier), into a ring in shared memory and never waits on anything but a free stage.
-//    Fifteen consumer warps dequantise nibbles straight into bf16 A fragments with one lop3
-//    and one bf16x2 subtract per pair (value 128 + c built from the exponent pattern 0x4300,
-//    then minus 136 gives c - 8 exactly), and run mma.sync m16n8k16 (bf16 in, fp32
+//  * vl_stream_kernel (NATIVE layout) -- a persistent stream-K kernel over (64-row block,
+//    64-input chunk) units.  Each CTA's units arrive stage by stage (the codes and scales of
+//    16 consecutive units, two bulk copies completing on an mbarrier) through a ring in
+//    shared memory; the warp that frees a stage last issues its refill, so there is no
+//    producer warp.  Every warp dequantises nibbles straight into bf16 A fragments with one
+//    lop3 and one bf16x2 subtract per pair (value 128 + c built from the exponent pattern
+//    0x4300, then minus 136 gives c - 8 exactly) and runs mma.sync m16n8k16 (bf16 in, fp32
 //    accumulate) against the activations as the B operand.  Every 32-input block gets a
 //    fresh accumulator that is scaled by its fp16 scale in fp32, so the only rounding is fp32
-//    accumulation.  Partial row blocks at the edges of a CTA's range are finished by the last
-//    CTA to arrive (an atomic ticket per row block, partials summed in CTA order:
-//    deterministic, no spinning).  A chain of matrices runs in one cooperative launch with a
-//    barrier among the consumer warps between matrices; the producer keeps streaming the
-//    next matrix's weights through it.
+//    accumulation.  A row block split between CTAs is finished by the CTA holding its first
+//    unit, from tagged partials the others store without waiting (summed in CTA order:
+//    deterministic).  A chain of matrices runs in one cooperative launch with a grid barrier
+//    between matrices; the weights of the next matrix keep streaming through it.
 //  * vl_simt_kernel (CANONICAL layout) -- the plain CUDA-core version: one warp per output
 //    row, each lane one 32-input block at a time, fp32 FMAs, warp-shuffle reduction.
 #include <cooperative_groups.h>
@@ -220,7 +219,8 @@ struct VlOp {
     const uint8_t *scales;
     const __nv_bfloat16 *X;
     float *Y;
-    int64_t in_f, out_f, n_kc, n_units;
+    int64_t in_f, out_f;
+    uint32_t n_kc, n_units;  // n_units * (CTAs + 1) < 2^32 (checked on the host)
 };
 
 template <int MAXOPS>
@@ -230,49 +230,66 @@ struct VlOps {
     VlOp op[MAXOPS];
 };
 
-// The units of an op are split into G_op = min(G, n_units) contiguous CTA ranges
-// [b n / G_op, (b+1) n / G_op); every CTA below G_op owns at least one unit.
-// owner_cta(n) is the CTA whose range holds unit n.
-__device__ __forceinline__ int64_t owner_cta(int64_t n, int64_t Gop, int64_t n_units) {
-    return ((n + 1) * Gop - 1) / n_units;
-}
-
 // ---- the tensor-core stream-K kernel ---------------------------------------------------
-constexpr int kPartialSlotFloats = 32 * kTiles * 4 * 4;  // largest warp partial (4 n-tiles)
+// Every warp is an independent stream-K worker.  The units of an op (64-row block x 64-input
+// chunk, row-block-major) are split into W_op = min(G * NW, n_units) contiguous ranges, one
+// per worker (warp w of CTA b is worker b * NW + w), so the shares differ by one unit at
+// most.  Each warp streams its own units through its own ring of R slots in shared memory:
+// its lane 0 issues the two bulk copies of a unit (codes, scales) R units ahead, completing
+// on the slot's mbarrier, and refills a slot as soon as the warp has read it, so no warp
+// waits for another while it computes.  A warp's unit sequence runs across op boundaries:
+// the weights of op i+1 are in flight while op i finishes.
+//
+// A 64-row block the warp covers whole goes straight to Y.  The partial blocks at the two
+// ends of its range are parked in shared memory, and when all warps of the CTA are done
+// with the op they are added block by block in worker order.  A block whose first unit lies
+// in this CTA is finished here (the CTA is its OWNER; if the block runs on into later CTAs,
+// their partials are added in CTA order); otherwise the CTA stores its partial -- each value
+// paired with a tag naming the launch and the op in one 64-bit store -- and moves on, and
+// the owner waits for the tags.  No tickets, no fences and a fixed summation order: the
+// result is deterministic.  Ops of a chain are separated by a barrier among all CTAs
+// (cooperative launch); op 0 waits for the preceding kernel with griddepcontrol.wait before
+// touching activations or the workspace.
+constexpr int kPartialMax = 32 * kTiles * 4 * 4;  // entries of the largest partial (NT = 4)
 
-// ---- the warp-specialised tensor-core stream-K kernel ------------------------------------
-// CTA = NWC consumer warps + 1 producer warp.  The producer's lane 0 walks the CTA's units of
-// every op (in op order) in stages of NWC consecutive units -- one contiguous byte range of
-// codes and one of scales, moved by two bulk copies -- into a ring of S stages, waiting only
-// for a stage to be released.  It never takes part in a barrier, so weights keep streaming
-// while the consumers synchronise.  Consumer warp w takes unit w of every stage: warps
-// interleave the chunks of a 64-row block; at the end of a block the CTA's consumers combine
-// their partials in shared memory (named barrier), and a block split between CTAs is finished
-// by the last CTA to arrive (a ticket per block; partials summed in CTA order).  Ops of a
-// chain are separated by a barrier among the consumer warps of all CTAs (cooperative launch);
-// op 0 waits for the preceding kernel with griddepcontrol.wait before touching activations.
-template <int NT, int NWC, int S>
-struct WsCfg {
-    static constexpr int kAcc = kTiles * NT * 4;    // fp32 accumulators per lane
-    static constexpr int kPartial = 32 * kAcc;      // floats per warp partial
-    static constexpr int kPer = (kPartial + NWC * 32 - 1) / (NWC * 32);
-    static constexpr int kStage = NWC * kUnitBytes;
-    static constexpr size_t kRing = (size_t)S * kStage;
-    static constexpr size_t kSmem = kRing + (size_t)NWC * kPartial * sizeof(float);
-    static constexpr int kThreads = (NWC + 1) * 32;
+template <int NT, int NW, int R, int MAXOPS>
+struct VlCfg {
+    static constexpr int kThreads = NW * 32;
+    static constexpr int kAcc = kTiles * NT * 4;  // fp32 accumulators per lane
+    static constexpr int kPartial = 32 * kAcc;    // entries of a warp's (or a CTA's) partial
+    static constexpr int kPer = (kPartial + kThreads - 1) / kThreads;
+    static constexpr size_t kRing = (size_t)NW * R * kUnitBytes;
+    static constexpr size_t kPark = (size_t)NW * 2 * kPartial * sizeof(float);
+    static constexpr size_t kSmem = kRing + kPark + (size_t)MAXOPS * sizeof(VlOp);
+    static_assert(kPartial <= kPartialMax, "partial slot size");
+    static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
 };
 
-__device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mbar) : "memory");
+// Tagged partial entries: the value's bits in the low word, the tag in the high word.  The
+// 64-bit store and load are single-copy atomic, so a matching tag guarantees the value.
+__device__ __forceinline__ void st_tagged(unsigned long long *p, float v, uint32_t tag) {
+    const unsigned long long w = ((unsigned long long)tag << 32) | __float_as_uint(v);
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
 }
-__device__ __forceinline__ void consumers_sync(int nthreads) {
-    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+__device__ __forceinline__ unsigned long long ld_tagged(const unsigned long long *p) {
+    unsigned long long w;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+    return w;
+}
+// Waits (bounded) for an entry carrying `tag` and returns its value.
+__device__ __forceinline__ float wait_tagged(const unsigned long long *p, uint32_t tag) {
+    unsigned long long w = ld_tagged(p);
+    for (int it = 0; (uint32_t)(w >> 32) != tag && it < (1 << 22); ++it) {
+        if (it > 64) __nanosleep(64);
+        w = ld_tagged(p);
+    }
+    return __uint_as_float((uint32_t)w);
 }
 
-// The gi-th barrier of a launch among the consumers of all G CTAs: one release-add per CTA
-// (after a CTA barrier, so it publishes every consumer's writes) on a counter in the
-// workspace, then acquire polling until the counter reaches gi * G.  Polling is bounded.
-__device__ __forceinline__ void consumer_grid_barrier(unsigned *gbar, unsigned target) {
+// The gi-th barrier of a launch among all G CTAs: one release-add per CTA (after a CTA
+// barrier, so it publishes every warp's writes) on a counter in the workspace, then acquire
+// polling until the counter reaches gi * G.  Polling is bounded.
+__device__ __forceinline__ void grid_barrier(unsigned *gbar, unsigned target) {
     asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(gbar) : "memory");
     for (int it = 0; it < (1 << 26); ++it) {
         unsigned v;
@@ -281,71 +298,108 @@ __device__ __forceinline__ void consumer_grid_barrier(unsigned *gbar, unsigned t
         if (it > 512) __nanosleep(32);
     }
 }
-
-// Ticket of a split row block: release this CTA's partial (written by all consumers before a
-// CTA barrier), take the ticket with acquire so that the last CTA sees every other partial.
-__device__ __forceinline__ unsigned take_ticket(unsigned *cnt) {
+__device__ __forceinline__ unsigned atom_add_acqrel_gpu(unsigned *p, unsigned v) {
     unsigned old;
-    asm volatile("fence.acq_rel.gpu;" ::: "memory");
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(cnt) : "memory");
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
     return old;
 }
+// Workspace words after the partial slots: [0] grid-barrier counter, [1] exit counter (both
+// returned to zero by the last CTA out), [2] launch epoch (advanced by the last CTA out).
+constexpr int kBarCount = 0, kBarExit = 1, kBarEpoch = 2;
 
-template <int NT, int NWC, int S, int MAXOPS, int MINB>
-__global__ void __launch_bounds__((NWC + 1) * 32, MINB)
-vl_ws_kernel(const __grid_constant__ VlOps<MAXOPS> P, float *__restrict__ ws_part,
-             unsigned int *__restrict__ ws_cnt, unsigned int *__restrict__ gbar) {
-    using Cfg = WsCfg<NT, NWC, S>;
+#ifndef SVD_PROBE
+#define SVD_PROBE(gi, what)  // timing hook for instrumented builds; nothing by default
+#endif
+
+template <int NT, int NW, int R, int MAXOPS>
+__global__ void __launch_bounds__(NW * 32, 1)
+vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__restrict__ part,
+                 unsigned *__restrict__ gbar) {
+    using Cfg = VlCfg<NT, NW, R, MAXOPS>;
     constexpr int kAcc = Cfg::kAcc, kPartial = Cfg::kPartial, kPer = Cfg::kPer;
-    constexpr int kCons = NWC * 32;
+    constexpr int kThreads = Cfg::kThreads;
+    constexpr uint32_t kNone = 0xFFFFFFFFu;
     extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ __align__(8) uint64_t s_full[S], s_empty[S];
-    __shared__ unsigned s_flag;
-    float *red = reinterpret_cast<float *>(smem + Cfg::kRing);
+    __shared__ __align__(8) uint64_t s_full[NW * R];
+    __shared__ uint32_t s_park_rb[NW * 2];    // row block of a parked partial, kNone if none
+    __shared__ uint32_t s_park_head[NW * 2];  // 1 if that partial starts at its block's start
+    __shared__ uint32_t s_epoch;
+    float *park = reinterpret_cast<float *>(smem + Cfg::kRing);
+    // The op descriptors live in shared memory: read from the parameter space with a
+    // run-time index they would go through the small constant cache on every access.
+    VlOp *ops = reinterpret_cast<VlOp *>(smem + Cfg::kRing + Cfg::kPark);
+    const int n_ops = P.n;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t G = gridDim.x, b = blockIdx.x;
-    const uint32_t full0 = smem_u32(&s_full[0]), empty0 = smem_u32(&s_empty[0]);
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < S; ++i) {
-            mbar_init(full0 + 8 * i, 1);
-            mbar_init(empty0 + 8 * i, NWC);
+    const uint32_t G = gridDim.x, b = blockIdx.x;
+    const uint32_t Wtot = G * NW, gw = b * NW + warp;
+    const uint32_t full0 = smem_u32(&s_full[warp * R]);
+    const uint32_t ring0 = smem_u32(smem + (size_t)warp * R * kUnitBytes);
+
+    // This worker's unit range of an op: [lo, hi), empty when the op has fewer units than
+    // there are workers and this one is not needed.
+    auto range = [&](const VlOp &o, uint32_t *lo, uint32_t *hi) {
+        const uint32_t Wop = min(Wtot, o.n_units);
+        if (gw < Wop) {
+            *lo = gw * o.n_units / Wop;
+            *hi = (gw + 1) * o.n_units / Wop;
+        } else {
+            *lo = *hi = 0u;
         }
+    };
+    // The CTA whose workers hold unit n of an op.
+    auto cta_of = [&](const VlOp &o, uint32_t n) {
+        const uint32_t Wop = min(Wtot, o.n_units);
+        return (((n + 1) * Wop - 1) / o.n_units) / NW;
+    };
+
+    {
+        static_assert(sizeof(VlOp) % 8 == 0, "op descriptor copied in 8-byte words");
+        const uint64_t *src = reinterpret_cast<const uint64_t *>(&P.op[0]);
+        uint64_t *dst = reinterpret_cast<uint64_t *>(ops);
+        for (int i = threadIdx.x; i < n_ops * (int)(sizeof(VlOp) / 8); i += kThreads) dst[i] = src[i];
+    }
+    if (lane == 0) {
+        for (int i = 0; i < R; ++i) mbar_init(full0 + 8 * i, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
 
-    if (warp == NWC) {
-        // ---- producer: weights never depend on earlier kernels or ops -----------------------
-        if (lane == 0) {
-            uint32_t sc = 0;
-            for (int gi = 0; gi < P.n; ++gi) {
-                const VlOp &o = P.op[gi];
-                const int64_t Gop = min(G, o.n_units);
-                if (b >= Gop) continue;
-                const int64_t st = b * o.n_units / Gop, en = (b + 1) * o.n_units / Gop;
-                for (int64_t u0 = st; u0 < en; u0 += NWC, ++sc) {
-                    const uint32_t slot = sc % S, round = sc / S;
-                    if (round > 0) mbar_wait(empty0 + 8 * slot, (round - 1) & 1u);
-                    const uint32_t n = (uint32_t)min((int64_t)NWC, en - u0);
-                    const uint32_t dst = smem_u32(smem + (size_t)slot * Cfg::kStage);
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    mbar_expect_tx(full0 + 8 * slot, n * kUnitBytes);
-                    bulk_g2s(dst, o.codes + u0 * kUnitCodeBytes, n * kUnitCodeBytes, full0 + 8 * slot);
-                    bulk_g2s(dst + NWC * kUnitCodeBytes, o.scales + u0 * kUnitScaleBytes,
-                             n * kUnitScaleBytes, full0 + 8 * slot);
+    // Issue cursor of this warp (uniform across its lanes; lane 0 issues): the next unit to
+    // load is unit c_u of op c_op, c_hi ends that op's range; c_issued counts issued units.
+    int c_op = 0;
+    uint32_t c_u = 0, c_hi = 0, c_issued = 0;
+    if (n_ops > 0) range(ops[0], &c_u, &c_hi);
+    auto issue = [&]() {
+        while (c_op < n_ops) {
+            if (c_u < c_hi) {
+                const VlOp &o = ops[c_op];
+                const uint32_t slot = c_issued % R;
+                if (lane == 0) {
+                    const uint32_t bar = full0 + 8 * slot, dst = ring0 + slot * kUnitBytes;
+                    mbar_expect_tx(bar, kUnitBytes);
+                    bulk_g2s(dst, o.codes + (size_t)c_u * kUnitCodeBytes, kUnitCodeBytes, bar);
+                    bulk_g2s(dst + kUnitCodeBytes, o.scales + (size_t)c_u * kUnitScaleBytes,
+                             kUnitScaleBytes, bar);
                 }
+                ++c_u;
+                ++c_issued;
+                return;
             }
+            if (++c_op < n_ops) range(ops[c_op], &c_u, &c_hi);
         }
-        return;
-    }
+    };
+    // weights never depend on earlier kernels: start streaming before waiting for them
+    for (int i = 0; i < R; ++i) issue();
 
-    // ---- consumers -------------------------------------------------------------------------
-    const int g4 = lane >> 2, t4 = lane & 3;
-    const int C = P.C;
     griddep_wait();
     griddep_launch_dependents();
+    if (threadIdx.x == 0) s_epoch = *reinterpret_cast<volatile unsigned *>(gbar + kBarEpoch);
+    __syncthreads();
+    const uint32_t epoch = s_epoch;
 
+    const int g4 = lane >> 2, t4 = lane & 3;
+    const int C = P.C;
     float acc[kTiles][NT][4];
 #pragma unroll
     for (int r = 0; r < kTiles; ++r)
@@ -354,69 +408,73 @@ vl_ws_kernel(const __grid_constant__ VlOps<MAXOPS> P, float *__restrict__ ws_par
 #pragma unroll
             for (int q = 0; q < 4; ++q) acc[r][nt][q] = 0.f;
 
-    uint32_t sc = 0;  // stage counter, in step with the producer's
-    for (int gi = 0; gi < P.n; ++gi) {
-        const VlOp &o = P.op[gi];
+    uint32_t c_used = 0;  // units this warp has consumed (its ring position)
+    for (int gi = 0; gi < n_ops; ++gi) {
+        const VlOp &o = ops[gi];
         if (gi > 0) {
-            consumers_sync(kCons);
-            if (threadIdx.x == 0) consumer_grid_barrier(gbar, (unsigned)gi * (unsigned)G);
-            consumers_sync(kCons);
+            __syncthreads();
+            if (threadIdx.x == 0) grid_barrier(gbar + kBarCount, (unsigned)gi * G);
+            __syncthreads();
         }
-        const int64_t Gop = min(G, o.n_units);
-        if (b >= Gop) continue;
-        const int64_t n_kc = o.n_kc, n_units = o.n_units, in_f = o.in_f, out_f = o.out_f;
-        const int64_t start = b * n_units / Gop, end = (b + 1) * n_units / Gop;
-        const int64_t span = end - start;
-        const int J = span > warp ? (int)((span - warp + NWC - 1) / NWC) : 0;
-        const int nstages = (int)((span + NWC - 1) / NWC);
+        SVD_PROBE(gi, 0);
+        const uint32_t n_kc = o.n_kc;
+        const int64_t in_f = o.in_f, out_f = o.out_f;
+        const uint32_t tag = ~((epoch << 8) | (uint32_t)(gi & 255));
+        // (row, column) of entry e of a partial: lane e / kAcc's accumulator e % kAcc
+        auto coords = [&](int e, uint32_t rb, int64_t *row, int *col) {
+            const int lsrc = e / kAcc, idx = e % kAcc, q = idx & 3, rn = idx >> 2;
+            const int r = rn / NT, nt = rn % NT;
+            *row = (int64_t)rb * kRowsPerBlock + 16 * r + (lsrc >> 2) + ((q >> 1) ? 8 : 0);
+            *col = nt * 8 + (lsrc & 3) * 2 + (q & 1);
+        };
+        if (lane < 2) {
+            s_park_rb[warp * 2 + lane] = kNone;
+            s_park_head[warp * 2 + lane] = 0u;
+        }
 
-        const __nv_bfloat16 *xrow[NT];
-        bool xok[NT];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int col = nt * 8 + g4;
-            xok[nt] = col < C;
-            xrow[nt] = o.X + (int64_t)(xok[nt] ? col : 0) * in_f + t4 * 8;
-        }
-        const bool tail32 = (in_f & 63) != 0;  // the last chunk holds a single 32-input block
-        auto load_x = [&](int64_t kc, uint4 (&xr)[NT][2]) {
-            const bool lastc = tail32 && (kc == n_kc - 1);
+        uint32_t lo, hi;
+        range(o, &lo, &hi);
+        if (lo < hi) {
+            const __nv_bfloat16 *xrow[NT];
+            bool xok[NT];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                const __nv_bfloat16 *src = xrow[nt] + kc * kChunk;
-                if constexpr (MAXOPS > 1) {
-                    xr[nt][0] = xok[nt] ? ldg_cg_v4(src) : make_uint4(0u, 0u, 0u, 0u);
-                    xr[nt][1] = (xok[nt] && !lastc) ? ldg_cg_v4(src + 32) : make_uint4(0u, 0u, 0u, 0u);
-                } else {
-                    xr[nt][0] = xok[nt] ? ldg_nc_v4(src) : make_uint4(0u, 0u, 0u, 0u);
-                    xr[nt][1] = (xok[nt] && !lastc) ? ldg_nc_v4(src + 32) : make_uint4(0u, 0u, 0u, 0u);
-                }
+                const int col = nt * 8 + g4;
+                xok[nt] = col < C;
+                xrow[nt] = o.X + (int64_t)(xok[nt] ? col : 0) * in_f + t4 * 8;
             }
-        };
+            const bool tail32 = (in_f & 63) != 0;  // the last chunk holds one 32-input block
+            auto load_x = [&](uint32_t kc, uint4 (&xr)[NT][2]) {
+                const bool lastc = tail32 && (kc == n_kc - 1);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const __nv_bfloat16 *src = xrow[nt] + (size_t)kc * kChunk;
+                    if constexpr (MAXOPS > 1) {
+                        xr[nt][0] = xok[nt] ? ldg_cg_v4(src) : make_uint4(0u, 0u, 0u, 0u);
+                        xr[nt][1] = (xok[nt] && !lastc) ? ldg_cg_v4(src + 32) : make_uint4(0u, 0u, 0u, 0u);
+                    } else {
+                        xr[nt][0] = xok[nt] ? ldg_nc_v4(src) : make_uint4(0u, 0u, 0u, 0u);
+                        xr[nt][1] = (xok[nt] && !lastc) ? ldg_nc_v4(src + 32) : make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+            };
 
-        int64_t u = start + warp;
-        int64_t kc = u % n_kc;
-        uint4 xr[NT][2];
-        if (J > 0) load_x(kc, xr);
-        int j = 0;
-        const int64_t rb_first = start / n_kc, rb_last = (end - 1) / n_kc;
-        for (int64_t rb = rb_first; rb <= rb_last; ++rb) {
-            const int64_t seg_lo = max(start, rb * n_kc), seg_hi = min(end, (rb + 1) * n_kc);
-            while (j < J && u < seg_hi) {
-                const uint32_t slot = sc % S;
-                mbar_wait(full0 + 8 * slot, (sc / S) & 1u);
+            uint32_t kc = lo % n_kc, rb = lo / n_kc, seg_lo = lo;
+            uint4 xr[NT][2];
+            load_x(kc, xr);
+            for (uint32_t u = lo; u < hi; ++u) {
+                const uint32_t slot = c_used % R;
+                mbar_wait(full0 + 8 * slot, (c_used / R) & 1u);
                 uint4 xc[NT][2];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     xc[nt][0] = xr[nt][0];
                     xc[nt][1] = xr[nt][1];
                 }
-                int64_t kn = kc + NWC;
-                while (kn >= n_kc) kn -= n_kc;
-                if (j + 1 < J) load_x(kn, xr);
-                const uint8_t *cbase = smem + (size_t)slot * Cfg::kStage + warp * kUnitCodeBytes;
-                const uint8_t *sbase =
-                    smem + (size_t)slot * Cfg::kStage + NWC * kUnitCodeBytes + warp * kUnitScaleBytes;
+                const uint32_t kn = (kc + 1 == n_kc) ? 0u : kc + 1;
+                if (u + 1 < hi) load_x(kn, xr);
+                const uint8_t *cbase = smem + (size_t)(warp * R + slot) * kUnitBytes;
+                const uint8_t *sbase = cbase + kUnitCodeBytes;
 #pragma unroll
                 for (int r = 0; r < kTiles; ++r) {
                     const uint4 cw = *reinterpret_cast<const uint4 *>(cbase + r * 512 + lane * 16);
@@ -441,116 +499,100 @@ vl_ws_kernel(const __grid_constant__ VlOps<MAXOPS> P, float *__restrict__ ws_par
                         }
                     }
                 }
-                __syncwarp();  // every lane has read the stage
-                if (lane == 0) mbar_arrive(empty0 + 8 * slot);
-                ++sc;
-                ++j;
-                u += NWC;
+                // the slot is read: refill it with the unit R places further on
+                __syncwarp();
+                if (lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue();
+                ++c_used;
+
+                // end of a segment (a row block's end, or the range's): a whole block goes
+                // to Y, a partial one is parked
+                const bool rb_end = kc + 1 == n_kc;
+                if (rb_end || u + 1 == hi) {
+                    const bool head = seg_lo == rb * n_kc;
+                    if (head && rb_end) {
+#pragma unroll
+                        for (int r = 0; r < kTiles; ++r)
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) {
+                                    int64_t row;
+                                    int col;
+                                    coords(lane * kAcc + (r * NT + nt) * 4 + q, rb, &row, &col);
+                                    if (row < out_f && col < C) o.Y[(int64_t)col * out_f + row] = acc[r][nt][q];
+                                }
+                    } else {
+                        const int k = seg_lo == lo ? 0 : 1;
+                        float4 *dst = reinterpret_cast<float4 *>(park + (warp * 2 + k) * kPartial + lane * kAcc);
+#pragma unroll
+                        for (int r = 0; r < kTiles; ++r)
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt)
+                                dst[r * NT + nt] = make_float4(acc[r][nt][0], acc[r][nt][1],
+                                                               acc[r][nt][2], acc[r][nt][3]);
+                        if (lane == 0) {
+                            s_park_rb[warp * 2 + k] = rb;
+                            s_park_head[warp * 2 + k] = head ? 1u : 0u;
+                        }
+                    }
+#pragma unroll
+                    for (int r = 0; r < kTiles; ++r)
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) acc[r][nt][q] = 0.f;
+                    seg_lo = u + 1;
+                    rb += rb_end ? 1u : 0u;
+                }
                 kc = kn;
             }
+        }
+        SVD_PROBE(gi, 1);
 
-            // ---- row block rb is finished by this CTA: combine the consumer warps' partials
-            {
-                float4 *dst = reinterpret_cast<float4 *>(red + warp * kPartial + lane * kAcc);
-#pragma unroll
-                for (int r = 0; r < kTiles; ++r)
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        dst[r * NT + nt] = make_float4(acc[r][nt][0], acc[r][nt][1],
-                                                       acc[r][nt][2], acc[r][nt][3]);
-                        acc[r][nt][0] = acc[r][nt][1] = acc[r][nt][2] = acc[r][nt][3] = 0.f;
-                    }
-            }
-            consumers_sync(kCons);
-            float vals[kPer];
+        // ---- all warps are done with the op: add the parked partials block by block, in
+        // worker order (slot 0 before slot 1 within a warp)
+        __syncthreads();
+        int p = 0;
+        while (true) {
+            while (p < 2 * NW && s_park_rb[p] == kNone) ++p;
+            if (p >= 2 * NW) break;
+            const uint32_t rb = s_park_rb[p];
+            const bool owner = s_park_head[p] != 0u;
+            int q = p + 1;
+            while (q < 2 * NW && (s_park_rb[q] == kNone || s_park_rb[q] == rb)) ++q;
+            // parked partials p..q-1 (the ones holding rb) form this block's CTA partial
+            const uint32_t b_last = owner ? cta_of(o, (rb + 1) * n_kc - 1) : b;
 #pragma unroll
             for (int m = 0; m < kPer; ++m) {
-                const int e = threadIdx.x + m * kCons;
+                const int e = threadIdx.x + m * kThreads;
+                if (e >= kPartial) break;
+                int64_t row;
+                int col;
+                coords(e, rb, &row, &col);
+                if (row >= out_f || col >= C) continue;
                 float v = 0.f;
-                if (e < kPartial) {
-#pragma unroll
-                    for (int w = 0; w < NWC; ++w) v += red[w * kPartial + e];
-                }
-                vals[m] = v;
-            }
-            auto coords = [&](int e, int64_t *row, int *col) {
-                const int lsrc = e / kAcc, idx = e % kAcc, q = idx & 3, rn = idx >> 2;
-                const int r = rn / NT, nt = rn % NT;
-                *row = rb * kRowsPerBlock + 16 * r + (lsrc >> 2) + ((q >> 1) ? 8 : 0);
-                *col = nt * 8 + (lsrc & 3) * 2 + (q & 1);
-            };
-            const bool full = (seg_lo == rb * n_kc) && (seg_hi == (rb + 1) * n_kc);
-            if (full) {
-#pragma unroll
-                for (int m = 0; m < kPer; ++m) {
-                    const int e = threadIdx.x + m * kCons;
-                    if (e >= kPartial) break;
-                    int64_t row;
-                    int col;
-                    coords(e, &row, &col);
-                    if (row < out_f && col < C) o.Y[(int64_t)col * out_f + row] = vals[m];
-                }
-            } else {
-                // Stream-K fix-up: publish this CTA's partial, take a ticket; the last CTA of
-                // the row block sums every partial in CTA order and resets the ticket.
-                const int slot_id = (rb == rb_first) ? 0 : 1;
-                float *mine = ws_part + (b * 2 + slot_id) * (int64_t)kPartialSlotFloats;
-#pragma unroll
-                for (int m = 0; m < kPer; ++m)
-                    if (threadIdx.x + m * kCons < kPartial) mine[threadIdx.x + m * kCons] = vals[m];
-                consumers_sync(kCons);
-                const int64_t b_first = owner_cta(rb * n_kc, Gop, n_units);
-                const int64_t b_last = owner_cta((rb + 1) * n_kc - 1, Gop, n_units);
-                if (threadIdx.x == 0) {
-                    const unsigned old = take_ticket(ws_cnt + rb);
-                    s_flag = (old == (unsigned)(b_last - b_first)) ? 1u : 0u;
-                }
-                consumers_sync(kCons);
-                if (s_flag) {
-                    auto part = [&](int64_t bb, int e) {
-                        const int64_t bb_first_rb = (bb * n_units / Gop) / n_kc;
-                        const int sid = (rb == bb_first_rb) ? 0 : 1;
-                        return __ldcg(ws_part + (bb * 2 + sid) * (int64_t)kPartialSlotFloats + e);
-                    };
-#pragma unroll
-                    for (int m = 0; m < kPer; ++m) {
-                        const int e = threadIdx.x + m * kCons;
-                        if (e >= kPartial) break;
-                        float v = 0.f;
-                        int64_t bb = b_first;
-                        for (; bb + 3 <= b_last; bb += 4) {  // four loads in flight, summed in order
-                            const float p0 = part(bb, e), p1 = part(bb + 1, e);
-                            const float p2 = part(bb + 2, e), p3 = part(bb + 3, e);
-                            v += p0;
-                            v += p1;
-                            v += p2;
-                            v += p3;
-                        }
-                        for (; bb <= b_last; ++bb) v += part(bb, e);
-                        int64_t row;
-                        int col;
-                        coords(e, &row, &col);
-                        if (row < out_f && col < C) o.Y[(int64_t)col * out_f + row] = v;
-                    }
-                    if (threadIdx.x == 0) ws_cnt[rb] = 0u;
+                for (int t = p; t < q; ++t)
+                    if (s_park_rb[t] == rb) v += park[t * kPartial + e];
+                if (owner) {
+                    for (uint32_t bb = b + 1; bb <= b_last; ++bb)
+                        v += wait_tagged(part + (size_t)bb * kPartialMax + e, tag);
+                    o.Y[(int64_t)col * out_f + row] = v;
+                } else {
+                    st_tagged(part + (size_t)b * kPartialMax + e, v, tag);
                 }
             }
-            consumers_sync(kCons);  // red and s_flag are free again
+            p = q;
         }
-        // stages of this op that hold no unit of this warp: release them in order
-        for (int k = J; k < nstages; ++k) {
-            const uint32_t slot = sc % S;
-            mbar_wait(full0 + 8 * slot, (sc / S) & 1u);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty0 + 8 * slot);
-            ++sc;
-        }
+        SVD_PROBE(gi, 2);
     }
-    // the last CTA out returns the barrier counters to zero for the next launch
+    // the last CTA out returns the barrier counters to zero and advances the epoch
+    __syncthreads();
     if (threadIdx.x == 0) {
-        if (take_ticket(gbar + 1) == (unsigned)G - 1u) {
-            gbar[0] = 0u;
-            gbar[1] = 0u;
+        if (atom_add_acqrel_gpu(gbar + kBarExit, 1u) == G - 1u) {
+            gbar[kBarCount] = 0u;
+            gbar[kBarExit] = 0u;
+            gbar[kBarEpoch] = epoch + 1u;
         }
     }
 }
@@ -614,48 +656,45 @@ vl_simt_kernel(const uint8_t *__restrict__ codes, const uint16_t *__restrict__ s
 }
 
 // ---- host side ---------------------------------------------------------------------------
-#ifndef SVD_NWC
-#define SVD_NWC 15
+#ifndef SVD_NW1
+#define SVD_NW1 16
 #endif
-#ifndef SVD_MINB
-#define SVD_MINB 1
+#ifndef SVD_R1
+#define SVD_R1 4
 #endif
-#ifndef SVD_S1
-#define SVD_S1 5
-#endif
-constexpr int kNWC1 = SVD_NWC;    // consumer warps per CTA, C <= 8 (plus one producer warp)
-constexpr int kMinB1 = SVD_MINB;  // CTAs per SM the C <= 8 kernel is compiled for
-constexpr int kS1 = SVD_S1;       // ring stages, C <= 8
-constexpr int kNWC2 = 8;          // consumer warps per CTA, C <= 16 / 32
-constexpr int kS2 = 8;            // ring stages, C <= 16
-constexpr int kS4 = 6;            // ring stages, C <= 32
+constexpr int kNW1 = SVD_NW1;     // warps per CTA, C <= 8
+constexpr int kR1 = SVD_R1;       // ring slots per warp, C <= 8
+constexpr int kNW2 = 8;           // warps per CTA, C <= 16 and C <= 32
+constexpr int kR2 = 8;            // ring slots per warp, C <= 16
+constexpr int kR4 = 4;            // ring slots per warp, C <= 32
 constexpr int kMaxCtasPerSm = 2;  // the workspace holds partial slots for this many
 constexpr int kChainMax = 256;    // ops per chain launch (kernel parameters, ~16 KB)
 
 static int ntiles_for(int C) { return C <= 8 ? 1 : (C <= 16 ? 2 : 4); }
 
-// Workspace: [partial slots: SMs x kMaxCtasPerSm CTAs x 2 x kPartialSlotFloats]
-//            [grid-barrier counters, 256 bytes][tickets, one per 64-row block].
-// The partial region has the same size and place for every matrix and C, so calls of any
-// shape can share one zero-filled workspace; every launch returns the counters and tickets
-// to zero.
+// Workspace: [partial slots: SMs x kMaxCtasPerSm CTAs x kPartialMax tagged 64-bit entries]
+//            [barrier words, 256 bytes: grid-barrier counter, exit counter, launch epoch].
+// It has the same size and layout for every matrix and C, so calls of any shape can share
+// one zero-filled workspace; every launch returns the counters to zero and advances the
+// epoch that tags its partials.
 static size_t partial_region_bytes() {
-    return align_up((size_t)sm_count() * kMaxCtasPerSm * 2 * kPartialSlotFloats * sizeof(float),
+    return align_up((size_t)sm_count() * kMaxCtasPerSm * kPartialMax * sizeof(unsigned long long),
                     256);
 }
 constexpr size_t kBarrierBytes = 256;
 
 size_t vl_workspace_bytes(int64_t in_f, int64_t out_f, int C) {
+    (void)in_f;
+    (void)out_f;
     (void)C;
-    const NativeGeom ng = native_geom(in_f, out_f);
-    return partial_region_bytes() + kBarrierBytes + align_up((size_t)ng.n_rb * sizeof(unsigned), 256);
+    return partial_region_bytes() + kBarrierBytes;
 }
 
-template <int NT, int NWC, int S, int MINB, int MAXOPS>
-static cudaError_t launch_ws(const VlOps<MAXOPS> &P, void *ws, bool pdl, bool coop,
-                             int64_t max_units, cudaStream_t stream) {
-    using Cfg = WsCfg<NT, NWC, S>;
-    auto kern = vl_ws_kernel<NT, NWC, S, MAXOPS, MINB>;
+template <int NT, int NW, int R, int MAXOPS>
+static cudaError_t launch_stream(const VlOps<MAXOPS> &P, void *ws, bool pdl, bool coop,
+                                 int64_t max_units, cudaStream_t stream) {
+    using Cfg = VlCfg<NT, NW, R, MAXOPS>;
+    auto kern = vl_stream_kernel<NT, NW, R, MAXOPS>;
     static int per_sm_cache[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -673,9 +712,8 @@ static cudaError_t launch_ws(const VlOps<MAXOPS> &P, void *ws, bool pdl, bool co
     if (!coop && G > max_units) G = max_units;  // a lone op never needs idle CTAs
     if (G < 1) G = 1;
     uint8_t *base = reinterpret_cast<uint8_t *>(ws);
-    float *part = reinterpret_cast<float *>(base);
+    auto *part = reinterpret_cast<unsigned long long *>(base);
     unsigned *gbar = reinterpret_cast<unsigned *>(base + partial_region_bytes());
-    unsigned *cnt = reinterpret_cast<unsigned *>(base + partial_region_bytes() + kBarrierBytes);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)G);
     cfg.blockDim = dim3(Cfg::kThreads);
@@ -693,7 +731,7 @@ static cudaError_t launch_ws(const VlOps<MAXOPS> &P, void *ws, bool pdl, bool co
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, kern, P, part, cnt, gbar);
+    return cudaLaunchKernelEx(&cfg, kern, P, part, gbar);
 }
 
 static VlOp make_op(const svd_qweight *W, const void *X, float *Y) {
@@ -705,20 +743,21 @@ static VlOp make_op(const svd_qweight *W, const void *X, float *Y) {
     o.Y = Y;
     o.in_f = W->in_features;
     o.out_f = W->out_features;
-    o.n_kc = ng.n_kc;
-    o.n_units = ng.n_units;
+    o.n_kc = (uint32_t)ng.n_kc;
+    o.n_units = (uint32_t)ng.n_units;
     return o;
 }
 
 template <int MAXOPS>
 static cudaError_t launch_ops(const VlOps<MAXOPS> &P, void *ws, bool pdl, cudaStream_t stream) {
     int64_t max_units = 0;
-    for (int i = 0; i < P.n; ++i) max_units = P.op[i].n_units > max_units ? P.op[i].n_units : max_units;
+    for (int i = 0; i < P.n; ++i)
+        max_units = (int64_t)P.op[i].n_units > max_units ? (int64_t)P.op[i].n_units : max_units;
     const bool coop = P.n > 1;
     switch (ntiles_for(P.C)) {
-        case 1: return launch_ws<1, kNWC1, kS1, kMinB1, MAXOPS>(P, ws, pdl, coop, max_units, stream);
-        case 2: return launch_ws<2, kNWC2, kS2, 1, MAXOPS>(P, ws, pdl, coop, max_units, stream);
-        default: return launch_ws<4, kNWC2, kS4, 1, MAXOPS>(P, ws, pdl, coop, max_units, stream);
+        case 1: return launch_stream<1, kNW1, kR1, MAXOPS>(P, ws, pdl, coop, max_units, stream);
+        case 2: return launch_stream<2, kNW2, kR2, MAXOPS>(P, ws, pdl, coop, max_units, stream);
+        default: return launch_stream<4, kNW2, kR4, MAXOPS>(P, ws, pdl, coop, max_units, stream);
     }
 }
 
@@ -754,6 +793,15 @@ static int check_qweight(const svd_qweight *W) {
     return SVD_OK;
 }
 
+// The stream-K kernel does its unit arithmetic in 32 bits: n_units * (workers + 1) must
+// stay below 2^32 (about 880 thousand units, 3.6 billion weights, on 152 SMs).
+static int check_native_size(const svd_qweight *W) {
+    const NativeGeom ng = native_geom(W->in_features, W->out_features);
+    const uint64_t workers = (uint64_t)sm_count() * kMaxCtasPerSm * 16 + 1;
+    if ((uint64_t)ng.n_units * workers > 0xFFFFFFFFull) return SVD_ERR_UNSUPPORTED;
+    return SVD_OK;
+}
+
 int verify_linear(const svd_qweight *W, const void *X, int C, float *Y, void *ws,
                   size_t ws_bytes, int flags, cudaStream_t stream) {
     int rc = check_qweight(W);
@@ -763,6 +811,8 @@ int verify_linear(const svd_qweight *W, const void *X, int C, float *Y, void *ws
     const bool pdl = (flags & SVD_F_PDL) != 0;
     if (sm_count() < 1) return SVD_ERR_CUDA;
     if (W->layout == SVD_LAYOUT_NATIVE) {
+        rc = check_native_size(W);
+        if (rc != SVD_OK) return rc;
         if (!ws || ws_bytes < vl_workspace_bytes(W->in_features, W->out_features, C))
             return SVD_ERR_WORKSPACE;
         VlOps<1> P;
@@ -791,13 +841,10 @@ int verify_linear(const svd_qweight *W, const void *X, int C, float *Y, void *ws
 }
 
 size_t chain_workspace_bytes(const svd_linear_op *ops, int n_ops, int C) {
-    int64_t n_rb = 1;
-    for (int i = 0; i < n_ops; ++i) {
-        const NativeGeom ng = native_geom(ops[i].W.in_features, ops[i].W.out_features);
-        n_rb = ng.n_rb > n_rb ? ng.n_rb : n_rb;
-    }
+    (void)ops;
+    (void)n_ops;
     (void)C;
-    return partial_region_bytes() + kBarrierBytes + align_up((size_t)n_rb * sizeof(unsigned), 256);
+    return partial_region_bytes() + kBarrierBytes;
 }
 
 int verify_chain(const svd_linear_op *ops, int n_ops, int C, void *ws, size_t ws_bytes, int flags,
@@ -808,6 +855,7 @@ int verify_chain(const svd_linear_op *ops, int n_ops, int C, void *ws, size_t ws
         const int rc = check_qweight(&ops[i].W);
         if (rc != SVD_OK) return rc;
         if (ops[i].W.layout != SVD_LAYOUT_NATIVE) return SVD_ERR_INVALID_ARG;
+        if (check_native_size(&ops[i].W) != SVD_OK) return SVD_ERR_UNSUPPORTED;
         if (!ops[i].X || !ops[i].Y || !aligned16(ops[i].X)) return SVD_ERR_INVALID_ARG;
     }
     if (sm_count() < 1) return SVD_ERR_CUDA;
@@ -879,17 +927,15 @@ int unpack(const svd_qweight *src, void *dc, void *ds, cudaStream_t stream) {
 }
 
 // ---- verify linear without caller scratch ----------------------------------------------
-// The stream-K kernel needs a small scratch area (partial sums of row blocks split between
-// CTAs, and one ticket counter per 64-row block).  svd_verify_linear takes it from the caller;
+// The stream-K kernel needs a small scratch area (tagged partial sums of row blocks split
+// between CTAs, and the barrier words).  svd_verify_linear takes it from the caller;
 // this variant takes it from a fixed array in the library's own device memory instead, for
 // callers that cannot allocate device memory.  The array is reserved when the library's
 // module is loaded on a device and stays there until the process exits.
 constexpr int kNoAllocMaxSms = 160;
-constexpr int64_t kNoAllocMaxRowBlocks = SVD_NOALLOC_MAX_OUT_FEATURES / kRowsPerBlock;
 constexpr size_t kNoAllocPartialBytes =
-    (size_t)kNoAllocMaxSms * kMaxCtasPerSm * 2 * kPartialSlotFloats * sizeof(float);
-constexpr size_t kNoAllocBytes =
-    kNoAllocPartialBytes + kBarrierBytes + kNoAllocMaxRowBlocks * sizeof(unsigned);
+    (size_t)kNoAllocMaxSms * kMaxCtasPerSm * kPartialMax * sizeof(unsigned long long);
+constexpr size_t kNoAllocBytes = kNoAllocPartialBytes + kBarrierBytes;
 static_assert(kNoAllocBytes <= SVD_NOALLOC_SCRATCH_BYTES, "scratch bound in svd.h");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
@@ -907,6 +953,7 @@ int verify_linear_noalloc(const svd_qweight *W, const void *X, int C, float *Y, 
     if (!X || !Y || C < 1 || C > SVD_C_MAX || !aligned16(X)) return SVD_ERR_INVALID_ARG;
     if (flags & ~SVD_F_PDL) return SVD_ERR_INVALID_ARG;
     if (W->out_features > SVD_NOALLOC_MAX_OUT_FEATURES) return SVD_ERR_UNSUPPORTED;
+    if (sm_count() >= 1 && check_native_size(W) != SVD_OK) return SVD_ERR_UNSUPPORTED;
     const int sms = sm_count();
     if (sms < 1) return SVD_ERR_CUDA;
     if (sms > kNoAllocMaxSms) return SVD_ERR_UNSUPPORTED;
@@ -923,13 +970,12 @@ int verify_linear_noalloc(const svd_qweight *W, const void *X, int C, float *Y, 
         }
         base = g_noalloc_ptr[dev];
     }
-    // Same layout as a caller workspace: partial slots, then the barrier counters and the
-    // tickets, which must start at zero.  Every call clears them again on the stream before
-    // its kernel, so a call never depends on what the previous one left behind.
-    const NativeGeom ng = native_geom(W->in_features, W->out_features);
+    // Same layout as a caller workspace: partial slots, then the barrier words.  Every call
+    // clears the two barrier counters on the stream before its kernel, so a call never depends
+    // on counters an earlier call left behind; the epoch word is kept, so partials written
+    // by earlier calls never carry the tag of a later one.
     unsigned char *counters = reinterpret_cast<unsigned char *>(base) + partial_region_bytes();
-    SVD_CUDA_TRY(cudaMemsetAsync(counters, 0, kBarrierBytes + (size_t)ng.n_rb * sizeof(unsigned),
-                                 stream));
+    SVD_CUDA_TRY(cudaMemsetAsync(counters, 0, 2 * sizeof(unsigned), stream));
     VlOps<1> P;
     P.n = 1;
     P.C = C;
