@@ -108,7 +108,7 @@ def kernel_traffic():
     """DRAM traffic per launch of the stack's verify-linear kernel from the committed ncu
     summary, if it was taken on the current kernel source (else None)."""
     src = os.path.join(ROOT, "speculative_decoding_verify_06_gb300", "csrc", "verify_linear.cu")
-    prof = os.path.join(ROOT, "profiles", "vl_ws_kernel_27b_stack_c4.txt")
+    prof = os.path.join(ROOT, "profiles", "vl_stream_kernel_27b_stack_c4.txt")
     try:
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         txt = open(prof).read()
@@ -319,9 +319,11 @@ def run_svd(args, rank, world, local_rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "C": args.C, "layers": args.layers,
                    "global_batch": world, "parallelism": f"replicas{world}",
-                   "l2": "inputs larger than L2: 11.9 GB of weights streamed per step",
+                   "l2": (f"inputs larger than L2: {vp.stack_bytes() / 1e9:.1f} GB of weights "
+                          f"streamed per step"),
                    "stack_launch": ("per-matrix launches, PDL" if args.no_chain else
-                                    "one persistent cooperative chain of 256 matrices"),
+                                    f"one persistent cooperative chain of {len(vp.linears)} "
+                                    f"matrices"),
                    "graph": "stack graph + tail graph per step",
                    "stack_only": bool(args.stack_only)},
         "stack": {"ms": stack_ms, "passes_per_s": 1000.0 / stack_ms, "bytes": stack_bytes,
@@ -332,7 +334,7 @@ def run_svd(args, rank, world, local_rank):
         "pass_bytes": vp.pass_bytes(),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind,
-                     "kernel": "vl_ws_kernel (one chain launch: the stack's 256 matrices)",
+                     "kernel": "vl_stream_kernel (one chain launch: the stack's 256 matrices)",
                      "traffic": None if traffic_pass is None else traffic_pass},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": Ke},

@@ -252,13 +252,14 @@ struct VlOps {
 // touching activations or the workspace.
 constexpr int kPartialMax = 32 * kTiles * 4 * 4;  // entries of the largest partial (NT = 4)
 
-template <int NT, int NW, int R, int MAXOPS>
+template <int NT, int NW, int R, int U, int MAXOPS>
 struct VlCfg {
     static constexpr int kThreads = NW * 32;
     static constexpr int kAcc = kTiles * NT * 4;  // fp32 accumulators per lane
     static constexpr int kPartial = 32 * kAcc;    // entries of a warp's (or a CTA's) partial
     static constexpr int kPer = (kPartial + kThreads - 1) / kThreads;
-    static constexpr size_t kRing = (size_t)NW * R * kUnitBytes;
+    static constexpr int kSlotBytes = U * kUnitBytes;  // codes of U units, then their scales
+    static constexpr size_t kRing = (size_t)NW * R * kSlotBytes;
     static constexpr size_t kPark = (size_t)NW * 2 * kPartial * sizeof(float);
     static constexpr size_t kSmem = kRing + kPark + (size_t)MAXOPS * sizeof(VlOp);
     static_assert(kPartial <= kPartialMax, "partial slot size");
@@ -287,13 +288,13 @@ __device__ __forceinline__ float wait_tagged(const unsigned long long *p, uint32
 }
 
 // The gi-th barrier of a launch among all G CTAs: one release-add per CTA (after a CTA
-// barrier, so it publishes every warp's writes) on a counter in the workspace, then acquire
-// polling until the counter reaches gi * G.  Polling is bounded.
-__device__ __forceinline__ void grid_barrier(unsigned *gbar, unsigned target) {
-    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(gbar) : "memory");
+// barrier, so that it carries every warp's writes) on a counter in the workspace, then
+// acquire polling until the counter reaches gi * G.  Polling is bounded.
+__device__ __forceinline__ void grid_barrier(unsigned *count, unsigned target) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(count) : "memory");
     for (int it = 0; it < (1 << 26); ++it) {
         unsigned v;
-        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(gbar) : "memory");
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(count) : "memory");
         if (v >= target) return;
         if (it > 512) __nanosleep(32);
     }
@@ -303,19 +304,20 @@ __device__ __forceinline__ unsigned atom_add_acqrel_gpu(unsigned *p, unsigned v)
     asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
     return old;
 }
-// Workspace words after the partial slots: [0] grid-barrier counter, [1] exit counter (both
-// returned to zero by the last CTA out), [2] launch epoch (advanced by the last CTA out).
-constexpr int kBarCount = 0, kBarExit = 1, kBarEpoch = 2;
+// Workspace words after the partial slots: [0] grid-barrier counter, [1] exit counter, both
+// returned to zero by the last CTA out; [63] launch epoch, advanced by the last CTA out.
+constexpr int kBarCount = 0, kBarExit = 1, kBarEpoch = 63;
 
 #ifndef SVD_PROBE
 #define SVD_PROBE(gi, what)  // timing hook for instrumented builds; nothing by default
 #endif
 
-template <int NT, int NW, int R, int MAXOPS>
+template <int NT, int NW, int R, int U, int MAXOPS>
 __global__ void __launch_bounds__(NW * 32, 1)
 vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__restrict__ part,
                  unsigned *__restrict__ gbar) {
-    using Cfg = VlCfg<NT, NW, R, MAXOPS>;
+    using Cfg = VlCfg<NT, NW, R, U, MAXOPS>;
+    constexpr int kSlotBytes = Cfg::kSlotBytes;
     constexpr int kAcc = Cfg::kAcc, kPartial = Cfg::kPartial, kPer = Cfg::kPer;
     constexpr int kThreads = Cfg::kThreads;
     constexpr uint32_t kNone = 0xFFFFFFFFu;
@@ -334,7 +336,8 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
     const uint32_t G = gridDim.x, b = blockIdx.x;
     const uint32_t Wtot = G * NW, gw = b * NW + warp;
     const uint32_t full0 = smem_u32(&s_full[warp * R]);
-    const uint32_t ring0 = smem_u32(smem + (size_t)warp * R * kUnitBytes);
+    uint8_t *const ring = smem + (size_t)warp * R * kSlotBytes;
+    const uint32_t ring0 = smem_u32(ring);
 
     // This worker's unit range of an op: [lo, hi), empty when the op has fewer units than
     // there are workers and this one is not needed.
@@ -366,28 +369,30 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
     __syncthreads();
 
     // Issue cursor of this warp (uniform across its lanes; lane 0 issues): the next unit to
-    // load is unit c_u of op c_op, c_hi ends that op's range; c_issued counts issued units.
-    int c_op = 0;
+    // load is unit c_u of op c_op, c_hi ends that op's range, c_codes / c_scales point at that
+    // unit's bytes; c_issued counts filled slots.  A slot takes the next U units of the
+    // range (fewer at its end; never units of two ops).
+    int c_op = -1;
     uint32_t c_u = 0, c_hi = 0, c_issued = 0;
-    if (n_ops > 0) range(ops[0], &c_u, &c_hi);
+    const uint8_t *c_codes = nullptr, *c_scales = nullptr;
     auto issue = [&]() {
-        while (c_op < n_ops) {
-            if (c_u < c_hi) {
-                const VlOp &o = ops[c_op];
-                const uint32_t slot = c_issued % R;
-                if (lane == 0) {
-                    const uint32_t bar = full0 + 8 * slot, dst = ring0 + slot * kUnitBytes;
-                    mbar_expect_tx(bar, kUnitBytes);
-                    bulk_g2s(dst, o.codes + (size_t)c_u * kUnitCodeBytes, kUnitCodeBytes, bar);
-                    bulk_g2s(dst + kUnitCodeBytes, o.scales + (size_t)c_u * kUnitScaleBytes,
-                             kUnitScaleBytes, bar);
-                }
-                ++c_u;
-                ++c_issued;
-                return;
-            }
-            if (++c_op < n_ops) range(ops[c_op], &c_u, &c_hi);
+        while (c_u >= c_hi) {
+            if (++c_op >= n_ops) return;
+            range(ops[c_op], &c_u, &c_hi);
+            c_codes = ops[c_op].codes + (size_t)c_u * kUnitCodeBytes;
+            c_scales = ops[c_op].scales + (size_t)c_u * kUnitScaleBytes;
         }
+        const uint32_t slot = c_issued % R, n = min((uint32_t)U, c_hi - c_u);
+        if (lane == 0) {
+            const uint32_t bar = full0 + 8 * slot, dst = ring0 + slot * kSlotBytes;
+            mbar_expect_tx(bar, n * kUnitBytes);
+            bulk_g2s(dst, c_codes, n * kUnitCodeBytes, bar);
+            bulk_g2s(dst + U * kUnitCodeBytes, c_scales, n * kUnitScaleBytes, bar);
+        }
+        c_u += n;
+        ++c_issued;
+        c_codes += n * kUnitCodeBytes;
+        c_scales += n * kUnitScaleBytes;
     };
     // weights never depend on earlier kernels: start streaming before waiting for them
     for (int i = 0; i < R; ++i) issue();
@@ -408,7 +413,7 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
 #pragma unroll
             for (int q = 0; q < 4; ++q) acc[r][nt][q] = 0.f;
 
-    uint32_t c_used = 0;  // units this warp has consumed (its ring position)
+    uint32_t c_used = 0;  // slots this warp has consumed (its ring position)
     for (int gi = 0; gi < n_ops; ++gi) {
         const VlOp &o = ops[gi];
         if (gi > 0) {
@@ -459,12 +464,12 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
                 }
             };
 
-            uint32_t kc = lo % n_kc, rb = lo / n_kc, seg_lo = lo;
+            uint32_t rb = lo / n_kc, kc = lo - rb * n_kc, seg_lo = lo;
             uint4 xr[NT][2];
             load_x(kc, xr);
             for (uint32_t u = lo; u < hi; ++u) {
-                const uint32_t slot = c_used % R;
-                mbar_wait(full0 + 8 * slot, (c_used / R) & 1u);
+                const uint32_t slot = c_used % R, in_slot = (u - lo) % U;
+                if (in_slot == 0u) mbar_wait(full0 + 8 * slot, (c_used / R) & 1u);
                 uint4 xc[NT][2];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
@@ -473,8 +478,8 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
                 }
                 const uint32_t kn = (kc + 1 == n_kc) ? 0u : kc + 1;
                 if (u + 1 < hi) load_x(kn, xr);
-                const uint8_t *cbase = smem + (size_t)(warp * R + slot) * kUnitBytes;
-                const uint8_t *sbase = cbase + kUnitCodeBytes;
+                const uint8_t *cbase = ring + slot * kSlotBytes + in_slot * kUnitCodeBytes;
+                const uint8_t *sbase = ring + slot * kSlotBytes + U * kUnitCodeBytes + in_slot * kUnitScaleBytes;
 #pragma unroll
                 for (int r = 0; r < kTiles; ++r) {
                     const uint4 cw = *reinterpret_cast<const uint4 *>(cbase + r * 512 + lane * 16);
@@ -499,11 +504,14 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
                         }
                     }
                 }
-                // the slot is read: refill it with the unit R places further on
-                __syncwarp();
-                if (lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                issue();
-                ++c_used;
+                // Once the slot is read, refill it with the units R slots further on.  Every
+                // value this warp loaded from the slot has been consumed by the instructions
+                // above (issued in order), so the bulk copy cannot overwrite a pending read.
+                if (in_slot == U - 1u || u + 1 == hi) {
+                    __syncwarp();
+                    issue();
+                    ++c_used;
+                }
 
                 // end of a segment (a row block's end, or the range's): a whole block goes
                 // to Y, a partial one is parked
@@ -551,38 +559,48 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
         SVD_PROBE(gi, 1);
 
         // ---- all warps are done with the op: add the parked partials block by block, in
-        // worker order (slot 0 before slot 1 within a warp)
+        // worker order (slot 0 before slot 1 within a warp).  Parked partial i (i < 2 NW) is
+        // looked at by lane i of every warp; runs of equal row blocks are found with ballots.
         __syncthreads();
-        int p = 0;
-        while (true) {
-            while (p < 2 * NW && s_park_rb[p] == kNone) ++p;
-            if (p >= 2 * NW) break;
-            const uint32_t rb = s_park_rb[p];
-            const bool owner = s_park_head[p] != 0u;
-            int q = p + 1;
-            while (q < 2 * NW && (s_park_rb[q] == kNone || s_park_rb[q] == rb)) ++q;
-            // parked partials p..q-1 (the ones holding rb) form this block's CTA partial
-            const uint32_t b_last = owner ? cta_of(o, (rb + 1) * n_kc - 1) : b;
+        {
+            static_assert(2 * NW <= 32, "one lane per parked partial");
+            const uint32_t my_rb = lane < 2 * NW ? s_park_rb[lane] : kNone;
+            const bool my_head = lane < 2 * NW && s_park_head[lane] != 0u;
+            const uint32_t valid = __ballot_sync(0xFFFFFFFFu, my_rb != kNone);
+            // previous parked partial in worker order, and whether this one starts a run
+            const uint32_t below = valid & ((1u << lane) - 1u);
+            const int prev = below ? 31 - __clz(below) : -1;
+            const uint32_t prev_rb = __shfl_sync(0xFFFFFFFFu, my_rb, prev < 0 ? lane : prev);
+            const uint32_t starts =
+                __ballot_sync(0xFFFFFFFFu, my_rb != kNone && (prev < 0 || prev_rb != my_rb));
+            for (uint32_t rest = starts; rest != 0u;) {
+                const int p = __ffs(rest) - 1;
+                rest &= rest - 1u;
+                const uint32_t next = rest ? (uint32_t)(__ffs(rest) - 1) : 32u;
+                const uint32_t members = valid & ~((1u << p) - 1u) & (next < 32u ? (1u << next) - 1u : 0xFFFFFFFFu);
+                const uint32_t rb = __shfl_sync(0xFFFFFFFFu, my_rb, p);
+                const bool owner = __shfl_sync(0xFFFFFFFFu, my_head ? 1 : 0, p) != 0;
+                const uint32_t b_last = owner ? cta_of(o, (rb + 1) * n_kc - 1) : b;
 #pragma unroll
-            for (int m = 0; m < kPer; ++m) {
-                const int e = threadIdx.x + m * kThreads;
-                if (e >= kPartial) break;
-                int64_t row;
-                int col;
-                coords(e, rb, &row, &col);
-                if (row >= out_f || col >= C) continue;
-                float v = 0.f;
-                for (int t = p; t < q; ++t)
-                    if (s_park_rb[t] == rb) v += park[t * kPartial + e];
-                if (owner) {
-                    for (uint32_t bb = b + 1; bb <= b_last; ++bb)
-                        v += wait_tagged(part + (size_t)bb * kPartialMax + e, tag);
-                    o.Y[(int64_t)col * out_f + row] = v;
-                } else {
-                    st_tagged(part + (size_t)b * kPartialMax + e, v, tag);
+                for (int m = 0; m < kPer; ++m) {
+                    const int e = threadIdx.x + m * kThreads;
+                    if (e >= kPartial) break;
+                    int64_t row;
+                    int col;
+                    coords(e, rb, &row, &col);
+                    if (row >= out_f || col >= C) continue;
+                    float v = 0.f;
+                    for (uint32_t mm = members; mm != 0u; mm &= mm - 1u)
+                        v += park[(__ffs(mm) - 1) * kPartial + e];
+                    if (owner) {
+                        for (uint32_t bb = b + 1; bb <= b_last; ++bb)
+                            v += wait_tagged(part + (size_t)bb * kPartialMax + e, tag);
+                        o.Y[(int64_t)col * out_f + row] = v;
+                    } else {
+                        st_tagged(part + (size_t)b * kPartialMax + e, v, tag);
+                    }
                 }
             }
-            p = q;
         }
         SVD_PROBE(gi, 2);
     }
@@ -660,13 +678,17 @@ vl_simt_kernel(const uint8_t *__restrict__ codes, const uint16_t *__restrict__ s
 #define SVD_NW1 16
 #endif
 #ifndef SVD_R1
-#define SVD_R1 4
+#define SVD_R1 2
+#endif
+#ifndef SVD_U
+#define SVD_U 2
 #endif
 constexpr int kNW1 = SVD_NW1;     // warps per CTA, C <= 8
 constexpr int kR1 = SVD_R1;       // ring slots per warp, C <= 8
+constexpr int kU = SVD_U;         // units per slot (one pair of bulk copies)
 constexpr int kNW2 = 8;           // warps per CTA, C <= 16 and C <= 32
-constexpr int kR2 = 8;            // ring slots per warp, C <= 16
-constexpr int kR4 = 4;            // ring slots per warp, C <= 32
+constexpr int kR2 = 4;            // ring slots per warp, C <= 16
+constexpr int kR4 = 2;            // ring slots per warp, C <= 32
 constexpr int kMaxCtasPerSm = 2;  // the workspace holds partial slots for this many
 constexpr int kChainMax = 256;    // ops per chain launch (kernel parameters, ~16 KB)
 
@@ -682,6 +704,7 @@ static size_t partial_region_bytes() {
                     256);
 }
 constexpr size_t kBarrierBytes = 256;
+static_assert((kBarEpoch + 1) * sizeof(unsigned) <= kBarrierBytes, "barrier words");
 
 size_t vl_workspace_bytes(int64_t in_f, int64_t out_f, int C) {
     (void)in_f;
@@ -690,11 +713,11 @@ size_t vl_workspace_bytes(int64_t in_f, int64_t out_f, int C) {
     return partial_region_bytes() + kBarrierBytes;
 }
 
-template <int NT, int NW, int R, int MAXOPS>
+template <int NT, int NW, int R, int U, int MAXOPS>
 static cudaError_t launch_stream(const VlOps<MAXOPS> &P, void *ws, bool pdl, bool coop,
                                  int64_t max_units, cudaStream_t stream) {
-    using Cfg = VlCfg<NT, NW, R, MAXOPS>;
-    auto kern = vl_stream_kernel<NT, NW, R, MAXOPS>;
+    using Cfg = VlCfg<NT, NW, R, U, MAXOPS>;
+    auto kern = vl_stream_kernel<NT, NW, R, U, MAXOPS>;
     static int per_sm_cache[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -755,9 +778,9 @@ static cudaError_t launch_ops(const VlOps<MAXOPS> &P, void *ws, bool pdl, cudaSt
         max_units = (int64_t)P.op[i].n_units > max_units ? (int64_t)P.op[i].n_units : max_units;
     const bool coop = P.n > 1;
     switch (ntiles_for(P.C)) {
-        case 1: return launch_stream<1, kNW1, kR1, MAXOPS>(P, ws, pdl, coop, max_units, stream);
-        case 2: return launch_stream<2, kNW2, kR2, MAXOPS>(P, ws, pdl, coop, max_units, stream);
-        default: return launch_stream<4, kNW2, kR4, MAXOPS>(P, ws, pdl, coop, max_units, stream);
+        case 1: return launch_stream<1, kNW1, kR1, kU, MAXOPS>(P, ws, pdl, coop, max_units, stream);
+        case 2: return launch_stream<2, kNW2, kR2, kU, MAXOPS>(P, ws, pdl, coop, max_units, stream);
+        default: return launch_stream<4, kNW2, kR4, kU, MAXOPS>(P, ws, pdl, coop, max_units, stream);
     }
 }
 
@@ -971,11 +994,11 @@ int verify_linear_noalloc(const svd_qweight *W, const void *X, int C, float *Y, 
         base = g_noalloc_ptr[dev];
     }
     // Same layout as a caller workspace: partial slots, then the barrier words.  Every call
-    // clears the two barrier counters on the stream before its kernel, so a call never depends
-    // on counters an earlier call left behind; the epoch word is kept, so partials written
-    // by earlier calls never carry the tag of a later one.
+    // clears the barrier counters on the stream before its kernel, so a call never
+    // depends on what an earlier call left behind; the epoch word (the last one) is kept, so
+    // partials written by earlier calls never carry the tag of a later one.
     unsigned char *counters = reinterpret_cast<unsigned char *>(base) + partial_region_bytes();
-    SVD_CUDA_TRY(cudaMemsetAsync(counters, 0, 2 * sizeof(unsigned), stream));
+    SVD_CUDA_TRY(cudaMemsetAsync(counters, 0, kBarEpoch * sizeof(unsigned), stream));
     VlOps<1> P;
     P.n = 1;
     P.C = C;
