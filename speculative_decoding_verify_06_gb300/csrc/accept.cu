@@ -17,9 +17,20 @@
 // keeps the slice that contains u' * R, and repeats on it until 32 elements are left; only the
 // first level streams the whole row from HBM, the deeper levels re-read a shrinking slice that
 // is still cached.
+//
+// Two kernels share that logic.  accept_kernel gives every window one CTA, which suits many
+// windows at once.  accept_cluster_kernel gives a window a cluster of eight CTAs on eight
+// SMs: the first level of the draw is split over the cluster (eight times the loads in
+// flight), the CTAs exchange their slice sums through distributed shared memory, and the CTA
+// whose slice holds the crossing finishes the search alone.  The host picks the cluster
+// kernel when there are fewer sampled windows than SMs, the case of one verify pass.
+#include <cooperative_groups.h>
+
 #include "svd_common.cuh"
 
 namespace svd {
+
+int sm_count();
 
 constexpr int kAccThreads = 256;
 constexpr int kAccWarps = kAccThreads / 32;
@@ -188,6 +199,74 @@ __device__ int64_t block_argmax(const float *row, int64_t V, int &st, AcceptShar
     return r;
 }
 
+// The accept tests of window w, one lane of the calling warp per drafted position: the first
+// rejected position j (k when every draft is accepted) and the resampling uniform of the draw
+// that follows go to sh.j and sh.m2, the status bits of positions up to j to sh.st_or[0];
+// the accepted drafts are written to tok when write_tok.
+__device__ void accept_tests(const float *__restrict__ p, const int64_t *__restrict__ p_rows,
+                             const float *__restrict__ q, const int64_t *__restrict__ q_rows,
+                             const int32_t *__restrict__ draft, int k, int64_t V, uint64_t seed,
+                             uint64_t woff, const float *__restrict__ uniforms, int64_t w,
+                             int32_t *tok, AcceptShared &sh, bool write_tok = true) {
+    const int lane = threadIdx.x & 31;
+    auto prow = [&](int i) -> const float * {
+        const int64_t r = p_rows ? p_rows[w * (k + 1) + i] : w * (k + 1) + i;
+        return p + r * V;
+    };
+    auto qrow = [&](int i) -> const float * {
+        const int64_t r = q_rows ? q_rows[w * k + i] : w * k + i;
+        return q + r * V;
+    };
+    const uint32_t key0 = (uint32_t)seed, key1 = (uint32_t)(seed >> 32);
+    const uint64_t widx = woff + (uint64_t)w;
+    int st = 0;
+    bool acc = false;
+    uint32_t m2 = 0;
+    if (lane < k) {
+        double u;
+        if (uniforms) {
+            u = (double)uniforms[(w * (k + 1) + lane) * 2];
+            const float u2 = uniforms[(w * (k + 1) + lane) * 2 + 1];
+            m2 = (uint32_t)fminf(fmaxf(floorf(u2 * 16777216.f), 0.f), 16777215.f);
+        } else {
+            const Philox4 r = philox4x32_10((uint32_t)widx, (uint32_t)(widx >> 32),
+                                            (uint32_t)lane, 0u, key0, key1);
+            u = (double)(r.v[0] >> 8) * (1.0 / 16777216.0);
+            m2 = r.v[1] >> 8;
+        }
+        const int32_t x = draft[w * k + lane];
+        if (x < 0 || x >= V) {
+            st |= SVD_ST_BAD_TOKEN;
+        } else {
+            const double pv = prob_clamped(__ldg(prow(lane) + x), st);
+            const double qv = prob_clamped(__ldg(qrow(lane) + x), st);
+            if (qv == 0.0) st |= SVD_ST_Q_ZERO;
+            acc = u * qv < pv;
+        }
+    }
+    const uint32_t kmask = (k >= 32) ? 0xffffffffu : ((1u << k) - 1u);
+    const uint32_t amask = __ballot_sync(0xffffffffu, acc) & kmask;
+    const uint32_t rej = (~amask) & kmask;
+    const int j = rej ? (__ffs(rej) - 1) : k;
+    const int st_all = __reduce_or_sync(0xffffffffu, lane <= j ? st : 0);
+    const uint32_t m2j = __shfl_sync(0xffffffffu, m2, j < 32 ? j : 0);
+    if (write_tok && lane < j) tok[lane] = draft[w * k + lane];
+    if (lane == 0) {
+        sh.j = j;
+        sh.st_or[0] = st_all;
+        if (j < k) {
+            sh.m2 = m2j;
+        } else if (uniforms) {
+            const float u2 = uniforms[(w * (k + 1) + k) * 2 + 1];
+            sh.m2 = (uint32_t)fminf(fmaxf(floorf(u2 * 16777216.f), 0.f), 16777215.f);
+        } else {
+            const Philox4 r = philox4x32_10((uint32_t)widx, (uint32_t)(widx >> 32),
+                                            (uint32_t)k, 0u, key0, key1);
+            sh.m2 = r.v[1] >> 8;
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kAccThreads)
 accept_kernel(const float *__restrict__ p, const int64_t *__restrict__ p_rows,
               const float *__restrict__ q, const int64_t *__restrict__ q_rows,
@@ -249,56 +328,7 @@ accept_kernel(const float *__restrict__ p, const int64_t *__restrict__ p_rows,
     }
 
     // ---- sampled: the accept tests, one lane per drafted position --------------------------
-    const uint32_t key0 = (uint32_t)seed, key1 = (uint32_t)(seed >> 32);
-    const uint64_t widx = woff + (uint64_t)w;
-    if (warp == 0) {
-        int st = 0;
-        bool acc = false;
-        uint32_t m2 = 0;
-        if (lane < k) {
-            double u;
-            if (uniforms) {
-                u = (double)uniforms[(w * (k + 1) + lane) * 2];
-                const float u2 = uniforms[(w * (k + 1) + lane) * 2 + 1];
-                m2 = (uint32_t)fminf(fmaxf(floorf(u2 * 16777216.f), 0.f), 16777215.f);
-            } else {
-                const Philox4 r = philox4x32_10((uint32_t)widx, (uint32_t)(widx >> 32),
-                                                (uint32_t)lane, 0u, key0, key1);
-                u = (double)(r.v[0] >> 8) * (1.0 / 16777216.0);
-                m2 = r.v[1] >> 8;
-            }
-            const int32_t x = draft[w * k + lane];
-            if (x < 0 || x >= V) {
-                st |= SVD_ST_BAD_TOKEN;
-            } else {
-                const double pv = prob_clamped(__ldg(prow(lane) + x), st);
-                const double qv = prob_clamped(__ldg(qrow(lane) + x), st);
-                if (qv == 0.0) st |= SVD_ST_Q_ZERO;
-                acc = u * qv < pv;
-            }
-        }
-        const uint32_t kmask = (k >= 32) ? 0xffffffffu : ((1u << k) - 1u);
-        const uint32_t amask = __ballot_sync(0xffffffffu, acc) & kmask;
-        const uint32_t rej = (~amask) & kmask;
-        const int j = rej ? (__ffs(rej) - 1) : k;
-        const int st_all = __reduce_or_sync(0xffffffffu, lane <= j ? st : 0);
-        const uint32_t m2j = __shfl_sync(0xffffffffu, m2, j < 32 ? j : 0);
-        if (lane < j) tok[lane] = draft[w * k + lane];
-        if (lane == 0) {
-            sh.j = j;
-            sh.st_or[0] = st_all;
-            if (j < k) {
-                sh.m2 = m2j;
-            } else if (uniforms) {
-                const float u2 = uniforms[(w * (k + 1) + k) * 2 + 1];
-                sh.m2 = (uint32_t)fminf(fmaxf(floorf(u2 * 16777216.f), 0.f), 16777215.f);
-            } else {
-                const Philox4 r = philox4x32_10((uint32_t)widx, (uint32_t)(widx >> 32),
-                                                (uint32_t)k, 0u, key0, key1);
-                sh.m2 = r.v[1] >> 8;
-            }
-        }
-    }
+    if (warp == 0) accept_tests(p, p_rows, q, q_rows, draft, k, V, seed, woff, uniforms, w, tok, sh);
     __syncthreads();
     const int j = sh.j;
     const uint32_t m2 = sh.m2;
@@ -425,6 +455,185 @@ accept_kernel(const float *__restrict__ p, const int64_t *__restrict__ p_rows,
     }
 }
 
+// ---- one window per cluster of eight CTAs --------------------------------------------------
+constexpr int kAccCluster = 8;
+
+// Inclusive scan of u128 values over a warp.
+__device__ __forceinline__ u128 warp_scan_u128(u128 x) {
+    const int lane = threadIdx.x & 31;
+    uint64_t lo = (uint64_t)x, hi = (uint64_t)(x >> 64);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t olo = __shfl_up_sync(0xffffffffu, lo, o);
+        const uint64_t ohi = __shfl_up_sync(0xffffffffu, hi, o);
+        if (lane >= o) {
+            const uint64_t nlo = lo + olo;
+            hi = hi + ohi + (nlo < lo ? 1ull : 0ull);
+            lo = nlo;
+        }
+    }
+    return ((u128)hi << 64) | lo;
+}
+
+__global__ void __cluster_dims__(kAccCluster, 1, 1) __launch_bounds__(kAccThreads)
+accept_cluster_kernel(const float *__restrict__ p, const int64_t *__restrict__ p_rows,
+                      const float *__restrict__ q, const int64_t *__restrict__ q_rows,
+                      const int32_t *__restrict__ draft, int k, int64_t V, uint64_t seed,
+                      uint64_t woff, const float *__restrict__ uniforms,
+                      int32_t *__restrict__ out_tokens, int32_t *__restrict__ n_emitted,
+                      int32_t *__restrict__ status, int vec_ok) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    __shared__ AcceptShared sh;
+    __shared__ u128 s_wsum[2][kAccWarps];  // this CTA's slice sums, per attempt
+    __shared__ int s_cst[2];               // status bits of this CTA's slices, per attempt
+    const int crank = (int)cluster.block_rank();
+    const int64_t w = blockIdx.x / kAccCluster;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int32_t *tok = out_tokens + w * (k + 1);
+    griddep_wait();
+    if (warp == 0)
+        accept_tests(p, p_rows, q, q_rows, draft, k, V, seed, woff, uniforms, w, tok, sh, false);
+    if (threadIdx.x < 2) s_cst[threadIdx.x] = 0;
+    __syncthreads();
+    const int j = sh.j;
+    const uint32_t m2 = sh.m2;
+    int st_win = sh.st_or[0];  // the accept tests' bits, the same in every CTA
+    const float *rp = p + (p_rows ? p_rows[w * (k + 1) + j] : w * (k + 1) + j) * V;
+    const float *rq = (j < k) ? q + (q_rows ? q_rows[w * k + j] : w * k + j) * V : nullptr;
+    const bool vec = vec_ok != 0;
+
+    // Level 1 over the cluster: CTA c takes piece c of the row, its warp i one eighth of that,
+    // so slice 8 c + i in cluster order is slice i of CTA c.
+    int64_t piece = (V + kAccCluster - 1) / kAccCluster;
+    if (vec) piece = (piece + 3) & ~int64_t(3);
+    auto slice_of = [&](int c, int i, int64_t *lo, int64_t *hi) {
+        const int64_t c_lo = min(V, (int64_t)c * piece), c_hi = min(V, c_lo + piece);
+        int64_t part = (c_hi - c_lo + kAccWarps - 1) / kAccWarps;
+        if (vec) part = (part + 3) & ~int64_t(3);
+        *lo = min(c_hi, c_lo + part * i);
+        *hi = min(c_hi, *lo + part);
+    };
+    int64_t lo, hi;
+    slice_of(crank, warp, &lo, &hi);
+    int found = -1;
+    u128 base = 0, total = 0, target = 0;
+    for (int attempt = 0; attempt < 2; ++attempt) {
+        int st = 0;
+        const u128 sum = (lo < hi) ? slice_sum(rp, rq, lo, hi, vec, st) : (u128)0;
+        st = __reduce_or_sync(0xffffffffu, st);
+        if (lane == 0) {
+            s_wsum[attempt][warp] = sum;
+            if (st) atomicOr(&s_cst[attempt], st);
+        }
+        cluster.sync();
+        if (warp == 0) {
+            // lane t holds the cluster's slices 2t and 2t+1 (in row order)
+            const int i0 = 2 * lane, i1 = 2 * lane + 1;
+            const u128 x0 = *cluster.map_shared_rank(&s_wsum[attempt][i0 % kAccWarps], i0 / kAccWarps);
+            const u128 x1 = *cluster.map_shared_rank(&s_wsum[attempt][i1 % kAccWarps], i1 / kAccWarps);
+            int sts = lane < kAccCluster ? *cluster.map_shared_rank(&s_cst[attempt], lane) : 0;
+            sts = __reduce_or_sync(0xffffffffu, sts);
+            const u128 incl = warp_scan_u128(x0 + x1);
+            const u128 excl = incl - (x0 + x1);
+            const uint64_t tlo = __shfl_sync(0xffffffffu, (uint64_t)incl, 31);
+            const uint64_t thi = __shfl_sync(0xffffffffu, (uint64_t)(incl >> 64), 31);
+            const u128 R = ((u128)thi << 64) | tlo;
+            const u128 tgt = (u128)m2 * R;
+            const uint32_t hm = __ballot_sync(0xffffffffu, R != 0 && (incl << 24) > tgt);
+            if (lane == 0) {
+                sh.total = R;
+                sh.target = tgt;
+                sh.st_or[1] = sts;
+                sh.found = -1;
+            }
+            if (hm && lane == __ffs(hm) - 1) {
+                const bool first = ((excl + x0) << 24) > tgt;
+                sh.found = first ? i0 : i1;
+                sh.base = first ? excl : excl + x0;
+            }
+        }
+        cluster.sync();  // every read of another CTA's shared memory is done
+        total = sh.total;
+        target = sh.target;
+        found = sh.found;
+        base = sh.base;
+        st_win |= sh.st_or[1];
+        if (total == 0 && rq != nullptr) {
+            st_win |= SVD_ST_ZERO_RESIDUAL;
+            rq = nullptr;  // READING: an empty residual falls back to p_j
+            continue;
+        }
+        break;
+    }
+    const int finisher = found >= 0 ? found / kAccWarps : 0;
+    if (crank != finisher) return;
+
+    // ---- the CTA holding the crossing narrows its slice down to 32 elements ------------------
+    int st = 0;
+    if (found >= 0) {
+        slice_of(finisher, found % kAccWarps, &lo, &hi);
+        while (hi - lo > 32) {
+            const int64_t part = (hi - lo + kAccWarps - 1) / kAccWarps;
+            const int64_t a = min(hi, lo + part * warp), bnd = min(hi, a + part);
+            const u128 sum = (a < bnd) ? slice_sum(rp, rq, a, bnd, false, st) : (u128)0;
+            if (lane == 0) sh.part[warp] = sum;
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                int chosen = -1;
+                u128 b = sh.base;
+                for (int i = 0; i < kAccWarps; ++i) {
+                    if (((b + sh.part[i]) << 24) > target) {
+                        chosen = i;
+                        break;
+                    }
+                    b += sh.part[i];
+                }
+                sh.found = chosen;
+                if (chosen >= 0) {
+                    sh.base = b;
+                    sh.lo = min(hi, lo + part * chosen);
+                    sh.hi = min(hi, sh.lo + part);
+                }
+            }
+            __syncthreads();
+            if (sh.found < 0) break;  // unreachable for consistent sums
+            lo = sh.lo;
+            hi = sh.hi;
+            base = sh.base;
+            __syncthreads();
+        }
+    }
+    // ---- final scan of at most 32 elements by warp 0 ------------------------------------------
+    int64_t token = -1;
+    if (warp == 0 && found >= 0) {
+        const int64_t v = lo + lane;
+        const u128 r = (v < hi) ? (u128)weight_fx(rp, rq, v, st) : (u128)0;
+        const u128 incl = warp_scan_u128(r);
+        const bool hit = (v < hi) && (((base + incl) << 24) > target);
+        const uint32_t hm = __ballot_sync(0xffffffffu, hit);
+        if (hm) {
+            token = lo + (__ffs(hm) - 1);
+        } else {  // unreachable for consistent sums: last element with weight
+            const uint32_t nz = __ballot_sync(0xffffffffu, (v < hi) && r != 0);
+            token = nz ? lo + (31 - __clz(nz)) : -1;
+        }
+    }
+    st = __reduce_or_sync(0xffffffffu, st);
+    if (lane == 0) sh.st_or[warp] = st;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int s2 = st_win;
+        for (int i = 0; i < kAccWarps; ++i) s2 |= sh.st_or[i];
+        for (int i = 0; i < j; ++i) tok[i] = draft[w * k + i];
+        for (int i = j; i <= k; ++i) tok[i] = -1;
+        if (token < 0) s2 |= SVD_ST_EMPTY;
+        else tok[j] = (int32_t)token;
+        n_emitted[w] = j + (token >= 0 ? 1 : 0);
+        status[w] = s2;
+    }
+}
+
 int accept(const float *p, const int64_t *p_rows, const float *q, const int64_t *q_rows,
            const int32_t *tgt_am, const int32_t *draft, int64_t n, int k, int64_t V,
            uint64_t seed, uint64_t woff, const float *uniforms, int32_t *out_tokens,
@@ -434,6 +643,13 @@ int accept(const float *p, const int64_t *p_rows, const float *q, const int64_t 
     if (!p || !draft || !out_tokens || !n_emitted || !status) return SVD_ERR_INVALID_ARG;
     if (n > 2147483647LL) return SVD_ERR_UNSUPPORTED;
     const int vec_ok = (aligned16(p) && (!q || aligned16(q)) && (V % 4 == 0)) ? 1 : 0;
+    // sampled windows fewer than the SMs (one verify pass): a cluster of eight CTAs each
+    if (q && n * kAccCluster <= (int64_t)kAccCluster * sm_count() && V > 32 * kAccCluster) {
+        SVD_CUDA_TRY(launch(accept_cluster_kernel, dim3((unsigned)(n * kAccCluster)),
+                            dim3(kAccThreads), 0, stream, false, p, p_rows, q, q_rows, draft, k,
+                            V, seed, woff, uniforms, out_tokens, n_emitted, status, vec_ok));
+        return SVD_OK;
+    }
     SVD_CUDA_TRY(launch(accept_kernel, dim3((unsigned)n), dim3(kAccThreads), 0, stream, false,
                         p, p_rows, q, q_rows, tgt_am, draft, k, V, seed, woff, uniforms,
                         out_tokens, n_emitted, status, vec_ok));

@@ -181,3 +181,25 @@ def test_uniform_hook_equals_philox():
     b = accept(p, draft, q=q, uniforms=uni)
     for x, y in zip(a, b):
         assert np.array_equal(x, y)
+
+
+def test_cluster_and_per_window_kernels_agree():
+    """Fewer sampled windows than SMs run on clusters of eight CTAs per window; more run one
+    CTA per window.  The same windows through both (the second call repeats them past the SM
+    count; window indices, hence the Philox uniforms, are the same) give the same bits, and
+    the oracle's."""
+    n, k, V = 40, 3, synth.VOCAB
+    lp = synth.normal_logits(n * (k + 1), V, seed=31, std=4.389)
+    lq = synth.perturb(lp.reshape(n, k + 1, V)[:, :k].reshape(n * k, V), 1.205, seed=32)
+    p, *_ = oracle.sampler(lp, np.float32(0.6), np.float32(0.95), np.float32(0.05))
+    q, *_ = oracle.sampler(lq, np.float32(0.6), np.float32(0.95), np.float32(0.05))
+    p, q = p.astype(np.float32), q.astype(np.float32)
+    draft = synth.draw_from(q, seed=33).reshape(n, k)
+    small = compare(p, draft, q=q, seed=9)  # n < SMs: the cluster kernel
+    reps = 8  # 320 windows: the per-window kernel
+    p_rows = np.tile(np.arange(n * (k + 1)).reshape(n, k + 1), (reps, 1))
+    q_rows = np.tile(np.arange(n * k).reshape(n, k), (reps, 1))
+    tok, ne, st = accept(p, np.tile(draft, (reps, 1)), q=q, p_rows=p_rows, q_rows=q_rows, seed=9)
+    # window w of the large call has index w: compare the first n with the small call
+    assert np.array_equal(tok[:n], small[0]) and np.array_equal(ne[:n], small[1])
+    assert np.array_equal(st[:n], small[2])
