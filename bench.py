@@ -121,6 +121,37 @@ def kernel_traffic():
     return None
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest x over the ranks of the default process group (the slowest replica's time),
+    or x itself when there is no group."""
+    import torch
+    import torch.distributed as td
+    if not (td.is_available() and td.is_initialized()) or td.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    td.all_reduce(t, op=td.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_rate(units_per_rank: int, world: int, ms_max: float) -> float:
+    """Whole-job rate of `world` replicas that each processed `units_per_rank` units, timed by
+    the slowest rank (units per second)."""
+    return world * units_per_rank / (ms_max / 1000.0)
+
+
+def percentiles(xs):
+    """median, p10 and p90 of a list of per-step times."""
+    ys = sorted(xs)
+    def pct(q):
+        if len(ys) == 1:
+            return ys[0]
+        i = q * (len(ys) - 1)
+        lo = int(i)
+        hi = min(lo + 1, len(ys) - 1)
+        return ys[lo] + (ys[hi] - ys[lo]) * (i - lo)
+    return {"median": pct(0.5), "p10": pct(0.1), "p90": pct(0.9)}
+
+
 def _cpu_model() -> str:
     try:
         for ln in open("/proc/cpuinfo"):
@@ -140,13 +171,13 @@ class OracleSample:
     its time is scaled by (weights of a pass) / (weights sampled).  The sampler over the 4
     positions and the acceptance of one window are timed once and added whole."""
 
-    def __init__(self, frac: float):
+    def __init__(self, frac: float, threads: int = 0):
         import numpy as np
 
         import oracle
         from speculative_decoding_verify_06_gb300 import synth
         self.np, self.oracle, self.synth = np, oracle, synth
-        self.threads = oracle.max_threads()
+        self.threads = threads or oracle.max_threads()
         C = 4
         self.frac = frac
         shapes = list(synth.LAYER_GEMMS) + [(synth.HIDDEN, synth.VOCAB // synth.LAYERS)]
@@ -219,6 +250,106 @@ def _gpu_id(dev) -> str:
         return str(dev.index or 0)
 
 
+SWEEP_C = (1, 2, 4, 6, 8, 32)
+
+
+def column_sweep(vp, dev, steps, tokens_per_pass, peak):
+    """The stack alone (one chain launch, same resident weights) at every window width of the
+    sweep; C = 32 is the batched case of 8 sequences x 4 columns."""
+    import torch
+
+    from speculative_decoding_verify_06_gb300 import stack
+    s = torch.cuda.current_stream(dev)
+    out = {}
+    for C in SWEEP_C:
+        view = stack.ColumnsView(vp, C, seed=C).capture()
+        for _ in range(3):
+            view.launch(s)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(s)
+        for _ in range(steps):
+            view.launch(s)
+        e1.record(s)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / steps
+        gbs = view.stack_bytes() / ms / 1e6
+        out[str(C)] = {"stack_ms": ms, "passes_per_s": 1000.0 / ms, "gb_s": gbs, "frac": gbs / peak}
+        del view
+        torch.cuda.empty_cache()
+    if "32" in out and "4" in out and tokens_per_pass:
+        out["batched_8x4"] = {
+            "sequences": 8,
+            "verify_tokens_per_s": 8 * out["32"]["passes_per_s"] * tokens_per_pass,
+            "hbm_frac_vs_c4": out["32"]["gb_s"] / out["4"]["gb_s"]}
+    return out
+
+
+def accept_throughput(dev, peak, n_windows=1_000_000, ks=(1, 3, 5), pool=256, seed=7):
+    """svd_accept on many windows whose rows come from a pool of (p, q) pairs larger than L2:
+    p from Zipf(1.1)-ranked logits under a random permutation, q from the same logits plus
+    tau * N(0, 1) noise (tau bisected for a mean sum min(p, q) of 0.6); every position of a
+    window draws its pair independently, so acceptances are i.i.d. with that mean.  Reports
+    windows/s, the bytes the kernel must read (the residual (p - q)+ row after a rejection,
+    the p row for the capping draw, the probed entries) per second against the copy peak,
+    and tokens per pass against (1 - a^(k+1)) / (1 - a)."""
+    import torch
+
+    from speculative_decoding_verify_06_gb300 import svd, synth
+    V = synth.VOCAB
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    base = -1.1 * torch.log(torch.arange(1, V + 1, device=dev, dtype=torch.float32))
+    perm = torch.argsort(torch.rand((pool, V), generator=g, device=dev), dim=1)
+    lp = base[perm]
+    eps = torch.randn((pool, V), generator=g, device=dev)
+    P = torch.softmax(lp, dim=1)
+
+    def mean_alpha(tau):
+        return float(torch.minimum(P, torch.softmax(lp + tau * eps, dim=1)).sum(1).mean())
+    lo, hi = 0.0, 64.0
+    for _ in range(40):
+        tau = 0.5 * (lo + hi)
+        if mean_alpha(tau) > 0.6:
+            lo = tau
+        else:
+            hi = tau
+    Q = torch.softmax(lp + tau * eps, dim=1).contiguous()
+    alpha = float(torch.minimum(P, Q).sum(1).mean())
+    P = P.contiguous()
+    samples = torch.multinomial(Q, 4096, replacement=True, generator=g)  # [pool, 4096]
+    out = {"alpha": alpha, "pool_bytes": 2 * pool * V * 4, "windows": n_windows}
+    s = torch.cuda.current_stream(dev)
+    for k in ks:
+        rows = torch.randint(0, pool, (n_windows, k + 1), generator=g, device=dev)
+        q_rows = rows[:, :k].contiguous()
+        pick = torch.randint(0, 4096, (n_windows, k), generator=g, device=dev)
+        draft = samples[q_rows, pick].to(torch.int32).contiguous()
+        tok = torch.empty((n_windows, k + 1), dtype=torch.int32, device=dev)
+        ne = torch.empty(n_windows, dtype=torch.int32, device=dev)
+        st = torch.empty(n_windows, dtype=torch.int32, device=dev)
+
+        def run(sd):
+            svd.svd_accept(P, draft, n_windows, k, V, tok, ne, st, q=Q, p_rows=rows, q_rows=q_rows,
+                           seed=sd, stream=s)
+        run(1)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        run(2)
+        e1.record(s)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1)
+        bonus = int((ne == k + 1).sum())
+        nbytes = (n_windows - bonus) * 8 * V + bonus * 4 * V + n_windows * 8 * k
+        out[f"k{k}"] = {"ms": ms, "windows_per_s": n_windows / (ms / 1000.0),
+                        "gb_s": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak,
+                        "tokens_per_pass": float(ne.double().mean()),
+                        "formula": (1 - alpha ** (k + 1)) / (1 - alpha),
+                        "status_nonzero": int((st != 0).sum())}
+    return out
+
+
 def run_svd(args, rank, world, local_rank):
     import torch
 
@@ -253,14 +384,11 @@ def run_svd(args, rank, world, local_rank):
     if dist:
         td.barrier()
     total_ms = ev[0][0].elapsed_time(ev[-1][2])
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
     stack_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     tail_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
-    t_max = total_ms
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        td.all_reduce(t, op=td.ReduceOp.MAX)
-        t_max = float(t.item())
-    passes_per_s = world * K / (t_max / 1000.0)
+    t_max = max_over_ranks(total_ms, dev)
+    passes_per_s = replica_rate(K, world, t_max)
 
     # tokens per pass of this window's (p, q): 20k windows drawn from the same rows (untimed)
     tokens_per_pass = None
@@ -301,12 +429,8 @@ def run_svd(args, rank, world, local_rank):
     e1.record(s)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - w0
-    e2e_ms = max(e0.elapsed_time(e1), wall * 1000.0)
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        td.all_reduce(t, op=td.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * Ke / (e2e_ms / 1000.0)
+    e2e_ms = max_over_ranks(max(e0.elapsed_time(e1), wall * 1000.0), dev)
+    e2e_value = replica_rate(Ke, world, e2e_ms)
 
     stack_bytes = vp.stack_bytes()
     achieved = stack_bytes / (stack_ms / 1000.0) / 1e9
@@ -328,6 +452,7 @@ def run_svd(args, rank, world, local_rank):
                    "stack_only": bool(args.stack_only)},
         "stack": {"ms": stack_ms, "passes_per_s": 1000.0 / stack_ms, "bytes": stack_bytes,
                   "gb_s": achieved, "tail_ms": tail_ms},
+        "step_ms": percentiles(step_ms),
         "tokens_per_pass": tokens_per_pass,
         "effective_tokens_per_s": (None if tokens_per_pass is None else
                                    passes_per_s * tokens_per_pass),
@@ -341,12 +466,19 @@ def run_svd(args, rank, world, local_rank):
         "gpu_launches": K * ((n_launch if args.no_chain else 1) + (1 + 4 + 1 if vp.head else 0)),
         "clocks": clk.summary(),
     }
+    if not args.no_sweep and not args.stack_only:
+        line["column_sweep"] = column_sweep(vp, dev, 20, tokens_per_pass, peak)
+        line["accept_throughput"] = accept_throughput(dev, peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         smp = OracleSample(frac=0.25)
         times = [smp.step() for _ in range(3)]
+        one = OracleSample(frac=1.0 / 64, threads=1)
+        t1 = [one.step()]
         line["cpu_baseline"] = {"value": smp.passes_per_s(times), "unit": UNIT,
                                 "cores": smp.threads, "kind": "oracle", "sample": smp.describe(3),
-                                "cpu": _cpu_model()}
+                                "cpu": _cpu_model(),
+                                "single_thread": {"value": one.passes_per_s(t1), "cores": 1,
+                                                  "sample": one.describe(1)}}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -364,6 +496,8 @@ def main():
     ap.add_argument("--no-chain", action="store_true",
                     help="one launch per matrix (with PDL) instead of the persistent chain")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the window-width sweep and the acceptance-throughput sample")
     ap.add_argument("--stack-only", action="store_true",
                     help="time the layer stack alone (no lm_head, sampler or acceptance); for "
                          "profiling small stacks")

@@ -169,3 +169,41 @@ class VerifyPass:
         if self.head:
             return [self.argmax]
         return [self.linears[-1].Y]
+
+
+class ColumnsView:
+    """The resident weights of a VerifyPass applied to a window of another width C: new
+    activations and outputs, the same 4-bit matrices, the stack as one chain launch (for the
+    sweep over window widths without re-creating 12 GB of weights)."""
+
+    def __init__(self, vp: VerifyPass, C: int, seed: int = 0):
+        self.vp, self.C = vp, C
+        dev = vp.device
+        self.X = [synth.activations_torch(C, lin.in_f, seed * 100003 + n, dev)
+                  for n, lin in enumerate(vp.linears)]
+        self.Y = [torch.empty((C, lin.out_f), dtype=torch.float32, device=dev) for lin in vp.linears]
+        self.ops = [(lin.W, x, y) for lin, x, y in zip(vp.linears, self.X, self.Y)]
+        self.ws = torch.zeros(svd.svd_verify_chain_workspace_bytes(self.ops, C), dtype=torch.uint8,
+                              device=dev)
+        self.graph = None
+
+    def enqueue(self, stream=None):
+        svd.svd_verify_chain(self.ops, self.C, self.ws, stream=stream)
+
+    def capture(self):
+        s = torch.cuda.Stream(device=self.vp.device)
+        s.wait_stream(torch.cuda.current_stream(self.vp.device))
+        with torch.cuda.stream(s):
+            self.enqueue(s)
+            s.synchronize()
+            svd.svd_graph_begin(s)
+            self.enqueue(s)
+            self.graph = svd.svd_graph_end(s)
+        s.synchronize()
+        return self
+
+    def launch(self, stream=None):
+        self.graph.launch(stream)
+
+    def stack_bytes(self) -> int:
+        return self.vp.layers * sum(roofline.linear_bytes(i, o, self.C) for i, o in self.vp.gemms)
