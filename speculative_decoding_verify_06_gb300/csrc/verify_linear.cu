@@ -252,16 +252,20 @@ struct VlOps {
 // touching activations or the workspace.
 constexpr int kPartialMax = 32 * kTiles * 4 * 4;  // entries of the largest partial (NT = 4)
 
-template <int NT, int NW, int R, int U, int MAXOPS>
+template <int NT, int NW, int TW, int R, int U, int MAXOPS>
 struct VlCfg {
     static constexpr int kThreads = NW * 32;
-    static constexpr int kAcc = kTiles * NT * 4;  // fp32 accumulators per lane
-    static constexpr int kPartial = 32 * kAcc;    // entries of a warp's (or a CTA's) partial
+    static constexpr int kWG = kTiles / TW;           // warps sharing a unit (one per TW tiles)
+    static constexpr int kNG = NW / kWG;              // worker groups per CTA
+    static constexpr int kAcc = kTiles * NT * 4;      // fp32 accumulators of a unit per lane
+    static constexpr int kAccW = TW * NT * 4;         // ... of the tiles one warp works on
+    static constexpr int kPartial = 32 * kAcc;        // entries of a row block's partial
     static constexpr int kPer = (kPartial + kThreads - 1) / kThreads;
     static constexpr int kSlotBytes = U * kUnitBytes;  // codes of U units, then their scales
-    static constexpr size_t kRing = (size_t)NW * R * kSlotBytes;
-    static constexpr size_t kPark = (size_t)NW * 2 * kPartial * sizeof(float);
+    static constexpr size_t kRing = (size_t)kNG * R * kSlotBytes;
+    static constexpr size_t kPark = (size_t)NW * 2 * 32 * kAccW * sizeof(float);
     static constexpr size_t kSmem = kRing + kPark + (size_t)MAXOPS * sizeof(VlOp);
+    static_assert(kTiles % TW == 0 && NW % kWG == 0 && (kWG == 1 || kNG <= 15), "worker groups");
     static_assert(kPartial <= kPartialMax, "partial slot size");
     static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
 };
@@ -312,17 +316,21 @@ constexpr int kBarCount = 0, kBarExit = 1, kBarEpoch = 63;
 #define SVD_PROBE(gi, what)  // timing hook for instrumented builds; nothing by default
 #endif
 
-template <int NT, int NW, int R, int U, int MAXOPS>
+template <int NT, int NW, int TW, int R, int U, int MAXOPS>
 __global__ void __launch_bounds__(NW * 32, 1)
 vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__restrict__ part,
                  unsigned *__restrict__ gbar) {
-    using Cfg = VlCfg<NT, NW, R, U, MAXOPS>;
-    constexpr int kSlotBytes = Cfg::kSlotBytes;
-    constexpr int kAcc = Cfg::kAcc, kPartial = Cfg::kPartial, kPer = Cfg::kPer;
+    using Cfg = VlCfg<NT, NW, TW, R, U, MAXOPS>;
+    constexpr int kSlotBytes = Cfg::kSlotBytes, kWG = Cfg::kWG, kNG = Cfg::kNG;
+    constexpr int kAcc = Cfg::kAcc, kAccW = Cfg::kAccW, kPartial = Cfg::kPartial, kPer = Cfg::kPer;
     constexpr int kThreads = Cfg::kThreads;
+    constexpr int kParkW = 32 * kAccW;  // floats of one parked partial
+    // With few columns the next unit's activations are loaded while this unit computes; with
+    // many the registers go to the accumulators and each unit loads its own.
+    constexpr bool kPrefetchX = NT <= 2;
     constexpr uint32_t kNone = 0xFFFFFFFFu;
     extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ __align__(8) uint64_t s_full[NW * R];
+    __shared__ __align__(8) uint64_t s_full[kNG * R];
     __shared__ uint32_t s_park_rb[NW * 2];    // row block of a parked partial, kNone if none
     __shared__ uint32_t s_park_head[NW * 2];  // 1 if that partial starts at its block's start
     __shared__ uint32_t s_epoch;
@@ -333,10 +341,11 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
     const int n_ops = P.n;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int grp = warp / kWG, sub = warp % kWG;  // worker group, and this warp's tiles in it
     const uint32_t G = gridDim.x, b = blockIdx.x;
-    const uint32_t Wtot = G * NW, gw = b * NW + warp;
-    const uint32_t full0 = smem_u32(&s_full[warp * R]);
-    uint8_t *const ring = smem + (size_t)warp * R * kSlotBytes;
+    const uint32_t Wtot = G * kNG, gw = b * kNG + grp;
+    const uint32_t full0 = smem_u32(&s_full[grp * R]);
+    uint8_t *const ring = smem + (size_t)grp * R * kSlotBytes;
     const uint32_t ring0 = smem_u32(ring);
 
     // This worker's unit range of an op: [lo, hi), empty when the op has fewer units than
@@ -353,7 +362,15 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
     // The CTA whose workers hold unit n of an op.
     auto cta_of = [&](const VlOp &o, uint32_t n) {
         const uint32_t Wop = min(Wtot, o.n_units);
-        return (((n + 1) * Wop - 1) / o.n_units) / NW;
+        return (((n + 1) * Wop - 1) / o.n_units) / kNG;
+    };
+    // The warps of a group have all read a slot.
+    auto group_sync = [&]() {
+        if constexpr (kWG == 1) {
+            __syncwarp();
+        } else {
+            asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(kWG * 32) : "memory");
+        }
     };
 
     {
@@ -362,16 +379,16 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
         uint64_t *dst = reinterpret_cast<uint64_t *>(ops);
         for (int i = threadIdx.x; i < n_ops * (int)(sizeof(VlOp) / 8); i += kThreads) dst[i] = src[i];
     }
-    if (lane == 0) {
+    if (sub == 0 && lane == 0) {
         for (int i = 0; i < R; ++i) mbar_init(full0 + 8 * i, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
 
-    // Issue cursor of this warp (uniform across its lanes; lane 0 issues): the next unit to
-    // load is unit c_u of op c_op, c_hi ends that op's range, c_codes / c_scales point at that
-    // unit's bytes; c_issued counts filled slots.  A slot takes the next U units of the
-    // range (fewer at its end; never units of two ops).
+    // Issue cursor of this group (uniform across its warps; the first warp's lane 0 issues):
+    // the next unit to load is unit c_u of op c_op, c_hi ends that op's range, c_codes /
+    // c_scales point at that unit's bytes; c_issued counts filled slots.  A slot takes the
+    // next U units of the range (fewer at its end; never units of two ops).
     int c_op = -1;
     uint32_t c_u = 0, c_hi = 0, c_issued = 0;
     const uint8_t *c_codes = nullptr, *c_scales = nullptr;
@@ -383,7 +400,7 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
             c_scales = ops[c_op].scales + (size_t)c_u * kUnitScaleBytes;
         }
         const uint32_t slot = c_issued % R, n = min((uint32_t)U, c_hi - c_u);
-        if (lane == 0) {
+        if (sub == 0 && lane == 0) {
             const uint32_t bar = full0 + 8 * slot, dst = ring0 + slot * kSlotBytes;
             mbar_expect_tx(bar, n * kUnitBytes);
             bulk_g2s(dst, c_codes, n * kUnitCodeBytes, bar);
@@ -405,15 +422,15 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
 
     const int g4 = lane >> 2, t4 = lane & 3;
     const int C = P.C;
-    float acc[kTiles][NT][4];
+    float acc[TW][NT][4];
 #pragma unroll
-    for (int r = 0; r < kTiles; ++r)
+    for (int r = 0; r < TW; ++r)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int q = 0; q < 4; ++q) acc[r][nt][q] = 0.f;
 
-    uint32_t c_used = 0;  // slots this warp has consumed (its ring position)
+    uint32_t c_used = 0;  // slots this group has consumed (its ring position)
     for (int gi = 0; gi < n_ops; ++gi) {
         const VlOp &o = ops[gi];
         if (gi > 0) {
@@ -425,16 +442,18 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
         const uint32_t n_kc = o.n_kc;
         const int64_t in_f = o.in_f, out_f = o.out_f;
         const uint32_t tag = ~((epoch << 8) | (uint32_t)(gi & 255));
-        // (row, column) of entry e of a partial: lane e / kAcc's accumulator e % kAcc
-        auto coords = [&](int e, uint32_t rb, int64_t *row, int *col) {
-            const int lsrc = e / kAcc, idx = e % kAcc, q = idx & 3, rn = idx >> 2;
-            const int r = rn / NT, nt = rn % NT;
-            *row = (int64_t)rb * kRowsPerBlock + 16 * r + (lsrc >> 2) + ((q >> 1) ? 8 : 0);
+        // (row, column) of accumulator q of n-tile nt of tile rt (0..kTiles-1) of lane lsrc
+        auto coords = [&](int lsrc, int rt, int nt, int q, uint32_t rb, int64_t *row, int *col) {
+            *row = (int64_t)rb * kRowsPerBlock + 16 * rt + (lsrc >> 2) + ((q >> 1) ? 8 : 0);
             *col = nt * 8 + (lsrc & 3) * 2 + (q & 1);
         };
+        // Parked partial k (0: the range's first segment, 1: its last) of warp `sub` of group
+        // `grp` goes to place (2 grp + k) kWG + sub, so that places in order hold nondecreasing
+        // row blocks (worker order) with the warps of a group side by side.
+        auto park_at = [&](int k) { return (2 * grp + k) * kWG + sub; };
         if (lane < 2) {
-            s_park_rb[warp * 2 + lane] = kNone;
-            s_park_head[warp * 2 + lane] = 0u;
+            s_park_rb[park_at(lane)] = kNone;
+            s_park_head[park_at(lane)] = 0u;
         }
 
         uint32_t lo, hi;
@@ -466,24 +485,29 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
 
             uint32_t rb = lo / n_kc, kc = lo - rb * n_kc, seg_lo = lo;
             uint4 xr[NT][2];
-            load_x(kc, xr);
+            if constexpr (kPrefetchX) load_x(kc, xr);
             for (uint32_t u = lo; u < hi; ++u) {
                 const uint32_t slot = c_used % R, in_slot = (u - lo) % U;
-                if (in_slot == 0u) mbar_wait(full0 + 8 * slot, (c_used / R) & 1u);
-                uint4 xc[NT][2];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    xc[nt][0] = xr[nt][0];
-                    xc[nt][1] = xr[nt][1];
-                }
                 const uint32_t kn = (kc + 1 == n_kc) ? 0u : kc + 1;
-                if (u + 1 < hi) load_x(kn, xr);
+                uint4 xc[NT][2];
+                if constexpr (kPrefetchX) {
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        xc[nt][0] = xr[nt][0];
+                        xc[nt][1] = xr[nt][1];
+                    }
+                    if (u + 1 < hi) load_x(kn, xr);
+                } else {
+                    load_x(kc, xc);
+                }
+                if (in_slot == 0u) mbar_wait(full0 + 8 * slot, (c_used / R) & 1u);
                 const uint8_t *cbase = ring + slot * kSlotBytes + in_slot * kUnitCodeBytes;
                 const uint8_t *sbase = ring + slot * kSlotBytes + U * kUnitCodeBytes + in_slot * kUnitScaleBytes;
 #pragma unroll
-                for (int r = 0; r < kTiles; ++r) {
-                    const uint4 cw = *reinterpret_cast<const uint4 *>(cbase + r * 512 + lane * 16);
-                    const uint2 scw = *reinterpret_cast<const uint2 *>(sbase + r * 64 + g4 * 8);
+                for (int r = 0; r < TW; ++r) {
+                    const int rt = sub * TW + r;
+                    const uint4 cw = *reinterpret_cast<const uint4 *>(cbase + rt * 512 + lane * 16);
+                    const uint2 scw = *reinterpret_cast<const uint2 *>(sbase + rt * 64 + g4 * 8);
                     const float2 s_lo = __half22float2(*reinterpret_cast<const __half2 *>(&scw.x));
                     const float2 s_hi = __half22float2(*reinterpret_cast<const __half2 *>(&scw.y));
 #pragma unroll
@@ -504,11 +528,12 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
                         }
                     }
                 }
-                // Once the slot is read, refill it with the units R slots further on.  Every
-                // value this warp loaded from the slot has been consumed by the instructions
-                // above (issued in order), so the bulk copy cannot overwrite a pending read.
+                // Once the group has read the slot, refill it with the units R slots further
+                // on.  Every value a warp loaded from the slot has been consumed by the
+                // instructions above (issued in order), so the bulk copy cannot overwrite a
+                // pending read.
                 if (in_slot == U - 1u || u + 1 == hi) {
-                    __syncwarp();
+                    group_sync();
                     issue();
                     ++c_used;
                 }
@@ -520,32 +545,32 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
                     const bool head = seg_lo == rb * n_kc;
                     if (head && rb_end) {
 #pragma unroll
-                        for (int r = 0; r < kTiles; ++r)
+                        for (int r = 0; r < TW; ++r)
 #pragma unroll
                             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                                 for (int q = 0; q < 4; ++q) {
                                     int64_t row;
                                     int col;
-                                    coords(lane * kAcc + (r * NT + nt) * 4 + q, rb, &row, &col);
+                                    coords(lane, sub * TW + r, nt, q, rb, &row, &col);
                                     if (row < out_f && col < C) o.Y[(int64_t)col * out_f + row] = acc[r][nt][q];
                                 }
                     } else {
                         const int k = seg_lo == lo ? 0 : 1;
-                        float4 *dst = reinterpret_cast<float4 *>(park + (warp * 2 + k) * kPartial + lane * kAcc);
+                        float4 *dst = reinterpret_cast<float4 *>(park + park_at(k) * kParkW + lane * kAccW);
 #pragma unroll
-                        for (int r = 0; r < kTiles; ++r)
+                        for (int r = 0; r < TW; ++r)
 #pragma unroll
                             for (int nt = 0; nt < NT; ++nt)
                                 dst[r * NT + nt] = make_float4(acc[r][nt][0], acc[r][nt][1],
                                                                acc[r][nt][2], acc[r][nt][3]);
                         if (lane == 0) {
-                            s_park_rb[warp * 2 + k] = rb;
-                            s_park_head[warp * 2 + k] = head ? 1u : 0u;
+                            s_park_rb[park_at(k)] = rb;
+                            s_park_head[park_at(k)] = head ? 1u : 0u;
                         }
                     }
 #pragma unroll
-                    for (int r = 0; r < kTiles; ++r)
+                    for (int r = 0; r < TW; ++r)
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -559,8 +584,10 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
         SVD_PROBE(gi, 1);
 
         // ---- all warps are done with the op: add the parked partials block by block, in
-        // worker order (slot 0 before slot 1 within a warp).  Parked partial i (i < 2 NW) is
+        // worker order (first segment before last within a group).  Parked partial i (i < 2 NW) is
         // looked at by lane i of every warp; runs of equal row blocks are found with ballots.
+        // Entry e of a block's partial is accumulator e % kAcc of lane e / kAcc of the whole
+        // unit; a parked partial holds the tiles of the warp that parked it.
         __syncthreads();
         {
             static_assert(2 * NW <= 32, "one lane per parked partial");
@@ -573,6 +600,14 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
             const uint32_t prev_rb = __shfl_sync(0xFFFFFFFFu, my_rb, prev < 0 ? lane : prev);
             const uint32_t starts =
                 __ballot_sync(0xFFFFFFFFu, my_rb != kNone && (prev < 0 || prev_rb != my_rb));
+            // parked partials of the warps working on tile group h: places congruent to h
+            uint32_t sub_mask[kWG];
+#pragma unroll
+            for (int h = 0; h < kWG; ++h) {
+                uint32_t m = 0u;
+                for (int i = h; i < 2 * NW; i += kWG) m |= 1u << i;
+                sub_mask[h] = m;
+            }
             for (uint32_t rest = starts; rest != 0u;) {
                 const int p = __ffs(rest) - 1;
                 rest &= rest - 1u;
@@ -585,13 +620,16 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
                 for (int m = 0; m < kPer; ++m) {
                     const int e = threadIdx.x + m * kThreads;
                     if (e >= kPartial) break;
+                    const int lsrc = e / kAcc, idx = e % kAcc, q = idx & 3, rn = idx >> 2;
+                    const int rt = rn / NT, nt = rn % NT, h = rt / TW;
                     int64_t row;
                     int col;
-                    coords(e, rb, &row, &col);
+                    coords(lsrc, rt, nt, q, rb, &row, &col);
                     if (row >= out_f || col >= C) continue;
+                    const int off = lsrc * kAccW + ((rt - h * TW) * NT + nt) * 4 + q;
                     float v = 0.f;
-                    for (uint32_t mm = members; mm != 0u; mm &= mm - 1u)
-                        v += park[(__ffs(mm) - 1) * kPartial + e];
+                    for (uint32_t mm = members & sub_mask[h]; mm != 0u; mm &= mm - 1u)
+                        v += park[(__ffs(mm) - 1) * kParkW + off];
                     if (owner) {
                         for (uint32_t bb = b + 1; bb <= b_last; ++bb)
                             v += wait_tagged(part + (size_t)bb * kPartialMax + e, tag);
@@ -686,9 +724,9 @@ vl_simt_kernel(const uint8_t *__restrict__ codes, const uint16_t *__restrict__ s
 constexpr int kNW1 = SVD_NW1;     // warps per CTA, C <= 8
 constexpr int kR1 = SVD_R1;       // ring slots per warp, C <= 8
 constexpr int kU = SVD_U;         // units per slot (one pair of bulk copies)
-constexpr int kNW2 = 8;           // warps per CTA, C <= 16 and C <= 32
-constexpr int kR2 = 4;            // ring slots per warp, C <= 16
-constexpr int kR4 = 2;            // ring slots per warp, C <= 32
+constexpr int kNW2 = 16;          // warps per CTA, C <= 16 and C <= 32: two warps per unit,
+constexpr int kTW2 = 2;           // each on two of its four 16-row tiles
+constexpr int kR2 = 2;            // ring slots per worker group, C <= 16 and C <= 32
 constexpr int kMaxCtasPerSm = 2;  // the workspace holds partial slots for this many
 constexpr int kChainMax = 256;    // ops per chain launch (kernel parameters, ~16 KB)
 
@@ -713,11 +751,11 @@ size_t vl_workspace_bytes(int64_t in_f, int64_t out_f, int C) {
     return partial_region_bytes() + kBarrierBytes;
 }
 
-template <int NT, int NW, int R, int U, int MAXOPS>
+template <int NT, int NW, int TW, int R, int U, int MAXOPS>
 static cudaError_t launch_stream(const VlOps<MAXOPS> &P, void *ws, bool pdl, bool coop,
                                  int64_t max_units, cudaStream_t stream) {
-    using Cfg = VlCfg<NT, NW, R, U, MAXOPS>;
-    auto kern = vl_stream_kernel<NT, NW, R, U, MAXOPS>;
+    using Cfg = VlCfg<NT, NW, TW, R, U, MAXOPS>;
+    auto kern = vl_stream_kernel<NT, NW, TW, R, U, MAXOPS>;
     static int per_sm_cache[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -778,9 +816,9 @@ static cudaError_t launch_ops(const VlOps<MAXOPS> &P, void *ws, bool pdl, cudaSt
         max_units = (int64_t)P.op[i].n_units > max_units ? (int64_t)P.op[i].n_units : max_units;
     const bool coop = P.n > 1;
     switch (ntiles_for(P.C)) {
-        case 1: return launch_stream<1, kNW1, kR1, kU, MAXOPS>(P, ws, pdl, coop, max_units, stream);
-        case 2: return launch_stream<2, kNW2, kR2, kU, MAXOPS>(P, ws, pdl, coop, max_units, stream);
-        default: return launch_stream<4, kNW2, kR4, kU, MAXOPS>(P, ws, pdl, coop, max_units, stream);
+        case 1: return launch_stream<1, kNW1, kTiles, kR1, kU, MAXOPS>(P, ws, pdl, coop, max_units, stream);
+        case 2: return launch_stream<2, kNW2, kTW2, kR2, kU, MAXOPS>(P, ws, pdl, coop, max_units, stream);
+        default: return launch_stream<4, kNW2, kTW2, kR2, kU, MAXOPS>(P, ws, pdl, coop, max_units, stream);
     }
 }
 
