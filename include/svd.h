@@ -258,6 +258,58 @@ void svd_graph_destroy(svd_graph *g);
  * size for); -1 on error. */
 int svd_device_sm_count(void);
 
+/* ---- host-side companions: depth policy and n-gram drafter ----------------------------- */
+/* No GPU work; safe to call from any host thread (a handle is not shared between threads
+ * without the caller's locking).
+ *
+ * Tokens per pass and speedup ("Decode is memory-bound ...", section "Speculative decoding"):
+ * with i.i.d. acceptance alpha in [0, 1] and depth k >= 0, a pass yields
+ * (1 - alpha^(k+1)) / (1 - alpha) tokens (k + 1 at alpha = 1); if one draft step costs
+ * draft_cost (>= 0) of a target pass, the speedup is that over (k * draft_cost + 1).  NaN on
+ * arguments out of range.  svd_best_depth returns the k in 1..k_max with the largest
+ * speedup (the shallower one on ties), or SVD_ERR_INVALID_ARG. */
+double svd_expected_tokens_per_pass(double alpha, int k);
+double svd_speedup(double alpha, int k, double draft_cost);
+int svd_best_depth(double alpha, double draft_cost, int k_max);
+
+/* Adaptive draft depth ("Decode is memory-bound ...", section "Two things the math says to
+ * do": throttle the depth when the measured acceptance falls below 35 %).  The handle keeps
+ * exponentially decayed counts of accepted drafts and of accept tests, fed with svd_accept's
+ * outputs: a window that emitted n tokens at depth k accepted n - 1 drafts and, when
+ * n - 1 < k, rejected one; windows with a non-zero status are skipped.  The decay halves a
+ * window's weight after half_life_windows later windows.
+ *   svd_spec_adapt_alpha: accepted / tests (NaN before the first test).
+ *   svd_spec_adapt_depth: k_max before the first test; 1 while the estimate is below
+ *   threshold (READING: the throttle drops to one draft, speculation stays on); otherwise
+ *   svd_best_depth(estimate, draft_cost, k_max).
+ * create returns NULL on bad arguments (k_max in 1..SVD_K_MAX, threshold in [0, 1],
+ * half_life_windows > 0); observe returns SVD_OK or SVD_ERR_INVALID_ARG. */
+typedef struct svd_spec_adapt svd_spec_adapt;
+svd_spec_adapt *svd_spec_adapt_create(int k_max, double draft_cost, double threshold,
+                                      double half_life_windows);
+int svd_spec_adapt_observe(svd_spec_adapt *a, const int32_t *n_emitted, const int32_t *status,
+                           int64_t n_windows, int k);
+double svd_spec_adapt_alpha(const svd_spec_adapt *a);
+int svd_spec_adapt_depth(const svd_spec_adapt *a);
+void svd_spec_adapt_destroy(svd_spec_adapt *a);
+
+/* n-gram drafter ("100 tokens per second ...", section "Lever 3: an n-gram overlay for
+ * repetition"): an incremental hash map from every key of key_len consecutive tokens (1..64;
+ * the page's sweep picked 6) to the position that followed its latest occurrence, over the
+ * prompt and everything appended since.  svd_ngram_append adds tokens (host int32 array);
+ * svd_ngram_propose looks up the last key_len tokens and, on a hit, writes up to k_max tokens
+ * of the continuation that followed the key's latest earlier occurrence (the history up to its
+ * end, at most) to out and returns how many; 0 on a miss or with fewer than key_len tokens.
+ * Keys are compared token by token, so a hash collision never yields a wrong proposal.
+ * create returns NULL on a bad key_len; the others return SVD_ERR_INVALID_ARG on null or
+ * negative arguments.  svd_ngram_length returns the history length (-1 for NULL). */
+typedef struct svd_ngram svd_ngram;
+svd_ngram *svd_ngram_create(int key_len);
+int svd_ngram_append(svd_ngram *g, const int32_t *tokens, int64_t n);
+int svd_ngram_propose(const svd_ngram *g, int32_t *out, int k_max);
+int64_t svd_ngram_length(const svd_ngram *g);
+void svd_ngram_destroy(svd_ngram *g);
+
 #if defined(__GNUC__)
 #pragma GCC visibility pop
 #endif

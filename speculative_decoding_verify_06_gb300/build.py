@@ -11,7 +11,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libsvd.so")
-SOURCES = ["verify_linear.cu", "accept.cu", "sampler.cu", "api.cu"]
+SOURCES = ["verify_linear.cu", "accept.cu", "sampler.cu", "api.cu", "host_policy.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CUDA_HOME = os.environ.get("CUDA_HOME", "/usr/local/cuda")
 
@@ -41,7 +41,7 @@ def build_library(force: bool = False, verbose: bool = False) -> str:
                     "-Xcompiler", "-fvisibility=hidden", "-I", os.path.join(ROOT, "include")]
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(obj_dir, src.replace(".cu", ".o"))
+        obj = os.path.join(obj_dir, os.path.splitext(src)[0] + ".o")
         cmd = [nvcc] + flags + ["-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd))

@@ -40,6 +40,10 @@ EXPORTS = (
     "svd_sampler_workspace_bytes", "svd_sampler_probs", "svd_lm_head_workspace_bytes",
     "svd_lm_head_softmax", "svd_accept", "svd_graph_begin", "svd_graph_end", "svd_graph_launch",
     "svd_graph_destroy", "svd_device_sm_count",
+    "svd_expected_tokens_per_pass", "svd_speedup", "svd_best_depth", "svd_spec_adapt_create",
+    "svd_spec_adapt_observe", "svd_spec_adapt_alpha", "svd_spec_adapt_depth",
+    "svd_spec_adapt_destroy", "svd_ngram_create", "svd_ngram_append", "svd_ngram_propose",
+    "svd_ngram_length", "svd_ngram_destroy",
 )
 
 
@@ -124,6 +128,19 @@ def load(path: str = LIB_PATH):
             "svd_graph_end": (i32, [P, P]),
             "svd_graph_launch": (i32, [P, P]),
             "svd_graph_destroy": (None, [P]),
+            "svd_expected_tokens_per_pass": (ctypes.c_double, [ctypes.c_double, i32]),
+            "svd_speedup": (ctypes.c_double, [ctypes.c_double, i32, ctypes.c_double]),
+            "svd_best_depth": (i32, [ctypes.c_double, ctypes.c_double, i32]),
+            "svd_spec_adapt_create": (P, [i32, ctypes.c_double, ctypes.c_double, ctypes.c_double]),
+            "svd_spec_adapt_observe": (i32, [P, P, P, i64, i32]),
+            "svd_spec_adapt_alpha": (ctypes.c_double, [P]),
+            "svd_spec_adapt_depth": (i32, [P]),
+            "svd_spec_adapt_destroy": (None, [P]),
+            "svd_ngram_create": (P, [i32]),
+            "svd_ngram_append": (i32, [P, P, i64]),
+            "svd_ngram_propose": (i32, [P, P, i32]),
+            "svd_ngram_length": (i64, [P]),
+            "svd_ngram_destroy": (None, [P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -300,3 +317,90 @@ def svd_graph_end(stream=None) -> Graph:
     h = ctypes.c_void_p()
     _check("svd_graph_end", load().svd_graph_end(_stream(stream), ctypes.byref(h)))
     return Graph(h.value)
+
+
+# ---- host-side companions: depth policy and n-gram drafter ------------------------------
+def _host_i32(a):
+    """A contiguous host int32 array (numpy) for a host-pointer argument."""
+    import numpy as np
+    if hasattr(a, "detach"):  # a torch tensor: must live on the host
+        if a.device.type != "cpu":
+            raise ValueError("host array expected")
+        a = a.detach().numpy()
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def svd_expected_tokens_per_pass(alpha: float, k: int) -> float:
+    return float(load().svd_expected_tokens_per_pass(float(alpha), int(k)))
+
+
+def svd_speedup(alpha: float, k: int, draft_cost: float) -> float:
+    return float(load().svd_speedup(float(alpha), int(k), float(draft_cost)))
+
+
+def svd_best_depth(alpha: float, draft_cost: float, k_max: int) -> int:
+    r = int(load().svd_best_depth(float(alpha), float(draft_cost), int(k_max)))
+    _check("svd_best_depth", r if r < 0 else SVD_OK)
+    return r
+
+
+class SpecAdapt:
+    """svd_spec_adapt: the draft depth throttled by the measured acceptance."""
+
+    def __init__(self, k_max: int, draft_cost: float, threshold: float = 0.35,
+                 half_life_windows: float = 256.0):
+        self._h = load().svd_spec_adapt_create(int(k_max), float(draft_cost), float(threshold),
+                                               float(half_life_windows))
+        if not self._h:
+            raise SvdError("svd_spec_adapt_create", SVD_ERR_INVALID_ARG)
+
+    def observe(self, n_emitted, k: int, status=None):
+        ne = _host_i32(n_emitted)
+        st = None if status is None else _host_i32(status)
+        _check("svd_spec_adapt_observe", load().svd_spec_adapt_observe(
+            self._h, ne.ctypes.data, None if st is None else st.ctypes.data, ne.size, int(k)))
+
+    @property
+    def alpha(self) -> float:
+        return float(load().svd_spec_adapt_alpha(self._h))
+
+    @property
+    def depth(self) -> int:
+        return int(load().svd_spec_adapt_depth(self._h))
+
+    def close(self):
+        if getattr(self, "_h", None):
+            load().svd_spec_adapt_destroy(self._h)
+            self._h = None
+
+    __del__ = close
+
+
+class NgramDrafter:
+    """svd_ngram: drafts from the continuation that followed the last key_len tokens before."""
+
+    def __init__(self, key_len: int = 6):
+        self._h = load().svd_ngram_create(int(key_len))
+        if not self._h:
+            raise SvdError("svd_ngram_create", SVD_ERR_INVALID_ARG)
+
+    def append(self, tokens):
+        t = _host_i32(tokens)
+        _check("svd_ngram_append", load().svd_ngram_append(self._h, t.ctypes.data, t.size))
+
+    def propose(self, k_max: int):
+        import numpy as np
+        out = np.empty(max(int(k_max), 1), dtype=np.int32)
+        r = int(load().svd_ngram_propose(self._h, out.ctypes.data, int(k_max)))
+        _check("svd_ngram_propose", r if r < 0 else SVD_OK)
+        return out[:r].copy()
+
+    def __len__(self) -> int:
+        return int(load().svd_ngram_length(self._h))
+
+    def close(self):
+        if getattr(self, "_h", None):
+            load().svd_ngram_destroy(self._h)
+            self._h = None
+
+    __del__ = close
