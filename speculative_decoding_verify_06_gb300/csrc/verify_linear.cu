@@ -631,8 +631,22 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
                     for (uint32_t mm = members & sub_mask[h]; mm != 0u; mm &= mm - 1u)
                         v += park[(__ffs(mm) - 1) * kParkW + off];
                     if (owner) {
-                        for (uint32_t bb = b + 1; bb <= b_last; ++bb)
-                            v += wait_tagged(part + (size_t)bb * kPartialMax + e, tag);
+                        // the other CTAs' partials, in CTA order: four loads in flight at a
+                        // time, then each waited for (normally already there) and added
+                        for (uint32_t bb = b + 1; bb <= b_last; bb += 4) {
+                            unsigned long long w4[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                if (bb + i <= b_last) w4[i] = ld_tagged(part + (size_t)(bb + i) * kPartialMax + e);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                if (bb + i > b_last) break;
+                                const float x = (uint32_t)(w4[i] >> 32) == tag
+                                                    ? __uint_as_float((uint32_t)w4[i])
+                                                    : wait_tagged(part + (size_t)(bb + i) * kPartialMax + e, tag);
+                                v += x;
+                            }
+                        }
                         o.Y[(int64_t)col * out_f + row] = v;
                     } else {
                         st_tagged(part + (size_t)b * kPartialMax + e, v, tag);
