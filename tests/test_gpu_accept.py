@@ -41,7 +41,7 @@ def compare(p, draft, q=None, **kw):
     for w in np.nonzero(~exact)[0]:
         j = ne_r[w] - 1
         assert ne[w] == ne_r[w] and np.array_equal(tok[w, :j], tok_r[w, :j])
-    # the benchmark spec's flag (u' within 1e-6 of a threshold), counted per comparison: a draw over
+    # the near-threshold flag (u' within 1e-6 of a threshold), counted per comparison: a draw over
     # V tokens is V threshold decisions, an accept test one
     draws = int(np.isfinite(margin).sum())
     decisions = draws * V + n * k
