@@ -59,6 +59,9 @@ def lib():
             L.orc_accept.restype = None
             L.orc_accept.argtypes = [P, P, P, P, P, P, i64, i32, i64, u64, u64, P, P, P, P, P, P,
                                      i32]
+            L.orc_kv_attention.restype = None
+            L.orc_kv_attention.argtypes = [P, P, P, P, P, i64, i64, i64, i64, i64, i64, dbl, P, P,
+                                           i32]
             L.orc_max_threads.restype = i32
             L.orc_max_threads.argtypes = []
             _lib = L
@@ -180,3 +183,36 @@ def accept(p, draft, q=None, target_argmax=None, seed=0, window_offset=0, unifor
     if return_margin:
         return tok, ne, st, nr, mg
     return tok, ne, st, nr
+
+
+def kv_attention(q_bf16, k_codes, k_scales, v_codes, v_scales, n_past: int, scale=None,
+                 nthreads: int = 0):
+    """Attention of the C window queries over a q8_0-key / q4_0-value cache, in fp64.
+
+    q_bf16: uint16 bf16 bits [C, Hq, D]; k_codes: int8 [Hkv, ld, D]; k_scales: uint16 fp16 bits
+    [Hkv, ld, D/32]; v_codes: uint8 [Hkv, ld, D/2] (low nibble = even dimension); v_scales:
+    uint16 fp16 bits [Hkv, ld, D/32].  The window occupies cache positions n_past .. n_past+C-1
+    and position c attends to 0 .. n_past+c; query head h reads kv head h // (Hq // Hkv).
+    scale defaults to 1/sqrt(D).  Returns (o, a), float64 [C, Hq, D]: the attention output and
+    sum_j p_j |v_j| (the scale of the parity tolerance).  Follows "Decode is memory-bound ..."
+    ("The ceiling": at long context the whole KV cache is read on every pass) and "100 tokens
+    per second ..." ("The wall": a 32K context with the cache at q8_0/q4_0).
+    """
+    q_bf16 = np.ascontiguousarray(q_bf16, dtype=np.uint16)
+    k_codes = np.ascontiguousarray(k_codes, dtype=np.int8)
+    k_scales = np.ascontiguousarray(k_scales, dtype=np.uint16)
+    v_codes = np.ascontiguousarray(v_codes, dtype=np.uint8)
+    v_scales = np.ascontiguousarray(v_scales, dtype=np.uint16)
+    C, Hq, D = q_bf16.shape
+    Hkv, ld, _ = k_codes.shape
+    assert D % 32 == 0 and Hq % Hkv == 0 and k_codes.shape == (Hkv, ld, D)
+    assert k_scales.shape == (Hkv, ld, D // 32) and v_scales.shape == (Hkv, ld, D // 32)
+    assert v_codes.shape == (Hkv, ld, D // 2) and 0 <= n_past and n_past + C <= ld
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    o = np.empty((C, Hq, D), np.float64)
+    a = np.empty((C, Hq, D), np.float64)
+    lib().orc_kv_attention(_p(q_bf16), _p(k_codes), _p(k_scales), _p(v_codes), _p(v_scales),
+                           Hq, Hkv, D, ld, int(n_past), C, float(scale), _p(o), _p(a),
+                           int(nthreads or max_threads()))
+    return o, a

@@ -408,6 +408,78 @@ void orc_accept(const float *p, const int64_t *p_rows, const float *q, const int
     }
 }
 
+/* ------------------------------------------------------------------------------------ */
+/* KV-read attention of a verify window ([P2] "The ceiling": at long context attention  */
+/* reads the whole KV cache on every pass, a second stream beside the weights; [P1]     */
+/* "The wall" and "The last mile": the target's cache held as q8_0 keys and q4_0        */
+/* values at 32K context).                                                              */
+/*                                                                                      */
+/* Cache format (READING: the pages name the formats only):                             */
+/*   keys:   8-bit code q in -128..127 with value s * q, one fp16 scale s per 32        */
+/*           consecutive dimensions of a position;                                      */
+/*           k_codes [Hkv][ld][D] int8, k_scales [Hkv][ld][D/32] fp16 bits;             */
+/*   values: 4-bit code c in 0..15 with value s * (c - 8), one fp16 scale per 32        */
+/*           dimensions; v_codes [Hkv][ld][D/2] bytes (dimension 2t in the low nibble, */
+/*           2t+1 in the high one), v_scales [Hkv][ld][D/32] fp16 bits.                 */
+/* The window's C positions sit at n_past .. n_past+C-1 of the cache (their keys and    */
+/* values already written), and window position c sees cache positions 0 .. n_past+c   */
+/* (causal).  Query head h reads kv head h / (Hq/Hkv) (consecutive groups).  Queries   */
+/* q [C][Hq][D] are bfloat16 bit patterns.  For every (c, h):                           */
+/*   s_j = scale * sum_i q[i] k_j[i],  w_j = exp(s_j - max s),                          */
+/*   o[d] = sum_j w_j v_j[d] / sum_j w_j,  a[d] = sum_j w_j |v_j[d]| / sum_j w_j        */
+/* (a is the scale of the parity tolerance).  o and a are [C][Hq][D] doubles.           */
+/* ------------------------------------------------------------------------------------ */
+void orc_kv_attention(const uint16_t *q_bf16, const int8_t *k_codes, const uint16_t *k_scales,
+                      const uint8_t *v_codes, const uint16_t *v_scales, int64_t Hq,
+                      int64_t Hkv, int64_t D, int64_t ld, int64_t n_past, int64_t C,
+                      double scale, double *o, double *a, int nthreads)
+{
+    int64_t G = Hq / Hkv, nb = D / 32, L = n_past + C;
+    if (nthreads <= 0) nthreads = 1;
+#pragma omp parallel num_threads(nthreads)
+    {
+        double *q = (double *)malloc(sizeof(double) * (size_t)D);
+        double *s = (double *)malloc(sizeof(double) * (size_t)L);
+        double *k = (double *)malloc(sizeof(double) * (size_t)D);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t row = 0; row < C * Hq; ++row) {
+            int64_t c = row / Hq, h = row % Hq, g = h / G, n = n_past + c + 1;
+            for (int64_t i = 0; i < D; ++i) q[i] = orc_bf16_to_f64(q_bf16[row * D + i]);
+            double m = -INFINITY;
+            for (int64_t j = 0; j < n; ++j) {
+                const int8_t *kc = k_codes + (g * ld + j) * D;
+                const uint16_t *ks = k_scales + (g * ld + j) * nb;
+                for (int64_t i = 0; i < D; ++i)
+                    k[i] = orc_f16_to_f64(ks[i / 32]) * (double)kc[i];
+                double dot = 0.0;
+                for (int64_t i = 0; i < D; ++i) dot += q[i] * k[i];
+                s[j] = scale * dot;
+                if (s[j] > m) m = s[j];
+            }
+            double l = 0.0;
+            for (int64_t j = 0; j < n; ++j) {
+                s[j] = exp(s[j] - m);
+                l += s[j];
+            }
+            for (int64_t d = 0; d < D; ++d) {
+                double acc = 0.0, mag = 0.0;
+                for (int64_t j = 0; j < n; ++j) {
+                    uint8_t byte = v_codes[(g * ld + j) * (D / 2) + d / 2];
+                    int code = (d & 1) ? (byte >> 4) : (byte & 15);
+                    double v = orc_f16_to_f64(v_scales[(g * ld + j) * nb + d / 32]) * (double)(code - 8);
+                    acc += s[j] * v;
+                    mag += s[j] * fabs(v);
+                }
+                o[row * D + d] = acc / l;
+                if (a) a[row * D + d] = mag / l;
+            }
+        }
+        free(q);
+        free(s);
+        free(k);
+    }
+}
+
 int orc_max_threads(void)
 {
 #ifdef _OPENMP

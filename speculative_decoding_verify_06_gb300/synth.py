@@ -11,6 +11,10 @@ for them):
 * window logits: N(0, std^2) fp32; a drafter that "shares" a fraction f of the target's logit
   variance draws l_q = sqrt(f) l_p + sqrt(1 - f) l', l' independent N(0, std^2).
 * Zipf-ranked logits: l(v) = -s ln(rank(v)) under a uniformly random ranking.
+* KV cache (keys q8_0-style, values q4_0-style): key codes uniform on -128..127 with fp16 scales
+  U(0.01, 0.04) per 32 dimensions (scores of N(0, 1) queries then spread with a standard
+  deviation near 2 after the 1/sqrt(128) scale); value codes uniform on 0..15 with the weights'
+  scale recipe; queries N(0, 1) bfloat16, [C][Hq][128].
 """
 from __future__ import annotations
 
@@ -27,6 +31,11 @@ LAYER_GEMMS = ((HIDDEN, HIDDEN + 1024 + 1024), (HIDDEN, HIDDEN), (HIDDEN, 2 * FF
 LAYER_GEMM_NAMES = ("qkv", "o", "gate_up", "down")
 
 SCALE_LO, SCALE_HI = 0.005, 0.02
+
+# Attention geometry of the same stack: the fused q|k|v output (5120 + 1024 + 1024) read as 40
+# query heads and 8 kv heads of dimension 128.
+N_Q_HEADS, N_KV_HEADS, HEAD_DIM = 40, 8, 128
+K_SCALE_LO, K_SCALE_HI = 0.01, 0.04
 
 
 def rng(seed: int) -> np.random.Generator:
@@ -110,3 +119,36 @@ def draw_from(probs: np.ndarray, seed: int) -> np.ndarray:
     cdf /= cdf[:, -1:]
     idx = (cdf <= u[:, None]).sum(axis=1)
     return np.minimum(idx, probs.shape[1] - 1).astype(np.int32)
+
+
+def kv_cache(Hkv: int, ld: int, D: int, seed: int):
+    """Canonical cache of ld positions: (k_codes int8 [Hkv, ld, D], k_scales fp16 bits
+    [Hkv, ld, D/32], v_codes uint8 [Hkv, ld, D/2] (low nibble = even dimension), v_scales fp16
+    bits [Hkv, ld, D/32])."""
+    assert D % 32 == 0
+    g = rng(seed)
+    kc = g.integers(-128, 128, size=(Hkv, ld, D), dtype=np.int8)
+    ks = f16_bits(g.uniform(K_SCALE_LO, K_SCALE_HI, size=(Hkv, ld, D // 32)))
+    vc = g.integers(0, 256, size=(Hkv, ld, D // 2), dtype=np.uint8)
+    vs = f16_bits(g.uniform(SCALE_LO, SCALE_HI, size=(Hkv, ld, D // 32)))
+    return kc, ks, vc, vs
+
+
+def queries(C: int, Hq: int, D: int, seed: int, std: float = 1.0) -> np.ndarray:
+    """bf16 bit patterns [C, Hq, D] drawn N(0, std^2)."""
+    return bf16_bits(rng(seed).normal(0.0, std, size=(C, Hq, D)).astype(np.float32))
+
+
+def kv_cache_torch(Hkv: int, ld: int, D: int, seed: int, device):
+    """The kv_cache recipe drawn on a device with torch's generator (for long contexts); returns
+    (k_codes int8, k_scales int16, v_codes uint8, v_scales int16), scales holding fp16 bits."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    kc = torch.randint(-128, 128, (Hkv, ld, D), dtype=torch.int8, device=device, generator=g)
+    ks = torch.empty((Hkv, ld, D // 32), dtype=torch.float32, device=device)
+    ks.uniform_(K_SCALE_LO, K_SCALE_HI, generator=g)
+    vc = torch.randint(0, 256, (Hkv, ld, D // 2), dtype=torch.uint8, device=device, generator=g)
+    vs = torch.empty((Hkv, ld, D // 32), dtype=torch.float32, device=device)
+    vs.uniform_(SCALE_LO, SCALE_HI, generator=g)
+    return kc, ks.to(torch.float16).view(torch.int16), vc, vs.to(torch.float16).view(torch.int16)
