@@ -350,6 +350,77 @@ def accept_throughput(dev, peak, n_windows=1_000_000, ks=(1, 3, 5), pool=256, se
     return out
 
 
+KV_CONTEXTS = (32768, 131072, 262144)
+
+
+def kv_read(dev, peak, stack_ms, layers=64, contexts=KV_CONTEXTS, steps=10, C=4, seed=5):
+    """The KV-read term of a pass: svd_kv_attention once per layer (40 query heads over 8 kv heads
+    of dimension 128, q8_0 keys and q4_0 values), each layer on its own cache, at the window's
+    last position n_past + C = context.  The 64 layer launches (split pass + merge each) are
+    recorded in one CUDA graph; all caches together exceed L2.  Reports the per-pass time, the
+    cache bytes read per second against the copy peak, and the pass rate of weights plus KV read
+    (this stack time plus the KV time, measured apart)."""
+    import torch
+
+    from speculative_decoding_verify_06_gb300 import svd, synth
+    Hq, Hkv, D = synth.N_Q_HEADS, synth.N_KV_HEADS, synth.HEAD_DIM
+    s = torch.cuda.current_stream(dev)
+    out = {}
+    for ctx in contexts:
+        n_past = ctx - C
+        nbytes = svd.svd_kv_cache_bytes(Hkv, ctx)
+        kc, ks, vc, vs = synth.kv_cache_torch(Hkv, ctx, D, seed, dev)
+        caches = []
+        for _ in range(layers):
+            cache = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+            svd.svd_kv_repack(kc, ks, vc, vs, Hkv, ctx, 0, ctx, cache, ctx, stream=s)
+            caches.append(cache)
+        del kc, ks, vc, vs
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        q = torch.randn((C, Hq, D), generator=g, device=dev).to(torch.bfloat16)
+        o = torch.empty((C, Hq, D), dtype=torch.float32, device=dev)
+        ws = torch.zeros(svd.svd_kv_attention_workspace_bytes(Hq, Hkv, C), dtype=torch.uint8,
+                         device=dev)
+        scale = 1.0 / D ** 0.5
+
+        def one_pass(st):
+            for cache in caches:
+                svd.svd_kv_attention(q, cache, ctx, Hq, Hkv, n_past, C, scale, o, ws, stream=st)
+        one_pass(s)
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        cs = torch.cuda.Stream(dev)
+        with torch.cuda.stream(cs):
+            graph.capture_begin()
+            one_pass(cs)
+            graph.capture_end()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(steps):
+            graph.replay()
+        e1.record(s)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / steps
+        read = layers * (Hkv * -(-ctx // 16) * svd.SVD_KV_UNIT_BYTES + C * Hq * D * (2 + 4))
+        gbs = read / ms / 1e6
+        flags = int(ws[:4].view(torch.int32).item())
+        out[str(ctx)] = {"kv_ms_per_pass": ms, "per_layer_us": 1000.0 * ms / layers,
+                         "kv_bytes_per_pass": read, "gb_s": gbs, "frac": gbs / peak,
+                         "wait_flags": flags}
+        if stack_ms:
+            out[str(ctx)]["passes_per_s_weights_plus_kv"] = 1000.0 / (stack_ms + ms)
+        del graph, caches, q, o, ws
+        torch.cuda.empty_cache()
+    out["launches_per_pass"] = 2 * layers
+    out["workload"] = (f"{layers} layers x svd_kv_attention: {Hq} query heads, {Hkv} kv heads, "
+                       f"dim {D}, K+1 = {C}, keys q8_0 / values q4_0, one cache per layer")
+    return out
+
+
 def run_svd(args, rank, world, local_rank):
     import torch
 
@@ -469,6 +540,9 @@ def run_svd(args, rank, world, local_rank):
     if not args.no_sweep and not args.stack_only:
         line["column_sweep"] = column_sweep(vp, dev, 20, tokens_per_pass, peak)
         line["accept_throughput"] = accept_throughput(dev, peak)
+    if not args.no_kv and not args.stack_only:
+        line["kv_read"] = kv_read(dev, peak, line["stack"]["ms"], layers=args.layers,
+                                  contexts=tuple(int(c) for c in args.kv_contexts.split(",")))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         smp = OracleSample(frac=0.25)
         times = [smp.step() for _ in range(3)]
@@ -496,6 +570,12 @@ def main():
     ap.add_argument("--no-chain", action="store_true",
                     help="one launch per matrix (with PDL) instead of the persistent chain")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-kv", action="store_true",
+                    help="skip the KV-read measurement (attention over q8_0/q4_0 caches)")
+    ap.add_argument("--kv-only", action="store_true",
+                    help="print only the KV-read measurement")
+    ap.add_argument("--kv-contexts", default=",".join(str(c) for c in KV_CONTEXTS),
+                    help="comma-separated context lengths of the KV-read measurement")
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the window-width sweep and the acceptance-throughput sample")
     ap.add_argument("--stack-only", action="store_true",
@@ -508,6 +588,18 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank)
+        return
+    if args.kv_only:
+        import torch
+
+        from speculative_decoding_verify_06_gb300 import build
+        build.build_library()
+        dev = torch.device("cuda", local_rank)
+        torch.cuda.set_device(dev)
+        peak, _ = peaks()
+        ctxs = tuple(int(c) for c in args.kv_contexts.split(","))
+        print(json.dumps({"kv_read": kv_read(dev, peak, None, layers=args.layers,
+                                             contexts=ctxs, steps=args.steps)}), flush=True)
         return
     if world > 1:
         import torch

@@ -258,6 +258,54 @@ void svd_graph_destroy(svd_graph *g);
  * size for); -1 on error. */
 int svd_device_sm_count(void);
 
+/* ---- KV-read attention of a verify window ------------------------------------------------ */
+/* "Decode is memory-bound ..." ("The ceiling"): at long context attention reads the whole KV
+ * cache on every pass, beside the weights; "100 tokens per second ..." ("The wall"): the
+ * target's cache at q8_0 keys and q4_0 values, 32K context.
+ *
+ * Canonical cache arrays of one layer (device, caller-owned), ld positions per kv head:
+ *   k_codes  int8  [Hkv][ld][128]     key value = d * q
+ *   k_scales fp16  [Hkv][ld][4]       one d per 32 dimensions
+ *   v_codes  uint8 [Hkv][ld][64]      value = d * (c - 8); dimension 2t in the low nibble
+ *   v_scales fp16  [Hkv][ld][4]
+ * Native cache: units of 16 positions of one kv head, SVD_KV_UNIT_BYTES each, laid out
+ * [Hkv][ceil(capacity / 16)][unit] (key codes, value codes, key scales, value scales in the
+ * tensor-core fragment order of the attention kernel); 16-byte aligned.
+ *
+ * svd_kv_cache_bytes: bytes of a native cache for `capacity` positions (0 on bad sizes).
+ * svd_kv_repack: writes positions [pos_begin, pos_end) of every kv head from the canonical
+ *   arrays into the native cache (the append of a window's keys and values, or a whole cache);
+ *   other positions are untouched.  svd_kv_unpack is its inverse (canonical arrays written for
+ *   those positions).  Both return SVD_ERR_INVALID_ARG for null pointers, a misaligned cache,
+ *   pos_end > capacity or pos_end > ld.
+ * svd_kv_attention: for window position c = 0..C-1 (cache position n_past + c, its key and value
+ *   already written) and query head h (kv head h / (Hq / Hkv)):
+ *     o[c][h] = sum_{j <= n_past + c} softmax_j(scale * <q[c][h], k_j>) v_j
+ *   q: bf16 [C][Hq][128]; out: fp32 [C][Hq][128]; both and the cache 16-byte aligned.
+ *   Queries are used as f16: exact for bf16 values of magnitude in [2^-14, 65504] (and 0),
+ *   rounded outside.  Positions of the cache beyond n_past + C are never read into the result,
+ *   whatever their bytes.  The workspace (svd_kv_attention_workspace_bytes, 16-byte aligned)
+ *   holds per-split partials; its first 32-bit word gets bit 0 set if a bounded wait of the
+ *   kernel gave up (zero it once to watch it).  Two kernels are enqueued (the split pass and its
+ *   merge, the latter a programmatic dependent launch).  Errors: SVD_ERR_INVALID_ARG for null or
+ *   misaligned pointers, Hq % Hkv != 0, C < 1, n_past < 0, n_past + C > capacity or a scale that
+ *   is not positive and finite; SVD_ERR_WORKSPACE for a short workspace.
+ */
+#define SVD_KV_HEAD_DIM 128
+#define SVD_KV_UNIT_POSITIONS 16
+#define SVD_KV_UNIT_BYTES 3328
+size_t svd_kv_cache_bytes(int n_kv_heads, int capacity);
+int svd_kv_repack(const int8_t *k_codes, const uint16_t *k_scales, const uint8_t *v_codes,
+                  const uint16_t *v_scales, int n_kv_heads, int ld, int pos_begin, int pos_end,
+                  void *cache, int capacity, svd_stream_t stream);
+int svd_kv_unpack(const void *cache, int capacity, int n_kv_heads, int pos_begin, int pos_end,
+                  int8_t *k_codes, uint16_t *k_scales, uint8_t *v_codes, uint16_t *v_scales,
+                  int ld, svd_stream_t stream);
+size_t svd_kv_attention_workspace_bytes(int n_q_heads, int n_kv_heads, int C);
+int svd_kv_attention(const uint16_t *q, const void *cache, int capacity, int n_q_heads,
+                     int n_kv_heads, int n_past, int C, float scale, float *out, void *workspace,
+                     size_t workspace_bytes, svd_stream_t stream);
+
 /* ---- host-side companions: depth policy and n-gram drafter ----------------------------- */
 /* No GPU work; safe to call from any host thread (a handle is not shared between threads
  * without the caller's locking).

@@ -141,24 +141,6 @@ __global__ void unpack_scales_kernel(const uint16_t *__restrict__ src, uint16_t 
 }
 
 // ---- device building blocks -----------------------------------------------------------
-// Bulk (TMA-engine) copies into shared memory completing on an mbarrier.
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(mbar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
-                                         uint32_t mbar) {
-    asm volatile(
-        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-        "l"(src), "r"(bytes), "r"(mbar)
-        : "memory");
-}
 // Activations read through L2 only: in a chain, op i+1 may read what op i wrote in the same
 // kernel, so the non-coherent path must not be used there.
 __device__ __forceinline__ uint4 ldg_cg_v4(const void *p) {
@@ -168,21 +150,6 @@ __device__ __forceinline__ uint4 ldg_cg_v4(const void *p) {
                  : "l"(p));
     return v;
 }
-// Waits for phase `parity` of an mbarrier; gives up after a bounded number of polls (each poll
-// may suspend the thread briefly), so a broken pipeline cannot hang the GPU.
-__device__ __forceinline__ void mbar_wait(uint32_t mbar, uint32_t parity) {
-    for (int it = 0; it < (1 << 22); ++it) {
-        uint32_t ok;
-        asm volatile(
-            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; "
-            "selp.u32 %0, 1, 0, p; }"
-            : "=r"(ok)
-            : "r"(mbar), "r"(parity)
-            : "memory");
-        if (ok) return;
-    }
-}
-
 // Four bf16x2 A registers from one native word: (bits >> 4p) & 0x000F000F | 0x43004300 is the
 // pair (128 + c_lo, 128 + c_hi) exactly; subtracting (136, 136) leaves (c - 8) exactly.
 __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t a[4]) {

@@ -31,6 +31,9 @@ SVD_LAYOUT_NATIVE = 1
 SVD_F_PDL = 1
 SVD_C_MAX = 32
 SVD_K_MAX = 32
+SVD_KV_HEAD_DIM = 128
+SVD_KV_UNIT_POSITIONS = 16
+SVD_KV_UNIT_BYTES = 3328
 
 # Every symbol include/svd.h declares (checked by the CPU test suite).
 EXPORTS = (
@@ -44,6 +47,8 @@ EXPORTS = (
     "svd_spec_adapt_observe", "svd_spec_adapt_alpha", "svd_spec_adapt_depth",
     "svd_spec_adapt_destroy", "svd_ngram_create", "svd_ngram_append", "svd_ngram_propose",
     "svd_ngram_length", "svd_ngram_destroy",
+    "svd_kv_cache_bytes", "svd_kv_repack", "svd_kv_unpack", "svd_kv_attention_workspace_bytes",
+    "svd_kv_attention",
 )
 
 
@@ -141,6 +146,12 @@ def load(path: str = LIB_PATH):
             "svd_ngram_propose": (i32, [P, P, i32]),
             "svd_ngram_length": (i64, [P]),
             "svd_ngram_destroy": (None, [P]),
+            "svd_kv_cache_bytes": (sz, [i32, i32]),
+            "svd_kv_repack": (i32, [P, P, P, P, i32, i32, i32, i32, P, i32, P]),
+            "svd_kv_unpack": (i32, [P, i32, i32, i32, i32, P, P, P, P, i32, P]),
+            "svd_kv_attention_workspace_bytes": (sz, [i32, i32, i32]),
+            "svd_kv_attention": (i32, [P, P, i32, i32, i32, i32, i32, ctypes.c_float, P, P, sz,
+                                       P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -404,3 +415,35 @@ class NgramDrafter:
             self._h = None
 
     __del__ = close
+
+
+def svd_kv_cache_bytes(n_kv_heads: int, capacity: int) -> int:
+    return int(load().svd_kv_cache_bytes(int(n_kv_heads), int(capacity)))
+
+
+def svd_kv_repack(k_codes, k_scales, v_codes, v_scales, n_kv_heads: int, ld: int,
+                  pos_begin: int, pos_end: int, cache, capacity: int, stream=None):
+    _check("svd_kv_repack", load().svd_kv_repack(
+        _ptr(k_codes), _ptr(k_scales), _ptr(v_codes), _ptr(v_scales), int(n_kv_heads), int(ld),
+        int(pos_begin), int(pos_end), _ptr(cache), int(capacity), _stream(stream)))
+
+
+def svd_kv_unpack(cache, capacity: int, n_kv_heads: int, pos_begin: int, pos_end: int,
+                  k_codes, k_scales, v_codes, v_scales, ld: int, stream=None):
+    _check("svd_kv_unpack", load().svd_kv_unpack(
+        _ptr(cache), int(capacity), int(n_kv_heads), int(pos_begin), int(pos_end), _ptr(k_codes),
+        _ptr(k_scales), _ptr(v_codes), _ptr(v_scales), int(ld), _stream(stream)))
+
+
+def svd_kv_attention_workspace_bytes(n_q_heads: int, n_kv_heads: int, C: int) -> int:
+    return int(load().svd_kv_attention_workspace_bytes(int(n_q_heads), int(n_kv_heads), int(C)))
+
+
+def svd_kv_attention(q, cache, capacity: int, n_q_heads: int, n_kv_heads: int, n_past: int,
+                     C: int, scale: float, out, workspace, workspace_bytes: int = 0,
+                     stream=None):
+    if not workspace_bytes and workspace is not None and not isinstance(workspace, int):
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check("svd_kv_attention", load().svd_kv_attention(
+        _ptr(q), _ptr(cache), int(capacity), int(n_q_heads), int(n_kv_heads), int(n_past), int(C),
+        float(scale), _ptr(out), _ptr(workspace), int(workspace_bytes), _stream(stream)))
