@@ -56,9 +56,13 @@ constexpr int kRing = 4;
 constexpr int kRowsPerGroup = 24;
 constexpr int kPitch = 132;  // floats per row of the merge buffer (conflict-free writes)
 constexpr float kLazy = 8.0f;
+constexpr int kQPitch = 272;  // bytes per f16 query row in shared memory (conflict-free ldmatrix)
 constexpr int kRingBytes = kWarps * kRing * kUnitBytes;
 constexpr int kMbarBytes = kWarps * kRing * 8;
-constexpr int kSmemBytes = kRingBytes + kMbarBytes + 2 * kWarps * kRowsPerGroup * 4;
+constexpr int kQBytes = kRowsPerGroup * kQPitch;
+constexpr int kCorrBytes = kRowsPerGroup * 4 * 4;
+constexpr int kSmemBytes = kRingBytes + kMbarBytes + kQBytes + kCorrBytes + 2 * kWarps * kRowsPerGroup * 4;
+constexpr int kMaxSplitRounds = 5;  // splits per row merged by one warp: up to 32 per round
 constexpr size_t kHeaderBytes = 256;
 constexpr size_t kPartialBytes = (size_t)kRowsPerGroup * kD * 4 + (size_t)kRowsPerGroup * 8;
 static_assert(kWarps * kRowsPerGroup * kPitch * 4 <= kRingBytes, "merge buffer fits the ring");
@@ -87,13 +91,12 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
                  : "r"(a));
     return v;
 }
-// Two f16 registers (1024 + u) from four biased key bytes, then minus 1152: the codes q exactly.
+// Two f16 registers (1024 + u) = q + 1152 from four biased key bytes u = q + 128 (exact); the
+// 1152 * sum(q) offset of each 32-dimension block is removed through the accumulator's initial
+// value.
 __device__ __forceinline__ void key_regs(uint32_t w, uint32_t &lo, uint32_t &hi) {
-    uint32_t a, b;
-    asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(w), "r"(0x64646464u));
-    asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(w), "r"(0x64646464u));
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
+    asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(w), "r"(0x64646464u));
+    asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(w), "r"(0x64646464u));
 }
 // Four bf16 registers (128 + c) - 136 = c - 8 exactly, from one value word.
 __device__ __forceinline__ void value_regs(uint32_t w, uint32_t a[4]) {
@@ -129,10 +132,49 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t r[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
 __device__ __forceinline__ uint32_t transpose8x8(uint32_t x) {
     uint32_t y;
     asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
     return y;
+}
+// Two fp32 values in one 64-bit register pair, for the paired fp32 instructions of sm_100+.
+typedef unsigned long long f2_t;
+__device__ __forceinline__ f2_t f2(float lo, float hi) {
+    f2_t r;
+    asm("mov.b64 %0, {%1,%2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unf2(f2_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0,%1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f2_t mul2(f2_t a, f2_t b) {
+    f2_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2_t fma2(f2_t a, f2_t b, f2_t c) {
+    f2_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ f2_t add2(f2_t a, f2_t b) {
+    f2_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+// First product of a block's accumulator: C = (c0, c1, c0, c1), the per-row offset removal.
+__device__ __forceinline__ void mma_f16_init(float d[4], const uint32_t a[4], uint32_t b0,
+                                             uint32_t b1, float c0, float c1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%10,%11,%10,%11};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c0), "f"(c1));
 }
 __device__ __forceinline__ float2 half2_bits_to_float2(uint32_t h) {
     return __half22float2(*reinterpret_cast<const __half2 *>(&h));
@@ -144,11 +186,12 @@ __global__ void __launch_bounds__(kThreads, 1) kv_attention_kernel(const KvaPara
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
     const int split = blockIdx.x, g = blockIdx.y, rg = blockIdx.z;
     const int cta = (rg * P.Hkv + g) * P.splits + split;
-    float *wm = reinterpret_cast<float *>(smem + kRingBytes + kMbarBytes);
+    float *corr_s = reinterpret_cast<float *>(smem + kRingBytes + kMbarBytes + kQBytes);
+    float *wm = corr_s + kRowsPerGroup * 4;
     float *wl = wm + kWarps * kRowsPerGroup;
+    const uint32_t qs = smem_u32(smem + kRingBytes + kMbarBytes);
 
     griddep_launch_dependents();  // the merge kernel may become resident and wait
-    griddep_wait();               // queries and cache written by the kernels before this one
 
     // This warp's run of units.
     const int cb = (int)((long long)split * P.n_units / P.splits);
@@ -162,6 +205,9 @@ __global__ void __launch_bounds__(kThreads, 1) kv_attention_kernel(const KvaPara
 #pragma unroll
         for (int r = 0; r < kRing; ++r) mbar_init(mb0 + 8 * r, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    griddep_wait();  // queries and cache written by the kernels before this one
+    if (lane == 0) {
 #pragma unroll
         for (int r = 0; r < kRing; ++r)
             if (wb + r < we) {
@@ -170,25 +216,48 @@ __global__ void __launch_bounds__(kThreads, 1) kv_attention_kernel(const KvaPara
                          mb0 + 8 * r);
             }
     }
-    __syncwarp();
 
-    // Query B fragments (f16): k-step ks, n-tile nt -> rows 8 nt + gid, dims 16 ks + 2 tig (+8).
-    uint32_t qf[8][NT][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const int row = rg * kRowsPerGroup + 8 * nt + gid;
-        const bool ok = row < P.rows;
-        const int c = ok ? row / P.G : 0, h = g * P.G + (ok ? row % P.G : 0);
-        const uint32_t *qrow = reinterpret_cast<const uint32_t *>(P.q + ((size_t)c * P.Hq + h) * kD);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const uint32_t bits = ok ? __ldg(qrow + 8 * ks + tig + 4 * j) : 0u;
-                qf[ks][nt][j] = pack_f16(__uint_as_float(bits << 16),
-                                         __uint_as_float(bits & 0xFFFF0000u));
-            }
+    // The CTA's query rows (row = c * G + head in group) as f16 in shared memory, zero past the
+    // last row; each warp reads them as B fragments with ldmatrix.
+    for (int idx = threadIdx.x; idx < kRowsPerGroup * (kD / 2); idx += kThreads) {
+        const int r = idx / (kD / 2), pr = idx % (kD / 2);
+        const int row = rg * kRowsPerGroup + r;
+        uint32_t bits = 0u;
+        if (row < P.rows) {
+            const int c = row / P.G, h = g * P.G + row % P.G;
+            bits = __ldg(reinterpret_cast<const uint32_t *>(P.q + ((size_t)c * P.Hq + h) * kD) + pr);
+        }
+        const uint32_t v = pack_f16(__uint_as_float(bits << 16), __uint_as_float(bits & 0xFFFF0000u));
+        asm volatile("st.shared.u32 [%0], %1;" ::"r"(qs + r * kQPitch + 4 * pr), "r"(v));
     }
+    __syncthreads();
+    // -1152 * (sum of the f16 query values of each row and 32-dimension block), in fp32.
+    if (threadIdx.x < kRowsPerGroup * 4) {
+        const int r = threadIdx.x >> 2, b = threadIdx.x & 3;
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 v = lds128(qs + r * kQPitch + 64 * b + 16 * i);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 f = half2_bits_to_float2(w[j]);
+                acc += f.x + f.y;
+            }
+        }
+        corr_s[r * 4 + b] = -1152.f * acc;
+    }
+    __syncthreads();
+    float corr[4][NT][2];
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) corr[b][nt][e] = corr_s[(8 * nt + 2 * tig + e) * 4 + b];
+    // ldmatrix row address of this lane: matrix i = lane / 8 covers k-step 2b + i / 2, dims
+    // +8 (i % 2); row 8 nt + lane % 8.
+    const uint32_t qlane = qs + (lane & 7) * kQPitch + 2 * (16 * (lane >> 4) + 8 * ((lane >> 3) & 1));
 
     float o[8][NT][4];
     float m[NT][2], l[NT][2];
@@ -205,6 +274,15 @@ __global__ void __launch_bounds__(kThreads, 1) kv_attention_kernel(const KvaPara
             for (int i = 0; i < 4; ++i) o[mt][nt][i] = 0.f;
     }
     const int L = P.n_past + P.C;
+    const float scl = P.scale_log2;
+    const f2_t scl2 = f2(scl, scl);
+    const float lazy = kLazy / scl;  // the rescale threshold in code units
+    f2_t nm[NT], lsum[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        nm[nt] = f2(0.f, 0.f);
+        lsum[nt] = f2(0.f, 0.f);
+    }
     bool failed = false;
     int it_f = 0;
 
@@ -218,46 +296,45 @@ __global__ void __launch_bounds__(kThreads, 1) kv_attention_kernel(const KvaPara
         }
         const uint32_t su = ring + slot * kUnitBytes;
         const uint4 ksr = lds128(su + kOffKS + 16 * gid);
-        const float scl = P.scale_log2;
         const float2 kA01 = half2_bits_to_float2(ksr.x), kA23 = half2_bits_to_float2(ksr.y);
         const float2 kB01 = half2_bits_to_float2(ksr.z), kB23 = half2_bits_to_float2(ksr.w);
-        const float kA[4] = {kA01.x * scl, kA01.y * scl, kA23.x * scl, kA23.y * scl};
-        const float kB[4] = {kB01.x * scl, kB01.y * scl, kB23.x * scl, kB23.y * scl};
+        const f2_t kA[4] = {f2(kA01.x, kA01.x), f2(kA01.y, kA01.y), f2(kA23.x, kA23.x),
+                            f2(kA23.y, kA23.y)};
+        const f2_t kB[4] = {f2(kB01.x, kB01.x), f2(kB01.y, kB01.y), f2(kB23.x, kB23.x),
+                            f2(kB23.y, kB23.y)};
 
-        // S^T = K Q^T, one fresh accumulator per 32-dimension block.
-        float s[NT][4];
+        // S^T = K Q^T in code units, one fresh accumulator per 32-dimension block scaled by its
+        // key scale: sA = the row pair of position gid, sB = of position gid + 8.
+        f2_t sA[NT], sB[NT];
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
             const uint4 kw = lds128(su + 512 * b + 16 * lane);
             float acc[NT][4];
+            uint32_t qb[NT][4];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
+            for (int nt = 0; nt < NT; ++nt) ldsm_x4(qlane + 8 * nt * kQPitch + 64 * b, qb[nt]);
             uint32_t a[4];
             key_regs(kw.x, a[0], a[1]);
             key_regs(kw.y, a[2], a[3]);
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma_f16(acc[nt], a, qf[2 * b][nt][0], qf[2 * b][nt][1]);
+            for (int nt = 0; nt < NT; ++nt)
+                mma_f16_init(acc[nt], a, qb[nt][0], qb[nt][1], corr[b][nt][0], corr[b][nt][1]);
             key_regs(kw.z, a[0], a[1]);
             key_regs(kw.w, a[2], a[3]);
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-                mma_f16(acc[nt], a, qf[2 * b + 1][nt][0], qf[2 * b + 1][nt][1]);
+            for (int nt = 0; nt < NT; ++nt) mma_f16(acc[nt], a, qb[nt][2], qb[nt][3]);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                if (b == 0) {
-                    s[nt][0] = kA[0] * acc[nt][0];
-                    s[nt][1] = kA[0] * acc[nt][1];
-                    s[nt][2] = kB[0] * acc[nt][2];
-                    s[nt][3] = kB[0] * acc[nt][3];
-                } else {
-                    s[nt][0] = fmaf(kA[b], acc[nt][0], s[nt][0]);
-                    s[nt][1] = fmaf(kA[b], acc[nt][1], s[nt][1]);
-                    s[nt][2] = fmaf(kB[b], acc[nt][2], s[nt][2]);
-                    s[nt][3] = fmaf(kB[b], acc[nt][3], s[nt][3]);
-                }
+                const f2_t x = f2(acc[nt][0], acc[nt][1]), y = f2(acc[nt][2], acc[nt][3]);
+                sA[nt] = b == 0 ? mul2(x, kA[0]) : fma2(x, kA[b], sA[nt]);
+                sB[nt] = b == 0 ? mul2(y, kB[0]) : fma2(y, kB[b], sB[nt]);
             }
+        }
+        float s[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            unf2(sA[nt], s[nt][0], s[nt][1]);
+            unf2(sB[nt], s[nt][2], s[nt][3]);
         }
 
         const uint4 vsr = lds128(su + kOffVS + 16 * gid);
@@ -280,7 +357,8 @@ __global__ void __launch_bounds__(kThreads, 1) kv_attention_kernel(const KvaPara
             if (pB >= L) vB01 = vB23 = make_float2(0.f, 0.f);
         }
 
-        // Online softmax with a lazy running max.
+        // Online softmax in base 2 with a lazy running max.  m is kept in code units (the scale
+        // is positive), with nm = -m * scale for the exponent's fused multiply-add.
         bool need = false;
         float mloc[NT][2];
 #pragma unroll
@@ -288,11 +366,12 @@ __global__ void __launch_bounds__(kThreads, 1) kv_attention_kernel(const KvaPara
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 mloc[nt][e] = fmaxf(s[nt][e], s[nt][e + 2]);
-                need |= mloc[nt][e] > m[nt][e] + kLazy;
+                need |= mloc[nt][e] > m[nt][e] + lazy;
             }
         if (__any_sync(0xFFFFFFFFu, need)) {
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+            for (int nt = 0; nt < NT; ++nt) {
+                float nmv[2], fv[2];
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     float mx = mloc[nt][e];
@@ -300,26 +379,31 @@ __global__ void __launch_bounds__(kThreads, 1) kv_attention_kernel(const KvaPara
                     mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
                     mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
                     const float mn = fmaxf(m[nt][e], mx);
-                    const float f = m[nt][e] == -INFINITY ? 0.f : ex2(m[nt][e] - mn);
+                    const float f = m[nt][e] == -INFINITY ? 0.f : ex2((m[nt][e] - mn) * scl);
                     m[nt][e] = mn;
-                    l[nt][e] *= f;
+                    nmv[e] = mn == -INFINITY ? 0.f : -mn * scl;
+                    fv[e] = f;
 #pragma unroll
                     for (int mt = 0; mt < 8; ++mt) {
                         o[mt][nt][e] *= f;
                         o[mt][nt][e + 2] *= f;
                     }
                 }
+                nm[nt] = f2(nmv[0], nmv[1]);
+                lsum[nt] = mul2(lsum[nt], f2(fv[0], fv[1]));
+            }
         }
+        // p = 2^(s * scale - m * scale); masked scores give exactly 0.
         float p[NT][4];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+        for (int nt = 0; nt < NT; ++nt) {
+            float t[4];
+            unf2(fma2(f2(s[nt][0], s[nt][1]), scl2, nm[nt]), t[0], t[1]);
+            unf2(fma2(f2(s[nt][2], s[nt][3]), scl2, nm[nt]), t[2], t[3]);
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const float ms = m[nt][e] == -INFINITY ? 0.f : m[nt][e];
-                p[nt][e] = ex2(s[nt][e] - ms);
-                p[nt][e + 2] = ex2(s[nt][e + 2] - ms);
-                l[nt][e] += p[nt][e] + p[nt][e + 2];
-            }
+            for (int i = 0; i < 4; ++i) p[nt][i] = ex2(t[i]);
+            lsum[nt] = add2(lsum[nt], add2(f2(p[nt][0], p[nt][1]), f2(p[nt][2], p[nt][3])));
+        }
 
         // O^T += V^T P'^T, P' = p * d_v of the value block.
         const uint4 vw0 = lds128(su + kOffV + 16 * lane);
@@ -330,15 +414,20 @@ __global__ void __launch_bounds__(kThreads, 1) kv_attention_kernel(const KvaPara
             mbar_expect_tx(mb0 + 8 * slot, kUnitBytes);
             bulk_g2s(su, head + (size_t)(u + kRing) * kUnitBytes, kUnitBytes, mb0 + 8 * slot);
         }
-        const float vA[4] = {vA01.x, vA01.y, vA23.x, vA23.y};
-        const float vB[4] = {vB01.x, vB01.y, vB23.x, vB23.y};
+        const f2_t vA[4] = {f2(vA01.x, vA01.x), f2(vA01.y, vA01.y), f2(vA23.x, vA23.x),
+                            f2(vA23.y, vA23.y)};
+        const f2_t vB[4] = {f2(vB01.x, vB01.x), f2(vB01.y, vB01.y), f2(vB23.x, vB23.x),
+                            f2(vB23.y, vB23.y)};
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
             uint32_t b0[NT], b1[NT];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                b0[nt] = transpose8x8(pack_bf16(p[nt][0] * vA[b], p[nt][1] * vA[b]));
-                b1[nt] = transpose8x8(pack_bf16(p[nt][2] * vB[b], p[nt][3] * vB[b]));
+                float x0, x1, y0, y1;
+                unf2(mul2(f2(p[nt][0], p[nt][1]), vA[b]), x0, x1);
+                unf2(mul2(f2(p[nt][2], p[nt][3]), vB[b]), y0, y1);
+                b0[nt] = transpose8x8(pack_bf16(x0, x1));
+                b1[nt] = transpose8x8(pack_bf16(y0, y1));
             }
 #pragma unroll
             for (int mm = 0; mm < 2; ++mm) {
@@ -362,7 +451,17 @@ __global__ void __launch_bounds__(kThreads, 1) kv_attention_kernel(const KvaPara
         __syncwarp();
     }
 
-    // Row sums over the 8 position lanes; m is already uniform across them.
+    // Row sums over the 8 position lanes; m is already uniform across them.  From here on m is
+    // in base-2 units (m * scale), as the merge expects.
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        float l0, l1;
+        unf2(lsum[nt], l0, l1);
+        l[nt][0] += l0;
+        l[nt][1] += l1;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) m[nt][e] = m[nt][e] * scl;
+    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -385,11 +484,13 @@ __global__ void __launch_bounds__(kThreads, 1) kv_attention_kernel(const KvaPara
     __syncthreads();  // every warp is done with its ring: the ring becomes the merge buffer
 
     float *buf = reinterpret_cast<float *>(smem);
+    const int rows_here = min(kRowsPerGroup, P.rows - rg * kRowsPerGroup);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int row = 8 * nt + 2 * tig + e;
+            if (row >= rows_here) continue;
             float M = -INFINITY;
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * kRowsPerGroup + row]);
@@ -404,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1) kv_attention_kernel(const KvaPara
         }
     __syncthreads();
 
-    for (int idx = threadIdx.x; idx < 8 * NT * 32; idx += kThreads) {
+    for (int idx = threadIdx.x; idx < rows_here * 32; idx += kThreads) {
         const int row = idx >> 5, d4 = idx & 31;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -418,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1) kv_attention_kernel(const KvaPara
         }
         *reinterpret_cast<float4 *>(P.part_o + ((size_t)cta * kRowsPerGroup + row) * kD + 4 * d4) = acc;
     }
-    if (threadIdx.x < 8 * NT) {
+    if (threadIdx.x < rows_here) {
         const int row = threadIdx.x;
         float M = -INFINITY, S = 0.f;
 #pragma unroll
@@ -432,8 +533,10 @@ __global__ void __launch_bounds__(kThreads, 1) kv_attention_kernel(const KvaPara
     }
 }
 
-// One warp per (row group, kv head, row): merges the splits' partials and writes o = O / l.
+// One warp per (row group, kv head, row): merges the splits' partials and writes o = O / l.  All
+// loads of a round of 32 splits are issued before any is used (one L2 round trip per round).
 __global__ void __launch_bounds__(128) kv_attention_merge_kernel(const KvaParams P) {
+    griddep_launch_dependents();  // the next layer's split pass may become resident and wait
     griddep_wait();
     const int lane = threadIdx.x & 31;
     const int wgl = blockIdx.x * 4 + (threadIdx.x >> 5);
@@ -444,26 +547,59 @@ __global__ void __launch_bounds__(128) kv_attention_merge_kernel(const KvaParams
     if (grow >= P.rows) return;
     const int c = grow / P.G, h = g * P.G + grow % P.G;
     const size_t base = (size_t)(rg * P.Hkv + g) * P.splits;
+    const float4 *po = reinterpret_cast<const float4 *>(P.part_o) + row * (kD / 4) + lane;
+    constexpr size_t kStride4 = (size_t)kRowsPerGroup * kD / 4;  // float4s per partial
+
+    float2 ml[kMaxSplitRounds];
+    float4 v[32];
+#pragma unroll
+    for (int k = 0; k < kMaxSplitRounds; ++k) {
+        const int s = lane + 32 * k;
+        ml[k] = s < P.splits ? P.part_ml[(base + s) * kRowsPerGroup + row] : make_float2(-INFINITY, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        if (i < P.splits) v[i] = po[(base + i) * kStride4];
     float M = -INFINITY;
-    for (int s = lane; s < P.splits; s += 32) M = fmaxf(M, P.part_ml[(base + s) * kRowsPerGroup + row].x);
-    M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, 1));
-    M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, 2));
-    M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, 4));
-    M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, 8));
-    M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, 16));
+#pragma unroll
+    for (int k = 0; k < kMaxSplitRounds; ++k) M = fmaxf(M, ml[k].x);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+    float wr[kMaxSplitRounds], S = 0.f;
+#pragma unroll
+    for (int k = 0; k < kMaxSplitRounds; ++k) {
+        wr[k] = ml[k].x == -INFINITY ? 0.f : ex2(ml[k].x - M);
+        S += wr[k] * ml[k].y;
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) S += __shfl_xor_sync(0xFFFFFFFFu, S, o);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float S = 0.f;
-#pragma unroll 4
-    for (int s = 0; s < P.splits; ++s) {
-        const float2 ml = P.part_ml[(base + s) * kRowsPerGroup + row];
-        const float w = ml.x == -INFINITY ? 0.f : ex2(ml.x - M);
-        const float4 v =
-            *reinterpret_cast<const float4 *>(P.part_o + ((base + s) * kRowsPerGroup + row) * kD + 4 * lane);
-        S += w * ml.y;
-        acc.x += w * v.x;
-        acc.y += w * v.y;
-        acc.z += w * v.z;
-        acc.w += w * v.w;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const float w = __shfl_sync(0xFFFFFFFFu, wr[0], i);
+        if (i < P.splits) {
+            acc.x += w * v[i].x;
+            acc.y += w * v[i].y;
+            acc.z += w * v[i].z;
+            acc.w += w * v[i].w;
+        }
+    }
+#pragma unroll
+    for (int k = 1; k < kMaxSplitRounds; ++k) {
+        if (32 * k >= P.splits) break;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (32 * k + i < P.splits) v[i] = po[(base + 32 * k + i) * kStride4];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float w = __shfl_sync(0xFFFFFFFFu, wr[k], i);
+            if (32 * k + i < P.splits) {
+                acc.x += w * v[i].x;
+                acc.y += w * v[i].y;
+                acc.z += w * v[i].z;
+                acc.w += w * v[i].w;
+            }
+        }
     }
     const float inv = 1.f / S;
     *reinterpret_cast<float4 *>(P.out + ((size_t)c * P.Hq + h) * kD + 4 * lane) =
@@ -555,6 +691,7 @@ bool kva_geom(int Hq, int Hkv, int n_past, int C, KvaGeom &k) {
     const int heads = Hkv * k.n_rg;
     int splits = std::max(1, sm_count() / heads);
     splits = std::min(splits, std::max(1, k.n_units / (2 * kWarps)));
+    splits = std::min(splits, 32 * kMaxSplitRounds);
     k.splits = splits;
     k.ctas = (size_t)splits * heads;
     return true;
@@ -580,7 +717,7 @@ cudaError_t launch_kva(const KvaParams &P, dim3 grid, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
-    e = launch(kv_attention_kernel<NT>, grid, dim3(kThreads), kSmemBytes, stream, false, P);
+    e = launch(kv_attention_kernel<NT>, grid, dim3(kThreads), kSmemBytes, stream, true, P);
     if (e != cudaSuccess) return e;
     const int warps = P.n_rg * P.Hkv * kRowsPerGroup;
     return launch(kv_attention_merge_kernel, dim3((warps + 3) / 4), dim3(128), 0, stream, true, P);
