@@ -421,6 +421,41 @@ def kv_read(dev, peak, stack_ms, layers=64, contexts=KV_CONTEXTS, steps=10, C=4,
     return out
 
 
+def pass_with_kv(vp, dev, peak, tail_ms, context=32768, steps=20):
+    """The verify pass with each layer's KV-read attention in its place (stack.KvPass: attention
+    over the layer's own cache between its q|k|v and o products, the matrices between two
+    attention steps in one chain launch; one CUDA graph), at the pages' 32K context, plus the
+    lm_head/sampler/acceptance tail measured in the main timed region.  Reports the pass rate
+    and the bytes of weights and cache per second."""
+    import torch
+
+    from speculative_decoding_verify_06_gb300 import stack
+    kp = stack.KvPass(vp, context).capture()
+    s = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        kp.launch(s)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        kp.launch(s)
+    e1.record(s)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    nbytes = vp.stack_bytes() + kp.kv_bytes()
+    out = {"context": context, "stack_with_kv_ms": ms, "tail_ms": tail_ms,
+           "passes_per_s": 1000.0 / (ms + tail_ms), "bytes": nbytes,
+           "gb_s": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak,
+           "launches_per_pass": kp.launches(),
+           "workload": ("svd_kv_attention (40 query heads over 8 kv heads, dim 128, q8_0 keys / "
+                        "q4_0 values) over each layer's own cache between its q|k|v and o "
+                        "products; the matrices between two attention steps in one chain launch "
+                        "(65 chain launches per pass); one CUDA graph")}
+    del kp
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_svd(args, rank, world, local_rank):
     import torch
 
@@ -543,6 +578,7 @@ def run_svd(args, rank, world, local_rank):
     if not args.no_kv and not args.stack_only:
         line["kv_read"] = kv_read(dev, peak, line["stack"]["ms"], layers=args.layers,
                                   contexts=tuple(int(c) for c in args.kv_contexts.split(",")))
+        line["pass_with_kv"] = pass_with_kv(vp, dev, peak, line["stack"]["tail_ms"])
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         smp = OracleSample(frac=0.25)
         times = [smp.step() for _ in range(3)]

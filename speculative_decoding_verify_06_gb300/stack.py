@@ -207,3 +207,74 @@ class ColumnsView:
 
     def stack_bytes(self) -> int:
         return self.vp.layers * sum(roofline.linear_bytes(i, o, self.C) for i, o in self.vp.gemms)
+
+
+class KvPass:
+    """The resident weights of a VerifyPass with the KV-read attention of every layer placed
+    where the model has it, between a layer's q|k|v product and its o product: svd_kv_attention of
+    the window's C queries over the layer's own q8_0-key / q4_0-value cache (40 query heads over
+    8 kv heads of dimension 128, the window at positions context - C .. context - 1).  The
+    matrices between two attention steps (o, gate|up and down of one layer with q|k|v of the
+    next) form one chain launch, so a pass is 65 chain launches and 64 attention steps.  "Decode is memory-bound ..." ("The ceiling"): at long
+    context the KV cache joins the weights on every pass.  Queries and attention outputs are
+    synthetic buffers of their own, like every activation of the stack; the stream order is the
+    model's.  The whole stack is recorded into one CUDA graph."""
+
+    def __init__(self, vp: VerifyPass, context: int, seed: int = 0):
+        self.vp, self.context = vp, context
+        dev, C = vp.device, vp.C
+        Hq, Hkv, D = synth.N_Q_HEADS, synth.N_KV_HEADS, synth.HEAD_DIM
+        self.Hq, self.Hkv, self.D = Hq, Hkv, D
+        kc, ks, vc, vs = synth.kv_cache_torch(Hkv, context, D, seed, dev)
+        nbytes = svd.svd_kv_cache_bytes(Hkv, context)
+        self.caches = []
+        for _ in range(vp.layers):
+            cache = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+            svd.svd_kv_repack(kc, ks, vc, vs, Hkv, context, 0, context, cache, context)
+            self.caches.append(cache)
+        del kc, ks, vc, vs
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed + 17)
+        self.q = torch.randn((C, Hq, D), generator=g, device=dev).to(torch.bfloat16)
+        self.o = torch.empty((C, Hq, D), dtype=torch.float32, device=dev)
+        self.att_ws = torch.zeros(svd.svd_kv_attention_workspace_bytes(Hq, Hkv, C),
+                                  dtype=torch.uint8, device=dev)
+        # Chain segments between the attention steps: q|k|v of layer 0; then o, gate|up, down of
+        # layer l with q|k|v of layer l + 1; the last layer's o, gate|up, down alone.
+        n = len(vp.gemms)
+        self.segments = [vp.ops[0:1]]
+        for l in range(vp.layers):
+            self.segments.append(vp.ops[n * l + 1:n * (l + 1) + 1])
+        self.graph = None
+        torch.cuda.synchronize()
+
+    def enqueue(self, stream=None):
+        vp = self.vp
+        for l in range(vp.layers):
+            svd.svd_verify_chain(self.segments[l], vp.C, vp.ws, stream=stream)
+            svd.svd_kv_attention(self.q, self.caches[l], self.context, self.Hq, self.Hkv,
+                                 self.context - vp.C, vp.C, 1.0 / self.D ** 0.5, self.o,
+                                 self.att_ws, stream=stream)
+        svd.svd_verify_chain(self.segments[vp.layers], vp.C, vp.ws, stream=stream)
+
+    def capture(self):
+        s = torch.cuda.Stream(device=self.vp.device)
+        s.wait_stream(torch.cuda.current_stream(self.vp.device))
+        with torch.cuda.stream(s):
+            self.enqueue(s)
+            s.synchronize()
+            svd.svd_graph_begin(s)
+            self.enqueue(s)
+            self.graph = svd.svd_graph_end(s)
+        s.synchronize()
+        return self
+
+    def launch(self, stream=None):
+        self.graph.launch(stream)
+
+    def kv_bytes(self) -> int:
+        return self.vp.layers * (self.Hkv * -(-self.context // 16) * svd.SVD_KV_UNIT_BYTES
+                                 + self.vp.C * self.Hq * self.D * (2 + 4))
+
+    def launches(self) -> int:
+        return len(self.segments) + 2 * self.vp.layers

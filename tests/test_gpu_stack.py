@@ -58,3 +58,34 @@ def test_chain_pdl_and_plain_launches_agree():
     torch.cuda.synchronize()
     for x, y, z in zip(a.linears, b.linears, c.linears):
         assert torch.equal(x.Y, y.Y) and torch.equal(x.Y, z.Y)
+
+
+def test_pass_with_kv_attention_matches_eager_and_oracle():
+    # Two layers of the stack with each layer's KV-read attention in its place (between its
+    # q|k|v and o products, the matrices in between as chain launches), recorded into one graph:
+    # replays equal the eager run, the attention output matches the oracle and the last linear's
+    # output equals the plain stack's.
+    lib()
+    vp = stack.VerifyPass(layers=2, C=4, seed=5, head=False)
+    vp.enqueue_stack()
+    torch.cuda.synchronize()
+    y_plain = vp.linears[-1].Y.clone()
+    ctx = 300
+    kp = stack.KvPass(vp, ctx, seed=9)
+    kp.enqueue()
+    torch.cuda.synchronize()
+    o_eager = kp.o.clone()
+    assert torch.equal(vp.linears[-1].Y, y_plain)
+    kp.o.fill_(float("nan"))
+    kp.capture()
+    for _ in range(2):
+        kp.launch()
+    torch.cuda.synchronize()
+    assert torch.equal(kp.o, o_eager)
+    # the oracle on host copies of the same cache bytes (every layer's cache holds this draw)
+    kc, ks, vc, vs = synth.kv_cache_torch(kp.Hkv, ctx, kp.D, 9, torch.device("cuda:0"))
+    q = kp.q.view(torch.int16).cpu().numpy().view(np.uint16)
+    o_ref, a_ref = oracle.kv_attention(q, kc.cpu().numpy(), ks.cpu().numpy().view(np.uint16),
+                                       vc.cpu().numpy(), vs.cpu().numpy().view(np.uint16), ctx - 4)
+    err = np.abs(o_eager.cpu().numpy().astype(np.float64) - o_ref)
+    assert np.all(err <= 2.0 ** -8 * a_ref)
