@@ -708,8 +708,9 @@ constexpr int kU = SVD_U;         // units per slot (one pair of bulk copies)
 constexpr int kNW2 = 16;          // warps per CTA, 8 < C <= 16: two warps per unit,
 constexpr int kTW2 = 2;           // each on two of its four 16-row tiles
 constexpr int kR2 = 2;            // ring slots per worker group, C <= 32
-constexpr int kNW4 = 8;           // warps per CTA, 16 < C <= 32: 255 registers a thread hold the
-                                  // four n-tiles' accumulators without spilling (16 warps spill)
+constexpr int kNW4 = 8;           // warps per CTA, 16 < C <= 32: one warp per unit (all four row
+constexpr int kTW4 = 4;           // tiles), so each activation fragment serves four tiles; 255
+                                  // registers a thread hold the accumulators (16 warps spill)
 constexpr int kMaxCtasPerSm = 2;  // the workspace holds partial slots for this many
 constexpr int kChainMax = 256;    // ops per chain launch (kernel parameters, ~16 KB)
 
@@ -801,7 +802,7 @@ static cudaError_t launch_ops(const VlOps<MAXOPS> &P, void *ws, bool pdl, cudaSt
     switch (ntiles_for(P.C)) {
         case 1: return launch_stream<1, kNW1, kTiles, kR1, kU, MAXOPS>(P, ws, pdl, coop, max_units, stream);
         case 2: return launch_stream<2, kNW2, kTW2, kR2, kU, MAXOPS>(P, ws, pdl, coop, max_units, stream);
-        default: return launch_stream<4, kNW4, kTW2, kR2, kU, MAXOPS>(P, ws, pdl, coop, max_units, stream);
+        default: return launch_stream<4, kNW4, kTW4, kR2, kU, MAXOPS>(P, ws, pdl, coop, max_units, stream);
     }
 }
 
