@@ -285,7 +285,28 @@ def column_sweep(vp, dev, steps, tokens_per_pass, peak):
     return out
 
 
-def accept_throughput(dev, peak, n_windows=1_000_000, ks=(1, 3, 5), pool=256, seed=7):
+def accept_oracle_sample(P, Q, samples, pool, n, g, dev, k=3):
+    """The oracle (fp64, every host thread) deciding n windows of k drafts drawn from the same
+    pool as the GPU measurement, as windows per second."""
+    import numpy as np
+    import torch
+
+    import oracle
+    rows = torch.randint(0, pool, (n, k + 1), generator=g, device=dev)
+    pick = torch.randint(0, samples.shape[1], (n, k), generator=g, device=dev)
+    draft = samples[rows[:, :k], pick].to(torch.int32).cpu().numpy()
+    Ph, Qh = P.cpu().numpy(), Q.cpu().numpy()
+    pr, qr = rows.cpu().numpy().astype(np.int64), rows[:, :k].contiguous().cpu().numpy().astype(np.int64)
+    threads = oracle.max_threads()
+    t0 = time.perf_counter()
+    oracle.accept(Ph, draft, q=Qh, p_rows=pr, q_rows=qr, seed=3, nthreads=threads)
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": "windows/s", "cores": threads, "kind": "oracle",
+            "seconds": dt, "sample": f"{n} windows at k = {k} from the same (p, q) pool, fp64"}
+
+
+def accept_throughput(dev, peak, n_windows=1_000_000, ks=(1, 3, 5), pool=256, seed=7,
+                      oracle_windows=0):
     """svd_accept on many windows whose rows come from a pool of (p, q) pairs larger than L2:
     p from Zipf(1.1)-ranked logits under a random permutation, q from the same logits plus
     tau * N(0, 1) noise (tau bisected for a mean sum min(p, q) of 0.6); every position of a
@@ -319,6 +340,8 @@ def accept_throughput(dev, peak, n_windows=1_000_000, ks=(1, 3, 5), pool=256, se
     P = P.contiguous()
     samples = torch.multinomial(Q, 4096, replacement=True, generator=g)  # [pool, 4096]
     out = {"alpha": alpha, "pool_bytes": 2 * pool * V * 4, "windows": n_windows}
+    if oracle_windows:
+        out["cpu_baseline"] = accept_oracle_sample(P, Q, samples, pool, oracle_windows, g, dev)
     s = torch.cuda.current_stream(dev)
     for k in ks:
         rows = torch.randint(0, pool, (n_windows, k + 1), generator=g, device=dev)
@@ -353,7 +376,31 @@ def accept_throughput(dev, peak, n_windows=1_000_000, ks=(1, 3, 5), pool=256, se
 KV_CONTEXTS = (32768, 131072, 262144)
 
 
-def kv_read(dev, peak, stack_ms, layers=64, contexts=KV_CONTEXTS, steps=10, C=4, seed=5):
+def kv_oracle_sample(q, kc, ks, vc, vs, n_past, C):
+    """The oracle (fp64, every host thread) on one kv head of a layer's cache -- its 5 query heads
+    at the window's C positions over the whole context -- as cache bytes per second."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from speculative_decoding_verify_06_gb300 import svd, synth
+    G = synth.N_Q_HEADS // synth.N_KV_HEADS
+    qh = q[:, :G].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    host = [kc[:1].cpu().numpy(), ks[:1].cpu().numpy().view(np.uint16), vc[:1].cpu().numpy(),
+            vs[:1].cpu().numpy().view(np.uint16)]
+    threads = oracle.max_threads()
+    t0 = time.perf_counter()
+    oracle.kv_attention(qh, *host, n_past, nthreads=threads)
+    dt = time.perf_counter() - t0
+    nbytes = -(-(n_past + C) // 16) * svd.SVD_KV_UNIT_BYTES
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "seconds": dt,
+            "sample": (f"one kv head ({G} query heads x {C} window positions) over {n_past + C} "
+                       f"positions, fp64; GB/s of its cache bytes")}
+
+
+def kv_read(dev, peak, stack_ms, layers=64, contexts=KV_CONTEXTS, steps=10, C=4, seed=5,
+            oracle_sample=False):
     """The KV-read term of a pass: svd_kv_attention once per layer (40 query heads over 8 kv heads
     of dimension 128, q8_0 keys and q4_0 values), each layer on its own cache, at the window's
     last position n_past + C = context.  The 64 layer launches (split pass + merge each) are
@@ -375,10 +422,12 @@ def kv_read(dev, peak, stack_ms, layers=64, contexts=KV_CONTEXTS, steps=10, C=4,
             cache = torch.empty(nbytes, dtype=torch.uint8, device=dev)
             svd.svd_kv_repack(kc, ks, vc, vs, Hkv, ctx, 0, ctx, cache, ctx, stream=s)
             caches.append(cache)
-        del kc, ks, vc, vs
         g = torch.Generator(device=dev)
         g.manual_seed(seed)
         q = torch.randn((C, Hq, D), generator=g, device=dev).to(torch.bfloat16)
+        if oracle_sample and "cpu_baseline" not in out:
+            out["cpu_baseline"] = kv_oracle_sample(q, kc, ks, vc, vs, ctx - C, C)
+        del kc, ks, vc, vs
         o = torch.empty((C, Hq, D), dtype=torch.float32, device=dev)
         ws = torch.zeros(svd.svd_kv_attention_workspace_bytes(Hq, Hkv, C), dtype=torch.uint8,
                          device=dev)
@@ -574,10 +623,14 @@ def run_svd(args, rank, world, local_rank):
     }
     if not args.no_sweep and not args.stack_only:
         line["column_sweep"] = column_sweep(vp, dev, 20, tokens_per_pass, peak)
-        line["accept_throughput"] = accept_throughput(dev, peak)
+        line["accept_throughput"] = accept_throughput(
+            dev, peak, oracle_windows=2000 if (rank == 0 and world == 1
+                                               and not args.no_cpu_baseline) else 0)
     if not args.no_kv and not args.stack_only:
         line["kv_read"] = kv_read(dev, peak, line["stack"]["ms"], layers=args.layers,
-                                  contexts=tuple(int(c) for c in args.kv_contexts.split(",")))
+                                  contexts=tuple(int(c) for c in args.kv_contexts.split(",")),
+                                  oracle_sample=(rank == 0 and world == 1
+                                                 and not args.no_cpu_baseline))
         line["pass_with_kv"] = pass_with_kv(vp, dev, peak, line["stack"]["tail_ms"])
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         smp = OracleSample(frac=0.25)
