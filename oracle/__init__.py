@@ -28,10 +28,12 @@ _lib = None
 
 
 def build(force: bool = False) -> str:
-    """Compile ``orc.c`` into ``liborc.so`` (plain gcc, -O2, OpenMP; no -march flags)."""
+    """Compile ``orc.c`` into ``liborc.so`` (plain gcc, -O2, OpenMP; no -march flags; no fused
+    multiply-adds, so fp32 steps round as written on every host)."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+        subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared",
+                               "-std=c11",
                                "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
@@ -62,6 +64,10 @@ def lib():
             L.orc_kv_attention.restype = None
             L.orc_kv_attention.argtypes = [P, P, P, P, P, i64, i64, i64, i64, i64, i64, dbl, P, P,
                                            i32]
+            L.orc_f32_to_f16.restype = ctypes.c_uint16
+            L.orc_f32_to_f16.argtypes = [ctypes.c_float]
+            L.orc_kv_quantize.restype = None
+            L.orc_kv_quantize.argtypes = [P, P, i64, i64, P, P, P, P]
             L.orc_max_threads.restype = i32
             L.orc_max_threads.argtypes = []
             _lib = L
@@ -216,3 +222,28 @@ def kv_attention(q_bf16, k_codes, k_scales, v_codes, v_scales, n_past: int, scal
                            Hq, Hkv, D, ld, int(n_past), C, float(scale), _p(o), _p(a),
                            int(nthreads or max_threads()))
     return o, a
+
+
+def f32_to_f16_bits(x: float) -> int:
+    """fp32 value -> IEEE binary16 bits, round to nearest even (from the formats' definitions)."""
+    return int(lib().orc_f32_to_f16(ctypes.c_float(x)))
+
+
+def kv_quantize(k, v):
+    """q8_0 keys and q4_0 values of rows of fp32 keys and values (the cache's write side).
+
+    k, v: float32 [rows, D], D % 32 == 0.  Returns (k_codes int8 [rows, D], k_scales uint16 fp16
+    bits [rows, D/32], v_codes uint8 [rows, D/2] (low nibble = even dimension), v_scales uint16
+    [rows, D/32]).  Follows "100 tokens per second ..." ("The wall": KV cache at q8_0/q4_0); the
+    block definitions are a reading (those of the llama.cpp types of the same names).
+    """
+    k = np.ascontiguousarray(k, dtype=np.float32)
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    rows, D = k.shape
+    assert v.shape == (rows, D) and D % 32 == 0
+    kc = np.empty((rows, D), np.int8)
+    ks = np.empty((rows, D // 32), np.uint16)
+    vc = np.zeros((rows, D // 2), np.uint8)
+    vs = np.empty((rows, D // 32), np.uint16)
+    lib().orc_kv_quantize(_p(k), _p(v), rows, D, _p(kc), _p(ks), _p(vc), _p(vs))
+    return kc, ks, vc, vs

@@ -480,6 +480,77 @@ void orc_kv_attention(const uint16_t *q_bf16, const int8_t *k_codes, const uint1
     }
 }
 
+/* ------------------------------------------------------------------------------------ */
+/* Quantisation of the window's keys and values on their way into the cache ([P1] "The  */
+/* wall": the cache is held as q8_0 keys and q4_0 values).  READING: the pages name the  */
+/* formats only; their definitions are those of the llama.cpp block types of the same    */
+/* names, in fp32 arithmetic, per block of 32 consecutive values:                        */
+/*   q8_0: d = max|x| / 127, q = round-half-away(x * (1/d)) (0 when d = 0);               */
+/*   q4_0: m = the value of largest magnitude (the first on ties), d = m / -8,            */
+/*         c = min(15, trunc(x * (1/d) + 8.5)) (8 when d = 0).                            */
+/* d is stored as fp16 (round to nearest even); codes use the fp32 d.                    */
+/* ------------------------------------------------------------------------------------ */
+
+/* fp32 -> IEEE binary16 bits, round to nearest even, from the two formats' definitions. */
+uint16_t orc_f32_to_f16(float f)
+{
+    uint32_t x;
+    memcpy(&x, &f, 4);
+    uint32_t sign = (x >> 16) & 0x8000u, ax = x & 0x7fffffffu;
+    if (ax >= 0x7f800000u) return (uint16_t)(sign | (ax > 0x7f800000u ? 0x7e00u : 0x7c00u));
+    if (ax >= 0x477ff000u) return (uint16_t)(sign | 0x7c00u);       /* >= 65520: infinity */
+    if (ax < 0x38800000u) {                                          /* below 2^-14 */
+        double m = (double)fabsf(f) * 16777216.0;                    /* units of 2^-24, exact */
+        return (uint16_t)(sign | (uint32_t)nearbyint(m));            /* ties to even */
+    }
+    uint32_t e = (ax >> 23) - 127u + 15u, mant = ax & 0x7fffffu;
+    uint32_t h = (e << 10) | (mant >> 13), rem = mant & 0x1fffu;
+    if (rem > 0x1000u || (rem == 0x1000u && (h & 1u))) h += 1u;      /* carry may bump e */
+    return (uint16_t)(sign | h);
+}
+
+/* rows x D fp32 keys and values (D a multiple of 32) -> k codes [rows][D], k scales
+ * [rows][D/32], v codes [rows][D/2] (dimension 2t in the low nibble), v scales [rows][D/32]. */
+void orc_kv_quantize(const float *k, const float *v, int64_t rows, int64_t D, int8_t *kc,
+                     uint16_t *ks, uint8_t *vc, uint16_t *vs)
+{
+    int64_t nb = D / 32;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b = 0; b < nb; ++b) {
+            const float *xk = k + r * D + 32 * b, *xv = v + r * D + 32 * b;
+            float amax = 0.0f;
+            for (int i = 0; i < 32; ++i)
+                if (fabsf(xk[i]) > amax) amax = fabsf(xk[i]);
+            float d = amax / 127.0f, id = d != 0.0f ? 1.0f / d : 0.0f;
+            ks[r * nb + b] = orc_f32_to_f16(d);
+            for (int i = 0; i < 32; ++i) {
+                float t = xk[i] * id;
+                kc[r * D + 32 * b + i] = (int8_t)roundf(t);
+            }
+            float mabs = 0.0f, m = 0.0f;
+            for (int i = 0; i < 32; ++i)
+                if (fabsf(xv[i]) > mabs) {
+                    mabs = fabsf(xv[i]);
+                    m = xv[i];
+                }
+            float dv = m / -8.0f, idv = dv != 0.0f ? 1.0f / dv : 0.0f;
+            vs[r * nb + b] = orc_f32_to_f16(dv);
+            for (int i = 0; i < 32; ++i) {
+                float t = xv[i] * idv;
+                t = t + 8.5f;
+                int c = (int)t;
+                if (c > 15) c = 15;
+                int dim = (int)(32 * b + i);
+                uint8_t *byte = vc + r * (D / 2) + dim / 2;
+                if (dim & 1)
+                    *byte = (uint8_t)((*byte & 0x0f) | (c << 4));
+                else
+                    *byte = (uint8_t)((*byte & 0xf0) | c);
+            }
+        }
+    }
+}
+
 int orc_max_threads(void)
 {
 #ifdef _OPENMP
