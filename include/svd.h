@@ -301,6 +301,18 @@ int svd_kv_repack(const int8_t *k_codes, const uint16_t *k_scales, const uint8_t
 int svd_kv_unpack(const void *cache, int capacity, int n_kv_heads, int pos_begin, int pos_end,
                   int8_t *k_codes, uint16_t *k_scales, uint8_t *v_codes, uint16_t *v_scales,
                   int ld, svd_stream_t stream);
+/* svd_kv_append: the cache's write side for a verify window -- quantises the window's fp32 keys
+ *   and values (position c at k + c * ld and v + c * ld, kv heads consecutive, 128 values each;
+ *   ld >= Hkv * 128 floats, e.g. the k and v columns of the fused q|k|v output) to q8_0 keys and
+ *   q4_0 values, per block of 32 in fp32 (READING: the llama.cpp block types of these names:
+ *   q8_0 d = max|x|/127, q = round-half-away(x/d); q4_0 d = m/-8 with m the value of largest
+ *   magnitude (lowest dimension on ties), c = min(15, trunc(x/d + 8.5)); 1/d is taken as 0 when
+ *   d = 0; d stored as fp16, round to nearest even), and writes them at cache positions
+ *   n_past .. n_past + C - 1 of the native cache.  Other positions are untouched.  Errors:
+ *   SVD_ERR_INVALID_ARG for null or misaligned pointers, non-positive sizes, ld < Hkv * 128 or
+ *   n_past + C > capacity. */
+int svd_kv_append(const float *k, const float *v, int ld, int C, int n_kv_heads, int n_past,
+                  void *cache, int capacity, svd_stream_t stream);
 size_t svd_kv_attention_workspace_bytes(int n_q_heads, int n_kv_heads, int C);
 int svd_kv_attention(const uint16_t *q, const void *cache, int capacity, int n_q_heads,
                      int n_kv_heads, int n_past, int C, float scale, float *out, void *workspace,

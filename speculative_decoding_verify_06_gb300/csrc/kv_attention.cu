@@ -672,6 +672,63 @@ __global__ void kv_unpack_kernel(const unsigned char *cache, int units_cap, int 
     }
 }
 
+// One warp per (window position c, kv head g): quantises the position's 128 key values to q8_0
+// and 128 value values to q4_0, block by block of 32 (lane l holds dimension 32 b + l), in the
+// fp32 steps of the formats' definitions (llama.cpp's block types of the same names):
+//   q8_0: d = max|x| / 127, q = round-half-away(x * (1/d)), 0 when d = 0;
+//   q4_0: m = the value of largest magnitude (the lowest dimension on ties), d = m / -8,
+//         c = min(15, trunc(x * (1/d) + 8.5)), 8 when d = 0;
+// and writes codes and fp16 scales (round to nearest even) into the native unit of cache
+// position n_past + c.
+__global__ void kv_append_kernel(const float *k, const float *v, int ld, int C, int Hkv,
+                                 int n_past, unsigned char *cache, int units_cap) {
+    const int w = (int)((blockIdx.x * (unsigned)blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
+    if (w >= C * Hkv) return;
+    const int c = w / Hkv, g = w % Hkv, pos = n_past + c, r = pos & 15;
+    unsigned char *unit = cache + ((size_t)g * units_cap + (pos >> 4)) * kUnitBytes;
+    const float *kr = k + (size_t)c * ld + (size_t)g * kD, *vr = v + (size_t)c * ld + (size_t)g * kD;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const int dim = 32 * b + lane;
+        const float x = kr[dim];
+        float amax = fabsf(x);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        const float d = __fdiv_rn(amax, 127.0f);
+        const float id = d != 0.f ? __fdiv_rn(1.0f, d) : 0.f;
+        const int q = (int)roundf(__fmul_rn(x, id));
+        unit[key_code_offset(r, dim)] = (unsigned char)(q + 128);
+        if (lane == 0)
+            *reinterpret_cast<uint16_t *>(unit + kOffKS + scale_offset(r, b)) =
+                __half_as_ushort(__float2half_rn(d));
+
+        const float y = vr[dim];
+        float ay = fabsf(y);
+        int at = lane;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float oa = __shfl_xor_sync(0xFFFFFFFFu, ay, o);
+            const int oi = __shfl_xor_sync(0xFFFFFFFFu, at, o);
+            if (oa > ay || (oa == ay && oi < at)) {
+                ay = oa;
+                at = oi;
+            }
+        }
+        const float m = __shfl_sync(0xFFFFFFFFu, y, at);
+        const float dv = __fdiv_rn(m, -8.0f);
+        const float idv = dv != 0.f ? __fdiv_rn(1.0f, dv) : 0.f;
+        const int cq = min(15, (int)__fadd_rn(__fmul_rn(y, idv), 8.5f));
+        // Dimensions 16 mt + j and 16 mt + j + 8 share a byte: lane l (l & 8 == 0) takes the code
+        // of lane l + 8 for the high nibble.
+        const int hi = __shfl_down_sync(0xFFFFFFFFu, cq, 8);
+        if ((lane & 8) == 0)
+            unit[value_byte_offset(r, dim >> 4, dim & 7)] = (unsigned char)(cq | (hi << 4));
+        if (lane == 0)
+            *reinterpret_cast<uint16_t *>(unit + kOffVS + scale_offset(r, b)) =
+                __half_as_ushort(__float2half_rn(dv));
+    }
+}
+
 int units_for(int positions) { return (positions + kUnitPos - 1) / kUnitPos; }
 
 struct KvaGeom {
@@ -806,5 +863,18 @@ extern "C" int svd_kv_attention(const uint16_t *q, const void *cache, int capaci
         default: e = launch_kva<3>(P, grid, (cudaStream_t)stream); break;
     }
     SVD_CUDA_TRY(e);
+    return SVD_OK;
+}
+
+extern "C" int svd_kv_append(const float *k, const float *v, int ld, int C, int n_kv_heads,
+                             int n_past, void *cache, int capacity, svd_stream_t stream) {
+    if (!k || !v || !cache || C <= 0 || n_kv_heads <= 0 || n_past < 0 || capacity <= 0 ||
+        (long long)n_past + C > capacity || ld < n_kv_heads * kD)
+        return SVD_ERR_INVALID_ARG;
+    if (!aligned16(cache)) return SVD_ERR_INVALID_ARG;
+    const long long warps = (long long)C * n_kv_heads;
+    kv_append_kernel<<<(unsigned)((warps + 3) / 4), 128, 0, (cudaStream_t)stream>>>(
+        k, v, ld, C, n_kv_heads, n_past, (unsigned char *)cache, units_for(capacity));
+    SVD_CUDA_TRY(cudaGetLastError());
     return SVD_OK;
 }

@@ -47,8 +47,8 @@ EXPORTS = (
     "svd_spec_adapt_observe", "svd_spec_adapt_alpha", "svd_spec_adapt_depth",
     "svd_spec_adapt_destroy", "svd_ngram_create", "svd_ngram_append", "svd_ngram_propose",
     "svd_ngram_length", "svd_ngram_destroy",
-    "svd_kv_cache_bytes", "svd_kv_repack", "svd_kv_unpack", "svd_kv_attention_workspace_bytes",
-    "svd_kv_attention",
+    "svd_kv_cache_bytes", "svd_kv_repack", "svd_kv_unpack", "svd_kv_append",
+    "svd_kv_attention_workspace_bytes", "svd_kv_attention",
 )
 
 
@@ -149,6 +149,7 @@ def load(path: str = LIB_PATH):
             "svd_kv_cache_bytes": (sz, [i32, i32]),
             "svd_kv_repack": (i32, [P, P, P, P, i32, i32, i32, i32, P, i32, P]),
             "svd_kv_unpack": (i32, [P, i32, i32, i32, i32, P, P, P, P, i32, P]),
+            "svd_kv_append": (i32, [P, P, i32, i32, i32, i32, P, i32, P]),
             "svd_kv_attention_workspace_bytes": (sz, [i32, i32, i32]),
             "svd_kv_attention": (i32, [P, P, i32, i32, i32, i32, i32, ctypes.c_float, P, P, sz,
                                        P]),
@@ -433,6 +434,13 @@ def svd_kv_unpack(cache, capacity: int, n_kv_heads: int, pos_begin: int, pos_end
     _check("svd_kv_unpack", load().svd_kv_unpack(
         _ptr(cache), int(capacity), int(n_kv_heads), int(pos_begin), int(pos_end), _ptr(k_codes),
         _ptr(k_scales), _ptr(v_codes), _ptr(v_scales), int(ld), _stream(stream)))
+
+
+def svd_kv_append(k, v, ld: int, C: int, n_kv_heads: int, n_past: int, cache, capacity: int,
+                  stream=None):
+    _check("svd_kv_append", load().svd_kv_append(
+        _ptr(k), _ptr(v), int(ld), int(C), int(n_kv_heads), int(n_past), _ptr(cache),
+        int(capacity), _stream(stream)))
 
 
 def svd_kv_attention_workspace_bytes(n_q_heads: int, n_kv_heads: int, C: int) -> int:

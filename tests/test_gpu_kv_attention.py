@@ -1,5 +1,6 @@
 """GPU parity of the KV-read attention (svd_kv_attention over a native cache written by
-svd_kv_repack) against the fp64 oracle, element by element.
+svd_kv_repack) against the fp64 oracle, element by element, and of the cache's write side
+(svd_kv_append: codes and scales bit-exact against the oracle's quantiser).
 
 Tolerance, from the arithmetic of the kernel: query-key products are exact (f16 codes and queries)
 and summed in fp32; the only coarse rounding is P' = p * d_v to bfloat16 (relative 2^-9 per term)
@@ -26,7 +27,7 @@ def _native(kc, ks, vc, vs, capacity, fill=None, ranges=None):
     if fill is not None:
         cache.fill_(fill)
     dev = [to_dev(a) for a in (kc, ks, vc, vs)]
-    for p0, p1 in (ranges or [(0, ld)]):
+    for p0, p1 in ([(0, ld)] if ranges is None else ranges):
         svd.svd_kv_repack(*dev, Hkv, ld, p0, p1, cache, capacity)
     return cache
 
@@ -179,3 +180,91 @@ def test_bad_arguments_are_rejected():
         svd.svd_kv_attention(q, cache, L, Hq, Hkv, L - C, C, 0.1, out, ws[:16])  # workspace
     with pytest.raises(svd.SvdError):
         svd.svd_kv_attention(q, cache[1:], L, Hq, Hkv, L - C, C, 0.1, out, ws)  # misaligned
+
+
+def _window_kv(C, Hkv, ld, seed):
+    """fp32 keys and values of a window, rows of ld floats (the kv heads' 128 values each at the
+    front), with a zero block, a tie between the two largest value magnitudes and magnitudes
+    from 1e-6 to 1e4."""
+    g = np.random.default_rng(seed)
+    k = np.zeros((C, ld), np.float32)
+    v = np.zeros((C, ld), np.float32)
+    for c in range(C):
+        for h in range(Hkv):
+            s = 10.0 ** g.uniform(-6, 4)
+            k[c, h * D:(h + 1) * D] = g.normal(0, s, D)
+            v[c, h * D:(h + 1) * D] = g.normal(0, s, D)
+    k[0, 32:64] = 0.0
+    v[0, 32:64] = 0.0
+    v[-1, 5], v[-1, 9] = 3.0, -3.0
+    v[-1, 0:32][np.abs(v[-1, 0:32]) > 2.5] = 0.5
+    v[-1, 5], v[-1, 9] = 3.0, -3.0
+    return k, v
+
+
+@pytest.mark.parametrize("C,n_past,Hkv", [(4, 0, 8), (4, 29, 8), (1, 15, 2), (8, 100, 8),
+                                          (3, 16, 1), (6, 8189, 8)])
+def test_append_matches_the_oracle_quantiser(C, n_past, Hkv):
+    lib()
+    ld = Hkv * D + 64
+    k, v = _window_kv(C, Hkv, ld, seed=C + n_past)
+    capacity = n_past + C + 7
+    # positions before the window hold an earlier cache, the rest a fill pattern
+    kc0, ks0, vc0, vs0 = synth.kv_cache(Hkv, capacity, D, seed=3)
+    cache = _native(kc0, ks0, vc0, vs0, capacity, ranges=[(0, n_past)] if n_past else [],
+                    fill=0xA5)
+    kd, vd = to_dev(k), to_dev(v)
+    svd.svd_kv_append(kd, vd, ld, C, Hkv, n_past, cache, capacity)
+    out = [torch.zeros_like(to_dev(a)) for a in (kc0, ks0, vc0, vs0)]
+    svd.svd_kv_unpack(cache, capacity, Hkv, 0, n_past + C, *out, capacity)
+    torch.cuda.synchronize()
+    kc, ks, vc, vs = (o.cpu().numpy() for o in out)
+    ks, vs = ks.view(np.uint16), vs.view(np.uint16)
+    rk = k[:, :Hkv * D].reshape(C * Hkv, D)
+    rv = v[:, :Hkv * D].reshape(C * Hkv, D)
+    qk, qks, qv, qvs = oracle.kv_quantize(rk, rv)
+    for c in range(C):
+        for h in range(Hkv):
+            i, p = c * Hkv + h, n_past + c
+            assert np.array_equal(kc[h, p], qk[i]) and np.array_equal(ks[h, p], qks[i])
+            assert np.array_equal(vc[h, p], qv[i]) and np.array_equal(vs[h, p], qvs[i])
+    # the positions before the window are untouched
+    assert np.array_equal(kc[:, :n_past], kc0[:, :n_past])
+    assert np.array_equal(vc[:, :n_past], vc0[:, :n_past])
+    assert np.array_equal(vs[:, :n_past], vs0[:, :n_past])
+
+
+def test_append_then_attend_matches_oracle():
+    # The window's keys and values go in through svd_kv_append, then the window attends over the
+    # whole cache: the oracle quantises the same rows and attends in fp64.
+    lib()
+    Hq, Hkv, n_past, C = 40, 8, 777, 4
+    ld = Hkv * D
+    L = n_past + C
+    kc, ks, vc, vs = synth.kv_cache(Hkv, L, D, seed=21)
+    g = np.random.default_rng(22)
+    k = g.normal(0, 3, (C, ld)).astype(np.float32)
+    v = g.normal(0, 0.1, (C, ld)).astype(np.float32)
+    cache = _native(kc, ks, vc, vs, L, ranges=[(0, n_past)])
+    svd.svd_kv_append(to_dev(k), to_dev(v), ld, C, Hkv, n_past, cache, L)
+    q = synth.queries(C, Hq, D, seed=23)
+    o = _attend(q, cache, L, Hq, Hkv, n_past)
+    qk, qks, qv, qvs = oracle.kv_quantize(k.reshape(C * Hkv, D), v.reshape(C * Hkv, D))
+    for c in range(C):
+        for h in range(Hkv):
+            i = c * Hkv + h
+            kc[h, n_past + c], ks[h, n_past + c] = qk[i], qks[i]
+            vc[h, n_past + c], vs[h, n_past + c] = qv[i], qvs[i]
+    o_ref, a_ref = oracle.kv_attention(q, kc, ks, vc, vs, n_past)
+    _check(o, o_ref, a_ref)
+
+
+def test_append_rejects_bad_arguments():
+    lib()
+    Hkv, C, L = 2, 4, 32
+    cache = torch.zeros(svd.svd_kv_cache_bytes(Hkv, L), dtype=torch.uint8, device=DEV)
+    k = torch.zeros((C, Hkv * D), dtype=torch.float32, device=DEV)
+    with pytest.raises(svd.SvdError):
+        svd.svd_kv_append(k, k, Hkv * D - 1, C, Hkv, 0, cache, L)     # ld too short
+    with pytest.raises(svd.SvdError):
+        svd.svd_kv_append(k, k, Hkv * D, C, Hkv, L - C + 1, cache, L)  # past capacity
