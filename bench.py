@@ -471,11 +471,11 @@ def kv_read(dev, peak, stack_ms, layers=64, contexts=KV_CONTEXTS, steps=10, C=4,
 
 
 def pass_with_kv(vp, dev, peak, tail_ms, context=32768, steps=20):
-    """The verify pass with each layer's KV-read attention in its place (stack.KvPass: attention
-    over the layer's own cache between its q|k|v and o products, the matrices between two
-    attention steps in one chain launch; one CUDA graph), at the pages' 32K context, plus the
-    lm_head/sampler/acceptance tail measured in the main timed region.  Reports the pass rate
-    and the bytes of weights and cache per second."""
+    """The verify pass with each layer's KV cache in its place (stack.KvPass: the window's keys
+    and values appended, then attention over the layer's own cache, between its q|k|v and o
+    products; the matrices between two attention steps in one chain launch; one CUDA graph), at
+    the pages' 32K context, plus the lm_head/sampler/acceptance tail measured in the main timed
+    region.  Reports the pass rate and the bytes of weights and cache per second."""
     import torch
 
     from speculative_decoding_verify_06_gb300 import stack
@@ -496,10 +496,12 @@ def pass_with_kv(vp, dev, peak, tail_ms, context=32768, steps=20):
            "passes_per_s": 1000.0 / (ms + tail_ms), "bytes": nbytes,
            "gb_s": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak,
            "launches_per_pass": kp.launches(),
-           "workload": ("svd_kv_attention (40 query heads over 8 kv heads, dim 128, q8_0 keys / "
-                        "q4_0 values) over each layer's own cache between its q|k|v and o "
-                        "products; the matrices between two attention steps in one chain launch "
-                        "(65 chain launches per pass); one CUDA graph")}
+           "workload": ("per layer, between its q|k|v and o products: svd_kv_attention_append "
+                        "(the window's keys and values from the q|k|v output quantised into the "
+                        "layer's own q8_0-key / q4_0-value cache, then 40 query heads over 8 kv "
+                        "heads of dim 128 attending over it, one kernel); the matrices between "
+                        "two attention steps in one chain launch (65 chain launches per pass); "
+                        "one CUDA graph")}
     del kp
     torch.cuda.empty_cache()
     return out

@@ -308,12 +308,23 @@ int svd_kv_unpack(const void *cache, int capacity, int n_kv_heads, int pos_begin
  *   q8_0 d = max|x|/127, q = round-half-away(x/d); q4_0 d = m/-8 with m the value of largest
  *   magnitude (lowest dimension on ties), c = min(15, trunc(x/d + 8.5)); 1/d is taken as 0 when
  *   d = 0; d stored as fp16, round to nearest even), and writes them at cache positions
- *   n_past .. n_past + C - 1 of the native cache.  Other positions are untouched.  Errors:
+ *   n_past .. n_past + C - 1 of the native cache.  Other positions are untouched.  One kernel
+ *   (a programmatic dependent launch: it reads k and v only after the preceding kernel on the
+ *   stream has completed).  Errors:
  *   SVD_ERR_INVALID_ARG for null or misaligned pointers, non-positive sizes, ld < Hkv * 128 or
  *   n_past + C > capacity. */
 int svd_kv_append(const float *k, const float *v, int ld, int C, int n_kv_heads, int n_past,
                   void *cache, int capacity, svd_stream_t stream);
 size_t svd_kv_attention_workspace_bytes(int n_q_heads, int n_kv_heads, int C);
+/* svd_kv_attention_append: svd_kv_append of the window (k, v, ld as there) followed by
+ *   svd_kv_attention, in one kernel when C * Hq / Hkv <= 24 (the CTAs whose units hold the
+ *   window's positions quantise them into the cache before streaming those units), else as the
+ *   two launches.  The cache is written as by svd_kv_append and the output equals
+ *   svd_kv_append followed by svd_kv_attention bit for bit.  Errors as for both. */
+int svd_kv_attention_append(const uint16_t *q, const float *k, const float *v, int ld, void *cache,
+                            int capacity, int n_q_heads, int n_kv_heads, int n_past, int C,
+                            float scale, float *out, void *workspace, size_t workspace_bytes,
+                            svd_stream_t stream);
 int svd_kv_attention(const uint16_t *q, const void *cache, int capacity, int n_q_heads,
                      int n_kv_heads, int n_past, int C, float scale, float *out, void *workspace,
                      size_t workspace_bytes, svd_stream_t stream);

@@ -75,6 +75,8 @@ struct KvaParams {
     float *part_o;                // [cta][24][128]
     float2 *part_ml;              // [cta][24]: (max, sum) in base-2 units
     unsigned *flags;              // bit 0: a ring wait gave up
+    const float *k_new, *v_new;   // the window's fp32 keys / values to append first, or null
+    int ld_new;                   // floats between window positions of k_new / v_new
     int Hq, Hkv, G, C, n_past, units_cap, n_units, splits, n_rg, rows;
     float scale_log2;
 };
@@ -180,6 +182,82 @@ __device__ __forceinline__ float2 half2_bits_to_float2(uint32_t h) {
     return __half22float2(*reinterpret_cast<const __half2 *>(&h));
 }
 
+// ---- native layout: byte offsets inside a unit ----------------------------------------------
+__device__ __forceinline__ int key_code_offset(int r, int i) {
+    const int ks = i >> 4, ii = i & 15, lane = (r & 7) * 4 + ((ii & 7) >> 1);
+    return 512 * (ks >> 1) + 16 * lane + 8 * (ks & 1) + 4 * (ii >> 3) + 2 * (r >> 3) + (ii & 1);
+}
+// Byte holding the value codes of dimensions 16 mt + gid (low nibble) and 16 mt + gid + 8 (high
+// nibble) at position r of the unit.
+__device__ __forceinline__ int value_byte_offset(int r, int mt, int gid) {
+    const int lane = gid * 4 + ((r & 7) >> 1);
+    return kOffV + 512 * (mt >> 2) + 16 * lane + 4 * (mt & 3) + (r >> 3) + 2 * (r & 1);
+}
+__device__ __forceinline__ int scale_offset(int r, int b) { return 16 * (r & 7) + 2 * (4 * (r >> 3) + b); }
+
+// One warp quantises one cache position of one kv head -- its 128 key values to q8_0 and 128
+// value values to q4_0, block by block of 32 (lane l holds dimension 32 b + l), in the fp32 steps
+// of the formats' definitions (llama.cpp's block types of the same names):
+//   q8_0: d = max|x| / 127, q = round-half-away(x * (1/d)), 0 when d = 0;
+//   q4_0: m = the value of largest magnitude (the lowest dimension on ties), d = m / -8,
+//         c = min(15, trunc(x * (1/d) + 8.5)), 8 when d = 0;
+// and writes the codes and fp16 scales (round to nearest even) into the position's native unit.
+__device__ __forceinline__ void append_position(const float *kr, const float *vr,
+                                                unsigned char *unit, int r, int lane) {
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const int dim = 32 * b + lane;
+        const float x = kr[dim];
+        float amax = fabsf(x);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        const float d = __fdiv_rn(amax, 127.0f);
+        const float id = d != 0.f ? __fdiv_rn(1.0f, d) : 0.f;
+        const int q = (int)roundf(__fmul_rn(x, id));
+        unit[key_code_offset(r, dim)] = (unsigned char)(q + 128);
+        if (lane == 0)
+            *reinterpret_cast<uint16_t *>(unit + kOffKS + scale_offset(r, b)) =
+                __half_as_ushort(__float2half_rn(d));
+
+        const float y = vr[dim];
+        float ay = fabsf(y);
+        int at = lane;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float oa = __shfl_xor_sync(0xFFFFFFFFu, ay, o);
+            const int oi = __shfl_xor_sync(0xFFFFFFFFu, at, o);
+            if (oa > ay || (oa == ay && oi < at)) {
+                ay = oa;
+                at = oi;
+            }
+        }
+        const float m = __shfl_sync(0xFFFFFFFFu, y, at);
+        const float dv = __fdiv_rn(m, -8.0f);
+        const float idv = dv != 0.f ? __fdiv_rn(1.0f, dv) : 0.f;
+        const int cq = min(15, (int)__fadd_rn(__fmul_rn(y, idv), 8.5f));
+        // Dimensions 16 mt + j and 16 mt + j + 8 share a byte: lane l (l & 8 == 0) takes the code
+        // of lane l + 8 for the high nibble.
+        const int hi = __shfl_down_sync(0xFFFFFFFFu, cq, 8);
+        if ((lane & 8) == 0)
+            unit[value_byte_offset(r, dim >> 4, dim & 7)] = (unsigned char)(cq | (hi << 4));
+        if (lane == 0)
+            *reinterpret_cast<uint16_t *>(unit + kOffVS + scale_offset(r, b)) =
+                __half_as_ushort(__float2half_rn(dv));
+    }
+}
+
+// One warp per (window position c, kv head g): appends position n_past + c (append_position).
+__global__ void kv_append_kernel(const float *k, const float *v, int ld, int C, int Hkv,
+                                 int n_past, unsigned char *cache, int units_cap) {
+    griddep_launch_dependents();  // the attention that reads these positions may become resident
+    griddep_wait();               // k and v come from the kernel before this one
+    const int w = (int)((blockIdx.x * (unsigned)blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
+    if (w >= C * Hkv) return;
+    const int c = w / Hkv, g = w % Hkv, pos = n_past + c;
+    append_position(k + (size_t)c * ld + (size_t)g * kD, v + (size_t)c * ld + (size_t)g * kD,
+                    cache + ((size_t)g * units_cap + (pos >> 4)) * kUnitBytes, pos & 15, lane);
+}
+
 template <int NT>
 __global__ void __launch_bounds__(kThreads, 1) kv_attention_kernel(const KvaParams P) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -207,6 +285,24 @@ __global__ void __launch_bounds__(kThreads, 1) kv_attention_kernel(const KvaPara
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     griddep_wait();  // queries and cache written by the kernels before this one
+    if (P.k_new) {
+        // The window's positions inside this CTA's units are quantised into the cache first,
+        // by this CTA (no other CTA reads them); the writes are made visible to the bulk copies
+        // that read them back.
+        const int p_lo = max(P.n_past, cb * kUnitPos), p_hi = min(P.n_past + P.C, ce * kUnitPos);
+        if (p_lo < p_hi) {
+            for (int pos = p_lo + warp; pos < p_hi; pos += kWarps) {
+                const int c = pos - P.n_past;
+                append_position(P.k_new + (size_t)c * P.ld_new + (size_t)g * kD,
+                                P.v_new + (size_t)c * P.ld_new + (size_t)g * kD,
+                                const_cast<unsigned char *>(head) + (size_t)(pos >> 4) * kUnitBytes,
+                                pos & 15, lane);
+            }
+            __threadfence();
+            __syncthreads();
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
+    }
     if (lane == 0) {
 #pragma unroll
         for (int r = 0; r < kRing; ++r)
@@ -606,19 +702,6 @@ __global__ void __launch_bounds__(128) kv_attention_merge_kernel(const KvaParams
         make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
 }
 
-// ---- native layout: byte offsets inside a unit ----------------------------------------------
-__device__ __forceinline__ int key_code_offset(int r, int i) {
-    const int ks = i >> 4, ii = i & 15, lane = (r & 7) * 4 + ((ii & 7) >> 1);
-    return 512 * (ks >> 1) + 16 * lane + 8 * (ks & 1) + 4 * (ii >> 3) + 2 * (r >> 3) + (ii & 1);
-}
-// Byte holding the value codes of dimensions 16 mt + gid (low nibble) and 16 mt + gid + 8 (high
-// nibble) at position r of the unit.
-__device__ __forceinline__ int value_byte_offset(int r, int mt, int gid) {
-    const int lane = gid * 4 + ((r & 7) >> 1);
-    return kOffV + 512 * (mt >> 2) + 16 * lane + 4 * (mt & 3) + (r >> 3) + 2 * (r & 1);
-}
-__device__ __forceinline__ int scale_offset(int r, int b) { return 16 * (r & 7) + 2 * (4 * (r >> 3) + b); }
-
 // One thread per (kv head, position): canonical row -> native unit bytes.
 __global__ void kv_repack_kernel(const int8_t *kc, const uint16_t *ks, const uint8_t *vc,
                                  const uint16_t *vs, int Hkv, int ld, int p0, int p1,
@@ -669,63 +752,6 @@ __global__ void kv_unpack_kernel(const unsigned char *cache, int units_cap, int 
     for (int b = 0; b < 4; ++b) {
         ks[row * 4 + b] = *reinterpret_cast<const uint16_t *>(unit + kOffKS + scale_offset(r, b));
         vs[row * 4 + b] = *reinterpret_cast<const uint16_t *>(unit + kOffVS + scale_offset(r, b));
-    }
-}
-
-// One warp per (window position c, kv head g): quantises the position's 128 key values to q8_0
-// and 128 value values to q4_0, block by block of 32 (lane l holds dimension 32 b + l), in the
-// fp32 steps of the formats' definitions (llama.cpp's block types of the same names):
-//   q8_0: d = max|x| / 127, q = round-half-away(x * (1/d)), 0 when d = 0;
-//   q4_0: m = the value of largest magnitude (the lowest dimension on ties), d = m / -8,
-//         c = min(15, trunc(x * (1/d) + 8.5)), 8 when d = 0;
-// and writes codes and fp16 scales (round to nearest even) into the native unit of cache
-// position n_past + c.
-__global__ void kv_append_kernel(const float *k, const float *v, int ld, int C, int Hkv,
-                                 int n_past, unsigned char *cache, int units_cap) {
-    const int w = (int)((blockIdx.x * (unsigned)blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
-    if (w >= C * Hkv) return;
-    const int c = w / Hkv, g = w % Hkv, pos = n_past + c, r = pos & 15;
-    unsigned char *unit = cache + ((size_t)g * units_cap + (pos >> 4)) * kUnitBytes;
-    const float *kr = k + (size_t)c * ld + (size_t)g * kD, *vr = v + (size_t)c * ld + (size_t)g * kD;
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-        const int dim = 32 * b + lane;
-        const float x = kr[dim];
-        float amax = fabsf(x);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-        const float d = __fdiv_rn(amax, 127.0f);
-        const float id = d != 0.f ? __fdiv_rn(1.0f, d) : 0.f;
-        const int q = (int)roundf(__fmul_rn(x, id));
-        unit[key_code_offset(r, dim)] = (unsigned char)(q + 128);
-        if (lane == 0)
-            *reinterpret_cast<uint16_t *>(unit + kOffKS + scale_offset(r, b)) =
-                __half_as_ushort(__float2half_rn(d));
-
-        const float y = vr[dim];
-        float ay = fabsf(y);
-        int at = lane;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float oa = __shfl_xor_sync(0xFFFFFFFFu, ay, o);
-            const int oi = __shfl_xor_sync(0xFFFFFFFFu, at, o);
-            if (oa > ay || (oa == ay && oi < at)) {
-                ay = oa;
-                at = oi;
-            }
-        }
-        const float m = __shfl_sync(0xFFFFFFFFu, y, at);
-        const float dv = __fdiv_rn(m, -8.0f);
-        const float idv = dv != 0.f ? __fdiv_rn(1.0f, dv) : 0.f;
-        const int cq = min(15, (int)__fadd_rn(__fmul_rn(y, idv), 8.5f));
-        // Dimensions 16 mt + j and 16 mt + j + 8 share a byte: lane l (l & 8 == 0) takes the code
-        // of lane l + 8 for the high nibble.
-        const int hi = __shfl_down_sync(0xFFFFFFFFu, cq, 8);
-        if ((lane & 8) == 0)
-            unit[value_byte_offset(r, dim >> 4, dim & 7)] = (unsigned char)(cq | (hi << 4));
-        if (lane == 0)
-            *reinterpret_cast<uint16_t *>(unit + kOffVS + scale_offset(r, b)) =
-                __half_as_ushort(__float2half_rn(dv));
     }
 }
 
@@ -827,14 +853,16 @@ extern "C" size_t svd_kv_attention_workspace_bytes(int n_q_heads, int n_kv_heads
     return kva_workspace(n_q_heads, n_kv_heads, C);
 }
 
-extern "C" int svd_kv_attention(const uint16_t *q, const void *cache, int capacity, int n_q_heads,
-                                int n_kv_heads, int n_past, int C, float scale, float *out,
-                                void *workspace, size_t workspace_bytes, svd_stream_t stream) {
+static int kv_attention_launch(const uint16_t *q, const float *k_new, const float *v_new, int ld,
+                               const void *cache, int capacity, int n_q_heads, int n_kv_heads,
+                               int n_past, int C, float scale, float *out, void *workspace,
+                               size_t workspace_bytes, cudaStream_t stream) {
     KvaGeom k;
     if (!q || !cache || !out || capacity <= 0 || !kva_geom(n_q_heads, n_kv_heads, n_past, C, k) ||
         (long long)n_past + C > capacity || !(scale > 0.f) || !(scale < INFINITY))
         return SVD_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(cache) || !aligned16(out)) return SVD_ERR_INVALID_ARG;
+    if (k_new && (!v_new || ld < n_kv_heads * kD)) return SVD_ERR_INVALID_ARG;
     const size_t need = kva_workspace(n_q_heads, n_kv_heads, C);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return SVD_ERR_WORKSPACE;
     KvaParams P;
@@ -855,15 +883,49 @@ extern "C" int svd_kv_attention(const uint16_t *q, const void *cache, int capaci
     P.n_rg = k.n_rg;
     P.rows = k.rows;
     P.scale_log2 = scale * 1.4426950408889634f;
+    P.k_new = P.v_new = nullptr;
+    P.ld_new = 0;
+    if (k_new) {
+        if (k.n_rg == 1) {
+            // One CTA reads each unit: the CTAs holding the window's positions append them.
+            P.k_new = k_new;
+            P.v_new = v_new;
+            P.ld_new = ld;
+        } else {
+            // Several row groups read the same units: append first, in a kernel of its own.
+            const long long warps = (long long)C * n_kv_heads;
+            SVD_CUDA_TRY(launch(kv_append_kernel, dim3((unsigned)((warps + 3) / 4)), dim3(128), 0,
+                                stream, true, k_new, v_new, ld, C, n_kv_heads, n_past,
+                                (unsigned char *)const_cast<void *>(cache), units_for(capacity)));
+        }
+    }
     const dim3 grid(k.splits, n_kv_heads, k.n_rg);
     cudaError_t e;
     switch (k.nt) {
-        case 1: e = launch_kva<1>(P, grid, (cudaStream_t)stream); break;
-        case 2: e = launch_kva<2>(P, grid, (cudaStream_t)stream); break;
-        default: e = launch_kva<3>(P, grid, (cudaStream_t)stream); break;
+        case 1: e = launch_kva<1>(P, grid, stream); break;
+        case 2: e = launch_kva<2>(P, grid, stream); break;
+        default: e = launch_kva<3>(P, grid, stream); break;
     }
     SVD_CUDA_TRY(e);
     return SVD_OK;
+}
+
+extern "C" int svd_kv_attention(const uint16_t *q, const void *cache, int capacity, int n_q_heads,
+                                int n_kv_heads, int n_past, int C, float scale, float *out,
+                                void *workspace, size_t workspace_bytes, svd_stream_t stream) {
+    return kv_attention_launch(q, nullptr, nullptr, 0, cache, capacity, n_q_heads, n_kv_heads,
+                               n_past, C, scale, out, workspace, workspace_bytes,
+                               (cudaStream_t)stream);
+}
+
+extern "C" int svd_kv_attention_append(const uint16_t *q, const float *k, const float *v, int ld,
+                                       void *cache, int capacity, int n_q_heads, int n_kv_heads,
+                                       int n_past, int C, float scale, float *out,
+                                       void *workspace, size_t workspace_bytes,
+                                       svd_stream_t stream) {
+    if (!k || !v) return SVD_ERR_INVALID_ARG;
+    return kv_attention_launch(q, k, v, ld, cache, capacity, n_q_heads, n_kv_heads, n_past, C,
+                               scale, out, workspace, workspace_bytes, (cudaStream_t)stream);
 }
 
 extern "C" int svd_kv_append(const float *k, const float *v, int ld, int C, int n_kv_heads,
@@ -873,8 +935,8 @@ extern "C" int svd_kv_append(const float *k, const float *v, int ld, int C, int 
         return SVD_ERR_INVALID_ARG;
     if (!aligned16(cache)) return SVD_ERR_INVALID_ARG;
     const long long warps = (long long)C * n_kv_heads;
-    kv_append_kernel<<<(unsigned)((warps + 3) / 4), 128, 0, (cudaStream_t)stream>>>(
-        k, v, ld, C, n_kv_heads, n_past, (unsigned char *)cache, units_for(capacity));
-    SVD_CUDA_TRY(cudaGetLastError());
+    SVD_CUDA_TRY(launch(kv_append_kernel, dim3((unsigned)((warps + 3) / 4)), dim3(128), 0,
+                        (cudaStream_t)stream, true, k, v, ld, C, n_kv_heads, n_past,
+                        (unsigned char *)cache, units_for(capacity)));
     return SVD_OK;
 }

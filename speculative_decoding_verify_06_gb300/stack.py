@@ -210,18 +210,19 @@ class ColumnsView:
 
 
 class KvPass:
-    """The resident weights of a VerifyPass with the KV-read attention of every layer placed
-    where the model has it, between a layer's q|k|v product and its o product: svd_kv_attention of
-    the window's C queries over the layer's own q8_0-key / q4_0-value cache (40 query heads over
-    8 kv heads of dimension 128, the window at positions context - C .. context - 1).  The
+    """The resident weights of a VerifyPass with every layer's KV cache in its place, between the
+    layer's q|k|v product and its o product: svd_kv_attention_append -- the window's keys and
+    values (the k and v columns of the q|k|v output) quantised to q8_0/q4_0 at the window's cache
+    positions, then the window's C queries attending over the layer's own cache (40 query heads
+    over 8 kv heads of dimension 128, the window at positions context - C .. context - 1).  The
     matrices between two attention steps (o, gate|up and down of one layer with q|k|v of the
-    next) form one chain launch, so a pass is 65 chain launches and 64 attention steps.  "Decode is memory-bound ..." ("The ceiling"): at long
-    context the KV cache joins the weights on every pass.  Queries and attention outputs are
-    synthetic buffers of their own, like every activation of the stack; the stream order is the
-    model's.  The whole stack is recorded into one CUDA graph."""
+    next) form one chain launch, so a pass is 65 chain launches and 64 append + attention steps,
+    recorded into one CUDA graph.  "Decode is memory-bound ..." ("The ceiling"): at long context
+    the KV cache joins the weights on every pass.  Queries and attention outputs are synthetic
+    buffers of their own, like the stack's other activations; the stream order is the model's."""
 
-    def __init__(self, vp: VerifyPass, context: int, seed: int = 0):
-        self.vp, self.context = vp, context
+    def __init__(self, vp: VerifyPass, context: int, seed: int = 0, append: bool = True):
+        self.vp, self.context, self.append = vp, context, append
         dev, C = vp.device, vp.C
         Hq, Hkv, D = synth.N_Q_HEADS, synth.N_KV_HEADS, synth.HEAD_DIM
         self.Hq, self.Hkv, self.D = Hq, Hkv, D
@@ -250,11 +251,22 @@ class KvPass:
 
     def enqueue(self, stream=None):
         vp = self.vp
+        n = len(vp.gemms)
         for l in range(vp.layers):
             svd.svd_verify_chain(self.segments[l], vp.C, vp.ws, stream=stream)
-            svd.svd_kv_attention(self.q, self.caches[l], self.context, self.Hq, self.Hkv,
-                                 self.context - vp.C, vp.C, 1.0 / self.D ** 0.5, self.o,
-                                 self.att_ws, stream=stream)
+            if self.append:
+                # the window's keys and values, columns 5120.. and 6144.. of the q|k|v output,
+                # quantised into the cache by the attention kernel itself
+                y = vp.linears[n * l].Y
+                base, row = y.data_ptr(), y.shape[1]
+                svd.svd_kv_attention_append(
+                    self.q, base + 4 * synth.HIDDEN, base + 4 * (synth.HIDDEN + self.Hkv * self.D),
+                    row, self.caches[l], self.context, self.Hq, self.Hkv, self.context - vp.C,
+                    vp.C, 1.0 / self.D ** 0.5, self.o, self.att_ws, stream=stream)
+            else:
+                svd.svd_kv_attention(self.q, self.caches[l], self.context, self.Hq, self.Hkv,
+                                     self.context - vp.C, vp.C, 1.0 / self.D ** 0.5, self.o,
+                                     self.att_ws, stream=stream)
         svd.svd_verify_chain(self.segments[vp.layers], vp.C, vp.ws, stream=stream)
 
     def capture(self):

@@ -48,7 +48,7 @@ EXPORTS = (
     "svd_spec_adapt_destroy", "svd_ngram_create", "svd_ngram_append", "svd_ngram_propose",
     "svd_ngram_length", "svd_ngram_destroy",
     "svd_kv_cache_bytes", "svd_kv_repack", "svd_kv_unpack", "svd_kv_append",
-    "svd_kv_attention_workspace_bytes", "svd_kv_attention",
+    "svd_kv_attention_workspace_bytes", "svd_kv_attention", "svd_kv_attention_append",
 )
 
 
@@ -151,6 +151,8 @@ def load(path: str = LIB_PATH):
             "svd_kv_unpack": (i32, [P, i32, i32, i32, i32, P, P, P, P, i32, P]),
             "svd_kv_append": (i32, [P, P, i32, i32, i32, i32, P, i32, P]),
             "svd_kv_attention_workspace_bytes": (sz, [i32, i32, i32]),
+            "svd_kv_attention_append": (i32, [P, P, P, i32, P, i32, i32, i32, i32, i32,
+                                              ctypes.c_float, P, P, sz, P]),
             "svd_kv_attention": (i32, [P, P, i32, i32, i32, i32, i32, ctypes.c_float, P, P, sz,
                                        P]),
         }
@@ -455,3 +457,14 @@ def svd_kv_attention(q, cache, capacity: int, n_q_heads: int, n_kv_heads: int, n
     _check("svd_kv_attention", load().svd_kv_attention(
         _ptr(q), _ptr(cache), int(capacity), int(n_q_heads), int(n_kv_heads), int(n_past), int(C),
         float(scale), _ptr(out), _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def svd_kv_attention_append(q, k, v, ld: int, cache, capacity: int, n_q_heads: int,
+                            n_kv_heads: int, n_past: int, C: int, scale: float, out, workspace,
+                            workspace_bytes: int = 0, stream=None):
+    if not workspace_bytes and workspace is not None and not isinstance(workspace, int):
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check("svd_kv_attention_append", load().svd_kv_attention_append(
+        _ptr(q), _ptr(k), _ptr(v), int(ld), _ptr(cache), int(capacity), int(n_q_heads),
+        int(n_kv_heads), int(n_past), int(C), float(scale), _ptr(out), _ptr(workspace),
+        int(workspace_bytes), _stream(stream)))

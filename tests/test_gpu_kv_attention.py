@@ -268,3 +268,31 @@ def test_append_rejects_bad_arguments():
         svd.svd_kv_append(k, k, Hkv * D - 1, C, Hkv, 0, cache, L)     # ld too short
     with pytest.raises(svd.SvdError):
         svd.svd_kv_append(k, k, Hkv * D, C, Hkv, L - C + 1, cache, L)  # past capacity
+
+
+@pytest.mark.parametrize("Hq,Hkv,n_past,C", [(40, 8, 1000, 4), (40, 8, 4093, 4), (10, 2, 14, 4),
+                                             (40, 8, 2000, 8), (5, 1, 0, 3)])
+def test_fused_append_equals_append_then_attend(Hq, Hkv, n_past, C):
+    # svd_kv_attention_append (one kernel when the window's rows fit one row group, else the two
+    # launches) leaves the same cache bytes and the same output, bit for bit, as svd_kv_append
+    # followed by svd_kv_attention.
+    lib()
+    L = n_past + C
+    kc, ks, vc, vs = synth.kv_cache(Hkv, L, D, seed=31)
+    ld = Hkv * D + 32
+    k, v = _window_kv(C, Hkv, ld, seed=32)
+    q = synth.queries(C, Hq, D, seed=33)
+    ranges = [(0, n_past)] if n_past else []
+    c1 = _native(kc, ks, vc, vs, L, ranges=ranges, fill=0x5A)
+    c2 = _native(kc, ks, vc, vs, L, ranges=ranges, fill=0x5A)
+    kd, vd, qd = to_dev(k), to_dev(v), to_dev(q)
+    ws = torch.zeros(svd.svd_kv_attention_workspace_bytes(Hq, Hkv, C), dtype=torch.uint8, device=DEV)
+    o1 = torch.empty((C, Hq, D), dtype=torch.float32, device=DEV)
+    o2 = torch.empty_like(o1)
+    svd.svd_kv_append(kd, vd, ld, C, Hkv, n_past, c1, L)
+    svd.svd_kv_attention(qd, c1, L, Hq, Hkv, n_past, C, 0.0884, o1, ws)
+    svd.svd_kv_attention_append(qd, kd, vd, ld, c2, L, Hq, Hkv, n_past, C, 0.0884, o2, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(c1, c2)
+    assert torch.equal(o1, o2)
+    assert int(ws[:4].view(torch.int32).item()) == 0

@@ -61,16 +61,17 @@ def test_chain_pdl_and_plain_launches_agree():
 
 
 def test_pass_with_kv_attention_matches_eager_and_oracle():
-    # Two layers of the stack with each layer's KV-read attention in its place (between its
-    # q|k|v and o products, the matrices in between as chain launches), recorded into one graph:
-    # replays equal the eager run, the attention output matches the oracle and the last linear's
-    # output equals the plain stack's.
+    # Two layers of the stack with each layer's KV cache in its place (the window's keys and
+    # values appended from the q|k|v output, then attention, between the q|k|v and o products;
+    # the matrices in between as chain launches), recorded into one graph: replays equal the
+    # eager run, the last attention output matches the oracle over the oracle-quantised window
+    # and the last linear's output equals the plain stack's.
     lib()
     vp = stack.VerifyPass(layers=2, C=4, seed=5, head=False)
     vp.enqueue_stack()
     torch.cuda.synchronize()
     y_plain = vp.linears[-1].Y.clone()
-    ctx = 300
+    ctx, C = 300, 4
     kp = stack.KvPass(vp, ctx, seed=9)
     kp.enqueue()
     torch.cuda.synchronize()
@@ -82,10 +83,21 @@ def test_pass_with_kv_attention_matches_eager_and_oracle():
         kp.launch()
     torch.cuda.synchronize()
     assert torch.equal(kp.o, o_eager)
-    # the oracle on host copies of the same cache bytes (every layer's cache holds this draw)
-    kc, ks, vc, vs = synth.kv_cache_torch(kp.Hkv, ctx, kp.D, 9, torch.device("cuda:0"))
+    # the oracle: the cache's draw, with the window's positions quantised from the last layer's
+    # q|k|v output (columns 5120.. for keys, 6144.. for values)
+    Hkv, D = kp.Hkv, kp.D
+    kc, ks, vc, vs = (a.cpu().numpy() for a in synth.kv_cache_torch(Hkv, ctx, D, 9,
+                                                                  torch.device("cuda:0")))
+    ks, vs = ks.view(np.uint16), vs.view(np.uint16)
+    y = vp.linears[len(vp.gemms)].Y.cpu().numpy()
+    kw = y[:, synth.HIDDEN:synth.HIDDEN + Hkv * D].reshape(C * Hkv, D)
+    vw = y[:, synth.HIDDEN + Hkv * D:synth.HIDDEN + 2 * Hkv * D].reshape(C * Hkv, D)
+    qk, qks, qv, qvs = oracle.kv_quantize(kw, vw)
+    for c in range(C):
+        for h in range(Hkv):
+            i, p = c * Hkv + h, ctx - C + c
+            kc[h, p], ks[h, p], vc[h, p], vs[h, p] = qk[i], qks[i], qv[i], qvs[i]
     q = kp.q.view(torch.int16).cpu().numpy().view(np.uint16)
-    o_ref, a_ref = oracle.kv_attention(q, kc.cpu().numpy(), ks.cpu().numpy().view(np.uint16),
-                                       vc.cpu().numpy(), vs.cpu().numpy().view(np.uint16), ctx - 4)
+    o_ref, a_ref = oracle.kv_attention(q, kc, ks, vc, vs, ctx - C)
     err = np.abs(o_eager.cpu().numpy().astype(np.float64) - o_ref)
     assert np.all(err <= 2.0 ** -8 * a_ref)
