@@ -305,71 +305,95 @@ def accept_oracle_sample(P, Q, samples, pool, n, g, dev, k=3):
             "seconds": dt, "sample": f"{n} windows at k = {k} from the same (p, q) pool, fp64"}
 
 
+ACCEPT_ALPHAS = (0.35, 0.5, 0.6, 0.7, 0.8, 0.9)
+
+
+def accept_pool(dev, V, pool, alpha, g):
+    """A pool of (p, q) pairs: p from Zipf(1.1)-ranked logits under a random permutation, q from
+    the same logits plus tau * N(0, 1) noise, tau bisected per pair so that sum min(p, q) is
+    alpha (within 1e-4 after 40 halvings)."""
+    import torch
+    base = -1.1 * torch.log(torch.arange(1, V + 1, device=dev, dtype=torch.float32))
+    lp = base[torch.argsort(torch.rand((pool, V), generator=g, device=dev), dim=1)]
+    eps = torch.randn((pool, V), generator=g, device=dev)
+    P = torch.softmax(lp, dim=1)
+    lo = torch.zeros(pool, device=dev)
+    hi = torch.full((pool,), 64.0, device=dev)
+    for _ in range(40):
+        tau = 0.5 * (lo + hi)
+        a = torch.minimum(P, torch.softmax(lp + tau[:, None] * eps, dim=1)).sum(1)
+        lo = torch.where(a > alpha, tau, lo)
+        hi = torch.where(a > alpha, hi, tau)
+    Q = torch.softmax(lp + (0.5 * (lo + hi))[:, None] * eps, dim=1)
+    del lp, eps
+    return P.contiguous(), Q.contiguous()
+
+
 def accept_throughput(dev, peak, n_windows=1_000_000, ks=(1, 3, 5), pool=256, seed=7,
-                      oracle_windows=0):
-    """svd_accept on many windows whose rows come from a pool of (p, q) pairs larger than L2:
-    p from Zipf(1.1)-ranked logits under a random permutation, q from the same logits plus
-    tau * N(0, 1) noise (tau bisected for a mean sum min(p, q) of 0.6); every position of a
-    window draws its pair independently, so acceptances are i.i.d. with that mean.  Reports
-    windows/s, the bytes the kernel must read (the residual (p - q)+ row after a rejection,
-    the p row for the capping draw, the probed entries) per second against the copy peak,
-    and tokens per pass against (1 - a^(k+1)) / (1 - a)."""
+                      alphas=ACCEPT_ALPHAS, oracle_windows=0):
+    """svd_accept on many windows whose rows come from a pool of (p, q) pairs larger than L2
+    (accept_pool), for every target acceptance alpha, a stochastic drafter (x ~ q) and a greedy
+    one (x = argmax q, with the one-hot q it stands for), and k in {1, 3, 5}: every position of
+    a window draws its pair independently, so acceptances are i.i.d. with the pool's mean alpha.
+    Reports windows/s, the bytes the kernel must read (the residual (p - q)+ row after a
+    rejection, the p row for the capping draw, the probed entries) per second against the copy
+    peak, and tokens per pass against (1 - a^(k+1)) / (1 - a) at the measured mean alpha."""
     import torch
 
     from speculative_decoding_verify_06_gb300 import svd, synth
     V = synth.VOCAB
     g = torch.Generator(device=dev)
     g.manual_seed(seed)
-    base = -1.1 * torch.log(torch.arange(1, V + 1, device=dev, dtype=torch.float32))
-    perm = torch.argsort(torch.rand((pool, V), generator=g, device=dev), dim=1)
-    lp = base[perm]
-    eps = torch.randn((pool, V), generator=g, device=dev)
-    P = torch.softmax(lp, dim=1)
-
-    def mean_alpha(tau):
-        return float(torch.minimum(P, torch.softmax(lp + tau * eps, dim=1)).sum(1).mean())
-    lo, hi = 0.0, 64.0
-    for _ in range(40):
-        tau = 0.5 * (lo + hi)
-        if mean_alpha(tau) > 0.6:
-            lo = tau
-        else:
-            hi = tau
-    Q = torch.softmax(lp + tau * eps, dim=1).contiguous()
-    alpha = float(torch.minimum(P, Q).sum(1).mean())
-    P = P.contiguous()
-    samples = torch.multinomial(Q, 4096, replacement=True, generator=g)  # [pool, 4096]
-    out = {"alpha": alpha, "pool_bytes": 2 * pool * V * 4, "windows": n_windows}
-    if oracle_windows:
-        out["cpu_baseline"] = accept_oracle_sample(P, Q, samples, pool, oracle_windows, g, dev)
     s = torch.cuda.current_stream(dev)
-    for k in ks:
-        rows = torch.randint(0, pool, (n_windows, k + 1), generator=g, device=dev)
-        q_rows = rows[:, :k].contiguous()
-        pick = torch.randint(0, 4096, (n_windows, k), generator=g, device=dev)
-        draft = samples[q_rows, pick].to(torch.int32).contiguous()
-        tok = torch.empty((n_windows, k + 1), dtype=torch.int32, device=dev)
-        ne = torch.empty(n_windows, dtype=torch.int32, device=dev)
-        st = torch.empty(n_windows, dtype=torch.int32, device=dev)
+    out = {"pool_pairs": pool, "pool_bytes": 2 * pool * V * 4, "windows": n_windows,
+           "by_alpha": {}}
+    for target in alphas:
+        P, Q = accept_pool(dev, V, pool, target, g)
+        samples = torch.multinomial(Q, 4096, replacement=True, generator=g)  # [pool, 4096]
+        am = Q.argmax(dim=1)
+        Q1 = torch.zeros_like(Q)
+        Q1.scatter_(1, am[:, None], 1.0)
+        if oracle_windows and abs(target - 0.6) < 1e-9:
+            out["cpu_baseline"] = accept_oracle_sample(P, Q, samples, pool, oracle_windows, g,
+                                                       dev)
+        res = {}
+        for drafter, Qd in (("stochastic", Q), ("greedy", Q1)):
+            alpha = float(torch.minimum(P, Qd).sum(1).mean())
+            r = {"alpha": alpha}
+            for k in ks:
+                rows = torch.randint(0, pool, (n_windows, k + 1), generator=g, device=dev)
+                q_rows = rows[:, :k].contiguous()
+                if drafter == "stochastic":
+                    pick = torch.randint(0, 4096, (n_windows, k), generator=g, device=dev)
+                    draft = samples[q_rows, pick].to(torch.int32).contiguous()
+                else:
+                    draft = am[q_rows].to(torch.int32).contiguous()
+                tok = torch.empty((n_windows, k + 1), dtype=torch.int32, device=dev)
+                ne = torch.empty(n_windows, dtype=torch.int32, device=dev)
+                st = torch.empty(n_windows, dtype=torch.int32, device=dev)
 
-        def run(sd):
-            svd.svd_accept(P, draft, n_windows, k, V, tok, ne, st, q=Q, p_rows=rows, q_rows=q_rows,
-                           seed=sd, stream=s)
-        run(1)
-        torch.cuda.synchronize(dev)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(s)
-        run(2)
-        e1.record(s)
-        torch.cuda.synchronize(dev)
-        ms = e0.elapsed_time(e1)
-        bonus = int((ne == k + 1).sum())
-        nbytes = (n_windows - bonus) * 8 * V + bonus * 4 * V + n_windows * 8 * k
-        out[f"k{k}"] = {"ms": ms, "windows_per_s": n_windows / (ms / 1000.0),
-                        "gb_s": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak,
-                        "tokens_per_pass": float(ne.double().mean()),
-                        "formula": (1 - alpha ** (k + 1)) / (1 - alpha),
-                        "status_nonzero": int((st != 0).sum())}
+                def run(sd):
+                    svd.svd_accept(P, draft, n_windows, k, V, tok, ne, st, q=Qd, p_rows=rows,
+                                   q_rows=q_rows, seed=sd, stream=s)
+                run(1)
+                torch.cuda.synchronize(dev)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(s)
+                run(2)
+                e1.record(s)
+                torch.cuda.synchronize(dev)
+                ms = e0.elapsed_time(e1)
+                bonus = int((ne == k + 1).sum())
+                nbytes = (n_windows - bonus) * 8 * V + bonus * 4 * V + n_windows * 8 * k
+                r[f"k{k}"] = {"ms": ms, "windows_per_s": n_windows / (ms / 1000.0),
+                              "gb_s": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak,
+                              "tokens_per_pass": float(ne.double().mean()),
+                              "formula": (1 - alpha ** (k + 1)) / (1 - alpha),
+                              "status_nonzero": int((st != 0).sum())}
+            res[drafter] = r
+        out["by_alpha"][f"{target:g}"] = res
+        del P, Q, Q1, samples
+        torch.cuda.empty_cache()
     return out
 
 
