@@ -318,9 +318,10 @@ int svd_kv_append(const float *k, const float *v, int ld, int C, int n_kv_heads,
 size_t svd_kv_attention_workspace_bytes(int n_q_heads, int n_kv_heads, int C);
 /* svd_kv_attention_append: svd_kv_append of the window (k, v, ld as there) followed by
  *   svd_kv_attention, in one kernel when C * Hq / Hkv <= 24 (the CTAs whose units hold the
- *   window's positions quantise them into the cache before streaming those units), else as the
- *   two launches.  The cache is written as by svd_kv_append and the output equals
- *   svd_kv_append followed by svd_kv_attention bit for bit.  Errors as for both. */
+ *   window's positions quantise them into the cache before streaming those units; the last
+ *   split of the context is made a little shorter to absorb that work), else as the two
+ *   launches.  The cache is written as by svd_kv_append; the output is that of svd_kv_append
+ *   followed by svd_kv_attention up to the order of the fp32 sums.  Errors as for both. */
 int svd_kv_attention_append(const uint16_t *q, const float *k, const float *v, int ld, void *cache,
                             int capacity, int n_q_heads, int n_kv_heads, int n_past, int C,
                             float scale, float *out, void *workspace, size_t workspace_bytes,

@@ -271,9 +271,11 @@ __global__ void __launch_bounds__(kThreads, 1) kv_attention_kernel(const KvaPara
 
     griddep_launch_dependents();  // the merge kernel may become resident and wait
 
-    // This warp's run of units.
-    const int cb = (int)((long long)split * P.n_units / P.splits);
-    const int ce = (int)((long long)(split + 1) * P.n_units / P.splits);
+    // This CTA's and this warp's runs of units.  In append mode the last split, which holds the
+    // window and quantises it first, gets about two units per warp fewer.
+    const int shift = P.k_new ? min(2 * kWarps, P.n_units / (2 * P.splits)) : 0;
+    const int cb = min(P.n_units, (int)((long long)split * (P.n_units + shift) / P.splits));
+    const int ce = min(P.n_units, (int)((long long)(split + 1) * (P.n_units + shift) / P.splits));
     const int wb = cb + (int)((long long)warp * (ce - cb) / kWarps);
     const int we = cb + (int)((long long)(warp + 1) * (ce - cb) / kWarps);
     const unsigned char *head = P.cache + (size_t)g * P.units_cap * kUnitBytes;
@@ -285,23 +287,36 @@ __global__ void __launch_bounds__(kThreads, 1) kv_attention_kernel(const KvaPara
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     griddep_wait();  // queries and cache written by the kernels before this one
-    if (P.k_new) {
-        // The window's positions inside this CTA's units are quantised into the cache first,
-        // by this CTA (no other CTA reads them); the writes are made visible to the bulk copies
-        // that read them back.
-        const int p_lo = max(P.n_past, cb * kUnitPos), p_hi = min(P.n_past + P.C, ce * kUnitPos);
-        if (p_lo < p_hi) {
-            for (int pos = p_lo + warp; pos < p_hi; pos += kWarps) {
-                const int c = pos - P.n_past;
-                append_position(P.k_new + (size_t)c * P.ld_new + (size_t)g * kD,
-                                P.v_new + (size_t)c * P.ld_new + (size_t)g * kD,
-                                const_cast<unsigned char *>(head) + (size_t)(pos >> 4) * kUnitBytes,
-                                pos & 15, lane);
+    // The window's positions inside this CTA's units (append mode) are quantised into the cache
+    // by this CTA (no other CTA reads them) and made visible to the bulk copies that read them
+    // back.  When no warp's first kRing units hold one, the prologue copies go first and the
+    // append overlaps their latency (ordered by the barrier after the query staging); otherwise
+    // it comes before the prologue.
+    const int p_lo = max(P.n_past, cb * kUnitPos), p_hi = min(P.n_past + P.C, ce * kUnitPos);
+    const bool do_append = P.k_new != nullptr && p_lo < p_hi;
+    bool late_ok = do_append;
+    if (do_append) {
+        for (int u = p_lo / kUnitPos; u <= (p_hi - 1) / kUnitPos; ++u)
+            for (int w = 0; w < kWarps; ++w) {
+                const int b0 = cb + (int)((long long)w * (ce - cb) / kWarps);
+                const int b1 = cb + (int)((long long)(w + 1) * (ce - cb) / kWarps);
+                if (u >= b0 && u < b1 && u < b0 + kRing) late_ok = false;
             }
-            __threadfence();
-            __syncthreads();
-            asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
+    auto append_window = [&]() {
+        for (int pos = p_lo + warp; pos < p_hi; pos += kWarps) {
+            const int c = pos - P.n_past;
+            append_position(P.k_new + (size_t)c * P.ld_new + (size_t)g * kD,
+                            P.v_new + (size_t)c * P.ld_new + (size_t)g * kD,
+                            const_cast<unsigned char *>(head) + (size_t)(pos >> 4) * kUnitBytes,
+                            pos & 15, lane);
         }
+        __threadfence();
+    };
+    if (do_append && !late_ok) {
+        append_window();
+        __syncthreads();
+        asm volatile("fence.proxy.async.global;" ::: "memory");
     }
     if (lane == 0) {
 #pragma unroll
@@ -326,7 +341,9 @@ __global__ void __launch_bounds__(kThreads, 1) kv_attention_kernel(const KvaPara
         const uint32_t v = pack_f16(__uint_as_float(bits << 16), __uint_as_float(bits & 0xFFFF0000u));
         asm volatile("st.shared.u32 [%0], %1;" ::"r"(qs + r * kQPitch + 4 * pr), "r"(v));
     }
+    if (do_append && late_ok) append_window();
     __syncthreads();
+    if (do_append && late_ok) asm volatile("fence.proxy.async.global;" ::: "memory");
     // -1152 * (sum of the f16 query values of each row and 32-dimension block), in fp32.
     if (threadIdx.x < kRowsPerGroup * 4) {
         const int r = threadIdx.x >> 2, b = threadIdx.x & 3;
