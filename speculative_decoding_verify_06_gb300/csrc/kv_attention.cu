@@ -373,14 +373,11 @@ __global__ void __launch_bounds__(kThreads, 1) kv_attention_kernel(const KvaPara
     const uint32_t qlane = qs + (lane & 7) * kQPitch + 2 * (16 * (lane >> 4) + 8 * ((lane >> 3) & 1));
 
     float o[8][NT][4];
-    float m[NT][2], l[NT][2];
+    float m[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            m[nt][e] = -INFINITY;
-            l[nt][e] = 0.f;
-        }
+        for (int e = 0; e < 2; ++e) m[nt][e] = -INFINITY;
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
@@ -566,12 +563,10 @@ __global__ void __launch_bounds__(kThreads, 1) kv_attention_kernel(const KvaPara
 
     // Row sums over the 8 position lanes; m is already uniform across them.  From here on m is
     // in base-2 units (m * scale), as the merge expects.
+    float l[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-        float l0, l1;
-        unf2(lsum[nt], l0, l1);
-        l[nt][0] += l0;
-        l[nt][1] += l1;
+        unf2(lsum[nt], l[nt][0], l[nt][1]);
 #pragma unroll
         for (int e = 0; e < 2; ++e) m[nt][e] = m[nt][e] * scl;
     }
