@@ -298,3 +298,56 @@ def test_fused_append_equals_append_then_attend(Hq, Hkv, n_past, C):
     scale = float(o1.abs().max())
     assert float((o1 - o2).abs().max()) <= 2.0 ** -16 * scale
     assert int(ws[:4].view(torch.int32).item()) == 0
+
+
+def test_full_size_262k_context_sampled_head():
+    # The benchmark's longest context in its launch configuration (8 kv heads, 19 splits each):
+    # the oracle checks kv head 3's five query heads at all four window rows.
+    Hq, Hkv, C = synth.N_Q_HEADS, synth.N_KV_HEADS, 4
+    L = 262144
+    n_past = L - C
+    kc, ks, vc, vs = synth.kv_cache(Hkv, L, D, seed=262)
+    q = synth.queries(C, Hq, D, seed=263)
+    cache = _native(kc, ks, vc, vs, L)
+    o = _attend(q, cache, L, Hq, Hkv, n_past)
+    G, g = Hq // Hkv, 3
+    sl = slice(g, g + 1)
+    o_ref, a_ref = oracle.kv_attention(q[:, g * G:(g + 1) * G], kc[sl], ks[sl], vc[sl], vs[sl], n_past)
+    _check(o[:, g * G:(g + 1) * G], o_ref, a_ref)
+
+
+def test_full_size_fused_append_32k():
+    # The pass's call at 32K: the window's keys and values quantised by the attention kernel
+    # itself (shortened last split), 40 query heads over 8 kv heads; kv heads 0 and 7 against
+    # the oracle over the oracle-quantised window.
+    Hq, Hkv, C = synth.N_Q_HEADS, synth.N_KV_HEADS, 4
+    L = 32768
+    n_past = L - C
+    kc, ks, vc, vs = synth.kv_cache(Hkv, L, D, seed=327)
+    cache = _native(kc, ks, vc, vs, L, ranges=[(0, n_past)])
+    ld = 7168
+    g0 = np.random.default_rng(328)
+    y = g0.normal(0, 4, (C, ld)).astype(np.float32)          # a q|k|v output row per position
+    k, v = y[:, 5120:5120 + Hkv * D], y[:, 5120 + Hkv * D:5120 + 2 * Hkv * D]
+    yd = to_dev(y)
+    q = synth.queries(C, Hq, D, seed=329)
+    out = torch.empty((C, Hq, D), dtype=torch.float32, device=DEV)
+    ws = torch.zeros(svd.svd_kv_attention_workspace_bytes(Hq, Hkv, C), dtype=torch.uint8, device=DEV)
+    base = yd.data_ptr()
+    svd.svd_kv_attention_append(to_dev(q), base + 4 * 5120, base + 4 * (5120 + Hkv * D), ld, cache,
+                                L, Hq, Hkv, n_past, C, 1.0 / np.sqrt(D), out, ws)
+    torch.cuda.synchronize()
+    o = out.cpu().numpy().astype(np.float64)
+    qk, qks, qv, qvs = oracle.kv_quantize(np.ascontiguousarray(k).reshape(C * Hkv, D),
+                                          np.ascontiguousarray(v).reshape(C * Hkv, D))
+    for c in range(C):
+        for h in range(Hkv):
+            i = c * Hkv + h
+            kc[h, n_past + c], ks[h, n_past + c] = qk[i], qks[i]
+            vc[h, n_past + c], vs[h, n_past + c] = qv[i], qvs[i]
+    G = Hq // Hkv
+    for g in (0, 7):
+        sl = slice(g, g + 1)
+        o_ref, a_ref = oracle.kv_attention(q[:, g * G:(g + 1) * G], kc[sl], ks[sl], vc[sl], vs[sl],
+                                           n_past)
+        _check(o[:, g * G:(g + 1) * G], o_ref, a_ref)
