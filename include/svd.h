@@ -48,7 +48,8 @@ enum {
     SVD_ERR_INVALID_ARG = -1, /* null pointer, bad size, misaligned pointer          */
     SVD_ERR_UNSUPPORTED = -2, /* a valid request this build does not implement       */
     SVD_ERR_CUDA = -3,        /* a CUDA call failed (see svd_last_cuda_error)        */
-    SVD_ERR_WORKSPACE = -4    /* workspace null or smaller than the query said       */
+    SVD_ERR_WORKSPACE = -4,   /* workspace null or smaller than the query said       */
+    SVD_ERR_TIMEOUT = -5      /* a bounded wait of a kernel gave up (svd_verify_status) */
 };
 
 /* Per-window status bits written by svd_accept (0 = clean). */
@@ -132,10 +133,12 @@ int svd_unpack_weights(const svd_qweight *src_native, void *dst_codes, void *dst
  *   NATIVE weights run the tensor-core stream-K kernel (bf16 MMA, fp32 accumulate, one fresh
  *   accumulator per 32-input block, scaled in fp32).  It needs a workspace of
  *   svd_verify_linear_workspace_bytes() bytes that is ZERO-FILLED before its first use (it
- *   holds barrier counters, which every call returns to zero, a launch counter, and partial
- *   sums of row blocks split between CTAs, tagged with the launch that wrote them), so one
- *   zeroed workspace serves any number of calls issued in stream order, for any matrix shape
- *   and C; calls that may run concurrently need separate workspaces.
+ *   holds barrier counters, which every call returns to zero, a launch epoch, a status word,
+ *   and partial sums of row blocks split between CTAs, tagged with the launch that wrote
+ *   them), so one zeroed workspace serves any number of calls issued in stream order, for any
+ *   matrix shape and C; calls that may run concurrently need separate workspaces.  Every wait
+ *   inside the kernel is bounded: one that gives up leaves Y undefined and records itself in
+ *   the workspace (svd_verify_status).
  *   CANONICAL weights run the CUDA-core warp-shuffle kernel (no workspace; needs
  *   C * in * 4 <= 196608 bytes, else SVD_ERR_UNSUPPORTED).
  *   The result is deterministic: the same inputs give the same bits on every call. */
@@ -163,6 +166,26 @@ size_t svd_verify_chain_workspace_bytes(const svd_linear_op *ops, int n_ops, int
 int svd_verify_chain(const svd_linear_op *ops, int n_ops, int C, void *workspace,
                      size_t workspace_bytes, int flags, svd_stream_t stream);
 
+/* Failure detection of svd_verify_linear / svd_verify_chain / svd_lm_head_softmax.  Each wait
+ * of their kernel (a bulk copy landing, a partial sum from another CTA, the grid barrier
+ * between the ops of a chain) is bounded; a wait that runs out sets a bit in the workspace's
+ * status word, every later wait of the CTA returns at once, the kernel runs to its end, lets
+ * its own copies in flight land and returns, and its outputs are undefined.
+ * svd_verify_status waits for `stream`, reads the status word of `workspace` (a workspace of
+ * at least svd_verify_linear_workspace_bytes() bytes; for svd_lm_head_softmax, the start of
+ * its workspace), clears it, stores the bits in *bits (when bits != NULL; 1 = a copy, 2 = a
+ * partial sum, 4 = the grid barrier) and returns SVD_OK when no wait gave up,
+ * SVD_ERR_TIMEOUT when one did.  It synchronises the stream.
+ * svd_verify_inject_stall (a test hook; no counterpart on the source pages) enqueues on `stream`
+ * a write into the workspace that makes the kernels launched with it afterwards issue no
+ * weight copy, as if the copy engine had stopped, and give up a wait after `polls` polls
+ * (checked every 256 polls), so that a wait really runs out; SVD_POLL_DEFAULT turns it off. */
+#define SVD_POLL_DEFAULT 0xFFFFFFFFu
+int svd_verify_status(const void *workspace, size_t workspace_bytes, uint32_t *bits,
+                      svd_stream_t stream);
+int svd_verify_inject_stall(void *workspace, size_t workspace_bytes, uint32_t polls,
+                            svd_stream_t stream);
+
 /* ---- verify linear without caller scratch -------------------------------------------- */
 /* (This entry point has no counterpart on the source pages; it is a deployment convenience.)
  * Some callers cannot allocate device memory at the point where they run the verify pass:
@@ -177,7 +200,10 @@ int svd_verify_chain(const svd_linear_op *ops, int n_ops, int C, void *workspace
  *   - out_features <= SVD_NOALLOC_MAX_OUT_FEATURES and at most 160 SMs, else
  *     SVD_ERR_UNSUPPORTED (other limits as for svd_verify_linear).
  *   - The first call on each device looks up the array's device address (with that device
- *     current); make that first call before any stream capture.
+ *     current); make that first call before any stream capture (a first call inside a capture
+ *     returns SVD_ERR_UNSUPPORTED).  Every later call outside a capture looks it up again, so a
+ *     new context on the device (after cudaDeviceReset) is handled; captured calls use the
+ *     address of the last call outside capture.
  *   - Every call clears the barrier counters with a memset on `stream` and then launches the
  *     kernel.
  *     All calls share the one array, so calls that may overlap on the GPU (different streams
@@ -286,7 +312,9 @@ int svd_device_sm_count(void);
  *   rounded outside.  Positions of the cache beyond n_past + C are never read into the result,
  *   whatever their bytes.  The workspace (svd_kv_attention_workspace_bytes, 16-byte aligned)
  *   holds per-split partials; its first 32-bit word gets bit 0 set if a bounded wait of the
- *   kernel gave up (zero it once to watch it).  Two kernels are enqueued (the split pass and its
+ *   kernel gave up (zero it once to watch it); its second word, when non-zero, is one more than
+ *   the number of polls after which such a wait gives up (a test hook: 1 makes every wait give
+ *   up at once; 0, the zero-filled value, keeps the default of about a second).  Two kernels are enqueued (the split pass and its
  *   merge, the latter a programmatic dependent launch).  Errors: SVD_ERR_INVALID_ARG for null or
  *   misaligned pointers, Hq % Hkv != 0, C < 1, n_past < 0, n_past + C > capacity or a scale that
  *   is not positive and finite; SVD_ERR_WORKSPACE for a short workspace.

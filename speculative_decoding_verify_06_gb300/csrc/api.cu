@@ -17,6 +17,8 @@ int verify_linear_noalloc(const svd_qweight *W, const void *X, int C, float *Y, 
 size_t chain_workspace_bytes(const svd_linear_op *ops, int n_ops, int C);
 int verify_chain(const svd_linear_op *ops, int n_ops, int C, void *ws, size_t ws_bytes, int flags,
                  cudaStream_t stream);
+int verify_status(const void *ws, size_t ws_bytes, uint32_t *bits, cudaStream_t stream);
+int verify_inject_stall(void *ws, size_t ws_bytes, uint32_t polls, cudaStream_t stream);
 size_t sampler_ws_bytes(int rows, int64_t V);
 int sampler_probs(const float *logits, int rows, int64_t V, const svd_sampler *s, float *probs,
                   int32_t *argmax, void *ws, size_t ws_bytes, cudaStream_t stream);
@@ -57,6 +59,7 @@ const char *svd_error_string(int code) {
         case SVD_ERR_UNSUPPORTED: return "SVD_ERR_UNSUPPORTED: request not implemented by this build";
         case SVD_ERR_CUDA: return "SVD_ERR_CUDA: a CUDA call failed (see svd_last_cuda_error)";
         case SVD_ERR_WORKSPACE: return "SVD_ERR_WORKSPACE: workspace missing or too small";
+        case SVD_ERR_TIMEOUT: return "SVD_ERR_TIMEOUT: a bounded wait of a kernel gave up";
         default: return "unknown svd error code";
     }
 }
@@ -100,6 +103,14 @@ size_t svd_verify_chain_workspace_bytes(const svd_linear_op *ops, int n_ops, int
 int svd_verify_chain(const svd_linear_op *ops, int n_ops, int C, void *ws, size_t ws_bytes,
                      int flags, svd_stream_t stream) {
     return svd::verify_chain(ops, n_ops, C, ws, ws_bytes, flags, (cudaStream_t)stream);
+}
+
+int svd_verify_status(const void *ws, size_t ws_bytes, uint32_t *bits, svd_stream_t stream) {
+    return svd::verify_status(ws, ws_bytes, bits, (cudaStream_t)stream);
+}
+
+int svd_verify_inject_stall(void *ws, size_t ws_bytes, uint32_t polls, svd_stream_t stream) {
+    return svd::verify_inject_stall(ws, ws_bytes, polls, (cudaStream_t)stream);
 }
 
 size_t svd_sampler_workspace_bytes(int rows, int64_t V) {

@@ -287,6 +287,10 @@ __global__ void __launch_bounds__(kThreads, 1) kv_attention_kernel(const KvaPara
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     griddep_wait();  // queries and cache written by the kernels before this one
+    // polls after which a ring wait gives up: word 1 of the workspace minus one when it is set
+    // (a test hook; 1 makes every ring wait give up at once)
+    const unsigned poll_set = *(reinterpret_cast<volatile const unsigned *>(P.flags) + 1);
+    const uint32_t poll_limit = poll_set ? poll_set - 1u : kDefaultPolls;
     // The window's positions inside this CTA's units (append mode) are quantised into the cache
     // by this CTA (no other CTA reads them) and made visible to the bulk copies that read them
     // back.  When no warp's first kRing units hold one, the prologue copies go first and the
@@ -398,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) kv_attention_kernel(const KvaPara
 
     for (int u = wb, it = 0; u < we; ++u, ++it) {
         const int slot = it % kRing;
-        const bool ok = mbar_wait_ok(mb0 + 8 * slot, (uint32_t)(it / kRing) & 1u);
+        const bool ok = mbar_wait_ok(mb0 + 8 * slot, (uint32_t)(it / kRing) & 1u, poll_limit);
         if (!__all_sync(0xFFFFFFFFu, ok)) {
             failed = true;
             it_f = it;

@@ -84,32 +84,34 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         "l"(src), "r"(bytes), "r"(mbar)
         : "memory");
 }
-// Waits for phase `parity` of an mbarrier; gives up after a bounded number of polls (each poll
-// may suspend the thread briefly), so a broken pipeline cannot hang the GPU.
-__device__ __forceinline__ void mbar_wait(uint32_t mbar, uint32_t parity) {
-    for (int it = 0; it < (1 << 22); ++it) {
-        uint32_t ok;
+// Waits for phase `parity` of an mbarrier and returns whether it completed within `limit`
+// polls, so a broken pipeline cannot hang the GPU.  With the default limit a poll is a try_wait
+// (which may suspend the thread briefly until the phase completes); a smaller limit (a test
+// hook) polls with the non-blocking test_wait, so that the wait really runs out.
+constexpr uint32_t kDefaultPolls = 1u << 22;
+__device__ __forceinline__ bool mbar_poll(uint32_t mbar, uint32_t parity, bool blocking) {
+    uint32_t ok;
+    if (blocking) {
         asm volatile(
             "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; "
             "selp.u32 %0, 1, 0, p; }"
             : "=r"(ok)
             : "r"(mbar), "r"(parity)
             : "memory");
-        if (ok) return;
+    } else {
+        asm volatile(
+            "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; "
+            "selp.u32 %0, 1, 0, p; }"
+            : "=r"(ok)
+            : "r"(mbar), "r"(parity)
+            : "memory");
     }
+    return ok != 0;
 }
-// The same wait returning whether the phase completed within the bound.
-__device__ __forceinline__ bool mbar_wait_ok(uint32_t mbar, uint32_t parity) {
-    for (int it = 0; it < (1 << 22); ++it) {
-        uint32_t ok;
-        asm volatile(
-            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; "
-            "selp.u32 %0, 1, 0, p; }"
-            : "=r"(ok)
-            : "r"(mbar), "r"(parity)
-            : "memory");
-        if (ok) return true;
-    }
+__device__ __forceinline__ bool mbar_wait_ok(uint32_t mbar, uint32_t parity, uint32_t limit = kDefaultPolls) {
+    const bool blocking = limit >= kDefaultPolls;
+    for (uint32_t it = 0; it < limit; ++it)
+        if (mbar_poll(mbar, parity, blocking)) return true;
     return false;
 }
 

@@ -248,10 +248,47 @@ __device__ __forceinline__ unsigned long long ld_tagged(const unsigned long long
     asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
     return w;
 }
-// Waits (bounded) for an entry carrying `tag` and returns its value.
-__device__ __forceinline__ float wait_tagged(const unsigned long long *p, uint32_t tag) {
+// Failure detection.  Every spin-wait of the kernel is bounded: kPollLimit polls, or fewer when
+// the workspace asks for a stall injection (a test hook, below).  A wait that runs out sets a
+// bit of the workspace's status word (read by svd_verify_status) and the CTA's stop flag; from
+// then on every wait of the CTA returns at once, a ring slot is refilled only if the wait for
+// its previous copy succeeded, the kernel runs to its end without waiting (its output is
+// undefined) and, before exiting, waits a bounded time for the copies it may have in flight.
+// The stall injection makes the kernel issue no weight copy at all, as if the copy engine had
+// stopped, so that a ring wait really runs out.
+constexpr uint32_t kPollLimit = kDefaultPolls;
+constexpr uint32_t kDrainLimit = 1u << 16;  // non-blocking polls: a few milliseconds at most
+// Workspace words after the partial slots: [0] grid-barrier counter, [1] exit counter, both
+// returned to zero by the last CTA out; [2] status bits; [3] stall injection (0 = none, else
+// one more than the number of polls after which a wait gives up); [63] launch epoch, advanced
+// by the last CTA out.
+constexpr int kBarCount = 0, kBarExit = 1, kBarStatus = 2, kBarPoll = 3, kBarEpoch = 63;
+constexpr unsigned kStCopy = 1u, kStPartial = 2u, kStOrder = 4u;  // status bits
+
+// The CTA's wait state in shared memory: the poll limit, the stop flag, the status word.
+struct WaitCtl {
+    uint32_t limit;
+    uint32_t stop;
+    unsigned *status;
+};
+__device__ __forceinline__ bool wait_stopped(const WaitCtl *wc) {
+    return *reinterpret_cast<const volatile uint32_t *>(&wc->stop) != 0u;
+}
+__device__ __forceinline__ void wait_fail(WaitCtl *wc, unsigned bit) {
+    if (!wait_stopped(wc)) {
+        *reinterpret_cast<volatile uint32_t *>(&wc->stop) = 1u;
+        atomicOr(wc->status, bit);
+    }
+}
+
+// Waits for an entry carrying `tag` and returns its value.
+__device__ __forceinline__ float wait_tagged(const unsigned long long *p, uint32_t tag, WaitCtl *wc) {
     unsigned long long w = ld_tagged(p);
-    for (int it = 0; (uint32_t)(w >> 32) != tag && it < (1 << 22); ++it) {
+    for (uint32_t it = 0; (uint32_t)(w >> 32) != tag; ++it) {
+        if (it >= wc->limit || wait_stopped(wc)) {
+            wait_fail(wc, kStPartial);
+            break;
+        }
         if (it > 64) __nanosleep(64);
         w = ld_tagged(p);
     }
@@ -260,24 +297,43 @@ __device__ __forceinline__ float wait_tagged(const unsigned long long *p, uint32
 
 // The gi-th barrier of a launch among all G CTAs: one release-add per CTA (after a CTA
 // barrier, so that it carries every warp's writes) on a counter in the workspace, then
-// acquire polling until the counter reaches gi * G.  Polling is bounded.
-__device__ __forceinline__ void grid_barrier(unsigned *count, unsigned target) {
+// acquire polling until the counter reaches gi * G.
+__device__ __forceinline__ void grid_barrier(unsigned *count, unsigned target, WaitCtl *wc) {
     asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(count) : "memory");
-    for (int it = 0; it < (1 << 26); ++it) {
+    for (uint32_t it = 0;; ++it) {
         unsigned v;
         asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(count) : "memory");
         if (v >= target) return;
+        if (it >= wc->limit || wait_stopped(wc)) {
+            wait_fail(wc, kStOrder);
+            return;
+        }
         if (it > 512) __nanosleep(32);
     }
+}
+// Waits for phase `parity` of a ring slot's barrier with try_wait (which may suspend the thread
+// until the phase completes); every 256 polls it checks the stop flag and the limit.  Returns
+// whether the phase completed.
+__device__ __forceinline__ bool slot_wait(uint32_t mbar, uint32_t parity, WaitCtl *wc) {
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_poll(mbar, parity, true)) return true;
+        if ((it & 255u) == 255u) {
+            if (wait_stopped(wc)) return false;
+            if (it >= wc->limit) break;
+        }
+    }
+    wait_fail(wc, kStCopy);
+    return false;
 }
 __device__ __forceinline__ unsigned atom_add_acqrel_gpu(unsigned *p, unsigned v) {
     unsigned old;
     asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
     return old;
 }
-// Workspace words after the partial slots: [0] grid-barrier counter, [1] exit counter, both
-// returned to zero by the last CTA out; [63] launch epoch, advanced by the last CTA out.
-constexpr int kBarCount = 0, kBarExit = 1, kBarEpoch = 63;
+// Partial tags: (e24 << 8) | op, where e24 = 1 + launch epoch mod (2^24 - 1) is never 0, so a
+// zero-filled slot never matches; when e24 comes back to 1 the last CTA out of the launch
+// before clears every partial slot, so a tag left from an earlier cycle never matches either.
+__host__ __device__ inline uint32_t partial_epoch24(uint32_t epoch) { return epoch % 0xFFFFFFu + 1u; }
 
 #ifndef SVD_PROBE
 #define SVD_PROBE(gi, what)  // timing hook for instrumented builds; nothing by default
@@ -286,7 +342,7 @@ constexpr int kBarCount = 0, kBarExit = 1, kBarEpoch = 63;
 template <int NT, int NW, int TW, int R, int U, int MAXOPS>
 __global__ void __launch_bounds__(NW * 32, 1)
 vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__restrict__ part,
-                 unsigned *__restrict__ gbar) {
+                 uint32_t part_entries, unsigned *__restrict__ gbar) {
     using Cfg = VlCfg<NT, NW, TW, R, U, MAXOPS>;
     constexpr int kSlotBytes = Cfg::kSlotBytes, kWG = Cfg::kWG, kNG = Cfg::kNG;
     constexpr int kAcc = Cfg::kAcc, kAccW = Cfg::kAccW, kPartial = Cfg::kPartial, kPer = Cfg::kPer;
@@ -300,7 +356,8 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
     __shared__ __align__(8) uint64_t s_full[kNG * R];
     __shared__ uint32_t s_park_rb[NW * 2];    // row block of a parked partial, kNone if none
     __shared__ uint32_t s_park_head[NW * 2];  // 1 if that partial starts at its block's start
-    __shared__ uint32_t s_epoch;
+    __shared__ uint32_t s_epoch, s_last;
+    __shared__ WaitCtl s_wc;
     float *park = reinterpret_cast<float *>(smem + Cfg::kRing);
     // The op descriptors live in shared memory: read from the parameter space with a
     // run-time index they would go through the small constant cache on every access.
@@ -350,6 +407,7 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
         for (int i = 0; i < R; ++i) mbar_init(full0 + 8 * i, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if (threadIdx.x == 0) s_wc.stop = 0u;
     __syncthreads();
 
     // Issue cursor of this group (uniform across its warps; the first warp's lane 0 issues):
@@ -358,6 +416,7 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
     // next U units of the range (fewer at its end; never units of two ops).
     int c_op = -1;
     uint32_t c_u = 0, c_hi = 0, c_issued = 0;
+
     const uint8_t *c_codes = nullptr, *c_scales = nullptr;
     auto issue = [&]() {
         while (c_u >= c_hi) {
@@ -378,12 +437,20 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
         c_codes += n * kUnitCodeBytes;
         c_scales += n * kUnitScaleBytes;
     };
+    // The stall injection (workspace word kBarPoll, written only by the test hook, never by an
+    // earlier kernel of the stream, so it may be read before the dependency wait): no copy.
+    if (*reinterpret_cast<volatile unsigned *>(gbar + kBarPoll) != 0u) c_op = n_ops;
     // weights never depend on earlier kernels: start streaming before waiting for them
     for (int i = 0; i < R; ++i) issue();
 
     griddep_wait();
     griddep_launch_dependents();
-    if (threadIdx.x == 0) s_epoch = *reinterpret_cast<volatile unsigned *>(gbar + kBarEpoch);
+    if (threadIdx.x == 0) {
+        s_epoch = *reinterpret_cast<volatile unsigned *>(gbar + kBarEpoch);
+        const unsigned lim = *reinterpret_cast<volatile unsigned *>(gbar + kBarPoll);
+        s_wc.limit = lim ? lim - 1u : kPollLimit;
+        s_wc.status = gbar + kBarStatus;
+    }
     __syncthreads();
     const uint32_t epoch = s_epoch;
 
@@ -402,13 +469,13 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
         const VlOp &o = ops[gi];
         if (gi > 0) {
             __syncthreads();
-            if (threadIdx.x == 0) grid_barrier(gbar + kBarCount, (unsigned)gi * G);
+            if (threadIdx.x == 0) grid_barrier(gbar + kBarCount, (unsigned)gi * G, &s_wc);
             __syncthreads();
         }
         SVD_PROBE(gi, 0);
         const uint32_t n_kc = o.n_kc;
         const int64_t in_f = o.in_f, out_f = o.out_f;
-        const uint32_t tag = ~((epoch << 8) | (uint32_t)(gi & 255));
+        const uint32_t tag = (partial_epoch24(epoch) << 8) | (uint32_t)(gi & 255);
         // (row, column) of accumulator q of n-tile nt of tile rt (0..kTiles-1) of lane lsrc
         auto coords = [&](int lsrc, int rt, int nt, int q, uint32_t rb, int64_t *row, int *col) {
             *row = (int64_t)rb * kRowsPerBlock + 16 * rt + (lsrc >> 2) + ((q >> 1) ? 8 : 0);
@@ -467,7 +534,9 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
                 } else {
                     load_x(kc, xc);
                 }
-                if (in_slot == 0u) mbar_wait(full0 + 8 * slot, (c_used / R) & 1u);
+                // a wait that gave up ends this warp's copies: its slot may still be filling, so it
+                // is never refilled (the issue cursor is exhausted)
+                if (in_slot == 0u && !slot_wait(full0 + 8 * slot, (c_used / R) & 1u, &s_wc)) c_op = n_ops;
                 const uint8_t *cbase = ring + slot * kSlotBytes + in_slot * kUnitCodeBytes;
                 const uint8_t *sbase = ring + slot * kSlotBytes + U * kUnitCodeBytes + in_slot * kUnitScaleBytes;
 #pragma unroll
@@ -610,7 +679,7 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
                                 if (bb + i > b_last) break;
                                 const float x = (uint32_t)(w4[i] >> 32) == tag
                                                     ? __uint_as_float((uint32_t)w4[i])
-                                                    : wait_tagged(part + (size_t)(bb + i) * kPartialMax + e, tag);
+                                                    : wait_tagged(part + (size_t)(bb + i) * kPartialMax + e, tag, &s_wc);
                                 v += x;
                             }
                         }
@@ -623,15 +692,27 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
         }
         SVD_PROBE(gi, 2);
     }
-    // the last CTA out returns the barrier counters to zero and advances the epoch
+    // after a give-up: wait (bounded) for the group's copies that may still be in flight -- the
+    // last copy issued into each slot -- so that none lands in shared memory after the CTA exits
+    if (sub == 0 && lane == 0 && wait_stopped(&s_wc)) {
+        for (uint32_t k = c_issued > (uint32_t)R ? c_issued - R : 0u; k < c_issued; ++k)
+            mbar_wait_ok(full0 + 8 * (k % R), (k / R) & 1u, kDrainLimit);
+    }
+    // the last CTA out returns the barrier counters to zero and advances the epoch; when the
+    // partial tags are about to repeat it also clears every partial slot
     __syncthreads();
     if (threadIdx.x == 0) {
+        s_last = 0u;
         if (atom_add_acqrel_gpu(gbar + kBarExit, 1u) == G - 1u) {
             gbar[kBarCount] = 0u;
             gbar[kBarExit] = 0u;
             gbar[kBarEpoch] = epoch + 1u;
+            s_last = partial_epoch24(epoch + 1u) == 1u ? 1u : 0u;
         }
     }
+    __syncthreads();
+    if (s_last)
+        for (uint32_t i = threadIdx.x; i < part_entries; i += kThreads) part[i] = 0ull;
 }
 
 // ---- the CUDA-core kernel (canonical layout) -------------------------------------------
@@ -721,6 +802,7 @@ static int ntiles_for(int C) { return C <= 8 ? 1 : (C <= 16 ? 2 : 4); }
 // It has the same size and layout for every matrix and C, so calls of any shape can share
 // one zero-filled workspace; every launch returns the counters to zero and advances the
 // epoch that tags its partials.
+static size_t partial_entries() { return (size_t)sm_count() * kMaxCtasPerSm * kPartialMax; }
 static size_t partial_region_bytes() {
     return align_up((size_t)sm_count() * kMaxCtasPerSm * kPartialMax * sizeof(unsigned long long),
                     256);
@@ -776,7 +858,7 @@ static cudaError_t launch_stream(const VlOps<MAXOPS> &P, void *ws, bool pdl, boo
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, kern, P, part, gbar);
+    return cudaLaunchKernelEx(&cfg, kern, P, part, (uint32_t)partial_entries(), gbar);
 }
 
 static VlOp make_op(const svd_qweight *W, const void *X, float *Y) {
@@ -971,6 +1053,38 @@ int unpack(const svd_qweight *src, void *dc, void *ds, cudaStream_t stream) {
     return SVD_OK;
 }
 
+// ---- failure detection: the workspace's status word and the stall injection -------------
+__global__ void set_word_kernel(unsigned *p, unsigned v) { *p = v; }
+
+static unsigned *workspace_counters(const void *ws) {
+    return reinterpret_cast<unsigned *>(reinterpret_cast<uint8_t *>(const_cast<void *>(ws)) +
+                                        partial_region_bytes());
+}
+
+int verify_status(const void *ws, size_t ws_bytes, uint32_t *bits, cudaStream_t stream) {
+    if (sm_count() < 1) return SVD_ERR_CUDA;
+    if (!ws || ws_bytes < partial_region_bytes() + kBarrierBytes) return SVD_ERR_WORKSPACE;
+    unsigned *st = workspace_counters(ws) + kBarStatus;
+    unsigned v = 0;
+    SVD_CUDA_TRY(cudaMemcpyAsync(&v, st, sizeof(v), cudaMemcpyDeviceToHost, stream));
+    SVD_CUDA_TRY(cudaStreamSynchronize(stream));
+    if (bits) *bits = v;
+    if (v == 0u) return SVD_OK;
+    set_word_kernel<<<1, 1, 0, stream>>>(st, 0u);
+    SVD_CUDA_TRY(cudaGetLastError());
+    SVD_CUDA_TRY(cudaStreamSynchronize(stream));
+    return SVD_ERR_TIMEOUT;
+}
+
+int verify_inject_stall(void *ws, size_t ws_bytes, uint32_t polls, cudaStream_t stream) {
+    if (sm_count() < 1) return SVD_ERR_CUDA;
+    if (!ws || ws_bytes < partial_region_bytes() + kBarrierBytes) return SVD_ERR_WORKSPACE;
+    const unsigned word = polls == SVD_POLL_DEFAULT ? 0u : polls + 1u;  // 0 keeps the default
+    set_word_kernel<<<1, 1, 0, stream>>>(workspace_counters(ws) + kBarPoll, word);
+    SVD_CUDA_TRY(cudaGetLastError());
+    return SVD_OK;
+}
+
 // ---- verify linear without caller scratch ----------------------------------------------
 // The stream-K kernel needs a small scratch area (tagged partial sums of row blocks split
 // between CTAs, and the barrier words).  svd_verify_linear takes it from the caller;
@@ -985,8 +1099,10 @@ static_assert(kNoAllocBytes <= SVD_NOALLOC_SCRATCH_BYTES, "scratch bound in svd.
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
-// Device address of g_noalloc_scratch, looked up once per device with that device current
-// (in host code the symbol is only a host-side handle and must never reach a kernel).
+// Device address of g_noalloc_scratch, looked up with the device current (in host code the
+// symbol is only a host-side handle and must never reach a kernel).  It is looked up again on
+// every call made outside stream capture, so a new context on the device (after
+// cudaDeviceReset) never sees a stale address; during capture the last address is used.
 static std::mutex g_noalloc_mu;
 static void *g_noalloc_ptr[64] = {nullptr};
 
@@ -1005,10 +1121,13 @@ int verify_linear_noalloc(const svd_qweight *W, const void *X, int C, float *Y, 
     int dev = 0;
     SVD_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= 64) return SVD_ERR_UNSUPPORTED;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    SVD_CUDA_TRY(cudaStreamIsCapturing(stream, &cap));
     void *base = nullptr;
     {
         std::lock_guard<std::mutex> lock(g_noalloc_mu);
-        if (!g_noalloc_ptr[dev]) {
+        if (!g_noalloc_ptr[dev] || cap == cudaStreamCaptureStatusNone) {
+            if (cap != cudaStreamCaptureStatusNone) return SVD_ERR_UNSUPPORTED;  // first call captured
             void *p = nullptr;
             SVD_CUDA_TRY(cudaGetSymbolAddress(&p, g_noalloc_scratch));
             g_noalloc_ptr[dev] = p;
@@ -1016,9 +1135,10 @@ int verify_linear_noalloc(const svd_qweight *W, const void *X, int C, float *Y, 
         base = g_noalloc_ptr[dev];
     }
     // Same layout as a caller workspace: partial slots, then the barrier words.  Every call
-    // clears the barrier counters on the stream before its kernel, so a call never
-    // depends on what an earlier call left behind; the epoch word (the last one) is kept, so
-    // partials written by earlier calls never carry the tag of a later one.
+    // clears the counters (and the status word and poll limit) on the stream before its
+    // kernel, so a call never depends on what an earlier call left behind; the epoch word (the
+    // last one) is kept, so partials written by earlier calls never carry the tag of a later
+    // one.
     unsigned char *counters = reinterpret_cast<unsigned char *>(base) + partial_region_bytes();
     SVD_CUDA_TRY(cudaMemsetAsync(counters, 0, kBarEpoch * sizeof(unsigned), stream));
     VlOps<1> P;

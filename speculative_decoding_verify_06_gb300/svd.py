@@ -19,6 +19,7 @@ SVD_ERR_INVALID_ARG = -1
 SVD_ERR_UNSUPPORTED = -2
 SVD_ERR_CUDA = -3
 SVD_ERR_WORKSPACE = -4
+SVD_ERR_TIMEOUT = -5
 
 SVD_ST_BAD_TOKEN = 1
 SVD_ST_Q_ZERO = 2
@@ -29,6 +30,7 @@ SVD_ST_EMPTY = 16
 SVD_LAYOUT_CANONICAL = 0
 SVD_LAYOUT_NATIVE = 1
 SVD_F_PDL = 1
+SVD_POLL_DEFAULT = 0xFFFFFFFF
 SVD_C_MAX = 32
 SVD_K_MAX = 32
 SVD_KV_HEAD_DIM = 128
@@ -40,6 +42,7 @@ EXPORTS = (
     "svd_error_string", "svd_last_cuda_error", "svd_native_sizes", "svd_repack_weights",
     "svd_unpack_weights", "svd_verify_linear_workspace_bytes", "svd_verify_linear",
     "svd_verify_linear_noalloc", "svd_verify_chain_workspace_bytes", "svd_verify_chain",
+    "svd_verify_status", "svd_verify_inject_stall",
     "svd_sampler_workspace_bytes", "svd_sampler_probs", "svd_lm_head_workspace_bytes",
     "svd_lm_head_softmax", "svd_accept", "svd_graph_begin", "svd_graph_end", "svd_graph_launch",
     "svd_graph_destroy", "svd_device_sm_count",
@@ -124,6 +127,8 @@ def load(path: str = LIB_PATH):
             "svd_verify_linear_noalloc": (i32, [P, P, i32, P, i32, P]),
             "svd_verify_chain_workspace_bytes": (sz, [P, i32, i32]),
             "svd_verify_chain": (i32, [P, i32, i32, P, sz, i32, P]),
+            "svd_verify_status": (i32, [P, sz, P, P]),
+            "svd_verify_inject_stall": (i32, [P, sz, ctypes.c_uint32, P]),
             "svd_sampler_workspace_bytes": (sz, [i32, i64]),
             "svd_sampler_probs": (i32, [P, i32, i64, P, P, P, P, sz, P]),
             "svd_lm_head_workspace_bytes": (sz, [i64, i64, i32]),
@@ -261,6 +266,30 @@ def svd_verify_chain(ops, C: int, workspace, workspace_bytes: int = 0, flags: in
         workspace_bytes = workspace.numel() * workspace.element_size()
     _check("svd_verify_chain", load().svd_verify_chain(
         arr, len(ops), int(C), _ptr(workspace), int(workspace_bytes), int(flags), _stream(stream)))
+
+
+def svd_verify_status(workspace, workspace_bytes: int = 0, stream=None):
+    """Returns (rc, bits): rc is SVD_OK or SVD_ERR_TIMEOUT (a bounded wait gave up); the status
+    word is cleared.  Other codes raise."""
+    if not workspace_bytes:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    bits = ctypes.c_uint32(0)
+    rc = int(load().svd_verify_status(_ptr(workspace), int(workspace_bytes), ctypes.byref(bits),
+                                      _stream(stream)))
+    if rc not in (SVD_OK, SVD_ERR_TIMEOUT):
+        raise SvdError("svd_verify_status", rc)
+    return rc, int(bits.value)
+
+
+def svd_verify_inject_stall(workspace, polls, workspace_bytes: int = 0, stream=None):
+    """Test hook: later kernels on this workspace issue no weight copy and give up a wait after
+    `polls` polls; polls=None turns it off."""
+    if polls is None:
+        polls = SVD_POLL_DEFAULT
+    if not workspace_bytes:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check("svd_verify_inject_stall", load().svd_verify_inject_stall(
+        _ptr(workspace), int(workspace_bytes), int(polls), _stream(stream)))
 
 
 def svd_sampler_workspace_bytes(rows: int, V: int) -> int:
