@@ -1,7 +1,9 @@
 """GPU parity of the acceptance kernel (svd_accept) against the oracle on identical p, q, drafts
-and Philox uniforms: emitted tokens, counts and status bit-exact, except windows whose
-resampling uniform lies within 1e-6 of a token boundary (flagged by the oracle), which must be
-rare."""
+and Philox uniforms: emitted tokens, counts and status bit-exact, except windows whose resampling
+uniform lies within 1e-9 of a token boundary, where the two summation orders may pick a
+neighbour; those windows must be under 1e-5 of the decisions (accept tests and draws).  The
+oracle also flags draws within 1e-6 of a boundary (the near-threshold flag), reported per window
+and per decision."""
 import numpy as np
 import pytest
 
@@ -41,14 +43,34 @@ def compare(p, draft, q=None, **kw):
     for w in np.nonzero(~exact)[0]:
         j = ne_r[w] - 1
         assert ne[w] == ne_r[w] and np.array_equal(tok[w, :j], tok_r[w, :j])
-    # the near-threshold flag (u' within 1e-6 of a threshold), counted per comparison: a draw over
-    # V tokens is V threshold decisions, an accept test one
-    draws = int(np.isfinite(margin).sum())
-    decisions = draws * V + n * k
-    assert near.sum() <= 1e-5 * decisions + 1, (near.sum(), decisions)
+    rates = excuse_rates(ne_r, margin, near, k, sampled=q is not None)
+    # windows excused from bit-exactness: under 1e-5 of the decisions (one per accept test, one
+    # per draw)
+    assert (~exact).sum() <= 1e-5 * rates["decisions"], rates
+    # the near-threshold flag (u' within 1e-6 of a threshold), counted per threshold comparison
+    # (a draw over V tokens compares u' R with V running sums, an accept test is one comparison):
+    # under 1e-5 of them
+    assert near.sum() <= 1e-5 * (rates["draws"] * V + rates["tests"]) + 1, rates
     ok = st == 0
     assert np.all((ne[ok] >= 1) & (ne[ok] <= k + 1))
     return tok, ne, st, near
+
+
+def excuse_rates(ne_r, margin, near, k, sampled=True):
+    """Counts behind the parity claim: accept tests (a window that emitted n tokens made
+    min(n, k) of them in sampled mode), draws, the windows excused from bit-exactness (margin
+    below EXACT_MARGIN) and the near-threshold flags (margin below 1e-6), per window and per
+    decision."""
+    tests = int(np.minimum(ne_r, k).sum()) if sampled else 0
+    draws = int(np.isfinite(margin).sum())
+    decisions = tests + draws
+    excused = int((margin < EXACT_MARGIN).sum())
+    n = len(ne_r)
+    return {"windows": n, "tests": tests, "draws": draws, "decisions": decisions,
+            "excused": excused, "near": int(near.sum()),
+            "near_per_window": float(near.sum()) / max(n, 1),
+            "near_per_decision": float(near.sum()) / max(decisions, 1),
+            "excused_per_decision": excused / max(decisions, 1)}
 
 
 def window_pq(n, k, V, seed, share=0.7, std=2.0):
@@ -203,3 +225,29 @@ def test_cluster_and_per_window_kernels_agree():
     # window w of the large call has index w: compare the first n with the small call
     assert np.array_equal(tok[:n], small[0]) and np.array_equal(ne[:n], small[1])
     assert np.array_equal(st[:n], small[2])
+
+
+def test_hundred_thousand_windows_bound_the_excused_decisions():
+    """A pool of 256 (p, q) row pairs at V = 4096 (config 1's logits) and 100k windows drawing
+    rows from it: enough decisions (~2e5) that "under 1e-5 of the decisions" allows a couple of
+    excused windows, so the bound means something.  The rates are printed."""
+    V, k, pool, n = 4096, 3, 256, 100_000
+    g = np.random.default_rng(5)
+    lp = synth.normal_logits(pool, V, seed=51, std=2.0)
+    lq = synth.shared_logits(lp, 0.7, seed=52, std=2.0)
+    P, Q = softmax_rows(lp), softmax_rows(lq)
+    p_rows = g.integers(0, pool, size=(n, k + 1))
+    q_rows = g.integers(0, pool, size=(n, k))
+    draft = np.empty((n, k), np.int32)
+    Qd = Q.astype(np.float64)
+    Qd /= Qd.sum(1, keepdims=True)
+    for row in range(pool):  # drafts drawn from each window's q row (host side)
+        w, i = np.nonzero(q_rows == row)
+        draft[w, i] = g.choice(V, size=len(w), p=Qd[row])
+    tok, ne, st, near = compare(P, draft, q=Q, p_rows=p_rows, q_rows=q_rows, seed=11)
+    _, ne_r, _, near_r, margin = oracle.accept(P, draft, q=Q, p_rows=p_rows, q_rows=q_rows, seed=11,
+                                               return_margin=True)
+    rates = excuse_rates(ne_r, margin, near_r, k)
+    print("acceptance excuse rates:", rates)
+    assert rates["decisions"] > 200_000
+    assert rates["excused_per_decision"] < 1e-5

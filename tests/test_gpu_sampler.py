@@ -27,6 +27,9 @@ def check(logits, T, top_p, min_p, greedy=False):
         if fl[r] == 0:
             assert np.array_equal(kept_g, kept_r), (r, kept_g.sum(), kept_r.sum())
             assert np.allclose(pg[r], pr[r], rtol=1e-5, atol=1e-12)
+    # rows excused from the kept-set comparison (a decision within rounding of a filter
+    # boundary): at most 1 % of the rows, and at most one in a small test
+    assert (fl != 0).sum() <= max(1, len(fl) // 100), fl
     return pg, pr, fl
 
 
@@ -107,3 +110,10 @@ def test_lm_head_softmax_matches_oracle():
         if fl[r] == 0:
             assert np.array_equal(pg[r] > 0, pr[r] > 0)
             assert np.allclose(pg[r], pr[r], rtol=1e-5, atol=1e-12)
+
+
+def test_many_rows_bound_the_excused_rows():
+    """512 rows of the tiny window's vocabulary: the flagged rows (whose kept set is not compared)
+    stay under 1 % of the rows; every other row matches the oracle's kept set exactly."""
+    _, _, fl = check(synth.normal_logits(512, 4096, seed=9, std=2.0), 0.6, 0.95, 0.05)
+    print("sampler rows flagged:", int((fl != 0).sum()), "of", len(fl))
