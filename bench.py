@@ -7,8 +7,8 @@ weights per step exceed the 129 MB L2, so no flush is needed between steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl svd|reference]
 
-Prints one JSON line on rank 0.  --impl reference times the fp64 CPU oracle on the host cores on
-a bounded sample of the same pass (one layer and 1/64 of the lm_head rows per step).
+Prints one JSON line on rank 0.  --impl reference times the fp64 CPU oracle on the host cores,
+one whole verify pass per step.
 """
 from __future__ import annotations
 
@@ -164,73 +164,91 @@ def _cpu_model() -> str:
 
 
 class OracleSample:
-    """The oracle timed on the host on a bounded slice of the pass, scaled to passes/s.
+    """The fp64 oracle timed on the host, one step = one whole verify pass at C = 4: the four
+    fused GEMMs of a layer (every row) 64 times -- one layer's matrices stand for all 64, the
+    same arithmetic and the same bytes streamed from host memory per layer -- then the whole
+    lm_head (5120 x 151936), the sampler over the 4 target and 3 drafter positions, and the
+    acceptance of one window of 3 drafts.  With `layers` < 64 a step is that many layers and the
+    lm_head share of the same fraction (a bounded sample: passes_per_s scales it, and `fraction`
+    says by how much)."""
 
-    A step runs, in fp64 on every host thread, the first `rows` rows of each of one layer's four
-    fused GEMMs and the matching share of the lm_head rows (1/64 of them per layer) at C = 4;
-    its time is scaled by (weights of a pass) / (weights sampled).  The sampler over the 4
-    positions and the acceptance of one window are timed once and added whole."""
-
-    def __init__(self, frac: float, threads: int = 0):
+    def __init__(self, layers: int = 64, threads: int = 0):
         import numpy as np
 
         import oracle
         from speculative_decoding_verify_06_gb300 import synth
         self.np, self.oracle, self.synth = np, oracle, synth
         self.threads = threads or oracle.max_threads()
+        self.layers = layers
+        self.fraction = layers / synth.LAYERS
         C = 4
-        self.frac = frac
-        shapes = list(synth.LAYER_GEMMS) + [(synth.HIDDEN, synth.VOCAB // synth.LAYERS)]
-        self.mats, self.xs, self.sampled, self.full = [], [], 0, 0
-        for g, (i, o) in enumerate(shapes):
-            r = max(16, int(round(o * frac)))
-            self.mats.append(synth.qweight(r, i, seed=1000 + g))
-            self.xs.append(synth.activations(C, i, seed=2000 + g))
-            self.sampled += r * i
-            self.full += o * i
-        lg = synth.normal_logits(C, synth.VOCAB, seed=4, std=4.389)
-        t0 = time.perf_counter()
-        f32 = np.float32
-        p, *_ = oracle.sampler(lg, f32(0.6), f32(0.95), f32(0.05), nthreads=self.threads)
-        q, *_ = oracle.sampler(synth.perturb(lg[:3], 1.205, 5), f32(0.6), f32(0.95), f32(0.05),
-                               nthreads=self.threads)
-        d = synth.draw_from(q, 6).reshape(1, 3)
-        oracle.accept(p.astype(np.float32), d, q=q.astype(np.float32), seed=1, nthreads=self.threads)
-        self.t_tail = time.perf_counter() - t0
+        self.mats = [synth.qweight(o, i, seed=1000 + g) for g, (i, o) in enumerate(synth.LAYER_GEMMS)]
+        self.xs = [synth.activations(C, i, seed=2000 + g) for g, (i, o) in enumerate(synth.LAYER_GEMMS)]
+        head_rows = max(16, int(round(synth.VOCAB * self.fraction)))
+        self.head = synth.qweight(head_rows, synth.HIDDEN, seed=1999)
+        self.hx = synth.activations(C, synth.HIDDEN, seed=2999)
+        self.weights = (layers * sum(i * o for i, o in synth.LAYER_GEMMS) + head_rows * synth.HIDDEN)
 
     def step(self) -> float:
+        np, oracle = self.np, self.oracle
+        f32 = np.float32
         t0 = time.perf_counter()
-        for (c, s), x in zip(self.mats, self.xs):
-            self.oracle.verify_linear(c, s, x, nthreads=self.threads)
+        for _ in range(self.layers):
+            for (c, s), x in zip(self.mats, self.xs):
+                oracle.verify_linear(c, s, x, nthreads=self.threads)
+        y, _ = oracle.verify_linear(self.head[0], self.head[1], self.hx, nthreads=self.threads)
+        lg = y.astype(f32)
+        p, *_ = oracle.sampler(lg, f32(0.6), f32(0.95), f32(0.05), nthreads=self.threads)
+        q, *_ = oracle.sampler(self.synth.perturb(lg[:3], 1.205, 5), f32(0.6), f32(0.95), f32(0.05),
+                               nthreads=self.threads)
+        d = self.synth.draw_from(q, 6).reshape(1, 3)
+        oracle.accept(p.astype(f32), d, q=q.astype(f32), seed=1, nthreads=self.threads)
         return time.perf_counter() - t0
 
     def passes_per_s(self, step_times) -> float:
-        t_layer = statistics.mean(step_times) * self.full / self.sampled
-        return 1.0 / (self.synth.LAYERS * t_layer + self.t_tail)
+        return self.fraction / statistics.mean(step_times)
 
     def describe(self, n: int) -> str:
-        return (f"{n} step(s), each {self.sampled / 1e6:.1f}M of a layer's {self.full / 1e6:.1f}M "
-                f"weights (all four fused GEMMs and 1/64 of the lm_head, same fraction of rows) "
-                f"at C=4 in fp64, scaled to 64 layers; sampler (4+3 rows of 151936) and one "
-                f"acceptance window timed once ({self.t_tail:.2f} s) and added")
+        what = ("one whole pass" if self.layers == self.synth.LAYERS else
+                f"{self.layers} of the 64 layers and the same share of the lm_head rows, scaled by "
+                f"{1 / self.fraction:g} to a pass")
+        return (f"{n} step(s), each {what} ({self.weights / 1e9:.2f}G weights) at C=4 in fp64: "
+                f"the 4 fused GEMMs of one layer's full-size matrices per layer, lm_head, sampler "
+                f"(4 + 3 rows of 151936), acceptance of one window")
+
+
+def lm_head_oracle_windows(n_windows: int = 16, threads: int = 0):
+    """The lm_head + sampler workload on the host: n_windows windows, each the 5120 x 151936
+    lm_head over K+1 = 6 columns and the sampler over the 6 rows, in fp64 (windows per second)."""
+    import numpy as np
+
+    import oracle
+    from speculative_decoding_verify_06_gb300 import synth
+    threads = threads or oracle.max_threads()
+    codes, scales = synth.qweight(synth.VOCAB, synth.HIDDEN, seed=4999)
+    f32 = np.float32
+    t0 = time.perf_counter()
+    for w in range(n_windows):
+        x = synth.activations(6, synth.HIDDEN, seed=5000 + w)
+        y, _ = oracle.verify_linear(codes, scales, x, nthreads=threads)
+        oracle.sampler(y.astype(f32), f32(0.6), f32(0.95), f32(0.05), nthreads=threads)
+    dt = time.perf_counter() - t0
+    return {"value": n_windows / dt, "unit": "windows/s", "cores": threads, "kind": "oracle",
+            "seconds": dt, "sample": f"{n_windows} whole windows (lm_head 5120 x 151936 at C = 6 "
+                                     f"+ sampler over 6 rows), fp64"}
 
 
 def run_reference(args, rank):
     if rank != 0:
         return
-    # size each step so that warm-up + timed steps stay near a minute of host time
-    probe = OracleSample(frac=1.0 / 64)
-    t_probe = probe.step()
-    budget_s = 60.0
-    frac = min(1.0, max(1.0 / 256, budget_s / max(1, args.steps + args.warmup) / (64 * t_probe)))
-    smp = OracleSample(frac=frac)
+    smp = OracleSample()  # one whole pass per step
     for _ in range(args.warmup):
         smp.step()
     times = [smp.step() for _ in range(args.steps)]
     v = smp.passes_per_s(times)
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / v,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * statistics.mean(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "C": 4, "oracle": "fp64 C, OpenMP", "cpu": _cpu_model()},
@@ -643,7 +661,10 @@ def run_svd(args, rank, world, local_rank):
                      "kernel": "vl_stream_kernel (one chain launch: the stack's 256 matrices)",
                      "traffic": None if traffic_pass is None else traffic_pass},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": Ke},
+                "d2h_bytes_per_step": d2h, "steps": Ke,
+                "copies": ("per step, from pinned host memory: the first layer's input (the "
+                           "embedded window), the drafter's q rows and the drafts; back: the "
+                           "emitted tokens, their count and the status word")},
         "gpu_launches": K * ((n_launch if args.no_chain else 1) + (1 + 4 + 1 if vp.head else 0)),
         "clocks": clk.summary(),
     }
@@ -659,15 +680,17 @@ def run_svd(args, rank, world, local_rank):
                                                  and not args.no_cpu_baseline))
         line["pass_with_kv"] = pass_with_kv(vp, dev, peak, line["stack"]["tail_ms"])
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        smp = OracleSample(frac=0.25)
-        times = [smp.step() for _ in range(3)]
-        one = OracleSample(frac=1.0 / 64, threads=1)
+        smp = OracleSample()  # one whole pass on every host thread
+        times = [smp.step()]
+        one = OracleSample(layers=1, threads=1)  # a bounded single-thread sample
         t1 = [one.step()]
         line["cpu_baseline"] = {"value": smp.passes_per_s(times), "unit": UNIT,
-                                "cores": smp.threads, "kind": "oracle", "sample": smp.describe(3),
-                                "cpu": _cpu_model(),
+                                "cores": smp.threads, "kind": "oracle", "sample": smp.describe(1),
+                                "seconds": times[0], "cpu": _cpu_model(),
                                 "single_thread": {"value": one.passes_per_s(t1), "cores": 1,
-                                                  "sample": one.describe(1)}}
+                                                  "sample": one.describe(1), "seconds": t1[0]}}
+        if not args.stack_only:
+            line["lm_head_window_cpu_baseline"] = lm_head_oracle_windows()
     if rank == 0:
         print(json.dumps(line), flush=True)
 

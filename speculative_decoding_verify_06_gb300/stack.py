@@ -155,10 +155,11 @@ class VerifyPass:
         return b
 
     def inputs(self):
-        """The tensors a step consumes (copied host -> device in the end-to-end measurement)."""
-        t = [lin.X for lin in self.linears]
-        if self.head:
-            t.append(self.lm.X)
+        """What a verify pass receives from the host (copied host -> device in the end-to-end
+        measurement): the first layer's input (the embedded window, C x 5120 bf16), the drafter's
+        distributions q and the drafts.  The other layers' activations stand for what the model
+        computes on the device from the previous layer's output, so they stay resident."""
+        t = [self.linears[0].X]
         if self.accept:
             t += [self.q, self.draft]
         return t

@@ -1,7 +1,7 @@
 """Host-side helpers of bench.py, run on CPU tensors: the per-pair bisection that gives every
 (p, q) pair of the acceptance pools its target overlap sum min(p, q), and the two oracle
-timings reported beside the KV-read and acceptance sections (they must return a positive rate
-with the thread count they used)."""
+timings reported beside the KV-read and acceptance sections and the whole-pass oracle timing of
+the main line (they must return a positive rate with the thread count they used)."""
 import os
 import sys
 
@@ -43,3 +43,11 @@ def test_accept_oracle_sample_reports_a_rate():
     r = bench.accept_oracle_sample(P, Q, samples, 4, 50, g, torch.device("cpu"))
     assert r["kind"] == "oracle" and r["unit"] == "windows/s" and r["value"] > 0
     assert np.isfinite(r["seconds"]) and r["cores"] >= 1
+
+
+def test_pass_oracle_sample_scales_a_one_layer_step():
+    smp = bench.OracleSample(layers=1)
+    dt = smp.step()
+    assert dt > 0 and smp.fraction == 1 / 64
+    assert smp.passes_per_s([dt]) == pytest.approx(1 / (64 * dt))
+    assert "1 of the 64 layers" in smp.describe(1) and smp.threads >= 1
