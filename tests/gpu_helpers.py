@@ -58,12 +58,16 @@ def assert_gemm_parity(y, y_ref, a_ref, tol=1e-3):
 
 
 def sampler(logits: np.ndarray, smp):
+    """svd_sampler_probs over the rows, SVD_C_MAX rows (one call's limit) at a time."""
     rows, V = logits.shape
     L = to_dev(logits.astype(np.float32))
     P = torch.empty_like(L)
     am = torch.empty(rows, dtype=torch.int32, device=DEV)
-    ws = torch.zeros(svd.svd_sampler_workspace_bytes(rows, V), dtype=torch.uint8, device=DEV)
-    svd.svd_sampler_probs(L, rows, V, smp, P, am, ws)
+    step = min(rows, svd.SVD_C_MAX)
+    ws = torch.zeros(svd.svd_sampler_workspace_bytes(step, V), dtype=torch.uint8, device=DEV)
+    for r0 in range(0, rows, step):
+        n = min(step, rows - r0)
+        svd.svd_sampler_probs(L[r0:r0 + n], n, V, smp, P[r0:r0 + n], am[r0:r0 + n], ws)
     torch.cuda.synchronize()
     return P.cpu().numpy(), am.cpu().numpy()
 

@@ -1,9 +1,11 @@
 """GPU parity of the acceptance kernel (svd_accept) against the oracle on identical p, q, drafts
 and Philox uniforms: emitted tokens, counts and status bit-exact, except windows whose resampling
 uniform lies within 1e-9 of a token boundary, where the two summation orders may pick a
-neighbour; those windows must be under 1e-5 of the decisions (accept tests and draws).  The
-oracle also flags draws within 1e-6 of a boundary (the near-threshold flag), reported per window
-and per decision."""
+neighbour.  A uniform u' lands within 1e-9 of one of a draw's V boundaries with probability at
+most 2e-9 V, so the excused windows may number 2e-9 V draws plus a Poisson tail of 3 (and the
+100k-window test shows them under 1e-5 of the accept tests and draws).  The oracle also flags
+draws within 1e-6 of a boundary (the near-threshold flag), which must be under 1e-5 of the
+threshold comparisons; both rates are reported per window and per decision."""
 import numpy as np
 import pytest
 
@@ -44,9 +46,9 @@ def compare(p, draft, q=None, **kw):
         j = ne_r[w] - 1
         assert ne[w] == ne_r[w] and np.array_equal(tok[w, :j], tok_r[w, :j])
     rates = excuse_rates(ne_r, margin, near, k, sampled=q is not None)
-    # windows excused from bit-exactness: under 1e-5 of the decisions (one per accept test, one
-    # per draw)
-    assert (~exact).sum() <= 1e-5 * rates["decisions"], rates
+    # windows excused from bit-exactness: no more than the 1e-9 band admits by chance (u' within
+    # 1e-9 of one of V boundaries: probability <= 2e-9 V per draw), plus 3 for the Poisson tail
+    assert (~exact).sum() <= 2 * EXACT_MARGIN * V * rates["draws"] + 3, rates
     # the near-threshold flag (u' within 1e-6 of a threshold), counted per threshold comparison
     # (a draw over V tokens compares u' R with V running sums, an accept test is one comparison):
     # under 1e-5 of them

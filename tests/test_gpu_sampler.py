@@ -1,6 +1,9 @@
 """GPU parity of the sampler (svd_sampler_probs) and of lm_head + sampler against the oracle on
 identical fp32 logits: argmax exact; the kept set exact wherever the oracle reports no decision
-within rounding of a filter boundary; kept probabilities within 1e-5 relative."""
+within rounding of a filter boundary; kept probabilities within 1e-5 relative.  Where the oracle
+does flag a boundary decision, the two kept sets must still be prefixes of the same (p
+descending, id ascending) order and may differ only by tokens inside the flagged band: a top-p
+crossing within 1e-5 of top_p, or a probability within relative 1e-6 of min_p * max p."""
 import numpy as np
 import pytest
 import torch
@@ -14,12 +17,38 @@ pytestmark = pytest.mark.gpu
 F32 = np.float32
 
 
+def check_flagged_row(pg, pr, base, flags, top_p, min_p):
+    """A row whose decision the oracle flags: the GPU's kept set is a prefix of the oracle's
+    order, it differs from the oracle's only by tokens inside the flagged band, and the
+    probabilities of the tokens both keep agree after renormalising over them."""
+    V = len(base)
+    order = np.lexsort((np.arange(V), -base))
+    kg, kr = pg[order] > 0, pr[order] > 0
+    ng, nr = int(kg.sum()), int(kr.sum())
+    assert kg[:ng].all() and kr[:nr].all()
+    if ng != nr:
+        lo, hi = min(ng, nr), max(ng, nr)
+        cum = np.cumsum(base[order])
+        # top-p: the GPU's cut lies where the oracle's running mass is within the band
+        in_top = bool(flags & 2) and (
+            cum[ng - 2] - top_p < 1e-5 if ng > nr else top_p - cum[ng - 1] <= 1e-5)
+        # min-p: every token on which the two differ sits at the threshold
+        thr = min_p * base.max()
+        in_min = bool(flags & 1) and np.all(np.abs(base[order[lo:hi]] - thr) <= 2e-6 * thr)
+        assert in_top or in_min, (ng, nr, flags)
+    common = (pg > 0) & (pr > 0)
+    a = pg[common].astype(np.float64)
+    b = pr[common]
+    assert np.allclose(a / a.sum(), b / b.sum(), rtol=1e-5, atol=1e-12)
+
+
 def check(logits, T, top_p, min_p, greedy=False):
     lib()
     smp = svd.Sampler(T, top_p, min_p, greedy)
     pg, amg = sampler(logits, smp)
     pr, amr, nk, fl = oracle.sampler(logits, F32(T), F32(top_p), F32(min_p), greedy)
     assert np.array_equal(amg, amr)
+    base = None
     for r in range(len(logits)):
         kept_g, kept_r = pg[r] > 0, pr[r] > 0
         assert kept_g[amr[r]]
@@ -27,9 +56,11 @@ def check(logits, T, top_p, min_p, greedy=False):
         if fl[r] == 0:
             assert np.array_equal(kept_g, kept_r), (r, kept_g.sum(), kept_r.sum())
             assert np.allclose(pg[r], pr[r], rtol=1e-5, atol=1e-12)
-    # rows excused from the kept-set comparison (a decision within rounding of a filter
-    # boundary): at most 1 % of the rows, and at most one in a small test
-    assert (fl != 0).sum() <= max(1, len(fl) // 100), fl
+        else:
+            if base is None:  # the unfiltered softmax at T, in the oracle's fp64
+                base, *_ = oracle.sampler(logits, F32(T), F32(1.0), F32(0.0))
+            check_flagged_row(pg[r], pr[r], base[r], int(fl[r]), float(F32(top_p)),
+                              float(F32(min_p)))
     return pg, pr, fl
 
 
@@ -113,7 +144,9 @@ def test_lm_head_softmax_matches_oracle():
 
 
 def test_many_rows_bound_the_excused_rows():
-    """512 rows of the tiny window's vocabulary: the flagged rows (whose kept set is not compared)
-    stay under 1 % of the rows; every other row matches the oracle's kept set exactly."""
+    """512 rows of the tiny window's vocabulary: the flagged rows (whose kept set is compared only
+    up to the flagged band) stay under 1 % of the rows; every other row matches the oracle's kept
+    set exactly."""
     _, _, fl = check(synth.normal_logits(512, 4096, seed=9, std=2.0), 0.6, 0.95, 0.05)
     print("sampler rows flagged:", int((fl != 0).sum()), "of", len(fl))
+    assert (fl != 0).sum() <= len(fl) // 100, fl
