@@ -73,10 +73,15 @@ enum {
 
 /* Flags for svd_verify_linear. */
 enum {
-    SVD_F_PDL = 1 /* launch with programmatic dependent launch: the kernel may start while the
+    SVD_F_PDL = 1, /* launch with programmatic dependent launch: the kernel may start while the
                      previous kernel on the stream is still running and stream its weights
                      early; it waits for that kernel before reading X or the workspace.  Set
                      only when nothing in flight on the stream writes the weights. */
+    SVD_F_FRAGMENT_MMA = 2 /* native layout, 17..32 columns: run the warp-level mma.sync kernel
+                     (bf16 operands, exact dequantisation, per-block fp32 rescale) instead of the
+                     tcgen05 kernel (fp16 operands: the block scale is folded into the weights
+                     with one fp16 rounding, activations rounded from bf16 to fp16).  Kept as the
+                     comparison for the tensor-core path; no effect for C <= 16. */
 };
 
 #define SVD_C_MAX 32 /* most activation columns (K+1 positions x sequences) per call */
@@ -130,8 +135,14 @@ int svd_unpack_weights(const svd_qweight *src_native, void *dst_codes, void *dst
  * weights are read once and applied to the K-wide batch of the window).
  *   X: bf16 [C][in] row-major (token-major), 16-byte aligned.  Y: fp32 [C][out].
  *   C in 1..SVD_C_MAX.
- *   NATIVE weights run the tensor-core stream-K kernel (bf16 MMA, fp32 accumulate, one fresh
- *   accumulator per 32-input block, scaled in fp32).  It needs a workspace of
+ *   NATIVE weights run a tensor-core stream-K kernel.  C <= 16: warp-level bf16 MMA with the
+ *   codes dequantised exactly, fp32 accumulate, one fresh accumulator per 32-input block,
+ *   scaled in fp32.  17 <= C <= 32 ("Why a hiring company is writing this": several
+ *   sequences' windows in one pass): tcgen05.mma with fp32 accumulators in tensor memory, the
+ *   A operand fp16(s * (code - 8)) (one fp16 rounding, relative 2^-11) and the B operand X
+ *   rounded to fp16 (|X| must stay below 65504; |X| < 2^-14 loses relative precision as an fp16
+ *   subnormal), which keeps |error| <= 2^-11 * sum |w x| plus fp32 accumulation;
+ *   SVD_F_FRAGMENT_MMA selects the warp-level kernel there too.  It needs a workspace of
  *   svd_verify_linear_workspace_bytes() bytes that is ZERO-FILLED before its first use (it
  *   holds barrier counters, which every call returns to zero, a launch epoch, a status word,
  *   and partial sums of row blocks split between CTAs, tagged with the launch that wrote

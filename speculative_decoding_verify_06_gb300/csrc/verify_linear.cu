@@ -773,6 +773,8 @@ vl_simt_kernel(const uint8_t *__restrict__ codes, const uint16_t *__restrict__ s
     }
 }
 
+#include "verify_linear_tc.cuh"
+
 // ---- host side ---------------------------------------------------------------------------
 #ifndef SVD_NW1
 #define SVD_NW1 16
@@ -875,8 +877,62 @@ static VlOp make_op(const svd_qweight *W, const void *X, float *Y) {
     return o;
 }
 
+// The tensor-core kernel: one CTA per SM (a cooperative launch for a chain), each holding
+// kTcTmemCols TMEM columns, so two CTAs overlapping under programmatic dependent launch fit in
+// one SM's 512.
 template <int MAXOPS>
-static cudaError_t launch_ops(const VlOps<MAXOPS> &P, void *ws, bool pdl, cudaStream_t stream) {
+static cudaError_t launch_tc(const VlOps<MAXOPS> &P, void *ws, bool pdl, bool coop, cudaStream_t stream) {
+    auto kern = vl_tc_kernel<MAXOPS>;
+    constexpr size_t smem = TcCfg<MAXOPS>::kSmem;
+    static bool ready[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !ready[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kTcThreads, smem);
+        if (e != cudaSuccess) return e;
+        if (per_sm < 1) return cudaErrorInvalidConfiguration;
+        if (dev >= 0 && dev < 64) ready[dev] = true;
+    }
+    int64_t max_units = 0;  // MMA units (128 rows x 64 inputs) of the largest op
+    for (int i = 0; i < P.n; ++i) {
+        const int64_t n_rb = P.op[i].n_units / P.op[i].n_kc;
+        const int64_t u = (n_rb + 1) / 2 * (int64_t)P.op[i].n_kc;
+        max_units = u > max_units ? u : max_units;
+    }
+    int64_t G = sm_count();
+    if (!coop && G > max_units) G = max_units;
+    if (G < 1) G = 1;
+    uint8_t *base = reinterpret_cast<uint8_t *>(ws);
+    auto *part = reinterpret_cast<unsigned long long *>(base);
+    unsigned *gbar = reinterpret_cast<unsigned *>(base + partial_region_bytes());
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)G);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (coop) {
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    } else if (pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kern, P, part, (uint32_t)partial_entries(), gbar);
+}
+
+// 17..32 columns run on the tensor-core kernel unless the caller asks for the fragment kernel.
+template <int MAXOPS>
+static cudaError_t launch_ops(const VlOps<MAXOPS> &P, void *ws, bool pdl, cudaStream_t stream,
+                              bool fragment_mma = false) {
     int64_t max_units = 0;
     for (int i = 0; i < P.n; ++i)
         max_units = (int64_t)P.op[i].n_units > max_units ? (int64_t)P.op[i].n_units : max_units;
@@ -884,7 +940,9 @@ static cudaError_t launch_ops(const VlOps<MAXOPS> &P, void *ws, bool pdl, cudaSt
     switch (ntiles_for(P.C)) {
         case 1: return launch_stream<1, kNW1, kTiles, kR1, kU, MAXOPS>(P, ws, pdl, coop, max_units, stream);
         case 2: return launch_stream<2, kNW2, kTW2, kR2, kU, MAXOPS>(P, ws, pdl, coop, max_units, stream);
-        default: return launch_stream<4, kNW4, kTW4, kR2, kU, MAXOPS>(P, ws, pdl, coop, max_units, stream);
+        default:
+            if (!fragment_mma) return launch_tc<MAXOPS>(P, ws, pdl, coop, stream);
+            return launch_stream<4, kNW4, kTW4, kR2, kU, MAXOPS>(P, ws, pdl, coop, max_units, stream);
     }
 }
 
@@ -934,7 +992,7 @@ int verify_linear(const svd_qweight *W, const void *X, int C, float *Y, void *ws
     int rc = check_qweight(W);
     if (rc != SVD_OK) return rc;
     if (!X || !Y || C < 1 || C > SVD_C_MAX || !aligned16(X)) return SVD_ERR_INVALID_ARG;
-    if (flags & ~SVD_F_PDL) return SVD_ERR_INVALID_ARG;
+    if (flags & ~(SVD_F_PDL | SVD_F_FRAGMENT_MMA)) return SVD_ERR_INVALID_ARG;
     const bool pdl = (flags & SVD_F_PDL) != 0;
     if (sm_count() < 1) return SVD_ERR_CUDA;
     if (W->layout == SVD_LAYOUT_NATIVE) {
@@ -946,7 +1004,7 @@ int verify_linear(const svd_qweight *W, const void *X, int C, float *Y, void *ws
         P.n = 1;
         P.C = C;
         P.op[0] = make_op(W, X, Y);
-        SVD_CUDA_TRY(launch_ops(P, ws, pdl, stream));
+        SVD_CUDA_TRY(launch_ops(P, ws, pdl, stream, (flags & SVD_F_FRAGMENT_MMA) != 0));
         return SVD_OK;
     }
     // canonical layout: CUDA-core kernel
@@ -977,7 +1035,7 @@ size_t chain_workspace_bytes(const svd_linear_op *ops, int n_ops, int C) {
 int verify_chain(const svd_linear_op *ops, int n_ops, int C, void *ws, size_t ws_bytes, int flags,
                  cudaStream_t stream) {
     if (!ops || n_ops < 1 || C < 1 || C > SVD_C_MAX) return SVD_ERR_INVALID_ARG;
-    if (flags & ~SVD_F_PDL) return SVD_ERR_INVALID_ARG;
+    if (flags & ~(SVD_F_PDL | SVD_F_FRAGMENT_MMA)) return SVD_ERR_INVALID_ARG;
     for (int i = 0; i < n_ops; ++i) {
         const int rc = check_qweight(&ops[i].W);
         if (rc != SVD_OK) return rc;
@@ -997,13 +1055,13 @@ int verify_chain(const svd_linear_op *ops, int n_ops, int C, void *ws, size_t ws
             P1.n = 1;
             P1.C = C;
             P1.op[0] = make_op(&ops[first].W, ops[first].X, ops[first].Y);
-            SVD_CUDA_TRY(launch_ops(P1, ws, first == 0 && (flags & SVD_F_PDL), stream));
+            SVD_CUDA_TRY(launch_ops(P1, ws, first == 0 && (flags & SVD_F_PDL), stream, (flags & SVD_F_FRAGMENT_MMA) != 0));
             continue;
         }
         P.n = n;
         P.C = C;
         for (int i = 0; i < n; ++i) P.op[i] = make_op(&ops[first + i].W, ops[first + i].X, ops[first + i].Y);
-        SVD_CUDA_TRY(launch_ops(P, ws, false, stream));
+        SVD_CUDA_TRY(launch_ops(P, ws, false, stream, (flags & SVD_F_FRAGMENT_MMA) != 0));
     }
     return SVD_OK;
 }
@@ -1112,7 +1170,7 @@ int verify_linear_noalloc(const svd_qweight *W, const void *X, int C, float *Y, 
     if (rc != SVD_OK) return rc;
     if (W->layout != SVD_LAYOUT_NATIVE) return SVD_ERR_INVALID_ARG;
     if (!X || !Y || C < 1 || C > SVD_C_MAX || !aligned16(X)) return SVD_ERR_INVALID_ARG;
-    if (flags & ~SVD_F_PDL) return SVD_ERR_INVALID_ARG;
+    if (flags & ~(SVD_F_PDL | SVD_F_FRAGMENT_MMA)) return SVD_ERR_INVALID_ARG;
     if (W->out_features > SVD_NOALLOC_MAX_OUT_FEATURES) return SVD_ERR_UNSUPPORTED;
     if (sm_count() >= 1 && check_native_size(W) != SVD_OK) return SVD_ERR_UNSUPPORTED;
     const int sms = sm_count();
@@ -1145,7 +1203,7 @@ int verify_linear_noalloc(const svd_qweight *W, const void *X, int C, float *Y, 
     P.n = 1;
     P.C = C;
     P.op[0] = make_op(W, X, Y);
-    SVD_CUDA_TRY(launch_ops(P, base, (flags & SVD_F_PDL) != 0, stream));
+    SVD_CUDA_TRY(launch_ops(P, base, (flags & SVD_F_PDL) != 0, stream, (flags & SVD_F_FRAGMENT_MMA) != 0));
     return SVD_OK;
 }
 

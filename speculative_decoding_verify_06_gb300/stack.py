@@ -177,8 +177,8 @@ class ColumnsView:
     activations and outputs, the same 4-bit matrices, the stack as one chain launch (for the
     sweep over window widths without re-creating 12 GB of weights)."""
 
-    def __init__(self, vp: VerifyPass, C: int, seed: int = 0):
-        self.vp, self.C = vp, C
+    def __init__(self, vp: VerifyPass, C: int, seed: int = 0, flags: int = 0):
+        self.vp, self.C, self.flags = vp, C, flags
         dev = vp.device
         self.X = [synth.activations_torch(C, lin.in_f, seed * 100003 + n, dev)
                   for n, lin in enumerate(vp.linears)]
@@ -189,7 +189,7 @@ class ColumnsView:
         self.graph = None
 
     def enqueue(self, stream=None):
-        svd.svd_verify_chain(self.ops, self.C, self.ws, stream=stream)
+        svd.svd_verify_chain(self.ops, self.C, self.ws, flags=self.flags, stream=stream)
 
     def capture(self):
         s = torch.cuda.Stream(device=self.vp.device)

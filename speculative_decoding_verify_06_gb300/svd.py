@@ -30,6 +30,7 @@ SVD_ST_EMPTY = 16
 SVD_LAYOUT_CANONICAL = 0
 SVD_LAYOUT_NATIVE = 1
 SVD_F_PDL = 1
+SVD_F_FRAGMENT_MMA = 2
 SVD_POLL_DEFAULT = 0xFFFFFFFF
 SVD_C_MAX = 32
 SVD_K_MAX = 32
