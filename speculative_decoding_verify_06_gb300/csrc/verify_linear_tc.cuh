@@ -19,61 +19,68 @@
 //
 // Decomposition.  An MMA unit is 128 weight rows (native row blocks 2q and 2q+1) x one 64-input
 // chunk; units are ordered row-group-major, and the grid splits them into contiguous ranges,
-// one per CTA (stream-K).  A CTA runs four PIPES of four warps.  The CTA's range is cut into
-// blocks of up to two units of one row group, dealt to the pipes round-robin; each pipe streams
-// its blocks through a ring of two slots (per block four bulk copies, one per warp: the codes and
-// the scales of the two row blocks), dequantises each half-chunk (128 rows x 32 inputs) into an
-// fp16 A stage, converts the activations of that half-chunk into an fp16 B stage, and issues two
-// tcgen05.mma (M 128, N 32, K 16) into its own accumulator (32 TMEM columns; two sets, by the
-// parity of the row-group segment).  When a segment (one row group of the range) is done, the
-// sixteen warps add the pipes' accumulators in pipe order -- pipe p reads TMEM columns 8p..8p+7
-// (tokens), warp j of a pipe rows 32j..32j+31 (its TMEM lane quarter) -- and write Y, or store a
-// tagged partial if an earlier CTA owns the row group; the owner adds the later CTAs' partials in
-// CTA order.  Summation order is fixed: results are deterministic.
+// one per CTA (stream-K).  A CTA runs three PIPES of four warps and one MMA warp.  The CTA's
+// range is cut into blocks of up to two units of one row group, dealt to the pipes round-robin.
+// A pipe streams its blocks through a ring of two slots (per block four bulk copies, one per
+// warp: the codes and the scales of the two row blocks); its warps dequantise each unit into an
+// fp16 A stage (warp j: rows 32j..32j+31), convert the unit's activations into an fp16 B stage
+// (warp j: tokens 8j..8j+7), and arrive on the stage's barrier.  The MMA warp takes the pipes'
+// stages in order and issues four tcgen05.mma (M 128, N 32, K 16) per stage into the pipe's
+// accumulator (32 TMEM columns; two sets, by the parity of the row-group segment).  When a
+// segment (one row group of the range) is done, the pipes' warps add the accumulators of the
+// segment in pipe order -- pipe p takes token groups p and p + 3 (8 TMEM columns each), warp j
+// of a pipe rows 32j..32j+31 (its TMEM lane quarter) -- and write Y, or store a tagged partial
+// if an earlier CTA owns the row group; the owner adds the later CTAs' partials in CTA order.
+// Summation order is fixed: results are deterministic.
 //
 // Every wait is bounded (the WaitCtl of the stream-K kernel): a wait that runs out sets a status
 // bit, later waits return at once, and before exiting the CTA waits a bounded time for its
 // tensor-core operations and bulk copies.
+//
 // Included by verify_linear.cu inside namespace svd, after the stream-K kernel whose op
 // descriptors, partial tags and bounded waits it shares.
 #pragma once
 
-constexpr int kTcPipes = 4;           // pipes per CTA
+constexpr int kTcPipes = 3;           // pipes per CTA
 constexpr int kTcPipeWarps = 4;       // warps per pipe (one per TMEM lane quarter)
-constexpr int kTcThreads = kTcPipes * kTcPipeWarps * 32;
+constexpr int kTcMmaWarp = kTcPipes * kTcPipeWarps;   // first of the pipes' MMA warps
+constexpr int kTcThreads = (kTcMmaWarp + kTcPipes) * 32;
 constexpr int kTcU = 2;               // units per block (per bulk copy)
 constexpr int kTcR = 2;               // ring slots per pipe
-constexpr int kTcS = 3;               // A/B stages per pipe
+constexpr int kTcS = 2;               // A/B stages per pipe
 constexpr int kTcN = 32;              // MMA N: activation columns
 constexpr int kTcRows = 2 * kRowsPerBlock;            // MMA M: 128 weight rows
 constexpr int kTcSlotBytes = 2 * kTcU * kUnitBytes;   // codes rb0, codes rb1, scales rb0, rb1
-constexpr int kTcAStage = kTcRows * 32 * 2;           // 128 rows x 32 inputs fp16
-constexpr int kTcBStage = kTcN * 32 * 2;              // 32 tokens x 32 inputs fp16
-constexpr int kTcPipeBytes = kTcR * kTcSlotBytes + kTcS * (kTcAStage + kTcBStage);
+constexpr int kTcAStage = kTcRows * kChunk * 2;       // 128 rows x 64 inputs fp16
+constexpr int kTcBStage = kTcN * kChunk * 2;          // 32 tokens x 64 inputs fp16
+// per pipe: the stages first (1024-byte aligned for the swizzle), then the ring
+constexpr int kTcPipeBytes = kTcS * (kTcAStage + kTcBStage) + kTcR * kTcSlotBytes;
 constexpr int kTcAccCols = kTcN;                      // TMEM columns per accumulator
-constexpr uint32_t kTcTmemCols = kTcPipes * 2 * kTcAccCols;  // 256 (power of two)
+constexpr uint32_t kTcTmemCols = 256;                 // kTcPipes * 2 * kTcAccCols, rounded to 2^k
 constexpr int kTcPartial = kTcRows * kTcN;            // entries of a CTA's partial
 static_assert(kTcPartial <= 2 * kPartialMax, "a tensor-core CTA uses two stream-K partial slots");
-static_assert(kRowsPerBlock == 64, "the MMA unit is two 64-row native blocks");
+static_assert(kRowsPerBlock == 64 && kChunk == 64, "the MMA unit is two 64-row native blocks x 64 inputs");
+static_assert(kTcPipes * 2 * kTcAccCols <= (int)kTcTmemCols, "accumulators fit the allocation");
+static_assert(kTcPipeBytes % 1024 == 0 && (kTcAStage % 1024) == 0 && (kTcBStage % 1024) == 0,
+              "stages stay on the swizzle's 1024-byte period");
 
 template <int MAXOPS>
 struct TcCfg {
-    // + 1 KB to align the stages to the 512-byte period of the 64-byte swizzle
+    // + 1 KB to align the stages to the 1024-byte period of the 128-byte swizzle
     static constexpr size_t kSmem = (size_t)kTcPipes * kTcPipeBytes + (size_t)MAXOPS * sizeof(VlOp) + 1024;
     static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
 };
 
 // ---- tcgen05 / TMEM -----------------------------------------------------------------------
-// Shared-memory matrix descriptor of a K-major operand stored with the 64-byte swizzle: each row
-// holds 32 fp16 inputs (64 bytes), row r at 64 r, and its 16-byte piece c sits at piece
-// c ^ ((r >> 1) & 3) (address bits 4-5 XOR bits 7-8), so a quarter-warp storing two rows writes
-// one contiguous 128 bytes.  Fields: start >> 4, leading offset (unused by swizzled K-major
-// layouts) >> 4 at bit 16, stride between 8-row groups (8 x 64 = 512 bytes) >> 4 at bit 32, the
-// descriptor version bit 46, layout 4 (64-byte swizzle) at bits 61-63.  The operand must lie
-// in a 512-byte-aligned region; a K step of 16 advances the start by 32 bytes.
-__device__ __forceinline__ uint64_t tc_sdesc_sw64(uint32_t addr) {
+// Shared-memory matrix descriptor of a K-major operand stored with the 128-byte swizzle: each row
+// holds 64 fp16 inputs (128 bytes), row r at 128 r, and its 16-byte piece c sits at piece
+// c ^ (r & 7) (address bits 4-6 XOR bits 7-9).  Fields: start >> 4, leading offset (unused by
+// swizzled K-major layouts) >> 4 at bit 16, stride between 8-row groups (8 x 128 = 1024 bytes)
+// >> 4 at bit 32, the descriptor version bit 46, layout 2 (128-byte swizzle) at bits 61-63.  The
+// operand must lie in a 1024-byte-aligned region; a K step of 16 advances the start by 32 bytes.
+__device__ __forceinline__ uint64_t tc_sdesc_sw128(uint32_t addr) {
     return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(16u >> 4) << 16) |
-           ((uint64_t)(512u >> 4) << 32) | (1ull << 46) | (4ull << 61);
+           ((uint64_t)(1024u >> 4) << 32) | (1ull << 46) | (2ull << 61);
 }
 // Instruction descriptor of kind::f16: D fp32 (bits 4-5 = 1), A and B fp16 (bits 7-9, 10-12 =
 // 0), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
@@ -187,23 +194,25 @@ __device__ __forceinline__ uint32_t tc_blocks(uint32_t s0, uint32_t s1) {
 struct TcIter {
     int op;               // current op; n_ops when exhausted
     uint32_t lo, hi;      // the CTA's range of that op
-    uint32_t s0, s1;      // current segment
+    uint32_t s0, s1, rg;  // current segment and its row group
     uint32_t jb, nb, cb;  // next block of this pipe in the segment, blocks in it, blocks before it
 
     __device__ __forceinline__ void start() {
         op = -1;
-        lo = hi = s0 = s1 = 0u;
+        lo = hi = s0 = s1 = rg = 0u;
         jb = nb = cb = 0u;
     }
-    // Next block of pipe p: op index, first unit and unit count; false when there is none.
+    // Next block of pipe p: op index, first unit, unit count and row group; false when there is
+    // none.
     __device__ __forceinline__ bool next(uint32_t p, const VlOp *ops, int n_ops, uint32_t G, uint32_t b,
-                                         int *op_out, uint32_t *u0, uint32_t *n) {
+                                         int *op_out, uint32_t *u0, uint32_t *n, uint32_t *rg_out) {
         for (;;) {
             if (op >= n_ops) return false;
             if (op >= 0 && jb < nb) {
                 *op_out = op;
                 *u0 = s0 + kTcU * jb;
                 *n = min((uint32_t)kTcU, s1 - *u0);
+                *rg_out = rg;
                 jb += kTcPipes;
                 return true;
             }
@@ -212,7 +221,8 @@ struct TcIter {
             if (op >= 0 && s1 < hi) {
                 const uint32_t n_kc = ops[op].n_kc;
                 s0 = s1;
-                s1 = min(hi, (s0 / n_kc + 1u) * n_kc);
+                rg = s0 / n_kc;
+                s1 = min(hi, (rg + 1u) * n_kc);
                 nb = tc_blocks(s0, s1);
                 jb = tc_first_block(p, cb);
                 continue;
@@ -229,33 +239,43 @@ struct TcSeg {
     uint32_t s0, s1, rg, cb, nb, k;
 };
 
+// What a pipe's stage holds, written by its warp 0 for the MMA warp: flags in bits 0-3, the
+// segment number k above them.
+constexpr uint32_t kTcMetaMma = 1u;     // a unit: issue its four MMAs
+constexpr uint32_t kTcMetaFirst = 2u;   // the pipe's first unit of the segment: start the accumulator
+constexpr uint32_t kTcMetaSegEnd = 4u;  // the pipe's last stage of the segment: signal its accumulator
+constexpr uint32_t kTcMetaEnd = 8u;     // the pipe has no more stages
+
 template <int MAXOPS>
 __global__ void __launch_bounds__(kTcThreads, 1)
 vl_tc_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__restrict__ part,
              uint32_t part_entries, unsigned *__restrict__ gbar) {
-    extern __shared__ __align__(1024) uint8_t smem[];
+    extern __shared__ __align__(128) uint8_t smem[];  // aligned to 1 KB below
     __shared__ __align__(8) uint64_t s_full[kTcPipes * kTcR];   // a ring slot's copies landed
+    __shared__ __align__(8) uint64_t s_stage[kTcPipes * kTcS];  // a stage is written (its 4 warps)
     __shared__ __align__(8) uint64_t s_empty[kTcPipes * kTcS];  // a stage's MMAs have read it
     __shared__ __align__(8) uint64_t s_done[kTcPipes * 2];      // a pipe's MMAs of a segment (per set)
     __shared__ __align__(8) uint64_t s_free[2];                 // a set's accumulators have been read
     __shared__ __align__(8) uint64_t s_final[kTcPipes];         // every MMA of a pipe, at exit
+    __shared__ uint32_t s_meta[kTcPipes * kTcS];
     __shared__ uint32_t s_tmem, s_epoch, s_last;
     __shared__ WaitCtl s_wc;
-    uint8_t *const sm0 = smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u);  // 1 KB aligned
+    uint8_t *const sm0 = smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u);
     VlOp *ops = reinterpret_cast<VlOp *>(sm0 + (size_t)kTcPipes * kTcPipeBytes);
     const int n_ops = P.n;
     const int C = P.C;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t pipe = (uint32_t)warp / kTcPipeWarps;
+    const bool mma_warp = warp >= kTcMmaWarp;  // warp kTcMmaWarp + p issues pipe p's MMAs
+    const uint32_t pipe = mma_warp ? (uint32_t)(warp - kTcMmaWarp) : (uint32_t)warp / kTcPipeWarps;
     const int wj = warp % kTcPipeWarps;  // warp in the pipe = its TMEM lane quarter
     const uint32_t G = gridDim.x, b = blockIdx.x;
-    const bool elected = wj == 0 && lane == 0;  // issues the pipe's MMAs
-    uint8_t *const ring = sm0 + (size_t)pipe * kTcPipeBytes;
-    const uint32_t ring0 = smem_u32(ring);
-    const uint32_t astage0 = ring0 + kTcR * kTcSlotBytes;
+    uint8_t *const ring = sm0 + (size_t)pipe * kTcPipeBytes + kTcS * (kTcAStage + kTcBStage);
+    const uint32_t astage0 = smem_u32(sm0) + pipe * kTcPipeBytes;
     const uint32_t bstage0 = astage0 + kTcS * kTcAStage;
+    const uint32_t ring0 = smem_u32(ring);
     const uint32_t full0 = smem_u32(&s_full[pipe * kTcR]);
+    const uint32_t stage0 = smem_u32(&s_stage[pipe * kTcS]);
     const uint32_t empty0 = smem_u32(&s_empty[pipe * kTcS]);
 
     {
@@ -266,35 +286,38 @@ vl_tc_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__rest
     }
     if (threadIdx.x == 0) {
         for (int i = 0; i < kTcPipes * kTcR; ++i) mbar_init(smem_u32(&s_full[i]), kTcPipeWarps);
-        for (int i = 0; i < kTcPipes * kTcS; ++i) mbar_init(smem_u32(&s_empty[i]), 1);
+        for (int i = 0; i < kTcPipes * kTcS; ++i) {
+            mbar_init(smem_u32(&s_stage[i]), kTcPipeWarps);
+            mbar_init(smem_u32(&s_empty[i]), 1);
+        }
         for (int i = 0; i < kTcPipes * 2; ++i) mbar_init(smem_u32(&s_done[i]), 1);
-        for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&s_free[i]), kTcPipes * kTcPipeWarps);
+        for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&s_free[i]), kTcMmaWarp);
         for (int i = 0; i < kTcPipes; ++i) mbar_init(smem_u32(&s_final[i]), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         s_wc.stop = 0u;
     }
     __syncthreads();
 
-    // Copy cursor of this pipe (uniform across its warps).  Warp wj copies one part of every
-    // block: wj = 0, 1 the codes of row block 2q + wj, wj = 2, 3 the scales of row block
-    // 2q + wj - 2; a row block past the matrix's end is not copied (its rows are never stored).
+    // Copy cursor of a pipe (uniform across its warps).  Warp wj copies one part of every block:
+    // the codes (wj even) or the scales (wj odd) of row block 2q + (wj >> 1), which are read by
+    // warps wj & ~1 and wj | 1 only; a row block past the matrix's end is not copied (its rows
+    // are never stored).
     TcIter it;
     it.start();
     uint32_t c_issued = 0;
     auto issue = [&]() {
         int op;
-        uint32_t u0, n;
-        if (!it.next(pipe, ops, n_ops, G, b, &op, &u0, &n)) return;
+        uint32_t u0, n, rg;
+        if (!it.next(pipe, ops, n_ops, G, b, &op, &u0, &n, &rg)) return;
         const VlOp &o = ops[op];
         const uint32_t slot = c_issued % kTcR, bar = full0 + 8u * slot;
         if (lane == 0) {
-            const uint32_t q = u0 / o.n_kc, kc = u0 - q * o.n_kc, h = (uint32_t)wj & 1u;
-            const uint32_t rb = 2u * q + h, n_rb = o.n_units / o.n_kc;
-            if (rb < n_rb) {
-                const size_t nu = (size_t)rb * o.n_kc + kc;  // native unit index
+            const uint32_t h = (uint32_t)wj >> 1, rb = 2u * rg + h;
+            if ((uint64_t)rb * o.n_kc < o.n_units) {
+                const size_t nu = (size_t)rb * o.n_kc + (u0 - rg * o.n_kc);  // native unit index
                 uint32_t dst, bytes;
                 const uint8_t *src;
-                if (wj < 2) {
+                if ((wj & 1) == 0) {
                     bytes = n * kUnitCodeBytes;
                     dst = ring0 + slot * kTcSlotBytes + h * (kTcU * kUnitCodeBytes);
                     src = o.codes + nu * kUnitCodeBytes;
@@ -311,18 +334,12 @@ vl_tc_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__rest
         }
         ++c_issued;
     };
-    // The consumer's next block (for the activation prefetch): one block ahead of it.
-    TcIter la;
-    la.start();
-    {
-        int op_;
-        uint32_t u_, n_;
-        la.next(pipe, ops, n_ops, G, b, &op_, &u_, &n_);
+    if (!mma_warp) {
+        // The stall injection (workspace word kBarPoll, written only by the test hook): no copy.
+        if (*reinterpret_cast<volatile unsigned *>(gbar + kBarPoll) != 0u) it.op = n_ops;
+        // weights never depend on earlier kernels: start streaming before waiting for them
+        for (int i = 0; i < kTcR; ++i) issue();
     }
-    // The stall injection (workspace word kBarPoll, written only by the test hook): no copy.
-    if (*reinterpret_cast<volatile unsigned *>(gbar + kBarPoll) != 0u) it.op = n_ops;
-    // weights never depend on earlier kernels: start streaming before waiting for them
-    for (int i = 0; i < kTcR; ++i) issue();
 
     griddep_wait();
     griddep_launch_dependents();
@@ -343,214 +360,275 @@ vl_tc_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__rest
     tc_fence_after();
     const uint32_t tmem = s_tmem, epoch = s_epoch;
 
-    const int g4 = lane >> 2, t4 = lane & 3;
-    const int hrb = wj >> 1;       // this warp's row block in the MMA unit (rows 32 wj .. 32 wj + 31)
-    const int t0 = 2 * (wj & 1);   // its first 16-row tile there
-    constexpr uint32_t kIdesc = tc_idesc_f16(kTcRows, kTcN);
-    // This lane's places in a stage (64-byte swizzle).  A: row g of tile t0 + r is row
-    // 64 hrb + 16 (t0 + r) + g of the unit, its inputs 8 t4 .. 8 t4 + 7 piece t4 ^ ((g >> 1) & 3);
-    // row g + 8 is 512 bytes further.  B: token 8 wj + g4, the same piece.
-    const uint32_t piece = (uint32_t)(t4 ^ ((g4 >> 1) & 3)) * 16u;
-    const uint32_t a_off = (uint32_t)(64 * hrb + 16 * t0 + g4) * 64u + piece;
-    const uint32_t b_off = (uint32_t)(8 * wj + g4) * 64u + piece;
-    const int xtok = 8 * wj + g4;  // the activation column this lane converts
-    constexpr uint32_t kQuarter = 1u << 16;  // TMEM lane field
-
-    uint32_t k = 0, cb = 0, stage_ctr = 0, slot_ctr = 0;
-    for (int gi = 0; gi < n_ops; ++gi) {
-        const VlOp &o = ops[gi];
-        if (gi > 0) {
-            __syncthreads();
-            if (threadIdx.x == 0) grid_barrier(gbar + kBarCount, (unsigned)gi * G, &s_wc);
-            __syncthreads();
-        }
-        const uint32_t n_kc = o.n_kc;
-        const int64_t in_f = o.in_f, out_f = o.out_f;
-        const uint32_t tag = (partial_epoch24(epoch) << 8) | (uint32_t)(gi & 255);
-        const __nv_bfloat16 *xrow = o.X + (int64_t)(xtok < C ? xtok : 0) * in_f + 8 * t4;
-        // this lane's 8 activations of the half-chunk starting at input col (zero past C or in)
-        auto load_x = [&](int64_t col) {
-            if (xtok >= C || col >= in_f) return make_uint4(0u, 0u, 0u, 0u);
-            if constexpr (MAXOPS > 1) return ldg_cg_v4(xrow + col);
-            else return ldg_nc_v4(xrow + col);
-        };
-        uint4 xcur = make_uint4(0u, 0u, 0u, 0u);
-        bool xpre = false;  // xcur holds the next stage's activations
-        uint32_t lo, hi;
-        tc_range(o, G, b, &lo, &hi);
-
-        // Epilogue of a segment: the pipes' accumulators of its set added in pipe order (this
-        // pipe takes tokens 8 pipe .. 8 pipe + 7, this warp its 32 rows), then Y -- or a tagged
-        // partial when an earlier CTA owns the row group; an owner whose row group runs on into
-        // later CTAs adds their partials in CTA order (only at the end of its range).
-        auto epilogue = [&](const TcSeg &sg) {
-            const uint32_t set = sg.k & 1u;
-            for (uint32_t pp = 0; pp < (uint32_t)kTcPipes; ++pp)
-                slot_wait(smem_u32(&s_done[pp * 2u + set]), (sg.k >> 1) & 1u, &s_wc);
-            tc_fence_after();
-            float v[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = 0.f;
-            for (uint32_t pp = 0; pp < (uint32_t)kTcPipes; ++pp) {
-                if (tc_first_block(pp, sg.cb) >= sg.nb) continue;  // no block of pipe pp here
-                uint32_t r[8];
-                tc_ld8(tmem + (uint32_t)wj * 32u * kQuarter + (pp * 2u + set) * kTcAccCols + 8u * pipe, r);
-                tc_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] += __uint_as_float(r[e]);
+    if (mma_warp) {
+        // ---- a pipe's MMA warp: the pipe's stages in order -------------------------------
+        // (blocking waits are safe here: a pipe's warps never wait on another pipe's MMA warp,
+        // and the epilogue of segment k - 2 that segment k waits for needs only the MMAs of
+        // segments up to k - 2, all issued before)
+        constexpr uint32_t kIdesc = tc_idesc_f16(kTcRows, kTcN);
+        const uint32_t abase0 = astage0, bbase0 = bstage0;
+        uint32_t ctr = 0u, kfree = 1u;  // segments up to kfree need no wait for a free set
+        for (;;) {
+            const uint32_t st = ctr % kTcS;
+            if (!slot_wait(stage0 + 8u * st, (ctr / kTcS) & 1u, &s_wc)) break;
+            const uint32_t meta = *reinterpret_cast<volatile uint32_t *>(&s_meta[pipe * kTcS + st]);
+            if (meta & kTcMetaEnd) break;
+            const uint32_t k = meta >> 4, set = k & 1u;
+            // segment k reuses set k & 1: the epilogue of segment k - 2 must have read it
+            if (k > kfree) {
+                slot_wait(smem_u32(&s_free[set]), ((k >> 1) - 1u) & 1u, &s_wc);
+                kfree = k;
             }
-            tc_fence_before();
+            if (lane == 0) {
+                tc_fence_after();
+                if (meta & kTcMetaMma) {
+                    const uint32_t dcol = tmem + (pipe * 2u + set) * kTcAccCols;
+                    const uint64_t da = tc_sdesc_sw128(abase0 + st * kTcAStage);
+                    const uint64_t db = tc_sdesc_sw128(bbase0 + st * kTcBStage);
+                    const uint32_t acc0 = (meta & kTcMetaFirst) ? 0u : 1u;
+#pragma unroll
+                    for (uint32_t kq = 0; kq < 4; ++kq)  // K step of 16 = 32 bytes = 2 in the start field
+                        tc_mma_f16(dcol, da + 2u * kq, db + 2u * kq, kIdesc, kq ? 1u : acc0);
+                }
+                tc_commit(empty0 + 8u * st);
+                if (meta & kTcMetaSegEnd) tc_commit(smem_u32(&s_done[pipe * 2u + set]));
+            }
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&s_free[set]));
+            ++ctr;
+        }
+        // every tensor-core operation of the pipe complete before the accumulators are released
+        if (lane == 0) {
+            tc_commit(smem_u32(&s_final[pipe]));
+            mbar_wait_ok(smem_u32(&s_final[pipe]), 0u);
+        }
+        __syncwarp();
+    } else {
+        // ---- the pipes: copies, dequantisation, activations, epilogues ----
+        const int g4 = lane >> 2, t4 = lane & 3;
+        const int hrb = wj >> 1;       // this warp's row block in the MMA unit (rows 32 wj .. 32 wj + 31)
+        const int t0 = 2 * (wj & 1);   // its first 16-row tile there
+        // This lane's places in a stage (128-byte swizzle: row R at 128 R, piece c at c ^ (R & 7)).
+        // A: row g of tile t0 + r is R = 64 hrb + 16 (t0 + r) + g (so R & 7 = g), row g + 8 is 1024
+        // bytes further; its inputs 32 hc + 8 t4 .. + 7 (scale block hc) go to piece 2 t4 + hc, so
+        // that the two rows a quarter-warp stores cover eight distinct bank groups.  B: token
+        // n = 8 wj + g4 (n & 7 = g4), the same pieces.  The MMA's k-th 16 inputs (pieces 2k and
+        // 2k + 1) are therefore inputs 8k .. 8k + 7 and 32 + 8k .. 32 + 8k + 7 of the chunk, in A
+        // and B alike.
+        const uint32_t a_row = (uint32_t)(64 * hrb + 16 * t0 + g4) * 128u;
+        const uint32_t b_row = (uint32_t)(8 * wj + g4) * 128u;
+        const uint32_t pc0 = (uint32_t)((2 * t4) ^ g4) * 16u, pc1 = (uint32_t)((2 * t4 + 1) ^ g4) * 16u;
+        const int xtok = 8 * wj + g4;  // the activation column this lane converts
+        constexpr uint32_t kQuarter = 1u << 16;  // TMEM lane field
+        const uint32_t pair_bar = 1u + pipe * 2u + (uint32_t)hrb;  // the two warps of one row block
+        uint32_t k = 0, cb = 0, stage_ctr = 0, slot_ctr = 0;
 
-            const uint32_t rl = 32u * (uint32_t)wj + (uint32_t)lane;
-            const int64_t row = (int64_t)sg.rg * kTcRows + rl;
-            const int c0 = 8 * (int)pipe;
-            const bool owner = sg.s0 == sg.rg * n_kc, whole = sg.s1 == (sg.rg + 1u) * n_kc;
-            if (!owner) {
+        // the next stage of this pipe, once the MMAs that read it last are done
+        auto stage_begin = [&]() {
+            const uint32_t st = stage_ctr % kTcS;
+            if (stage_ctr >= (uint32_t)kTcS) slot_wait(empty0 + 8u * st, ((stage_ctr / kTcS) - 1u) & 1u, &s_wc);
+            return st;
+        };
+        // hands a written stage to the MMA warp
+        auto post = [&](uint32_t st, uint32_t meta) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                if (wj == 0) s_meta[pipe * kTcS + st] = meta;
+                mbar_arrive(stage0 + 8u * st);
+            }
+            ++stage_ctr;
+        };
+
+        for (int gi = 0; gi < n_ops; ++gi) {
+            const VlOp &o = ops[gi];
+            if (gi > 0) {  // the pipes' warps (the MMA warp runs on) order op gi after op gi - 1
+                asm volatile("bar.sync 15, %0;" ::"r"(kTcMmaWarp * 32) : "memory");
+                if (threadIdx.x == 0) grid_barrier(gbar + kBarCount, (unsigned)gi * G, &s_wc);
+                asm volatile("bar.sync 15, %0;" ::"r"(kTcMmaWarp * 32) : "memory");
+            }
+            const uint32_t n_kc = o.n_kc;
+            const int64_t in_f = o.in_f, out_f = o.out_f;
+            const uint32_t tag = (partial_epoch24(epoch) << 8) | (uint32_t)(gi & 255);
+            const __nv_bfloat16 *xrow = o.X + (int64_t)(xtok < C ? xtok : 0) * in_f + 8 * t4;
+            // this lane's 8 activations at input col (zero past C or in)
+            auto load_x = [&](int64_t col) {
+                if (xtok >= C || col >= in_f) return make_uint4(0u, 0u, 0u, 0u);
+                if constexpr (MAXOPS > 1) return ldg_cg_v4(xrow + col);
+                else return ldg_nc_v4(xrow + col);
+            };
+            uint4 xa = make_uint4(0u, 0u, 0u, 0u), xb = xa;  // the next unit's (scale blocks 0, 1)
+            bool xpre = false;
+            uint32_t lo, hi;
+            tc_range(o, G, b, &lo, &hi);
+
+            // Epilogue of a segment: the pipes' accumulators of its set added in pipe order, then
+            // Y -- or a tagged partial when an earlier CTA owns the row group; an owner whose row
+            // group runs on into later CTAs adds their partials in CTA order (only at the end of
+            // its range).  This pipe takes token groups pipe and pipe + kTcPipes (8 columns each).
+            auto epilogue = [&](const TcSeg &sg) {
+                const uint32_t set = sg.k & 1u;
+                for (uint32_t pp = 0; pp < (uint32_t)kTcPipes; ++pp)
+                    slot_wait(smem_u32(&s_done[pp * 2u + set]), (sg.k >> 1) & 1u, &s_wc);
+                tc_fence_after();
+                float v[2][8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    if (c0 + e < C) st_tagged(part + (size_t)b * kTcPartial + (size_t)(c0 + e) * kTcRows + rl, v[e], tag);
-            } else if (row < out_f) {
-                if (!whole) {
-                    const uint32_t b_last = tc_cta_of(o, G, (sg.rg + 1u) * n_kc - 1u);
-                    for (uint32_t bb = b + 1u; bb <= b_last; ++bb) {
-                        const unsigned long long *src = part + (size_t)bb * kTcPartial + rl;
-                        unsigned long long w[8];
+                for (int gq = 0; gq < 2; ++gq) {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            if (c0 + e < C) w[e] = ld_tagged(src + (size_t)(c0 + e) * kTcRows);
+                    for (int e = 0; e < 8; ++e) v[gq][e] = 0.f;
+                    const uint32_t cg = pipe + (uint32_t)gq * kTcPipes;
+                    if (cg >= (uint32_t)(kTcN / 8) || (int)(8 * cg) >= C) continue;
+                    for (uint32_t pp = 0; pp < (uint32_t)kTcPipes; ++pp) {
+                        if (tc_first_block(pp, sg.cb) >= sg.nb) continue;  // no block of pipe pp here
+                        uint32_t r[8];
+                        tc_ld8(tmem + (uint32_t)wj * 32u * kQuarter + (pp * 2u + set) * kTcAccCols + 8u * cg, r);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) v[gq][e] += __uint_as_float(r[e]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&s_free[set]));
+
+                const uint32_t rl = 32u * (uint32_t)wj + (uint32_t)lane;
+                const int64_t row = (int64_t)sg.rg * kTcRows + rl;
+                const bool owner = sg.s0 == sg.rg * n_kc, whole = sg.s1 == (sg.rg + 1u) * n_kc;
+#pragma unroll
+                for (int gq = 0; gq < 2; ++gq) {
+                    const uint32_t cg = pipe + (uint32_t)gq * kTcPipes;
+                    const int c0 = 8 * (int)cg;
+                    if (cg >= (uint32_t)(kTcN / 8) || c0 >= C) continue;
+                    if (!owner) {
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
                             if (c0 + e < C)
-                                v[e] += (uint32_t)(w[e] >> 32) == tag
-                                            ? __uint_as_float((uint32_t)w[e])
-                                            : wait_tagged(src + (size_t)(c0 + e) * kTcRows, tag, &s_wc);
+                                st_tagged(part + (size_t)b * kTcPartial + (size_t)(c0 + e) * kTcRows + rl, v[gq][e], tag);
+                    } else if (row < out_f) {
+                        if (!whole) {
+                            const uint32_t b_last = tc_cta_of(o, G, (sg.rg + 1u) * n_kc - 1u);
+                            for (uint32_t bb = b + 1u; bb <= b_last; ++bb) {
+                                const unsigned long long *src = part + (size_t)bb * kTcPartial + rl;
+                                unsigned long long w[8];
+#pragma unroll
+                                for (int e = 0; e < 8; ++e)
+                                    if (c0 + e < C) w[e] = ld_tagged(src + (size_t)(c0 + e) * kTcRows);
+#pragma unroll
+                                for (int e = 0; e < 8; ++e)
+                                    if (c0 + e < C)
+                                        v[gq][e] += (uint32_t)(w[e] >> 32) == tag
+                                                        ? __uint_as_float((uint32_t)w[e])
+                                                        : wait_tagged(src + (size_t)(c0 + e) * kTcRows, tag, &s_wc);
+                            }
+                        }
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            if (c0 + e < C) o.Y[(int64_t)(c0 + e) * out_f + row] = v[gq][e];
                     }
                 }
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    if (c0 + e < C) o.Y[(int64_t)(c0 + e) * out_f + row] = v[e];
-            }
-        };
+            };
 
-        // Segments in order; the epilogue of each runs after the next one's MMAs are issued
-        // (or at the end of the range), while the next one fills the other accumulator set.
-        TcSeg prev;
-        bool have_prev = false;
-        for (uint32_t s0 = lo, s1;; s0 = s1) {
-            if (s0 >= hi) {
-                if (have_prev) epilogue(prev);
-                break;
-            }
-            const uint32_t rg = s0 / n_kc;
-            s1 = min(hi, (rg + 1u) * n_kc);
-            const uint32_t nb = tc_blocks(s0, s1), set = k & 1u;
-            const uint32_t dcol = tmem + (pipe * 2u + set) * kTcAccCols;
-            // the elected thread waits, before the segment's first MMA or its end, until the
-            // epilogue of segment k - 2 (same set) has read the accumulators
-            bool need_free = k >= 2u;
-            uint32_t accum = 0u;
-            for (uint32_t jb = tc_first_block(pipe, cb); jb < nb; jb += kTcPipes) {
-                const uint32_t u0 = s0 + kTcU * jb, n = min((uint32_t)kTcU, s1 - u0);
-                const uint32_t kc0 = u0 - rg * n_kc;
-                // the pipe's next block, if it belongs to this op: its first activations are
-                // prefetched during this block's last stage
-                int nop;
-                uint32_t nu0, nn;
-                const bool nxt = la.next(pipe, ops, n_ops, G, b, &nop, &nu0, &nn) && nop == gi;
-                const uint32_t slot = slot_ctr % kTcR;
-                // a wait that gave up ends the pipe's copies (the slot may still be filling)
-                if (!slot_wait(full0 + 8u * slot, (slot_ctr / kTcR) & 1u, &s_wc)) it.op = n_ops;
-                const uint8_t *sl = ring + slot * kTcSlotBytes;
-#pragma unroll
-                for (int i = 0; i < kTcU; ++i) {
-                    if (i >= (int)n) break;
-                    const uint8_t *cbase = sl + hrb * (kTcU * kUnitCodeBytes) + i * kUnitCodeBytes + lane * 16;
-                    const uint8_t *sbase = sl + 2 * kTcU * kUnitCodeBytes + hrb * (kTcU * kUnitScaleBytes) +
-                                           i * kUnitScaleBytes + g4 * 8;
-                    uint4 cw[2];
-                    uint2 sc[2];
-#pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        cw[r] = *reinterpret_cast<const uint4 *>(cbase + (t0 + r) * 512);
-                        sc[r] = *reinterpret_cast<const uint2 *>(sbase + (t0 + r) * 64);
+            // Segments in order; the epilogue of each runs after the next one's stages are posted
+            // (or at the end of the range), while the next one fills the other accumulator set.
+            TcSeg prev;
+            bool have_prev = false;
+            for (uint32_t s0 = lo, s1;; s0 = s1) {
+                if (s0 >= hi) {
+                    if (have_prev) epilogue(prev);
+                    break;
+                }
+                const uint32_t rg = s0 / n_kc;
+                s1 = min(hi, (rg + 1u) * n_kc);
+                const uint32_t nb = tc_blocks(s0, s1), kmeta = k << 4;
+                const uint32_t jb0 = tc_first_block(pipe, cb);
+                uint32_t first = kTcMetaFirst;
+                if (jb0 >= nb) post(stage_begin(), kmeta | kTcMetaSegEnd);  // no block of this pipe here
+                for (uint32_t jb = jb0; jb < nb; jb += kTcPipes) {
+                    const uint32_t u0 = s0 + kTcU * jb, n = min((uint32_t)kTcU, s1 - u0);
+                    const uint32_t kc0 = u0 - rg * n_kc;
+                    const bool last_block = jb + kTcPipes >= nb;
+                    // the chunk of the pipe's next block, if it belongs to this op (this segment
+                    // or the next): its activations are loaded during this block's last unit
+                    bool nxt = !last_block;
+                    uint32_t nkc = kc0 + kTcU * kTcPipes;
+                    if (last_block && s1 < hi) {
+                        const uint32_t nb2 = tc_blocks(s1, min(hi, s1 + n_kc)), j2 = tc_first_block(pipe, cb + nb);
+                        nxt = j2 < nb2;
+                        nkc = kTcU * j2;
                     }
+                    const uint32_t slot = slot_ctr % kTcR;
+                    // a wait that gave up ends the pipe's copies (the slot may still be filling)
+                    if (!slot_wait(full0 + 8u * slot, (slot_ctr / kTcR) & 1u, &s_wc)) it.op = n_ops;
+                    const uint8_t *sl = ring + slot * kTcSlotBytes;
 #pragma unroll
-                    for (int hc = 0; hc < 2; ++hc) {
-                        // this stage's activations (prefetched by the previous stage, else now),
-                        // then the next stage's
-                        if (!xpre) xcur = load_x((int64_t)(kc0 + i) * kChunk + 32 * hc);
-                        const uint4 xv = xcur;
+                    for (int i = 0; i < kTcU; ++i) {
+                        if (i >= (int)n) break;
+                        if (!xpre) {
+                            xa = load_x((int64_t)(kc0 + i) * kChunk);
+                            xb = load_x((int64_t)(kc0 + i) * kChunk + 32);
+                        }
+                        const uint4 xva = xa, xvb = xb;
                         xpre = true;
-                        if (hc == 0)
-                            xcur = load_x((int64_t)(kc0 + i) * kChunk + 32);
-                        else if (i + 1 < (int)n)
-                            xcur = load_x((int64_t)(kc0 + i + 1) * kChunk);
-                        else if (nxt)
-                            xcur = load_x((int64_t)(nu0 - (nu0 / n_kc) * n_kc) * kChunk);
-                        else
+                        if (i + 1 < (int)n) {
+                            xa = load_x((int64_t)(kc0 + i + 1) * kChunk);
+                            xb = load_x((int64_t)(kc0 + i + 1) * kChunk + 32);
+                        } else if (nxt) {
+                            const int64_t c = (int64_t)nkc * kChunk;
+                            xa = load_x(c);
+                            xb = load_x(c + 32);
+                        } else {
                             xpre = false;
-                        const uint32_t st = stage_ctr % kTcS;
-                        if (stage_ctr >= (uint32_t)kTcS)
-                            slot_wait(empty0 + 8u * st, ((stage_ctr / kTcS) - 1u) & 1u, &s_wc);
-                        const uint32_t abase = astage0 + st * kTcAStage, bbase = bstage0 + st * kTcBStage;
-                        const uint32_t sel = hc ? 0x3232u : 0x1010u;  // block hc's scale in both halves
+                        }
+                        const uint8_t *cbase = sl + hrb * (kTcU * kUnitCodeBytes) + i * kUnitCodeBytes + lane * 16;
+                        const uint8_t *sbase = sl + 2 * kTcU * kUnitCodeBytes + hrb * (kTcU * kUnitScaleBytes) +
+                                               i * kUnitScaleBytes + g4 * 8;
+                        uint4 cw[2];
+                        uint2 sc[2];
 #pragma unroll
                         for (int r = 0; r < 2; ++r) {
-                            const uint32_t w0 = hc ? cw[r].z : cw[r].x, w1 = hc ? cw[r].w : cw[r].y;
-                            const uint32_t sg = __byte_perm(sc[r].x, sc[r].x, sel);
-                            const uint32_t sg8 = __byte_perm(sc[r].y, sc[r].y, sel);
-                            uint32_t o0[4], o1[4];
-                            dequant_word_f16(w0, sg, sg8, o0);
-                            dequant_word_f16(w1, sg, sg8, o1);
-                            st_shared_v4(abase + a_off + r * 1024u, o0[0], o0[2], o1[0], o1[2]);
-                            st_shared_v4(abase + a_off + r * 1024u + 512u, o0[1], o0[3], o1[1], o1[3]);
+                            cw[r] = *reinterpret_cast<const uint4 *>(cbase + (t0 + r) * 512);
+                            sc[r] = *reinterpret_cast<const uint2 *>(sbase + (t0 + r) * 64);
                         }
-                        st_shared_v4(bbase + b_off, bf16x2_to_f16x2(xv.x), bf16x2_to_f16x2(xv.y),
-                                     bf16x2_to_f16x2(xv.z), bf16x2_to_f16x2(xv.w));
-                        fence_proxy_async_smem();
-                        asm volatile("bar.sync %0, %1;" ::"r"(1 + pipe), "r"(kTcPipeWarps * 32) : "memory");
-                        if (elected) {
-                            if (need_free) {
-                                slot_wait(smem_u32(&s_free[set]), ((k >> 1) - 1u) & 1u, &s_wc);
-                                need_free = false;
-                            }
-                            tc_fence_after();
+                        const uint32_t st = stage_begin();
+                        const uint32_t abase = astage0 + st * kTcAStage, bbase = bstage0 + st * kTcBStage;
 #pragma unroll
-                            for (uint32_t kq = 0; kq < 2; ++kq)
-                                tc_mma_f16(dcol, tc_sdesc_sw64(abase + 32u * kq), tc_sdesc_sw64(bbase + 32u * kq),
-                                           kIdesc, accum | kq);
-                            tc_commit(empty0 + 8u * st);
-                        }
-                        accum = 1u;
-                        ++stage_ctr;
+                        for (int r = 0; r < 2; ++r)
+#pragma unroll
+                            for (int hc = 0; hc < 2; ++hc) {
+                                const uint32_t sel = hc ? 0x3232u : 0x1010u;  // block hc's scale, both halves
+                                const uint32_t sg = __byte_perm(sc[r].x, sc[r].x, sel);
+                                const uint32_t sg8 = __byte_perm(sc[r].y, sc[r].y, sel);
+                                uint32_t o0[4], o1[4];
+                                dequant_word_f16(hc ? cw[r].z : cw[r].x, sg, sg8, o0);
+                                dequant_word_f16(hc ? cw[r].w : cw[r].y, sg, sg8, o1);
+                                const uint32_t at = abase + a_row + (uint32_t)r * 2048u + (hc ? pc1 : pc0);
+                                st_shared_v4(at, o0[0], o0[2], o1[0], o1[2]);
+                                st_shared_v4(at + 1024u, o0[1], o0[3], o1[1], o1[3]);
+                            }
+                        st_shared_v4(bbase + b_row + pc0, bf16x2_to_f16x2(xva.x), bf16x2_to_f16x2(xva.y),
+                                     bf16x2_to_f16x2(xva.z), bf16x2_to_f16x2(xva.w));
+                        st_shared_v4(bbase + b_row + pc1, bf16x2_to_f16x2(xvb.x), bf16x2_to_f16x2(xvb.y),
+                                     bf16x2_to_f16x2(xvb.z), bf16x2_to_f16x2(xvb.w));
+                        const bool seg_end = last_block && i + 1 == (int)n;
+                        post(st, kmeta | kTcMetaMma | first | (seg_end ? kTcMetaSegEnd : 0u));
+                        first = 0u;
                     }
+                    // both warps reading this row block's part of the slot are done with it: refill
+                    asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+                    issue();
+                    ++slot_ctr;
                 }
-                // every warp of the pipe has read the slot (the barrier above): refill it
-                issue();
-                ++slot_ctr;
+                if (have_prev) epilogue(prev);
+                prev = TcSeg{s0, s1, rg, cb, nb, k};
+                have_prev = true;
+                cb += nb;
+                ++k;
             }
-            if (elected) {
-                if (need_free) slot_wait(smem_u32(&s_free[set]), ((k >> 1) - 1u) & 1u, &s_wc);
-                tc_commit(smem_u32(&s_done[pipe * 2u + set]));
-            }
-            if (have_prev) epilogue(prev);
-            prev = TcSeg{s0, s1, rg, cb, nb, k};
-            have_prev = true;
-            cb += nb;
-            ++k;
         }
-    }
-
-    // every tensor-core operation of the pipe is complete before the accumulators are released
-    if (elected) {
-        tc_commit(smem_u32(&s_final[pipe]));
-        mbar_wait_ok(smem_u32(&s_final[pipe]), 0u);
+        post(stage_begin(), kTcMetaEnd);  // this pipe has no more stages
     }
     // after a give-up: wait (bounded) for copies that may still be in flight -- the last part
     // this warp copied into each slot -- so that none lands in shared memory after the CTA exits
-    if (lane == 0 && wait_stopped(&s_wc)) {
+    if (!mma_warp && lane == 0 && wait_stopped(&s_wc)) {
         for (uint32_t kk = c_issued > (uint32_t)kTcR ? c_issued - kTcR : 0u; kk < c_issued; ++kk)
             mbar_wait_ok(full0 + 8u * (kk % kTcR), (kk / kTcR) & 1u, kDrainLimit);
     }
