@@ -104,13 +104,22 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def kernel_source_sha16() -> str:
+    """First 16 hex digits of the sha256 of the verify-linear translation unit's sources
+    (verify_linear.cu followed by the headers it includes from the package)."""
+    d = os.path.join(ROOT, "speculative_decoding_verify_06_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in ("verify_linear.cu", "verify_linear_tc.cuh", "svd_common.cuh"):
+        h.update(open(os.path.join(d, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def kernel_traffic():
     """DRAM traffic per launch of the stack's verify-linear kernel from the committed ncu
     summary, if it was taken on the current kernel source (else None)."""
-    src = os.path.join(ROOT, "speculative_decoding_verify_06_gb300", "csrc", "verify_linear.cu")
     prof = os.path.join(ROOT, "profiles", "vl_stream_kernel_27b_stack_c4.txt")
     try:
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        sha = kernel_source_sha16()
         txt = open(prof).read()
         m_sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", txt)
         m_tr = re.search(r"dram_bytes_per_stack_launch_avg:\s*([0-9.eE+]+)", txt)
@@ -268,19 +277,20 @@ def _gpu_id(dev) -> str:
         return str(dev.index or 0)
 
 
-SWEEP_C = (1, 2, 4, 6, 8, 32)
+SWEEP_C = (1, 2, 4, 6, 8, 16, 24, 32)
 
 
 def column_sweep(vp, dev, steps, tokens_per_pass, peak):
     """The stack alone (one chain launch, same resident weights) at every window width of the
-    sweep; C = 32 is the batched case of 8 sequences x 4 columns."""
+    sweep; C = 32 is the batched case of 8 sequences x 4 columns.  Widths above 16 run the
+    tcgen05 kernel; "32_fragment" is C = 32 on the warp-level mma.sync kernel for comparison."""
     import torch
 
-    from speculative_decoding_verify_06_gb300 import stack
+    from speculative_decoding_verify_06_gb300 import stack, svd
     s = torch.cuda.current_stream(dev)
     out = {}
-    for C in SWEEP_C:
-        view = stack.ColumnsView(vp, C, seed=C).capture()
+    for C, flags, name in [(c, 0, str(c)) for c in SWEEP_C] + [(32, svd.SVD_F_FRAGMENT_MMA, "32_fragment")]:
+        view = stack.ColumnsView(vp, C, seed=C, flags=flags).capture()
         for _ in range(3):
             view.launch(s)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -292,7 +302,8 @@ def column_sweep(vp, dev, steps, tokens_per_pass, peak):
         torch.cuda.synchronize(dev)
         ms = e0.elapsed_time(e1) / steps
         gbs = view.stack_bytes() / ms / 1e6
-        out[str(C)] = {"stack_ms": ms, "passes_per_s": 1000.0 / ms, "gb_s": gbs, "frac": gbs / peak}
+        out[name] = {"stack_ms": ms, "passes_per_s": 1000.0 / ms, "gb_s": gbs, "frac": gbs / peak,
+                     "kernel": "tcgen05" if (C > 16 and not flags) else "mma.sync"}
         del view
         torch.cuda.empty_cache()
     if "32" in out and "4" in out and tokens_per_pass:
