@@ -676,7 +676,9 @@ def run_svd(args, rank, world, local_rank):
                 "copies": ("per step, from pinned host memory: the first layer's input (the "
                            "embedded window), the drafter's q rows and the drafts; back: the "
                            "emitted tokens, their count and the status word")},
-        "gpu_launches": K * ((n_launch if args.no_chain else 1) + (1 + 4 + 1 if vp.head else 0)),
+        # per step: the stack (one chain launch, or one per matrix), the lm_head, the sampler
+        # (one cluster launch) and the acceptance
+        "gpu_launches": K * ((n_launch if args.no_chain else 1) + (1 + 1 + 1 if vp.head else 0)),
         "clocks": clk.summary(),
     }
     if not args.no_sweep and not args.stack_only:
