@@ -146,8 +146,10 @@ int svd_unpack_weights(const svd_qweight *src_native, void *dst_codes, void *dst
  *   svd_verify_linear_workspace_bytes() bytes that is ZERO-FILLED before its first use (it
  *   holds barrier counters, which every call returns to zero, a launch epoch, a status word,
  *   and partial sums of row blocks split between CTAs, tagged with the launch that wrote
- *   them), so one zeroed workspace serves any number of calls issued in stream order, for any
- *   matrix shape and C; calls that may run concurrently need separate workspaces.  Every wait
+ *   them; for 17..32 columns also the fp16 B tiles of the activations, 4 KB per 64 inputs), so
+ *   one zeroed workspace serves any number of calls issued in stream order, for any matrix shape
+ *   and C whose size it covers (up to 16 columns the size does not depend on the shape); calls
+ *   that may run concurrently need separate workspaces.  Every wait
  *   inside the kernel is bounded: one that gives up leaves Y undefined and records itself in
  *   the workspace (svd_verify_status).
  *   CANONICAL weights run the CUDA-core warp-shuffle kernel (no workspace; needs
@@ -210,6 +212,8 @@ int svd_verify_inject_stall(void *workspace, size_t workspace_bytes, uint32_t po
  * process exits.  It calls no allocator of any kind.
  *   - out_features <= SVD_NOALLOC_MAX_OUT_FEATURES and at most 160 SMs, else
  *     SVD_ERR_UNSUPPORTED (other limits as for svd_verify_linear).
+ *   - For 17..32 columns it runs the warp-level kernel (as svd_verify_linear with
+ *     SVD_F_FRAGMENT_MMA): the array has no room for the tensor-core kernel's B tiles.
  *   - The first call on each device looks up the array's device address (with that device
  *     current); make that first call before any stream capture (a first call inside a capture
  *     returns SVD_ERR_UNSUPPORTED).  Every later call outside a capture looks it up again, so a

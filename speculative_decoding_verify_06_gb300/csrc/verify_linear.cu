@@ -800,10 +800,12 @@ constexpr int kChainMax = 256;    // ops per chain launch (kernel parameters, ~1
 static int ntiles_for(int C) { return C <= 8 ? 1 : (C <= 16 ? 2 : 4); }
 
 // Workspace: [partial slots: SMs x kMaxCtasPerSm CTAs x kPartialMax tagged 64-bit entries]
-//            [barrier words, 256 bytes: grid-barrier counter, exit counter, launch epoch].
-// It has the same size and layout for every matrix and C, so calls of any shape can share
-// one zero-filled workspace; every launch returns the counters to zero and advances the
-// epoch that tags its partials.
+//            [barrier words, 256 bytes: grid-barrier counter, exit counter, launch epoch]
+//            [17..32 columns only: the fp16 B tiles of the op's activations, 4 KB per 64
+//             inputs of the widest op, 1024-byte aligned].
+// Up to 16 columns it has the same size for every matrix, so calls of any shape can share one
+// zero-filled workspace; every launch returns the counters to zero and advances the epoch that
+// tags its partials.
 static size_t partial_entries() { return (size_t)sm_count() * kMaxCtasPerSm * kPartialMax; }
 static size_t partial_region_bytes() {
     return align_up((size_t)sm_count() * kMaxCtasPerSm * kPartialMax * sizeof(unsigned long long),
@@ -811,12 +813,18 @@ static size_t partial_region_bytes() {
 }
 constexpr size_t kBarrierBytes = 256;
 static_assert((kBarEpoch + 1) * sizeof(unsigned) <= kBarrierBytes, "barrier words");
+// B tiles of the tensor-core kernel (C > 16), after the barrier words; 1 KB of alignment slack
+static size_t tc_xb_region(int64_t max_in_f, int C) {
+    return C > 16 ? tc_xb_bytes(max_in_f) + 1024 : 0;
+}
+static uint8_t *tc_xb_ptr(void *ws) {
+    const uintptr_t p = reinterpret_cast<uintptr_t>(ws) + partial_region_bytes() + kBarrierBytes;
+    return reinterpret_cast<uint8_t *>((p + 1023) & ~(uintptr_t)1023);
+}
 
 size_t vl_workspace_bytes(int64_t in_f, int64_t out_f, int C) {
-    (void)in_f;
     (void)out_f;
-    (void)C;
-    return partial_region_bytes() + kBarrierBytes;
+    return partial_region_bytes() + kBarrierBytes + tc_xb_region(in_f, C);
 }
 
 template <int NT, int NW, int TW, int R, int U, int MAXOPS>
@@ -926,7 +934,7 @@ static cudaError_t launch_tc(const VlOps<MAXOPS> &P, void *ws, bool pdl, bool co
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, kern, P, part, (uint32_t)partial_entries(), gbar);
+    return cudaLaunchKernelEx(&cfg, kern, P, part, (uint32_t)partial_entries(), gbar, tc_xb_ptr(ws));
 }
 
 // 17..32 columns run on the tensor-core kernel unless the caller asks for the fragment kernel.
@@ -1026,10 +1034,10 @@ int verify_linear(const svd_qweight *W, const void *X, int C, float *Y, void *ws
 }
 
 size_t chain_workspace_bytes(const svd_linear_op *ops, int n_ops, int C) {
-    (void)ops;
-    (void)n_ops;
-    (void)C;
-    return partial_region_bytes() + kBarrierBytes;
+    int64_t max_in = 0;
+    for (int i = 0; ops && i < n_ops; ++i)
+        max_in = ops[i].W.in_features > max_in ? ops[i].W.in_features : max_in;
+    return partial_region_bytes() + kBarrierBytes + tc_xb_region(max_in, C);
 }
 
 int verify_chain(const svd_linear_op *ops, int n_ops, int C, void *ws, size_t ws_bytes, int flags,
@@ -1203,7 +1211,9 @@ int verify_linear_noalloc(const svd_qweight *W, const void *X, int C, float *Y, 
     P.n = 1;
     P.C = C;
     P.op[0] = make_op(W, X, Y);
-    SVD_CUDA_TRY(launch_ops(P, base, (flags & SVD_F_PDL) != 0, stream, (flags & SVD_F_FRAGMENT_MMA) != 0));
+    // above 16 columns the fixed array has no room for the tensor-core kernel's B tiles: the
+    // warp-level kernel runs instead
+    SVD_CUDA_TRY(launch_ops(P, base, (flags & SVD_F_PDL) != 0, stream, true));
     return SVD_OK;
 }
 

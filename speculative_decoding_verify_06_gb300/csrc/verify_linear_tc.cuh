@@ -47,22 +47,36 @@ constexpr int kTcMmaWarp = kTcPipes * kTcPipeWarps;   // first of the pipes' MMA
 constexpr int kTcThreads = (kTcMmaWarp + kTcPipes) * 32;
 constexpr int kTcU = 2;               // units per block (per bulk copy)
 constexpr int kTcR = 2;               // ring slots per pipe
-constexpr int kTcS = 2;               // A/B stages per pipe
+constexpr int kTcS = 2;               // A stages per pipe
 constexpr int kTcN = 32;              // MMA N: activation columns
 constexpr int kTcRows = 2 * kRowsPerBlock;            // MMA M: 128 weight rows
-constexpr int kTcSlotBytes = 2 * kTcU * kUnitBytes;   // codes rb0, codes rb1, scales rb0, rb1
 constexpr int kTcAStage = kTcRows * kChunk * 2;       // 128 rows x 64 inputs fp16
-constexpr int kTcBStage = kTcN * kChunk * 2;          // 32 tokens x 64 inputs fp16
-// per pipe: the stages first (1024-byte aligned for the swizzle), then the ring
-constexpr int kTcPipeBytes = kTcS * (kTcAStage + kTcBStage) + kTcR * kTcSlotBytes;
+constexpr int kTcBTile = kTcN * kChunk * 2;           // 32 tokens x 64 inputs fp16 (one chunk)
+// a ring slot: the B tiles of the block's units, then the codes of its two row blocks, then
+// their scales
+constexpr int kTcSlotCodes = kTcU * kTcBTile;
+constexpr int kTcSlotScales = kTcSlotCodes + 2 * kTcU * kUnitCodeBytes;
+constexpr int kTcSlotBytes = kTcSlotScales + 2 * kTcU * kUnitScaleBytes;
+// per pipe: the A stages, then the ring (all 1024-byte aligned for the swizzle)
+constexpr int kTcPipeBytes = kTcS * kTcAStage + kTcR * kTcSlotBytes;
 constexpr int kTcAccCols = kTcN;                      // TMEM columns per accumulator
 constexpr uint32_t kTcTmemCols = 256;                 // kTcPipes * 2 * kTcAccCols, rounded to 2^k
 constexpr int kTcPartial = kTcRows * kTcN;            // entries of a CTA's partial
 static_assert(kTcPartial <= 2 * kPartialMax, "a tensor-core CTA uses two stream-K partial slots");
 static_assert(kRowsPerBlock == 64 && kChunk == 64, "the MMA unit is two 64-row native blocks x 64 inputs");
 static_assert(kTcPipes * 2 * kTcAccCols <= (int)kTcTmemCols, "accumulators fit the allocation");
-static_assert(kTcPipeBytes % 1024 == 0 && (kTcAStage % 1024) == 0 && (kTcBStage % 1024) == 0,
-              "stages stay on the swizzle's 1024-byte period");
+static_assert(kTcPipeBytes % 1024 == 0 && kTcAStage % 1024 == 0 && kTcSlotBytes % 1024 == 0 &&
+                  kTcBTile % 1024 == 0,
+              "stages and B tiles stay on the swizzle's 1024-byte period");
+
+// The fp16 B layout of an op's activations (one 4 KB tile per 64-input chunk, written once per
+// op into the workspace and bulk-copied with each block's weights): token n at 128 n, the
+// inputs 32 h + 8 t .. + 7 of the chunk (scale block h) in piece 2 t + h, stored at piece
+// (2 t + h) ^ (n & 7) -- the 128-byte swizzle, and the permutation that makes the A stores
+// conflict-free.
+__host__ __device__ constexpr size_t tc_xb_bytes(int64_t in_f) {
+    return (size_t)((in_f + kChunk - 1) / kChunk) * kTcBTile;
+}
 
 template <int MAXOPS>
 struct TcCfg {
@@ -245,19 +259,25 @@ constexpr uint32_t kTcMetaMma = 1u;     // a unit: issue its four MMAs
 constexpr uint32_t kTcMetaFirst = 2u;   // the pipe's first unit of the segment: start the accumulator
 constexpr uint32_t kTcMetaSegEnd = 4u;  // the pipe's last stage of the segment: signal its accumulator
 constexpr uint32_t kTcMetaEnd = 8u;     // the pipe has no more stages
+constexpr uint32_t kTcMetaBlockEnd = 16u;  // the block's last unit: its ring slot's B tiles are free after
+constexpr int kTcMetaSlotShift = 5;     // ring slot of the unit (its B tile), 1 bit
+constexpr int kTcMetaUnitShift = 6;     // unit within the block, 1 bit
+constexpr int kTcMetaKShift = 8;        // segment number
 
 template <int MAXOPS>
 __global__ void __launch_bounds__(kTcThreads, 1)
 vl_tc_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__restrict__ part,
-             uint32_t part_entries, unsigned *__restrict__ gbar) {
+             uint32_t part_entries, unsigned *__restrict__ gbar, uint8_t *__restrict__ xb) {
     extern __shared__ __align__(128) uint8_t smem[];  // aligned to 1 KB below
     __shared__ __align__(8) uint64_t s_full[kTcPipes * kTcR];   // a ring slot's copies landed
     __shared__ __align__(8) uint64_t s_stage[kTcPipes * kTcS];  // a stage is written (its 4 warps)
+    __shared__ __align__(8) uint64_t s_bfree[kTcPipes * kTcR];  // a slot's B tiles have been read
     __shared__ __align__(8) uint64_t s_empty[kTcPipes * kTcS];  // a stage's MMAs have read it
     __shared__ __align__(8) uint64_t s_done[kTcPipes * 2];      // a pipe's MMAs of a segment (per set)
     __shared__ __align__(8) uint64_t s_free[2];                 // a set's accumulators have been read
     __shared__ __align__(8) uint64_t s_final[kTcPipes];         // every MMA of a pipe, at exit
     __shared__ uint32_t s_meta[kTcPipes * kTcS];
+    __shared__ uint32_t s_bblk[kTcPipes * kTcR][3];             // a slot's block: op, first chunk, units
     __shared__ uint32_t s_tmem, s_epoch, s_last;
     __shared__ WaitCtl s_wc;
     uint8_t *const sm0 = smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u);
@@ -270,9 +290,8 @@ vl_tc_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__rest
     const uint32_t pipe = mma_warp ? (uint32_t)(warp - kTcMmaWarp) : (uint32_t)warp / kTcPipeWarps;
     const int wj = warp % kTcPipeWarps;  // warp in the pipe = its TMEM lane quarter
     const uint32_t G = gridDim.x, b = blockIdx.x;
-    uint8_t *const ring = sm0 + (size_t)pipe * kTcPipeBytes + kTcS * (kTcAStage + kTcBStage);
+    uint8_t *const ring = sm0 + (size_t)pipe * kTcPipeBytes + kTcS * kTcAStage;
     const uint32_t astage0 = smem_u32(sm0) + pipe * kTcPipeBytes;
-    const uint32_t bstage0 = astage0 + kTcS * kTcAStage;
     const uint32_t ring0 = smem_u32(ring);
     const uint32_t full0 = smem_u32(&s_full[pipe * kTcR]);
     const uint32_t stage0 = smem_u32(&s_stage[pipe * kTcS]);
@@ -285,7 +304,10 @@ vl_tc_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__rest
         for (int i = threadIdx.x; i < n_ops * (int)(sizeof(VlOp) / 8); i += kTcThreads) dst[i] = src[i];
     }
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kTcPipes * kTcR; ++i) mbar_init(smem_u32(&s_full[i]), kTcPipeWarps);
+        for (int i = 0; i < kTcPipes * kTcR; ++i) {
+            mbar_init(smem_u32(&s_full[i]), kTcPipeWarps + 1);  // four weight parts and the B tiles
+            mbar_init(smem_u32(&s_bfree[i]), 1);
+        }
         for (int i = 0; i < kTcPipes * kTcS; ++i) {
             mbar_init(smem_u32(&s_stage[i]), kTcPipeWarps);
             mbar_init(smem_u32(&s_empty[i]), 1);
@@ -301,29 +323,48 @@ vl_tc_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__rest
     // Copy cursor of a pipe (uniform across its warps).  Warp wj copies one part of every block:
     // the codes (wj even) or the scales (wj odd) of row block 2q + (wj >> 1), which are read by
     // warps wj & ~1 and wj | 1 only; a row block past the matrix's end is not copied (its rows
-    // are never stored).
+    // are never stored).  Warp 1 also copies the block's B tiles, but only once its op's
+    // activations have been converted (the weights of later ops stream ahead of that) and the
+    // MMAs of the block that used the slot before have read its B tiles.
     TcIter it;
     it.start();
-    uint32_t c_issued = 0;
+    uint32_t c_issued = 0, b_next = 0;  // blocks whose weights / B tiles have been issued
+    int conv_op = -1;                   // ops up to this one have their B layout in the workspace
+    auto issue_b = [&]() {
+        while (b_next < c_issued) {
+            const uint32_t slot = b_next % kTcR;
+            const uint32_t *bi = s_bblk[pipe * kTcR + slot];
+            if ((int)bi[0] > conv_op) return;
+            if (b_next >= (uint32_t)kTcR)
+                slot_wait(smem_u32(&s_bfree[pipe * kTcR + slot]), ((b_next / kTcR) - 1u) & 1u, &s_wc);
+            if (lane == 0) {
+                const uint32_t bar = full0 + 8u * slot, bytes = bi[2] * (uint32_t)kTcBTile;
+                mbar_expect_tx(bar, bytes);
+                bulk_g2s(ring0 + slot * kTcSlotBytes, xb + (size_t)bi[1] * kTcBTile, bytes, bar);
+            }
+            ++b_next;
+        }
+    };
     auto issue = [&]() {
         int op;
         uint32_t u0, n, rg;
         if (!it.next(pipe, ops, n_ops, G, b, &op, &u0, &n, &rg)) return;
         const VlOp &o = ops[op];
         const uint32_t slot = c_issued % kTcR, bar = full0 + 8u * slot;
+        const uint32_t kc = u0 - rg * o.n_kc;
         if (lane == 0) {
             const uint32_t h = (uint32_t)wj >> 1, rb = 2u * rg + h;
             if ((uint64_t)rb * o.n_kc < o.n_units) {
-                const size_t nu = (size_t)rb * o.n_kc + (u0 - rg * o.n_kc);  // native unit index
+                const size_t nu = (size_t)rb * o.n_kc + kc;  // native unit index
                 uint32_t dst, bytes;
                 const uint8_t *src;
                 if ((wj & 1) == 0) {
                     bytes = n * kUnitCodeBytes;
-                    dst = ring0 + slot * kTcSlotBytes + h * (kTcU * kUnitCodeBytes);
+                    dst = ring0 + slot * kTcSlotBytes + kTcSlotCodes + h * (kTcU * kUnitCodeBytes);
                     src = o.codes + nu * kUnitCodeBytes;
                 } else {
                     bytes = n * kUnitScaleBytes;
-                    dst = ring0 + slot * kTcSlotBytes + 2u * kTcU * kUnitCodeBytes + h * (kTcU * kUnitScaleBytes);
+                    dst = ring0 + slot * kTcSlotBytes + kTcSlotScales + h * (kTcU * kUnitScaleBytes);
                     src = o.scales + nu * kUnitScaleBytes;
                 }
                 mbar_expect_tx(bar, bytes);
@@ -331,8 +372,15 @@ vl_tc_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__rest
             } else {
                 mbar_arrive(bar);
             }
+            if (wj == 1) {
+                s_bblk[pipe * kTcR + slot][0] = (uint32_t)op;
+                s_bblk[pipe * kTcR + slot][1] = kc;
+                s_bblk[pipe * kTcR + slot][2] = n;
+            }
         }
+        __syncwarp();
         ++c_issued;
+        if (wj == 1) issue_b();
     };
     if (!mma_warp) {
         // The stall injection (workspace word kBarPoll, written only by the test hook): no copy.
@@ -366,14 +414,15 @@ vl_tc_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__rest
         // and the epilogue of segment k - 2 that segment k waits for needs only the MMAs of
         // segments up to k - 2, all issued before)
         constexpr uint32_t kIdesc = tc_idesc_f16(kTcRows, kTcN);
-        const uint32_t abase0 = astage0, bbase0 = bstage0;
+        const uint32_t abase0 = astage0, ring00 = ring0;
         uint32_t ctr = 0u, kfree = 1u;  // segments up to kfree need no wait for a free set
         for (;;) {
             const uint32_t st = ctr % kTcS;
             if (!slot_wait(stage0 + 8u * st, (ctr / kTcS) & 1u, &s_wc)) break;
             const uint32_t meta = *reinterpret_cast<volatile uint32_t *>(&s_meta[pipe * kTcS + st]);
             if (meta & kTcMetaEnd) break;
-            const uint32_t k = meta >> 4, set = k & 1u;
+            const uint32_t k = meta >> kTcMetaKShift, set = k & 1u;
+            const uint32_t slot = (meta >> kTcMetaSlotShift) & 1u, unit = (meta >> kTcMetaUnitShift) & 1u;
             // segment k reuses set k & 1: the epilogue of segment k - 2 must have read it
             if (k > kfree) {
                 slot_wait(smem_u32(&s_free[set]), ((k >> 1) - 1u) & 1u, &s_wc);
@@ -384,13 +433,14 @@ vl_tc_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__rest
                 if (meta & kTcMetaMma) {
                     const uint32_t dcol = tmem + (pipe * 2u + set) * kTcAccCols;
                     const uint64_t da = tc_sdesc_sw128(abase0 + st * kTcAStage);
-                    const uint64_t db = tc_sdesc_sw128(bbase0 + st * kTcBStage);
+                    const uint64_t db = tc_sdesc_sw128(ring00 + slot * kTcSlotBytes + unit * kTcBTile);
                     const uint32_t acc0 = (meta & kTcMetaFirst) ? 0u : 1u;
 #pragma unroll
                     for (uint32_t kq = 0; kq < 4; ++kq)  // K step of 16 = 32 bytes = 2 in the start field
                         tc_mma_f16(dcol, da + 2u * kq, db + 2u * kq, kIdesc, kq ? 1u : acc0);
                 }
                 tc_commit(empty0 + 8u * st);
+                if (meta & kTcMetaBlockEnd) tc_commit(smem_u32(&s_bfree[pipe * kTcR + slot]));
                 if (meta & kTcMetaSegEnd) tc_commit(smem_u32(&s_done[pipe * 2u + set]));
             }
             __syncwarp();
@@ -410,14 +460,12 @@ vl_tc_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__rest
         // This lane's places in a stage (128-byte swizzle: row R at 128 R, piece c at c ^ (R & 7)).
         // A: row g of tile t0 + r is R = 64 hrb + 16 (t0 + r) + g (so R & 7 = g), row g + 8 is 1024
         // bytes further; its inputs 32 hc + 8 t4 .. + 7 (scale block hc) go to piece 2 t4 + hc, so
-        // that the two rows a quarter-warp stores cover eight distinct bank groups.  B: token
-        // n = 8 wj + g4 (n & 7 = g4), the same pieces.  The MMA's k-th 16 inputs (pieces 2k and
-        // 2k + 1) are therefore inputs 8k .. 8k + 7 and 32 + 8k .. 32 + 8k + 7 of the chunk, in A
-        // and B alike.
+        // that the two rows a quarter-warp stores cover eight distinct bank groups.  The B tiles
+        // use the same pieces (tc_xb_bytes), so the MMA's k-th 16 inputs (pieces 2k and 2k + 1)
+        // are inputs 8k .. 8k + 7 and 32 + 8k .. 32 + 8k + 7 of the chunk in A and B alike.
         const uint32_t a_row = (uint32_t)(64 * hrb + 16 * t0 + g4) * 128u;
-        const uint32_t b_row = (uint32_t)(8 * wj + g4) * 128u;
         const uint32_t pc0 = (uint32_t)((2 * t4) ^ g4) * 16u, pc1 = (uint32_t)((2 * t4 + 1) ^ g4) * 16u;
-        const int xtok = 8 * wj + g4;  // the activation column this lane converts
+        uint32_t nbar = 0;  // grid barriers passed
         constexpr uint32_t kQuarter = 1u << 16;  // TMEM lane field
         const uint32_t pair_bar = 1u + pipe * 2u + (uint32_t)hrb;  // the two warps of one row block
         uint32_t k = 0, cb = 0, stage_ctr = 0, slot_ctr = 0;
@@ -439,25 +487,44 @@ vl_tc_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__rest
             ++stage_ctr;
         };
 
+        // a barrier of the pipes' warps (the MMA warps run on), then of the grid
+        auto grid_sync = [&]() {
+            asm volatile("bar.sync 15, %0;" ::"r"(kTcMmaWarp * 32) : "memory");
+            ++nbar;
+            if (threadIdx.x == 0) grid_barrier(gbar + kBarCount, nbar * G, &s_wc);
+            asm volatile("bar.sync 15, %0;" ::"r"(kTcMmaWarp * 32) : "memory");
+        };
         for (int gi = 0; gi < n_ops; ++gi) {
             const VlOp &o = ops[gi];
-            if (gi > 0) {  // the pipes' warps (the MMA warp runs on) order op gi after op gi - 1
-                asm volatile("bar.sync 15, %0;" ::"r"(kTcMmaWarp * 32) : "memory");
-                if (threadIdx.x == 0) grid_barrier(gbar + kBarCount, (unsigned)gi * G, &s_wc);
-                asm volatile("bar.sync 15, %0;" ::"r"(kTcMmaWarp * 32) : "memory");
-            }
+            if (gi > 0) grid_sync();  // op gi - 1 has written its outputs
             const uint32_t n_kc = o.n_kc;
             const int64_t in_f = o.in_f, out_f = o.out_f;
             const uint32_t tag = (partial_epoch24(epoch) << 8) | (uint32_t)(gi & 255);
-            const __nv_bfloat16 *xrow = o.X + (int64_t)(xtok < C ? xtok : 0) * in_f + 8 * t4;
-            // this lane's 8 activations at input col (zero past C or in)
-            auto load_x = [&](int64_t col) {
-                if (xtok >= C || col >= in_f) return make_uint4(0u, 0u, 0u, 0u);
-                if constexpr (MAXOPS > 1) return ldg_cg_v4(xrow + col);
-                else return ldg_nc_v4(xrow + col);
-            };
-            uint4 xa = make_uint4(0u, 0u, 0u, 0u), xb = xa;  // the next unit's (scale blocks 0, 1)
-            bool xpre = false;
+            // This CTA's share of the op's B tiles: chunks [G0, G1), one 16-byte piece (8
+            // activations of one token) per thread and step, zero past C or in_f.  The generic
+            // writes are fenced against the bulk copies (async proxy) that read them after the
+            // grid barrier.
+            {
+                const uint32_t k0 = (uint32_t)((uint64_t)b * n_kc / G), k1 = (uint32_t)((uint64_t)(b + 1) * n_kc / G);
+                for (uint32_t idx = threadIdx.x; idx < (k1 - k0) * 256u; idx += kTcMmaWarp * 32) {
+                    const uint32_t kc = k0 + idx / 256u, n = (idx / 8u) % 32u, p16 = idx % 8u;
+                    const int64_t col = (int64_t)kc * kChunk + 8 * p16;
+                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                    if ((int)n < C && col < in_f) {
+                        const __nv_bfloat16 *src = o.X + (int64_t)n * in_f + col;
+                        if constexpr (MAXOPS > 1) v = ldg_cg_v4(src);
+                        else v = ldg_nc_v4(src);
+                    }
+                    const uint32_t pc = 2u * (p16 & 3u) + (p16 >> 2);
+                    *reinterpret_cast<uint4 *>(xb + (size_t)kc * kTcBTile + n * 128u + ((pc ^ (n & 7u)) * 16u)) =
+                        make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
+                                   bf16x2_to_f16x2(v.w));
+                }
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+            }
+            grid_sync();  // every CTA's share of the B tiles is written
+            conv_op = gi;
+            if (wj == 1) issue_b();  // the B tiles of this op's blocks already in flight
             uint32_t lo, hi;
             tc_range(o, G, b, &lo, &hi);
 
@@ -538,7 +605,7 @@ vl_tc_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__rest
                 }
                 const uint32_t rg = s0 / n_kc;
                 s1 = min(hi, (rg + 1u) * n_kc);
-                const uint32_t nb = tc_blocks(s0, s1), kmeta = k << 4;
+                const uint32_t nb = tc_blocks(s0, s1), kmeta = k << kTcMetaKShift;
                 const uint32_t jb0 = tc_first_block(pipe, cb);
                 uint32_t first = kTcMetaFirst;
                 if (jb0 >= nb) post(stage_begin(), kmeta | kTcMetaSegEnd);  // no block of this pipe here
@@ -546,15 +613,6 @@ vl_tc_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__rest
                     const uint32_t u0 = s0 + kTcU * jb, n = min((uint32_t)kTcU, s1 - u0);
                     const uint32_t kc0 = u0 - rg * n_kc;
                     const bool last_block = jb + kTcPipes >= nb;
-                    // the chunk of the pipe's next block, if it belongs to this op (this segment
-                    // or the next): its activations are loaded during this block's last unit
-                    bool nxt = !last_block;
-                    uint32_t nkc = kc0 + kTcU * kTcPipes;
-                    if (last_block && s1 < hi) {
-                        const uint32_t nb2 = tc_blocks(s1, min(hi, s1 + n_kc)), j2 = tc_first_block(pipe, cb + nb);
-                        nxt = j2 < nb2;
-                        nkc = kTcU * j2;
-                    }
                     const uint32_t slot = slot_ctr % kTcR;
                     // a wait that gave up ends the pipe's copies (the slot may still be filling)
                     if (!slot_wait(full0 + 8u * slot, (slot_ctr / kTcR) & 1u, &s_wc)) it.op = n_ops;
@@ -562,24 +620,8 @@ vl_tc_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__rest
 #pragma unroll
                     for (int i = 0; i < kTcU; ++i) {
                         if (i >= (int)n) break;
-                        if (!xpre) {
-                            xa = load_x((int64_t)(kc0 + i) * kChunk);
-                            xb = load_x((int64_t)(kc0 + i) * kChunk + 32);
-                        }
-                        const uint4 xva = xa, xvb = xb;
-                        xpre = true;
-                        if (i + 1 < (int)n) {
-                            xa = load_x((int64_t)(kc0 + i + 1) * kChunk);
-                            xb = load_x((int64_t)(kc0 + i + 1) * kChunk + 32);
-                        } else if (nxt) {
-                            const int64_t c = (int64_t)nkc * kChunk;
-                            xa = load_x(c);
-                            xb = load_x(c + 32);
-                        } else {
-                            xpre = false;
-                        }
-                        const uint8_t *cbase = sl + hrb * (kTcU * kUnitCodeBytes) + i * kUnitCodeBytes + lane * 16;
-                        const uint8_t *sbase = sl + 2 * kTcU * kUnitCodeBytes + hrb * (kTcU * kUnitScaleBytes) +
+                        const uint8_t *cbase = sl + kTcSlotCodes + hrb * (kTcU * kUnitCodeBytes) + i * kUnitCodeBytes + lane * 16;
+                        const uint8_t *sbase = sl + kTcSlotScales + hrb * (kTcU * kUnitScaleBytes) +
                                                i * kUnitScaleBytes + g4 * 8;
                         uint4 cw[2];
                         uint2 sc[2];
@@ -589,7 +631,7 @@ vl_tc_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__rest
                             sc[r] = *reinterpret_cast<const uint2 *>(sbase + (t0 + r) * 64);
                         }
                         const uint32_t st = stage_begin();
-                        const uint32_t abase = astage0 + st * kTcAStage, bbase = bstage0 + st * kTcBStage;
+                        const uint32_t abase = astage0 + st * kTcAStage;
 #pragma unroll
                         for (int r = 0; r < 2; ++r)
 #pragma unroll
@@ -604,12 +646,10 @@ vl_tc_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__rest
                                 st_shared_v4(at, o0[0], o0[2], o1[0], o1[2]);
                                 st_shared_v4(at + 1024u, o0[1], o0[3], o1[1], o1[3]);
                             }
-                        st_shared_v4(bbase + b_row + pc0, bf16x2_to_f16x2(xva.x), bf16x2_to_f16x2(xva.y),
-                                     bf16x2_to_f16x2(xva.z), bf16x2_to_f16x2(xva.w));
-                        st_shared_v4(bbase + b_row + pc1, bf16x2_to_f16x2(xvb.x), bf16x2_to_f16x2(xvb.y),
-                                     bf16x2_to_f16x2(xvb.z), bf16x2_to_f16x2(xvb.w));
-                        const bool seg_end = last_block && i + 1 == (int)n;
-                        post(st, kmeta | kTcMetaMma | first | (seg_end ? kTcMetaSegEnd : 0u));
+                        const bool blk_end = i + 1 == (int)n, seg_end = last_block && blk_end;
+                        post(st, kmeta | kTcMetaMma | first | (seg_end ? kTcMetaSegEnd : 0u) |
+                                     (blk_end ? kTcMetaBlockEnd : 0u) | (slot << kTcMetaSlotShift) |
+                                     ((uint32_t)i << kTcMetaUnitShift));
                         first = 0u;
                     }
                     // both warps reading this row block's part of the slot are done with it: refill
