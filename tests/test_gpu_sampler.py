@@ -152,3 +152,19 @@ def test_many_rows_bound_the_excused_rows():
     print("sampler rows flagged: top-p", int(((fl & 2) != 0).sum()), "min-p",
           int(((fl & 1) != 0).sum()), "of", len(fl))
     assert ((fl & 1) != 0).sum() <= len(fl) // 100, fl
+
+
+@pytest.mark.parametrize("V", [1, 3, 7, 9, 17])
+def test_vocabularies_smaller_than_the_cluster(V):
+    """Rows shorter than the eight slices of a row's cluster: the slices past the row's end
+    are empty and must not disturb the max, the masses or the survivors."""
+    logits = synth.normal_logits(5, V, seed=V, std=2.0)
+    logits[1, 0] = logits[1, V - 1] = 9.0  # a tie at the ends: the lowest id wins
+    check(logits, 0.6, 0.95, 0.05)
+    check(logits, 1.0, 0.5, 0.0)
+    check(logits, 0.6, 0.95, 0.05, greedy=True)
+
+
+def test_thirty_two_rows_one_call():
+    """The largest window the ABI takes in one call (SVD_C_MAX rows), one cluster per row."""
+    check(synth.normal_logits(32, 20000, seed=77, std=3.0), 0.6, 0.95, 0.05)
