@@ -8,20 +8,24 @@
 //
 //     Y[c][j] = sum_b s[j][b] * sum_{i in block b} (code[j][i] - 8) * X[c][i]
 //
-// Two kernels:
-//  * vl_stream_kernel (NATIVE layout) -- a persistent stream-K kernel over (64-row block,
-//    64-input chunk) units.  Each CTA's units arrive stage by stage (the codes and scales of
-//    16 consecutive units, two bulk copies completing on an mbarrier) through a ring in
-//    shared memory; the warp that frees a stage last issues its refill, so there is no
-//    producer warp.  Every warp dequantises nibbles straight into bf16 A fragments with one
-//    lop3 and one bf16x2 subtract per pair (value 128 + c built from the exponent pattern
-//    0x4300, then minus 136 gives c - 8 exactly) and runs mma.sync m16n8k16 (bf16 in, fp32
-//    accumulate) against the activations as the B operand.  Every 32-input block gets a
-//    fresh accumulator that is scaled by its fp16 scale in fp32, so the only rounding is fp32
-//    accumulation.  A row block split between CTAs is finished by the CTA holding its first
-//    unit, from tagged partials the others store without waiting (summed in CTA order:
-//    deterministic).  A chain of matrices runs in one cooperative launch with a grid barrier
-//    between matrices; the weights of the next matrix keep streaming through it.
+// Three kernels:
+//  * vl_stream_kernel (NATIVE layout, C <= 16; C <= 32 on request) -- a persistent stream-K
+//    kernel over (64-row block, 64-input chunk) units.  Every warp is a stream-K worker with
+//    its own ring of bulk-copy slots (the codes and scales of two consecutive units, completing
+//    on the slot's mbarrier) that its lane 0 refills as soon as the warp has read a slot, so no
+//    warp waits for another while it computes.  Each warp dequantises nibbles straight into
+//    bf16 A fragments with one lop3 and one bf16x2 subtract per pair (value 128 + c built from
+//    the exponent pattern 0x4300, then minus 136 gives c - 8 exactly) and runs mma.sync
+//    m16n8k16 (bf16 in, fp32 accumulate) against the activations as the B operand.  Every
+//    32-input block gets a fresh accumulator that is scaled by its fp16 scale in fp32, so the
+//    only rounding is fp32 accumulation.  A row block split between CTAs is finished by the
+//    CTA holding its first unit, from tagged partials the others store without waiting
+//    (summed in CTA order: deterministic).  A chain of matrices runs in one cooperative launch
+//    with a grid barrier between matrices; the weights of the next matrix keep streaming
+//    through it.
+//  * vl_tc_kernel (NATIVE layout, 17 <= C <= 32; verify_linear_tc.cuh) -- the same stream-K
+//    decomposition over 128-row units on the tcgen05 tensor cores: fp16 A operands with the
+//    block scale folded in, staged in shared memory, fp32 accumulators in tensor memory.
 //  * vl_simt_kernel (CANONICAL layout) -- the plain CUDA-core version: one warp per output
 //    row, each lane one 32-input block at a time, fp32 FMAs, warp-shuffle reduction.
 #include <cooperative_groups.h>
