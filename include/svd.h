@@ -66,9 +66,17 @@ enum {
 enum {
     SVD_LAYOUT_CANONICAL = 0, /* codes[out][in/2] bytes, input 2t in the low nibble,
                                  input 2t+1 in the high nibble; scales[out][in/32] fp16 */
-    SVD_LAYOUT_NATIVE = 1     /* the tensor-core fragment order made by
+    SVD_LAYOUT_NATIVE = 1,    /* the tensor-core fragment order made by
                                  svd_repack_weights (opaque; same byte count, rows
                                  padded to 64, inputs padded to 64)                   */
+    SVD_LAYOUT_Q4K = 2        /* K-quant 4-bit super-blocks (the 4-bit tensors of the pages'
+                                 Q4_K_M / UD-Q4_K_XL checkpoints; "100 tokens per second
+                                 ...", "The wall"): codes -> [out][in/256] blocks of 144
+                                 bytes = fp16 d, fp16 dmin, 12 bytes of packed 6-bit
+                                 sub-block scales and mins, 128 bytes of 4-bit codes;
+                                 weight = d sc[j] q - dmin m[j] for sub-block j of 32;
+                                 scales must be NULL; in_features % 256 == 0.  Read by a
+                                 CUDA-core kernel (svd_verify_linear only, C <= 8)       */
 };
 
 /* Flags for svd_verify_linear. */

@@ -11,7 +11,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libsvd.so")
-SOURCES = ["verify_linear.cu", "kv_attention.cu", "accept.cu", "sampler.cu", "api.cu",
+SOURCES = ["verify_linear.cu", "kquant.cu", "kv_attention.cu", "accept.cu", "sampler.cu", "api.cu",
            "host_policy.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CUDA_HOME = os.environ.get("CUDA_HOME", "/usr/local/cuda")

@@ -980,15 +980,23 @@ static cudaError_t launch_simt(const svd_qweight *W, const void *X, float *Y, bo
 }
 
 static int check_qweight(const svd_qweight *W) {
-    if (!W || !W->codes || !W->scales) return SVD_ERR_INVALID_ARG;
+    if (!W || !W->codes) return SVD_ERR_INVALID_ARG;
     if (W->in_features <= 0 || W->out_features <= 0 || W->in_features % 32 != 0)
         return SVD_ERR_INVALID_ARG;
     if (W->reserved != 0) return SVD_ERR_INVALID_ARG;
+    if (W->layout == SVD_LAYOUT_Q4K) {  // super-blocks only: no separate scales
+        if (W->scales || W->in_features % 256 != 0 || !aligned16(W->codes)) return SVD_ERR_INVALID_ARG;
+        return SVD_OK;
+    }
+    if (!W->scales) return SVD_ERR_INVALID_ARG;
     if (W->layout != SVD_LAYOUT_CANONICAL && W->layout != SVD_LAYOUT_NATIVE)
         return SVD_ERR_INVALID_ARG;
     if (!aligned16(W->codes) || !aligned16(W->scales)) return SVD_ERR_INVALID_ARG;
     return SVD_OK;
 }
+
+int verify_linear_q4k(const svd_qweight *W, const void *X, int C, float *Y, bool pdl,
+                      cudaStream_t stream);
 
 // The stream-K kernel does its unit arithmetic in 32 bits: n_units * (workers + 1) must
 // stay below 2^32 (about 880 thousand units, 3.6 billion weights, on 152 SMs).
@@ -1018,6 +1026,10 @@ int verify_linear(const svd_qweight *W, const void *X, int C, float *Y, void *ws
         P.op[0] = make_op(W, X, Y);
         SVD_CUDA_TRY(launch_ops(P, ws, pdl, stream, (flags & SVD_F_FRAGMENT_MMA) != 0));
         return SVD_OK;
+    }
+    if (W->layout == SVD_LAYOUT_Q4K) {  // K-quant super-blocks: CUDA-core kernel (kquant.cu)
+        if (C > 8) return SVD_ERR_UNSUPPORTED;
+        return verify_linear_q4k(W, X, C, Y, pdl, stream);
     }
     // canonical layout: CUDA-core kernel
     if ((int64_t)C * W->in_features * 4 > 196608) return SVD_ERR_UNSUPPORTED;

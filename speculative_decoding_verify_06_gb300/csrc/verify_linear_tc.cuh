@@ -611,7 +611,6 @@ vl_tc_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__rest
                 if (jb0 >= nb) post(stage_begin(), kmeta | kTcMetaSegEnd);  // no block of this pipe here
                 for (uint32_t jb = jb0; jb < nb; jb += kTcPipes) {
                     const uint32_t u0 = s0 + kTcU * jb, n = min((uint32_t)kTcU, s1 - u0);
-                    const uint32_t kc0 = u0 - rg * n_kc;
                     const bool last_block = jb + kTcPipes >= nb;
                     const uint32_t slot = slot_ctr % kTcR;
                     // a wait that gave up ends the pipe's copies (the slot may still be filling)

@@ -29,6 +29,7 @@ SVD_ST_EMPTY = 16
 
 SVD_LAYOUT_CANONICAL = 0
 SVD_LAYOUT_NATIVE = 1
+SVD_LAYOUT_Q4K = 2
 SVD_F_PDL = 1
 SVD_F_FRAGMENT_MMA = 2
 SVD_POLL_DEFAULT = 0xFFFFFFFF

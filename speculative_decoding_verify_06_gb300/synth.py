@@ -80,6 +80,38 @@ def qweight_torch(out_f: int, in_f: int, seed: int, device):
     return codes, s.to(torch.float16).view(torch.int16)
 
 
+# Q4_K super-block fields: d and dmin drawn U(Q4K_D_LO, Q4K_D_HI) and rounded to fp16 (6-bit
+# sub-block scales up to 63 then give per-weight steps up to ~0.13, like the symmetric recipe's
+# 8 x 0.02); scale and code bytes uniform.
+Q4K_D_LO, Q4K_D_HI = 5e-4, 2e-3
+
+
+def q4k_blocks(out_f: int, in_f: int, seed: int) -> np.ndarray:
+    """Q4_K matrix: uint8 [out, in / 256 * 144], super-blocks of (fp16 d, fp16 dmin, 12 scale
+    bytes, 128 code bytes) with uniform bytes and d, dmin from the recipe above."""
+    assert in_f % 256 == 0
+    g = rng(seed)
+    nsb = in_f // 256
+    b = g.integers(0, 256, size=(out_f, nsb, 144), dtype=np.uint8)
+    dd = f16_bits(g.uniform(Q4K_D_LO, Q4K_D_HI, size=(out_f, nsb, 2)))
+    b[..., 0:4] = dd.view(np.uint8).reshape(out_f, nsb, 4)
+    return b.reshape(out_f, nsb * 144)
+
+
+def q4k_blocks_torch(out_f: int, in_f: int, seed: int, device):
+    """The same recipe drawn on a device with torch's generator."""
+    import torch
+    assert in_f % 256 == 0
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    nsb = in_f // 256
+    b = torch.randint(0, 256, (out_f, nsb, 144), dtype=torch.uint8, device=device, generator=g)
+    dd = torch.empty((out_f, nsb, 2), dtype=torch.float32, device=device)
+    dd.uniform_(Q4K_D_LO, Q4K_D_HI, generator=g)
+    b[..., 0:4] = dd.to(torch.float16).view(torch.uint8).reshape(out_f, nsb, 4)
+    return b.reshape(out_f, nsb * 144)
+
+
 def activations_torch(C: int, in_f: int, seed: int, device, std: float = 1.0):
     import torch
     g = torch.Generator(device=device)
