@@ -76,7 +76,13 @@ enum {
                                  sub-block scales and mins, 128 bytes of 4-bit codes;
                                  weight = d sc[j] q - dmin m[j] for sub-block j of 32;
                                  scales must be NULL; in_features % 256 == 0.  Read by a
-                                 CUDA-core kernel (svd_verify_linear only, C <= 8)       */
+                                 CUDA-core kernel (svd_verify_linear only, C <= 8)       */,
+    SVD_LAYOUT_Q4K_NATIVE = 3 /* the same super-blocks repacked by svd_repack_weights for the
+                                 tensor-core stream kernel (opaque; same byte count, rows
+                                 padded to 64): codes -> units of 64 rows x 256 inputs,
+                                 8192 bytes of codes in fragment order; scales -> the
+                                 units' 64 super-block headers (16 bytes each).  Streamed
+                                 by svd_verify_linear and svd_verify_chain, C <= 8      */
 };
 
 /* Flags for svd_verify_linear. */
@@ -126,6 +132,12 @@ int svd_last_cuda_error(void); /* cudaError_t of the thread's last SVD_ERR_CUDA 
 int svd_native_sizes(int64_t in_features, int64_t out_features, size_t *codes_bytes,
                      size_t *scales_bytes);
 
+/* Byte sizes of the Q4_K native layout (rows padded to 64): codes_bytes = 8192 per unit of 64
+ * rows x 256 inputs, headers_bytes = 1024 per unit.  SVD_ERR_INVALID_ARG for in % 256 != 0 or
+ * non-positive sizes. */
+int svd_q4k_native_sizes(int64_t in_features, int64_t out_features, size_t *codes_bytes,
+                         size_t *headers_bytes);
+
 /* Permute a CANONICAL matrix into the NATIVE layout the tensor-core kernel streams: for each
  * 64-row block and each 64-input chunk, the 16-byte word every lane of a warp loads holds its
  * A-fragment nibbles for four k16 MMA steps, and the scales follow in fragment order.  A pure
@@ -133,7 +145,12 @@ int svd_native_sizes(int64_t in_features, int64_t out_features, size_t *codes_by
  * dst buffers must hold svd_native_sizes() bytes and must not overlap src. */
 int svd_repack_weights(const svd_qweight *src_canonical, void *dst_codes, void *dst_scales,
                        svd_stream_t stream);
-/* Inverse of svd_repack_weights (drops the padding). */
+/* A Q4K matrix (src->layout SVD_LAYOUT_Q4K, scales NULL) is repacked into SVD_LAYOUT_Q4K_NATIVE
+ * instead: dst_codes receives the units' codes (the nibble of input i of a unit's 64-input
+ * sub-chunk at the place the NATIVE layout gives it, value q), dst_scales the headers, sizes
+ * from svd_q4k_native_sizes; padding rows have code 0 and a zero header. */
+/* Inverse of svd_repack_weights (drops the padding).  For SVD_LAYOUT_Q4K_NATIVE the raw Q4K
+ * bytes [out][in/256 * 144] go to dst_codes and dst_scales must be NULL. */
 int svd_unpack_weights(const svd_qweight *src_native, void *dst_codes, void *dst_scales,
                        svd_stream_t stream);
 

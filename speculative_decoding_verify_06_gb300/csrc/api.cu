@@ -10,6 +10,7 @@ size_t vl_workspace_bytes(int64_t in_f, int64_t out_f, int C);
 int verify_linear(const svd_qweight *W, const void *X, int C, float *Y, void *ws, size_t ws_bytes,
                   int flags, cudaStream_t stream);
 int native_sizes(int64_t in_f, int64_t out_f, size_t *cb, size_t *sb);
+int kq_native_sizes(int64_t in_f, int64_t out_f, size_t *cb, size_t *hb);
 int repack(const svd_qweight *src, void *dc, void *ds, cudaStream_t stream);
 int unpack(const svd_qweight *src, void *dc, void *ds, cudaStream_t stream);
 int verify_linear_noalloc(const svd_qweight *W, const void *X, int C, float *Y, int flags,
@@ -70,6 +71,10 @@ int svd_device_sm_count(void) { return svd::sm_count(); }
 
 int svd_native_sizes(int64_t in_f, int64_t out_f, size_t *cb, size_t *sb) {
     return svd::native_sizes(in_f, out_f, cb, sb);
+}
+
+int svd_q4k_native_sizes(int64_t in_f, int64_t out_f, size_t *cb, size_t *hb) {
+    return svd::kq_native_sizes(in_f, out_f, cb, hb);
 }
 
 int svd_repack_weights(const svd_qweight *src, void *dc, void *ds, svd_stream_t stream) {

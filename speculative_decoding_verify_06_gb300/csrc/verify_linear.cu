@@ -46,7 +46,6 @@ constexpr int kRowsPerBlock = 16 * kTiles;
 constexpr int kChunk = 64;              // inputs per unit (2 scale blocks, 4 k16 steps)
 constexpr int kUnitCodeBytes = 512 * kTiles;   // rows x 64 inputs x 4 bit
 constexpr int kUnitScaleBytes = 64 * kTiles;   // rows x 2 blocks x fp16
-constexpr int kUnitBytes = kUnitCodeBytes + kUnitScaleBytes;
 
 struct NativeGeom {
     int64_t n_rb, n_kc, n_units;
@@ -55,6 +54,25 @@ static NativeGeom native_geom(int64_t in_f, int64_t out_f) {
     NativeGeom g;
     g.n_rb = (out_f + kRowsPerBlock - 1) / kRowsPerBlock;
     g.n_kc = (in_f + kChunk - 1) / kChunk;
+    g.n_units = g.n_rb * g.n_kc;
+    return g;
+}
+
+// Q4_K native layout (SVD_LAYOUT_Q4K_NATIVE): units of 64 rows x 256 inputs (one super-block
+// column of a 64-row block), row-block-major like the native units.  A unit is 8192 bytes of
+// codes -- four 64-input sub-chunks, each laid out exactly like a native unit's codes, the
+// nibble holding the super-block's code q -- in the codes array, and the 64 rows' 16-byte
+// super-block headers (fp16 d, fp16 dmin, 12 packed scale bytes) in row order in the header
+// array: 144 bytes per 256 weights of a row, the format's own size.
+constexpr int kKqIn = 256;                              // inputs per Q4_K unit
+constexpr int kKqSub = kKqIn / kChunk;                  // 64-input sub-chunks per unit
+constexpr int kKqUnitCodeBytes = kKqSub * kUnitCodeBytes;
+constexpr int kKqUnitHdrBytes = kRowsPerBlock * 16;
+constexpr int kKqBlockBytes = 144;                      // one super-block of the raw format
+static NativeGeom kq_geom(int64_t in_f, int64_t out_f) {
+    NativeGeom g;
+    g.n_rb = (out_f + kRowsPerBlock - 1) / kRowsPerBlock;
+    g.n_kc = in_f / kKqIn;
     g.n_units = g.n_rb * g.n_kc;
     return g;
 }
@@ -144,6 +162,78 @@ __global__ void unpack_scales_kernel(const uint16_t *__restrict__ src, uint16_t 
     dst[idx] = src[(((rb * n_kc + kc) * kTiles + r) * 8 + g) * 4 + q];
 }
 
+// Q4_K -> Q4_K native.  Word wid of the codes: unit wid / 2048, sub-chunk (wid >> 9) & 3, tile
+// (wid >> 7) & 3, lane (wid >> 2) & 31, k16 step wid & 3; input 256 kc + 64 sub + (native
+// input of the word's nibble), whose code sits in byte 16 + 32 (j / 2) + (i mod 32) of its
+// super-block, low nibble for even sub-block j.  Padding rows get code 0 and a zero header
+// (d = dmin = 0: every weight 0).
+static_assert(kTiles == 4, "the Q4_K unit layout assumes four 16-row tiles per row block");
+__global__ void kq_repack_codes_kernel(const uint8_t *__restrict__ src, uint32_t *__restrict__ dst,
+                                       int64_t in_f, int64_t out_f, int64_t n_kc, int64_t n_words) {
+    const int64_t wid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (wid >= n_words) return;
+    const int s = (int)(wid & 3), lane = (int)((wid >> 2) & 31), r = (int)((wid >> 7) & 3);
+    const int sub = (int)((wid >> 9) & 3);
+    const int64_t unit = wid >> 11, rb = unit / n_kc, kc = unit % n_kc;
+    const int g = lane >> 2, t = lane & 3;
+    const int64_t row_bytes = in_f / kKqIn * kKqBlockBytes;
+    uint32_t word = 0;
+#pragma unroll
+    for (int p = 0; p < 4; ++p)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            int rt, ic;
+            native_word_coords(s, p, h, g, t, &rt, &ic);
+            const int64_t row = rb * kRowsPerBlock + 16 * r + rt;
+            const int i = kChunk * sub + ic;  // input within the super-block
+            uint32_t nib = 0;
+            if (row < out_f) {
+                const int j = i >> 5;
+                const uint8_t byte = src[row * row_bytes + kc * kKqBlockBytes + 16 + 32 * (j >> 1) + (i & 31)];
+                nib = (j & 1) ? (byte >> 4) : (byte & 15);
+            }
+            word |= nib << (4 * p + 16 * h);
+        }
+    dst[wid] = word;
+}
+
+__global__ void kq_repack_hdr_kernel(const uint8_t *__restrict__ src, uint4 *__restrict__ dst,
+                                     int64_t in_f, int64_t out_f, int64_t n_kc, int64_t n_rows) {
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= n_rows) return;
+    const int64_t unit = idx / kRowsPerBlock, rb = unit / n_kc, kc = unit % n_kc;
+    const int64_t row = rb * kRowsPerBlock + idx % kRowsPerBlock;
+    const int64_t row_bytes = in_f / kKqIn * kKqBlockBytes;
+    dst[idx] = row < out_f ? *reinterpret_cast<const uint4 *>(src + row * row_bytes + kc * kKqBlockBytes)
+                           : make_uint4(0u, 0u, 0u, 0u);
+}
+
+// Q4_K native -> Q4_K: one thread per byte of the raw matrix.
+__global__ void kq_unpack_kernel(const uint32_t *__restrict__ codes, const uint8_t *__restrict__ hdr,
+                                 uint8_t *__restrict__ dst, int64_t in_f, int64_t out_f, int64_t n_kc) {
+    const int64_t row_bytes = in_f / kKqIn * kKqBlockBytes;
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= out_f * row_bytes) return;
+    const int64_t row = idx / row_bytes, b = idx % row_bytes, kc = b / kKqBlockBytes;
+    const int off = (int)(b % kKqBlockBytes);
+    const int64_t rb = row / kRowsPerBlock, rr = row % kRowsPerBlock, unit = rb * n_kc + kc;
+    if (off < 16) {
+        dst[idx] = hdr[(unit * kRowsPerBlock + rr) * 16 + off];
+        return;
+    }
+    const int r = (int)(rr / 16), rt = (int)(rr % 16), g = rt % 8, prow = rt / 8;
+    uint8_t outb = 0;
+    for (int hi = 0; hi < 2; ++hi) {
+        const int j = 2 * ((off - 16) / 32) + hi, i = 32 * j + (off - 16) % 32;  // input in block
+        const int sub = i / kChunk, ic = i % kChunk, sblk = ic / 32, iw = ic % 32, t = iw / 8;
+        const int slo = (iw % 8) / 4, e = iw % 4;
+        const int s = 2 * sblk + slo, p = 2 * (e >> 1) + prow, h = e & 1;
+        const int64_t wid = ((((unit * kKqSub + sub) * kTiles + r) * 32) + (4 * g + t)) * 4 + s;
+        outb |= (uint8_t)(((codes[wid] >> (4 * p + 16 * h)) & 15u) << (4 * hi));
+    }
+    dst[idx] = outb;
+}
+
 // ---- device building blocks -----------------------------------------------------------
 // Activations read through L2 only: in a chain, op i+1 may read what op i wrote in the same
 // kernel, so the non-coherent path must not be used there.
@@ -164,6 +254,18 @@ __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t a[4]) {
         const uint32_t sh = w >> (4 * p);
         asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(v) : "r"(sh), "r"(0x000F000Fu), "r"(magic));
         asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(a[p]) : "r"(v), "r"(bias));
+    }
+}
+
+// The same with the value q itself (subtract 128): the Q4_K codes.
+__device__ __forceinline__ void dequant_word_q(uint32_t w, uint32_t a[4]) {
+    const uint32_t magic = 0x43004300u;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        uint32_t v;
+        const uint32_t sh = w >> (4 * p);
+        asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(v) : "r"(sh), "r"(0x000F000Fu), "r"(magic));
+        asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(a[p]) : "r"(v), "r"(magic));
     }
 }
 
@@ -223,7 +325,7 @@ struct VlOps {
 // touching activations or the workspace.
 constexpr int kPartialMax = 32 * kTiles * 4 * 4;  // entries of the largest partial (NT = 4)
 
-template <int NT, int NW, int TW, int R, int U, int MAXOPS>
+template <int NT, int NW, int TW, int R, int U, int MAXOPS, int KQ>
 struct VlCfg {
     static constexpr int kThreads = NW * 32;
     static constexpr int kWG = kTiles / TW;           // warps sharing a unit (one per TW tiles)
@@ -232,10 +334,17 @@ struct VlCfg {
     static constexpr int kAccW = TW * NT * 4;         // ... of the tiles one warp works on
     static constexpr int kPartial = 32 * kAcc;        // entries of a row block's partial
     static constexpr int kPer = (kPartial + kThreads - 1) / kThreads;
-    static constexpr int kSlotBytes = U * kUnitBytes;  // codes of U units, then their scales
+    static constexpr int kUC = KQ ? kKqUnitCodeBytes : kUnitCodeBytes;  // codes of a unit
+    static constexpr int kUS = KQ ? kKqUnitHdrBytes : kUnitScaleBytes;   // its scales / headers
+    static constexpr int kSlotBytes = U * (kUC + kUS);  // codes of U units, then their scales
     static constexpr size_t kRing = (size_t)kNG * R * kSlotBytes;
     static constexpr size_t kPark = (size_t)NW * 2 * 32 * kAccW * sizeof(float);
-    static constexpr size_t kSmem = kRing + kPark + (size_t)MAXOPS * sizeof(VlOp);
+    // Q4_K: each warp's decoded headers of its rows of the current unit (floats): sub-block
+    // scales [TW][8 j][8 g][2], min pairs [TW * 16 rows][4] (bf16x2), (d, dmin) [TW * 16 rows]
+    static constexpr int kKqScrW = TW * 224;
+    static constexpr size_t kScratch = KQ ? (size_t)NW * kKqScrW * sizeof(float) : 0;
+    static constexpr size_t kSmem = kRing + kPark + kScratch + (size_t)MAXOPS * sizeof(VlOp);
+    static_assert(!KQ || NT == 1, "Q4_K units take up to 8 columns");
     static_assert(kTiles % TW == 0 && NW % kWG == 0 && (kWG == 1 || kNG <= 15), "worker groups");
     static_assert(kPartial <= kPartialMax, "partial slot size");
     static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
@@ -343,12 +452,13 @@ __host__ __device__ inline uint32_t partial_epoch24(uint32_t epoch) { return epo
 #define SVD_PROBE(gi, what)  // timing hook for instrumented builds; nothing by default
 #endif
 
-template <int NT, int NW, int TW, int R, int U, int MAXOPS>
+template <int NT, int NW, int TW, int R, int U, int MAXOPS, int KQ>
 __global__ void __launch_bounds__(NW * 32, 1)
 vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__restrict__ part,
                  uint32_t part_entries, unsigned *__restrict__ gbar) {
-    using Cfg = VlCfg<NT, NW, TW, R, U, MAXOPS>;
+    using Cfg = VlCfg<NT, NW, TW, R, U, MAXOPS, KQ>;
     constexpr int kSlotBytes = Cfg::kSlotBytes, kWG = Cfg::kWG, kNG = Cfg::kNG;
+    constexpr int kUC = Cfg::kUC, kUS = Cfg::kUS;
     constexpr int kAcc = Cfg::kAcc, kAccW = Cfg::kAccW, kPartial = Cfg::kPartial, kPer = Cfg::kPer;
     constexpr int kThreads = Cfg::kThreads;
     constexpr int kParkW = 32 * kAccW;  // floats of one parked partial
@@ -365,10 +475,11 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
     float *park = reinterpret_cast<float *>(smem + Cfg::kRing);
     // The op descriptors live in shared memory: read from the parameter space with a
     // run-time index they would go through the small constant cache on every access.
-    VlOp *ops = reinterpret_cast<VlOp *>(smem + Cfg::kRing + Cfg::kPark);
+    VlOp *ops = reinterpret_cast<VlOp *>(smem + Cfg::kRing + Cfg::kPark + Cfg::kScratch);
     const int n_ops = P.n;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float *const kq_scr = reinterpret_cast<float *>(smem + Cfg::kRing + Cfg::kPark) + warp * Cfg::kKqScrW;
     const int grp = warp / kWG, sub = warp % kWG;  // worker group, and this warp's tiles in it
     const uint32_t G = gridDim.x, b = blockIdx.x;
     const uint32_t Wtot = G * kNG, gw = b * kNG + grp;
@@ -426,20 +537,20 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
         while (c_u >= c_hi) {
             if (++c_op >= n_ops) return;
             range(ops[c_op], &c_u, &c_hi);
-            c_codes = ops[c_op].codes + (size_t)c_u * kUnitCodeBytes;
-            c_scales = ops[c_op].scales + (size_t)c_u * kUnitScaleBytes;
+            c_codes = ops[c_op].codes + (size_t)c_u * kUC;
+            c_scales = ops[c_op].scales + (size_t)c_u * kUS;
         }
         const uint32_t slot = c_issued % R, n = min((uint32_t)U, c_hi - c_u);
         if (sub == 0 && lane == 0) {
             const uint32_t bar = full0 + 8 * slot, dst = ring0 + slot * kSlotBytes;
-            mbar_expect_tx(bar, n * kUnitBytes);
-            bulk_g2s(dst, c_codes, n * kUnitCodeBytes, bar);
-            bulk_g2s(dst + U * kUnitCodeBytes, c_scales, n * kUnitScaleBytes, bar);
+            mbar_expect_tx(bar, n * (kUC + kUS));
+            bulk_g2s(dst, c_codes, n * kUC, bar);
+            bulk_g2s(dst + U * kUC, c_scales, n * kUS, bar);
         }
         c_u += n;
         ++c_issued;
-        c_codes += n * kUnitCodeBytes;
-        c_scales += n * kUnitScaleBytes;
+        c_codes += n * kUC;
+        c_scales += n * kUS;
     };
     // The stall injection (workspace word kBarPoll, written only by the test hook, never by an
     // earlier kernel of the stream, so it may be read before the dependency wait): no copy.
@@ -523,10 +634,109 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
 
             uint32_t rb = lo / n_kc, kc = lo - rb * n_kc, seg_lo = lo;
             uint4 xr[NT][2];
-            if constexpr (kPrefetchX) load_x(kc, xr);
+            if constexpr (kPrefetchX) load_x(KQ ? kKqSub * kc : kc, xr);
             for (uint32_t u = lo; u < hi; ++u) {
                 const uint32_t slot = c_used % R, in_slot = (u - lo) % U;
                 const uint32_t kn = (kc + 1 == n_kc) ? 0u : kc + 1;
+                if constexpr (KQ) {
+                    // ---- a Q4_K unit: 64 rows x 256 inputs; this warp's TW tiles of it
+                    if (in_slot == 0u && !slot_wait(full0 + 8 * slot, (c_used / R) & 1u, &s_wc)) c_op = n_ops;
+                    const uint8_t *cbase = ring + slot * kSlotBytes + in_slot * kUC + lane * 16;
+                    const uint8_t *hbase = ring + slot * kSlotBytes + U * kUC + in_slot * kUS;
+                    float *sc_s = kq_scr;
+                    uint32_t *m_s = reinterpret_cast<uint32_t *>(kq_scr + TW * 128);
+                    float2 *d_s = reinterpret_cast<float2 *>(kq_scr + TW * 192);
+                    // decode the headers of this warp's rows: lane l takes local rows l, l + 32, ...
+                    for (int lr = lane; lr < TW * 16; lr += 32) {
+                        const uint4 hd = *reinterpret_cast<const uint4 *>(hbase + (sub * TW * 16 + lr) * 16);
+                        uint32_t scv[8], mv[8];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            scv[j] = (hd.y >> (8 * j)) & 63u;
+                            mv[j] = (hd.z >> (8 * j)) & 63u;
+                            const uint32_t lo4 = (hd.w >> (8 * j)) & 255u;
+                            scv[j + 4] = (lo4 & 15u) | (((hd.y >> (8 * j + 6)) & 3u) << 4);
+                            mv[j + 4] = (lo4 >> 4) | (((hd.z >> (8 * j + 6)) & 3u) << 4);
+                        }
+                        const int r = lr >> 4, rt = lr & 15, g = rt & 7, hh = rt >> 3;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) sc_s[((r * 8 + j) * 8 + g) * 2 + hh] = (float)scv[j];
+                        uint32_t mw[4];  // (m[2t], m[2t+1]) as bf16 pairs, exact (m < 64)
+#pragma unroll
+                        for (int t = 0; t < 4; ++t)
+                            mw[t] = (__float_as_uint((float)mv[2 * t]) >> 16) |
+                                    (__float_as_uint((float)mv[2 * t + 1]) & 0xFFFF0000u);
+                        *reinterpret_cast<uint4 *>(m_s + lr * 4) = make_uint4(mw[0], mw[1], mw[2], mw[3]);
+                        d_s[lr] = make_float2(__half2float(__ushort_as_half((unsigned short)(hd.x & 0xFFFFu))),
+                                              __half2float(__ushort_as_half((unsigned short)(hd.x >> 16))));
+                    }
+                    __syncwarp();
+                    // per tile T = sum_j sc_j (sum_{i in j} q_i x_i); and the sub-block sums of x
+                    // as an MMA of X (rows = columns) against an indicator: D[col][j] = sum_{i in j} x
+                    float T[TW][4], xsd[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int r = 0; r < TW; ++r)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) T[r][q] = 0.f;
+#pragma unroll
+                    for (int s4 = 0; s4 < kKqSub; ++s4) {
+                        uint4 xq[NT][2];
+                        if constexpr (kPrefetchX) {
+                            xq[0][0] = xr[0][0];
+                            xq[0][1] = xr[0][1];
+                            if (s4 + 1 < kKqSub) load_x(kKqSub * kc + s4 + 1, xr);
+                            else if (u + 1 < hi) load_x(kKqSub * kn, xr);
+                        } else {
+                            load_x(kKqSub * kc + s4, xq);
+                        }
+#pragma unroll
+                        for (int r = 0; r < TW; ++r) {
+                            const uint4 cw = *reinterpret_cast<const uint4 *>(cbase + s4 * kUnitCodeBytes + (sub * TW + r) * 512);
+#pragma unroll
+                            for (int blk = 0; blk < 2; ++blk) {
+                                uint32_t a0[4], a1[4];
+                                dequant_word_q(blk ? cw.z : cw.x, a0);
+                                dequant_word_q(blk ? cw.w : cw.y, a1);
+                                const float2 sc2 = *reinterpret_cast<const float2 *>(sc_s + ((r * 8 + 2 * s4 + blk) * 8 + g4) * 2);
+                                float d4[4] = {0.f, 0.f, 0.f, 0.f};
+                                mma_bf16_16816(d4, a0, xq[0][blk].x, xq[0][blk].y);
+                                mma_bf16_16816(d4, a1, xq[0][blk].z, xq[0][blk].w);
+                                T[r][0] = fmaf(sc2.x, d4[0], T[r][0]);
+                                T[r][1] = fmaf(sc2.x, d4[1], T[r][1]);
+                                T[r][2] = fmaf(sc2.y, d4[2], T[r][2]);
+                                T[r][3] = fmaf(sc2.y, d4[3], T[r][3]);
+                            }
+                        }
+#pragma unroll
+                        for (int blk = 0; blk < 2; ++blk) {
+                            const uint32_t ind = (g4 == 2 * s4 + blk) ? 0x3F803F80u : 0u;  // bf16 (1, 1)
+                            const uint32_t ax0[4] = {xq[0][blk].x, 0u, xq[0][blk].y, 0u};
+                            const uint32_t ax1[4] = {xq[0][blk].z, 0u, xq[0][blk].w, 0u};
+                            mma_bf16_16816(xsd, ax0, ind, ind);
+                            mma_bf16_16816(xsd, ax1, ind, ind);
+                        }
+                    }
+                    // lane (g, t) holds the sums of sub-blocks 2t, 2t+1 for column g: exactly the
+                    // B fragment of the mins' product sum_j m_j xs_j, split into bf16 hi + lo
+                    const __nv_bfloat162 hi2 = __floats2bfloat162_rn(xsd[0], xsd[1]);
+                    const float2 hif = __bfloat1622float2(hi2);
+                    const __nv_bfloat162 lo2 = __floats2bfloat162_rn(xsd[0] - hif.x, xsd[1] - hif.y);
+                    const uint32_t bh = *reinterpret_cast<const uint32_t *>(&hi2);
+                    const uint32_t bl = *reinterpret_cast<const uint32_t *>(&lo2);
+#pragma unroll
+                    for (int r = 0; r < TW; ++r) {
+                        const uint32_t m0 = m_s[(16 * r + g4) * 4 + t4], m1 = m_s[(16 * r + g4 + 8) * 4 + t4];
+                        const uint32_t am[4] = {m0, m1, m0, m1};
+                        float d2[4] = {0.f, 0.f, 0.f, 0.f};
+                        mma_bf16_16816(d2, am, bh, bl);
+                        const float2 e0 = d_s[16 * r + g4], e1 = d_s[16 * r + g4 + 8];
+                        acc[r][0][0] = fmaf(e0.x, T[r][0], fmaf(-e0.y, d2[0], acc[r][0][0]));
+                        acc[r][0][1] = fmaf(e0.x, T[r][1], fmaf(-e0.y, d2[1], acc[r][0][1]));
+                        acc[r][0][2] = fmaf(e1.x, T[r][2], fmaf(-e1.y, d2[2], acc[r][0][2]));
+                        acc[r][0][3] = fmaf(e1.x, T[r][3], fmaf(-e1.y, d2[3], acc[r][0][3]));
+                    }
+                    __syncwarp();  // the scratch is rewritten for the next unit
+                } else {
                 uint4 xc[NT][2];
                 if constexpr (kPrefetchX) {
 #pragma unroll
@@ -568,6 +778,7 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
                         }
                     }
                 }
+                }  // native unit
                 // Once the group has read the slot, refill it with the units R slots further
                 // on.  Every value a warp loaded from the slot has been consumed by the
                 // instructions above (issued in order), so the bulk copy cannot overwrite a
@@ -798,6 +1009,10 @@ constexpr int kR2 = 2;            // ring slots per worker group, C <= 32
 constexpr int kNW4 = 8;           // warps per CTA, 16 < C <= 32: one warp per unit (all four row
 constexpr int kTW4 = 4;           // tiles), so each activation fragment serves four tiles; 255
                                   // registers a thread hold the accumulators (16 warps spill)
+constexpr int kNWq = 16;          // Q4_K units (64 rows x 256 inputs, 9 KB), C <= 8: two warps
+constexpr int kTWq = 2;           // per unit, each on two 16-row tiles; one unit per slot, two
+constexpr int kRq = 2;            // slots per worker group
+constexpr int kUq = 1;
 constexpr int kMaxCtasPerSm = 2;  // the workspace holds partial slots for this many
 constexpr int kChainMax = 256;    // ops per chain launch (kernel parameters, ~16 KB)
 
@@ -831,11 +1046,11 @@ size_t vl_workspace_bytes(int64_t in_f, int64_t out_f, int C) {
     return partial_region_bytes() + kBarrierBytes + tc_xb_region(in_f, C);
 }
 
-template <int NT, int NW, int TW, int R, int U, int MAXOPS>
+template <int NT, int NW, int TW, int R, int U, int MAXOPS, int KQ = 0>
 static cudaError_t launch_stream(const VlOps<MAXOPS> &P, void *ws, bool pdl, bool coop,
                                  int64_t max_units, cudaStream_t stream) {
-    using Cfg = VlCfg<NT, NW, TW, R, U, MAXOPS>;
-    auto kern = vl_stream_kernel<NT, NW, TW, R, U, MAXOPS>;
+    using Cfg = VlCfg<NT, NW, TW, R, U, MAXOPS, KQ>;
+    auto kern = vl_stream_kernel<NT, NW, TW, R, U, MAXOPS, KQ>;
     static int per_sm_cache[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -876,7 +1091,8 @@ static cudaError_t launch_stream(const VlOps<MAXOPS> &P, void *ws, bool pdl, boo
 }
 
 static VlOp make_op(const svd_qweight *W, const void *X, float *Y) {
-    const NativeGeom ng = native_geom(W->in_features, W->out_features);
+    const NativeGeom ng = W->layout == SVD_LAYOUT_Q4K_NATIVE ? kq_geom(W->in_features, W->out_features)
+                                                             : native_geom(W->in_features, W->out_features);
     VlOp o;
     o.codes = reinterpret_cast<const uint8_t *>(W->codes);
     o.scales = reinterpret_cast<const uint8_t *>(W->scales);
@@ -942,13 +1158,15 @@ static cudaError_t launch_tc(const VlOps<MAXOPS> &P, void *ws, bool pdl, bool co
 }
 
 // 17..32 columns run on the tensor-core kernel unless the caller asks for the fragment kernel.
+// Q4_K native ops (C <= 8, checked by the callers) run the stream kernel on Q4_K units.
 template <int MAXOPS>
 static cudaError_t launch_ops(const VlOps<MAXOPS> &P, void *ws, bool pdl, cudaStream_t stream,
-                              bool fragment_mma = false) {
+                              bool fragment_mma = false, bool q4k = false) {
     int64_t max_units = 0;
     for (int i = 0; i < P.n; ++i)
         max_units = (int64_t)P.op[i].n_units > max_units ? (int64_t)P.op[i].n_units : max_units;
     const bool coop = P.n > 1;
+    if (q4k) return launch_stream<1, kNWq, kTWq, kRq, kUq, MAXOPS, 1>(P, ws, pdl, coop, max_units, stream);
     switch (ntiles_for(P.C)) {
         case 1: return launch_stream<1, kNW1, kTiles, kR1, kU, MAXOPS>(P, ws, pdl, coop, max_units, stream);
         case 2: return launch_stream<2, kNW2, kTW2, kR2, kU, MAXOPS>(P, ws, pdl, coop, max_units, stream);
@@ -989,7 +1207,9 @@ static int check_qweight(const svd_qweight *W) {
         return SVD_OK;
     }
     if (!W->scales) return SVD_ERR_INVALID_ARG;
-    if (W->layout != SVD_LAYOUT_CANONICAL && W->layout != SVD_LAYOUT_NATIVE)
+    if (W->layout == SVD_LAYOUT_Q4K_NATIVE && W->in_features % 256 != 0) return SVD_ERR_INVALID_ARG;
+    if (W->layout != SVD_LAYOUT_CANONICAL && W->layout != SVD_LAYOUT_NATIVE &&
+        W->layout != SVD_LAYOUT_Q4K_NATIVE)
         return SVD_ERR_INVALID_ARG;
     if (!aligned16(W->codes) || !aligned16(W->scales)) return SVD_ERR_INVALID_ARG;
     return SVD_OK;
@@ -1001,7 +1221,8 @@ int verify_linear_q4k(const svd_qweight *W, const void *X, int C, float *Y, bool
 // The stream-K kernel does its unit arithmetic in 32 bits: n_units * (workers + 1) must
 // stay below 2^32 (about 880 thousand units, 3.6 billion weights, on 152 SMs).
 static int check_native_size(const svd_qweight *W) {
-    const NativeGeom ng = native_geom(W->in_features, W->out_features);
+    const NativeGeom ng = W->layout == SVD_LAYOUT_Q4K_NATIVE ? kq_geom(W->in_features, W->out_features)
+                                                             : native_geom(W->in_features, W->out_features);
     const uint64_t workers = (uint64_t)sm_count() * kMaxCtasPerSm * 16 + 1;
     if ((uint64_t)ng.n_units * workers > 0xFFFFFFFFull) return SVD_ERR_UNSUPPORTED;
     return SVD_OK;
@@ -1015,7 +1236,9 @@ int verify_linear(const svd_qweight *W, const void *X, int C, float *Y, void *ws
     if (flags & ~(SVD_F_PDL | SVD_F_FRAGMENT_MMA)) return SVD_ERR_INVALID_ARG;
     const bool pdl = (flags & SVD_F_PDL) != 0;
     if (sm_count() < 1) return SVD_ERR_CUDA;
-    if (W->layout == SVD_LAYOUT_NATIVE) {
+    if (W->layout == SVD_LAYOUT_NATIVE || W->layout == SVD_LAYOUT_Q4K_NATIVE) {
+        const bool q4k = W->layout == SVD_LAYOUT_Q4K_NATIVE;
+        if (q4k && C > 8) return SVD_ERR_UNSUPPORTED;
         rc = check_native_size(W);
         if (rc != SVD_OK) return rc;
         if (!ws || ws_bytes < vl_workspace_bytes(W->in_features, W->out_features, C))
@@ -1024,7 +1247,7 @@ int verify_linear(const svd_qweight *W, const void *X, int C, float *Y, void *ws
         P.n = 1;
         P.C = C;
         P.op[0] = make_op(W, X, Y);
-        SVD_CUDA_TRY(launch_ops(P, ws, pdl, stream, (flags & SVD_F_FRAGMENT_MMA) != 0));
+        SVD_CUDA_TRY(launch_ops(P, ws, pdl, stream, (flags & SVD_F_FRAGMENT_MMA) != 0, q4k));
         return SVD_OK;
     }
     if (W->layout == SVD_LAYOUT_Q4K) {  // K-quant super-blocks: CUDA-core kernel (kquant.cu)
@@ -1060,10 +1283,13 @@ int verify_chain(const svd_linear_op *ops, int n_ops, int C, void *ws, size_t ws
                  cudaStream_t stream) {
     if (!ops || n_ops < 1 || C < 1 || C > SVD_C_MAX) return SVD_ERR_INVALID_ARG;
     if (flags & ~(SVD_F_PDL | SVD_F_FRAGMENT_MMA)) return SVD_ERR_INVALID_ARG;
+    // one layout for the whole chain: native, or Q4_K native (up to 8 columns)
+    const bool q4k = ops[0].W.layout == SVD_LAYOUT_Q4K_NATIVE;
+    if (q4k && C > 8) return SVD_ERR_UNSUPPORTED;
     for (int i = 0; i < n_ops; ++i) {
         const int rc = check_qweight(&ops[i].W);
         if (rc != SVD_OK) return rc;
-        if (ops[i].W.layout != SVD_LAYOUT_NATIVE) return SVD_ERR_INVALID_ARG;
+        if (ops[i].W.layout != (q4k ? SVD_LAYOUT_Q4K_NATIVE : SVD_LAYOUT_NATIVE)) return SVD_ERR_INVALID_ARG;
         if (check_native_size(&ops[i].W) != SVD_OK) return SVD_ERR_UNSUPPORTED;
         if (!ops[i].X || !ops[i].Y || !aligned16(ops[i].X)) return SVD_ERR_INVALID_ARG;
     }
@@ -1079,13 +1305,13 @@ int verify_chain(const svd_linear_op *ops, int n_ops, int C, void *ws, size_t ws
             P1.n = 1;
             P1.C = C;
             P1.op[0] = make_op(&ops[first].W, ops[first].X, ops[first].Y);
-            SVD_CUDA_TRY(launch_ops(P1, ws, first == 0 && (flags & SVD_F_PDL), stream, (flags & SVD_F_FRAGMENT_MMA) != 0));
+            SVD_CUDA_TRY(launch_ops(P1, ws, first == 0 && (flags & SVD_F_PDL), stream, (flags & SVD_F_FRAGMENT_MMA) != 0, q4k));
             continue;
         }
         P.n = n;
         P.C = C;
         for (int i = 0; i < n; ++i) P.op[i] = make_op(&ops[first + i].W, ops[first + i].X, ops[first + i].Y);
-        SVD_CUDA_TRY(launch_ops(P, ws, false, stream, (flags & SVD_F_FRAGMENT_MMA) != 0));
+        SVD_CUDA_TRY(launch_ops(P, ws, false, stream, (flags & SVD_F_FRAGMENT_MMA) != 0, q4k));
     }
     return SVD_OK;
 }
@@ -1098,9 +1324,45 @@ int native_sizes(int64_t in_f, int64_t out_f, size_t *cb, size_t *sb) {
     return SVD_OK;
 }
 
+int kq_native_sizes(int64_t in_f, int64_t out_f, size_t *cb, size_t *hb) {
+    if (in_f <= 0 || out_f <= 0 || in_f % kKqIn != 0) return SVD_ERR_INVALID_ARG;
+    const NativeGeom ng = kq_geom(in_f, out_f);
+    if (cb) *cb = (size_t)ng.n_units * kKqUnitCodeBytes;
+    if (hb) *hb = (size_t)ng.n_units * kKqUnitHdrBytes;
+    return SVD_OK;
+}
+
+static int kq_repack(const svd_qweight *src, void *dc, void *dh, cudaStream_t stream) {
+    if (!dc || !dh || !aligned16(dc) || !aligned16(dh)) return SVD_ERR_INVALID_ARG;
+    const NativeGeom ng = kq_geom(src->in_features, src->out_features);
+    const int64_t n_words = ng.n_units * (kKqUnitCodeBytes / 4);
+    const int64_t n_rows = ng.n_units * kRowsPerBlock;
+    kq_repack_codes_kernel<<<(unsigned)((n_words + 255) / 256), 256, 0, stream>>>(
+        reinterpret_cast<const uint8_t *>(src->codes), reinterpret_cast<uint32_t *>(dc),
+        src->in_features, src->out_features, ng.n_kc, n_words);
+    SVD_CUDA_TRY(cudaGetLastError());
+    kq_repack_hdr_kernel<<<(unsigned)((n_rows + 255) / 256), 256, 0, stream>>>(
+        reinterpret_cast<const uint8_t *>(src->codes), reinterpret_cast<uint4 *>(dh),
+        src->in_features, src->out_features, ng.n_kc, n_rows);
+    SVD_CUDA_TRY(cudaGetLastError());
+    return SVD_OK;
+}
+
+static int kq_unpack(const svd_qweight *src, void *dst, void *dnull, cudaStream_t stream) {
+    if (!dst || dnull) return SVD_ERR_INVALID_ARG;
+    const NativeGeom ng = kq_geom(src->in_features, src->out_features);
+    const int64_t nb = src->out_features * (src->in_features / kKqIn * kKqBlockBytes);
+    kq_unpack_kernel<<<(unsigned)((nb + 255) / 256), 256, 0, stream>>>(
+        reinterpret_cast<const uint32_t *>(src->codes), reinterpret_cast<const uint8_t *>(src->scales),
+        reinterpret_cast<uint8_t *>(dst), src->in_features, src->out_features, ng.n_kc);
+    SVD_CUDA_TRY(cudaGetLastError());
+    return SVD_OK;
+}
+
 int repack(const svd_qweight *src, void *dc, void *ds, cudaStream_t stream) {
     int rc = check_qweight(src);
     if (rc != SVD_OK) return rc;
+    if (src->layout == SVD_LAYOUT_Q4K) return kq_repack(src, dc, ds, stream);
     if (src->layout != SVD_LAYOUT_CANONICAL || !dc || !ds || !aligned16(dc) || !aligned16(ds))
         return SVD_ERR_INVALID_ARG;
     const NativeGeom ng = native_geom(src->in_features, src->out_features);
@@ -1120,6 +1382,7 @@ int repack(const svd_qweight *src, void *dc, void *ds, cudaStream_t stream) {
 int unpack(const svd_qweight *src, void *dc, void *ds, cudaStream_t stream) {
     int rc = check_qweight(src);
     if (rc != SVD_OK) return rc;
+    if (src->layout == SVD_LAYOUT_Q4K_NATIVE) return kq_unpack(src, dc, ds, stream);
     if (src->layout != SVD_LAYOUT_NATIVE || !dc || !ds) return SVD_ERR_INVALID_ARG;
     const NativeGeom ng = native_geom(src->in_features, src->out_features);
     const int64_t nb = src->out_features * (src->in_features / 2);

@@ -30,6 +30,7 @@ SVD_ST_EMPTY = 16
 SVD_LAYOUT_CANONICAL = 0
 SVD_LAYOUT_NATIVE = 1
 SVD_LAYOUT_Q4K = 2
+SVD_LAYOUT_Q4K_NATIVE = 3
 SVD_F_PDL = 1
 SVD_F_FRAGMENT_MMA = 2
 SVD_POLL_DEFAULT = 0xFFFFFFFF
@@ -41,7 +42,8 @@ SVD_KV_UNIT_BYTES = 3328
 
 # Every symbol include/svd.h declares (checked by the CPU test suite).
 EXPORTS = (
-    "svd_error_string", "svd_last_cuda_error", "svd_native_sizes", "svd_repack_weights",
+    "svd_error_string", "svd_last_cuda_error", "svd_native_sizes", "svd_q4k_native_sizes",
+    "svd_repack_weights",
     "svd_unpack_weights", "svd_verify_linear_workspace_bytes", "svd_verify_linear",
     "svd_verify_linear_noalloc", "svd_verify_chain_workspace_bytes", "svd_verify_chain",
     "svd_verify_status", "svd_verify_inject_stall",
@@ -122,6 +124,7 @@ def load(path: str = LIB_PATH):
             "svd_last_cuda_error": (i32, []),
             "svd_device_sm_count": (i32, []),
             "svd_native_sizes": (i32, [i64, i64, P, P]),
+            "svd_q4k_native_sizes": (i32, [i64, i64, P, P]),
             "svd_repack_weights": (i32, [P, P, P, P]),
             "svd_unpack_weights": (i32, [P, P, P, P]),
             "svd_verify_linear_workspace_bytes": (sz, [i64, i64, i32]),
@@ -210,6 +213,13 @@ def svd_native_sizes(in_features: int, out_features: int):
     _check("svd_native_sizes",
            load().svd_native_sizes(in_features, out_features, ctypes.byref(cb), ctypes.byref(sb)))
     return cb.value, sb.value
+
+
+def svd_q4k_native_sizes(in_features: int, out_features: int):
+    cb, hb = ctypes.c_size_t(), ctypes.c_size_t()
+    _check("svd_q4k_native_sizes", load().svd_q4k_native_sizes(
+        in_features, out_features, ctypes.byref(cb), ctypes.byref(hb)))
+    return cb.value, hb.value
 
 
 def svd_repack_weights(src: QWeight, dst_codes, dst_scales, stream=None):

@@ -7,7 +7,7 @@ import torch
 
 from oracle import kquant
 from speculative_decoding_verify_06_gb300 import svd, synth
-from gpu_helpers import DEV, assert_gemm_parity, lib, to_dev
+from gpu_helpers import DEV, assert_gemm_parity, lib, native_weight, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -65,4 +65,165 @@ def test_q4k_argument_errors():
     W = svd.QWeight(b, None, 512, 16, svd.SVD_LAYOUT_Q4K)
     with pytest.raises(svd.SvdError) as e:
         svd.svd_verify_chain([(W, X, Y)], 4, torch.zeros(1 << 20, dtype=torch.uint8, device=DEV))
+    assert e.value.code == svd.SVD_ERR_INVALID_ARG
+
+
+# ---- the Q4_K native layout: repacked super-blocks streamed by the tensor-core kernel ----------
+
+def q4k_native(blocks_dev, in_f, out_f):
+    cb, hb = svd.svd_q4k_native_sizes(in_f, out_f)
+    codes = torch.empty(cb, dtype=torch.uint8, device=DEV)
+    hdr = torch.empty(hb, dtype=torch.uint8, device=DEV)
+    svd.svd_repack_weights(svd.QWeight(blocks_dev, None, in_f, out_f, svd.SVD_LAYOUT_Q4K), codes, hdr)
+    return svd.QWeight(codes, hdr, in_f, out_f, svd.SVD_LAYOUT_Q4K_NATIVE), (codes, hdr)
+
+
+def run_native(W, x, out_f, ws=None, flags=0):
+    C = x.shape[0]
+    if ws is None:
+        ws = torch.zeros(svd.svd_verify_linear_workspace_bytes(W.in_features, out_f, C),
+                         dtype=torch.uint8, device=DEV)
+    Y = torch.full((C, out_f), float("nan"), dtype=torch.float32, device=DEV)
+    svd.svd_verify_linear(W, to_dev(x), C, Y, ws, flags=flags)
+    torch.cuda.synchronize()
+    return Y.cpu().numpy()
+
+
+@pytest.mark.parametrize("out_f,in_f", [(37, 768), (130, 512), (64, 256), (1, 2048)])
+def test_q4k_native_repack_round_trip(out_f, in_f):
+    lib()
+    blocks = synth.q4k_blocks(out_f, in_f, seed=out_f * 7 + in_f)
+    W, _ = q4k_native(to_dev(blocks), in_f, out_f)
+    back = torch.empty((out_f, in_f // 256 * 144), dtype=torch.uint8, device=DEV)
+    svd.svd_unpack_weights(W, back, None)
+    torch.cuda.synchronize()
+    assert np.array_equal(back.cpu().numpy(), blocks)
+
+
+@pytest.mark.parametrize("out_f,in_f,C", [
+    (37, 768, 1), (37, 768, 4), (64, 256, 8), (300, 5120, 3), (33, 2304, 5), (131, 4096, 2),
+    (8, 2048, 6), (1, 256, 7), (200, 17408, 4), (1100, 1280, 8),
+])
+def test_q4k_native_matches_oracle(out_f, in_f, C):
+    lib()
+    blocks = synth.q4k_blocks(out_f, in_f, seed=out_f + 3 * in_f + C)
+    x = synth.activations(C, in_f, seed=C + 11)
+    W, _ = q4k_native(to_dev(blocks), in_f, out_f)
+    y = run_native(W, x, out_f, flags=svd.SVD_F_PDL if C % 2 else 0)
+    y_ref, a_ref = kquant.verify_linear(blocks, in_f, x)
+    assert_gemm_parity(y, y_ref, a_ref)
+
+
+def test_q4k_native_edge_values():
+    """Zero and extreme scale fields: d = 0 rows, dmin = 0 rows, all sc and m at 63, codes all 0
+    or all 15, large activations."""
+    lib()
+    out_f, in_f, C = 64, 512, 4
+    blocks = synth.q4k_blocks(out_f, in_f, seed=5).reshape(out_f, 2, 144)
+    blocks[0:8, :, 0:2] = 0                                  # d = 0: only the mins remain
+    blocks[8:16, :, 2:4] = 0                                 # dmin = 0: no mins
+    blocks[16:24, :, 4:16] = 0xFF                            # every sc, m = 63
+    blocks[24:32, :, 16:] = 0x00                             # codes 0
+    blocks[32:40, :, 16:] = 0xFF                             # codes 15
+    blocks = blocks.reshape(out_f, 2 * 144)
+    x = synth.activations(C, in_f, seed=6, std=30.0)
+    W, _ = q4k_native(to_dev(blocks), in_f, out_f)
+    y = run_native(W, x, out_f)
+    y_ref, a_ref = kquant.verify_linear(blocks, in_f, x)
+    assert_gemm_parity(y, y_ref, a_ref)
+
+
+@pytest.mark.parametrize("out_f,in_f", [(7168, 5120), (5120, 17408), (34816, 5120)])
+def test_q4k_native_full_size_sampled_rows(out_f, in_f):
+    lib()
+    C = 4
+    b = synth.q4k_blocks_torch(out_f, in_f, seed=13, device=DEV)
+    W, keep = q4k_native(b, in_f, out_f)
+    x = synth.activations(C, in_f, seed=14)
+    y = run_native(W, x, out_f)
+    rows = np.unique(np.r_[synth.rng(15).choice(out_f, 40, replace=False), 0, 63, 64, out_f - 1])
+    host = b[torch.as_tensor(rows, device=DEV)].cpu().numpy()
+    y_ref, a_ref = kquant.verify_linear(host, in_f, x)
+    assert_gemm_parity(y[:, rows], y_ref, a_ref)
+
+
+@pytest.mark.parametrize("C", [1, 4, 8])
+def test_q4k_native_chain_equals_single_launches_and_oracle(C):
+    lib()
+    shapes = [(5120, 1024), (96, 256), (544, 2048), (2048, 160), (64, 512), (1024, 3000)]
+    mats, ops, keep = [], [], []
+    for i, (in_f, out_f) in enumerate(shapes):
+        in_f = (in_f + 255) // 256 * 256
+        blocks = synth.q4k_blocks(out_f, in_f, seed=100 + i + C)
+        x = synth.activations(C, in_f, seed=200 + i)
+        W, k = q4k_native(to_dev(blocks), in_f, out_f)
+        keep.append(k)
+        mats.append((blocks, in_f, x))
+        ops.append((W, to_dev(x), torch.full((C, out_f), float("nan"), dtype=torch.float32, device=DEV)))
+    ws = torch.zeros(svd.svd_verify_chain_workspace_bytes(ops, C), dtype=torch.uint8, device=DEV)
+    svd.svd_verify_chain(ops, C, ws)
+    torch.cuda.synchronize()
+    chained = [Y.clone() for _, _, Y in ops]
+    for (W, X, Y), ref in zip(ops, chained):
+        Y.fill_(float("nan"))
+        svd.svd_verify_linear(W, X, C, Y, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(Y, ref)
+    for (blocks, in_f, x), y in zip(mats, chained):
+        y_ref, a_ref = kquant.verify_linear(blocks, in_f, x)
+        assert_gemm_parity(y.cpu().numpy(), y_ref, a_ref)
+
+
+def test_q4k_native_chain_reads_what_the_previous_op_wrote():
+    lib()
+    C, in_f, out_f = 4, 256, 128
+    blocks = synth.q4k_blocks(out_f, in_f, seed=21)
+    W, keep = q4k_native(to_dev(blocks), in_f, out_f)
+    X = to_dev(synth.activations(C, in_f, seed=22))
+
+    def run(chained):
+        Y0 = torch.zeros((C, out_f), dtype=torch.float32, device=DEV)
+        X1 = Y0.view(torch.int16)  # [C][256] bf16 bit patterns
+        Y1 = torch.zeros((C, out_f), dtype=torch.float32, device=DEV)
+        ops = [(W, X, Y0), (W, X1, Y1)]
+        ws = torch.zeros(svd.svd_verify_chain_workspace_bytes(ops, C), dtype=torch.uint8, device=DEV)
+        if chained:
+            svd.svd_verify_chain(ops, C, ws)
+        else:
+            for Wi, Xi, Yi in ops:
+                svd.svd_verify_linear(Wi, Xi, C, Yi, ws)
+        torch.cuda.synchronize()
+        return Y1.view(torch.int32).clone()
+
+    a, b = run(True), run(False)
+    assert torch.equal(a, b)
+    assert torch.count_nonzero(a) > 0
+
+
+def test_q4k_native_argument_errors():
+    lib()
+    blocks = to_dev(synth.q4k_blocks(16, 512, seed=1))
+    W, keep = q4k_native(blocks, 512, 16)
+    X = to_dev(synth.activations(9, 512, seed=2))
+    Y = torch.empty((9, 16), dtype=torch.float32, device=DEV)
+    ws = torch.zeros(svd.svd_verify_linear_workspace_bytes(512, 16, 9), dtype=torch.uint8, device=DEV)
+    with pytest.raises(svd.SvdError) as e:                       # C > 8
+        svd.svd_verify_linear(W, X, 9, Y, ws)
+    assert e.value.code == svd.SVD_ERR_UNSUPPORTED
+    with pytest.raises(svd.SvdError) as e:                       # no workspace
+        svd.svd_verify_linear(W, X, 4, Y, None)
+    assert e.value.code == svd.SVD_ERR_WORKSPACE
+    with pytest.raises(svd.SvdError) as e:                       # in % 256
+        svd.svd_verify_linear(svd.QWeight(W.codes, W.scales, 480, 16, svd.SVD_LAYOUT_Q4K_NATIVE), X, 4, Y, ws)
+    assert e.value.code == svd.SVD_ERR_INVALID_ARG
+    with pytest.raises(svd.SvdError) as e:                       # unpack wants dst_scales NULL
+        svd.svd_unpack_weights(W, torch.empty(16 * 288, dtype=torch.uint8, device=DEV), ws)
+    assert e.value.code == svd.SVD_ERR_INVALID_ARG
+    # a chain takes one layout
+    codes, scales = synth.qweight(16, 512, seed=3)
+    Wn, _ = native_weight(codes, scales)
+    ops = [(W, X, Y), (Wn, X, Y)]
+    cws = torch.zeros(svd.svd_verify_chain_workspace_bytes(ops, 4), dtype=torch.uint8, device=DEV)
+    with pytest.raises(svd.SvdError) as e:
+        svd.svd_verify_chain(ops, 4, cws)
     assert e.value.code == svd.SVD_ERR_INVALID_ARG
