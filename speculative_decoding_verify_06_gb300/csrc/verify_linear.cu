@@ -257,15 +257,13 @@ __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t a[4]) {
     }
 }
 
-// The same with the value q itself (subtract 128): the Q4_K codes.
-__device__ __forceinline__ void dequant_word_q(uint32_t w, uint32_t a[4]) {
-    const uint32_t magic = 0x43004300u;
+// The pairs (128 + q_lo, 128 + q_hi) alone, without the subtraction: the Q4_K path takes the
+// 128 x (sum of the activations) out afterwards, once per tile and unit.
+__device__ __forceinline__ void dequant_word_b128(uint32_t w, uint32_t a[4]) {
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
-        uint32_t v;
         const uint32_t sh = w >> (4 * p);
-        asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(v) : "r"(sh), "r"(0x000F000Fu), "r"(magic));
-        asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(a[p]) : "r"(v), "r"(magic));
+        asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(a[p]) : "r"(sh), "r"(0x000F000Fu), "r"(0x43004300u));
     }
 }
 
@@ -340,8 +338,9 @@ struct VlCfg {
     static constexpr size_t kRing = (size_t)kNG * R * kSlotBytes;
     static constexpr size_t kPark = (size_t)NW * 2 * 32 * kAccW * sizeof(float);
     // Q4_K: each warp's decoded headers of its rows of the current unit (floats): sub-block
-    // scales [TW][8 j][8 g][2], min pairs [TW * 16 rows][4] (bf16x2), (d, dmin) [TW * 16 rows]
-    static constexpr int kKqScrW = TW * 224;
+    // scales [TW][8 j][8 g][2]; per row the pairs (m[2t], m[2t+1]) then (sc[2t], sc[2t+1]) as
+    // bf16x2 [TW * 16 rows][8]; (d, dmin) [TW * 16 rows]
+    static constexpr int kKqScrW = TW * 288;
     static constexpr size_t kScratch = KQ ? (size_t)NW * kKqScrW * sizeof(float) : 0;
     static constexpr size_t kSmem = kRing + kPark + kScratch + (size_t)MAXOPS * sizeof(VlOp);
     static_assert(!KQ || NT == 1, "Q4_K units take up to 8 columns");
@@ -645,7 +644,7 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
                     const uint8_t *hbase = ring + slot * kSlotBytes + U * kUC + in_slot * kUS;
                     float *sc_s = kq_scr;
                     uint32_t *m_s = reinterpret_cast<uint32_t *>(kq_scr + TW * 128);
-                    float2 *d_s = reinterpret_cast<float2 *>(kq_scr + TW * 192);
+                    float2 *d_s = reinterpret_cast<float2 *>(kq_scr + TW * 256);
                     // decode the headers of this warp's rows: lane l takes local rows l, l + 32, ...
                     for (int lr = lane; lr < TW * 16; lr += 32) {
                         const uint4 hd = *reinterpret_cast<const uint4 *>(hbase + (sub * TW * 16 + lr) * 16);
@@ -661,18 +660,22 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
                         const int r = lr >> 4, rt = lr & 15, g = rt & 7, hh = rt >> 3;
 #pragma unroll
                         for (int j = 0; j < 8; ++j) sc_s[((r * 8 + j) * 8 + g) * 2 + hh] = (float)scv[j];
-                        uint32_t mw[4];  // (m[2t], m[2t+1]) as bf16 pairs, exact (m < 64)
+                        uint32_t mw[8];  // (m[2t], m[2t+1]), (sc[2t], sc[2t+1]) as bf16 pairs, exact (< 64)
 #pragma unroll
-                        for (int t = 0; t < 4; ++t)
+                        for (int t = 0; t < 4; ++t) {
                             mw[t] = (__float_as_uint((float)mv[2 * t]) >> 16) |
                                     (__float_as_uint((float)mv[2 * t + 1]) & 0xFFFF0000u);
-                        *reinterpret_cast<uint4 *>(m_s + lr * 4) = make_uint4(mw[0], mw[1], mw[2], mw[3]);
+                            mw[4 + t] = (__float_as_uint((float)scv[2 * t]) >> 16) |
+                                        (__float_as_uint((float)scv[2 * t + 1]) & 0xFFFF0000u);
+                        }
+                        *reinterpret_cast<uint4 *>(m_s + lr * 8) = make_uint4(mw[0], mw[1], mw[2], mw[3]);
+                        *reinterpret_cast<uint4 *>(m_s + lr * 8 + 4) = make_uint4(mw[4], mw[5], mw[6], mw[7]);
                         d_s[lr] = make_float2(__half2float(__ushort_as_half((unsigned short)(hd.x & 0xFFFFu))),
                                               __half2float(__ushort_as_half((unsigned short)(hd.x >> 16))));
                     }
                     __syncwarp();
-                    // per tile T = sum_j sc_j (sum_{i in j} q_i x_i); and the sub-block sums of x
-                    // as an MMA of X (rows = columns) against an indicator: D[col][j] = sum_{i in j} x
+                    // per tile T = sum_j sc_j (sum_{i in j} (128 + q_i) x_i); and the sub-block sums
+                    // of x as an MMA of X (rows = columns) against an indicator: D[col][j] = sum_{i in j} x
                     float T[TW][4], xsd[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int r = 0; r < TW; ++r)
@@ -695,8 +698,8 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
 #pragma unroll
                             for (int blk = 0; blk < 2; ++blk) {
                                 uint32_t a0[4], a1[4];
-                                dequant_word_q(blk ? cw.z : cw.x, a0);
-                                dequant_word_q(blk ? cw.w : cw.y, a1);
+                                dequant_word_b128(blk ? cw.z : cw.x, a0);
+                                dequant_word_b128(blk ? cw.w : cw.y, a1);
                                 const float2 sc2 = *reinterpret_cast<const float2 *>(sc_s + ((r * 8 + 2 * s4 + blk) * 8 + g4) * 2);
                                 float d4[4] = {0.f, 0.f, 0.f, 0.f};
                                 mma_bf16_16816(d4, a0, xq[0][blk].x, xq[0][blk].y);
@@ -717,7 +720,8 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
                         }
                     }
                     // lane (g, t) holds the sums of sub-blocks 2t, 2t+1 for column g: exactly the
-                    // B fragment of the mins' product sum_j m_j xs_j, split into bf16 hi + lo
+                    // B fragment of the products sum_j m_j xs_j (the mins) and sum_j sc_j xs_j (the
+                    // 128 offset of the codes), with xs split into bf16 hi + lo
                     const __nv_bfloat162 hi2 = __floats2bfloat162_rn(xsd[0], xsd[1]);
                     const float2 hif = __bfloat1622float2(hi2);
                     const __nv_bfloat162 lo2 = __floats2bfloat162_rn(xsd[0] - hif.x, xsd[1] - hif.y);
@@ -725,15 +729,17 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
                     const uint32_t bl = *reinterpret_cast<const uint32_t *>(&lo2);
 #pragma unroll
                     for (int r = 0; r < TW; ++r) {
-                        const uint32_t m0 = m_s[(16 * r + g4) * 4 + t4], m1 = m_s[(16 * r + g4 + 8) * 4 + t4];
-                        const uint32_t am[4] = {m0, m1, m0, m1};
-                        float d2[4] = {0.f, 0.f, 0.f, 0.f};
-                        mma_bf16_16816(d2, am, bh, bl);
+                        const uint32_t *p0 = m_s + (16 * r + g4) * 8 + t4, *p1 = m_s + (16 * r + g4 + 8) * 8 + t4;
+                        const uint32_t am[4] = {p0[0], p1[0], p0[0], p1[0]};
+                        const uint32_t as[4] = {p0[4], p1[4], p0[4], p1[4]};
+                        float dm[4] = {0.f, 0.f, 0.f, 0.f}, ds[4] = {0.f, 0.f, 0.f, 0.f};
+                        mma_bf16_16816(dm, am, bh, bl);
+                        mma_bf16_16816(ds, as, bh, bl);
                         const float2 e0 = d_s[16 * r + g4], e1 = d_s[16 * r + g4 + 8];
-                        acc[r][0][0] = fmaf(e0.x, T[r][0], fmaf(-e0.y, d2[0], acc[r][0][0]));
-                        acc[r][0][1] = fmaf(e0.x, T[r][1], fmaf(-e0.y, d2[1], acc[r][0][1]));
-                        acc[r][0][2] = fmaf(e1.x, T[r][2], fmaf(-e1.y, d2[2], acc[r][0][2]));
-                        acc[r][0][3] = fmaf(e1.x, T[r][3], fmaf(-e1.y, d2[3], acc[r][0][3]));
+                        acc[r][0][0] = fmaf(e0.x, fmaf(-128.f, ds[0], T[r][0]), fmaf(-e0.y, dm[0], acc[r][0][0]));
+                        acc[r][0][1] = fmaf(e0.x, fmaf(-128.f, ds[1], T[r][1]), fmaf(-e0.y, dm[1], acc[r][0][1]));
+                        acc[r][0][2] = fmaf(e1.x, fmaf(-128.f, ds[2], T[r][2]), fmaf(-e1.y, dm[2], acc[r][0][2]));
+                        acc[r][0][3] = fmaf(e1.x, fmaf(-128.f, ds[3], T[r][3]), fmaf(-e1.y, dm[3], acc[r][0][3]));
                     }
                     __syncwarp();  // the scratch is rewritten for the next unit
                 } else {
@@ -1009,9 +1015,18 @@ constexpr int kR2 = 2;            // ring slots per worker group, C <= 32
 constexpr int kNW4 = 8;           // warps per CTA, 16 < C <= 32: one warp per unit (all four row
 constexpr int kTW4 = 4;           // tiles), so each activation fragment serves four tiles; 255
                                   // registers a thread hold the accumulators (16 warps spill)
-constexpr int kNWq = 16;          // Q4_K units (64 rows x 256 inputs, 9 KB), C <= 8: two warps
-constexpr int kTWq = 2;           // per unit, each on two 16-row tiles; one unit per slot, two
-constexpr int kRq = 2;            // slots per worker group
+#ifndef SVD_TWQ
+#define SVD_TWQ 2
+#endif
+#ifndef SVD_RQ
+#define SVD_RQ 2
+#endif
+#ifndef SVD_NWQ
+#define SVD_NWQ 16
+#endif
+constexpr int kNWq = SVD_NWQ;     // Q4_K units (64 rows x 256 inputs, 9 KB), C <= 8: two warps
+constexpr int kTWq = SVD_TWQ;     // per unit, each on two 16-row tiles; one unit per slot, two
+constexpr int kRq = SVD_RQ;       // slots per worker group
 constexpr int kUq = 1;
 constexpr int kMaxCtasPerSm = 2;  // the workspace holds partial slots for this many
 constexpr int kChainMax = 256;    // ops per chain launch (kernel parameters, ~16 KB)
