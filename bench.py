@@ -523,6 +523,39 @@ def kv_read(dev, peak, stack_ms, layers=64, contexts=KV_CONTEXTS, steps=10, C=4,
     return out
 
 
+def q4k_stack(dev, peak, tail_ms, layers=64, C=4, steps=20):
+    """The stack with Q4_K super-block weights (stack.Q4kStack: the pages' checkpoint format,
+    repacked once into the Q4_K native layout; one chain launch in a CUDA graph), timed like the
+    main stack; the pass rate adds the lm_head/sampler/acceptance tail of the main timed region."""
+    import torch
+
+    from speculative_decoding_verify_06_gb300 import stack, svd
+    qs = stack.Q4kStack(layers=layers, C=C, seed=11, device=dev).capture()
+    s = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        qs.launch(s)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        qs.launch(s)
+    e1.record(s)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    nbytes = qs.stack_bytes()
+    rc, bits = svd.svd_verify_status(qs.ws)
+    out = {"C": C, "stack_ms": ms, "bytes": nbytes, "gb_s": nbytes / ms / 1e6,
+           "frac": nbytes / ms / 1e6 / peak, "passes_per_s": 1000.0 / (ms + tail_ms),
+           "status_bits": bits,
+           "kernel": "vl_stream_kernel on Q4_K units (64 rows x 256 inputs), one chain launch",
+           "workload": (f"{layers} layers x (q|k|v 5120->7168, o 5120->5120, gate|up "
+                        "5120->34816, down 17408->5120) in Q4_K super-blocks (fp16 d, dmin, "
+                        "6-bit sub-block scales and mins, 4-bit codes), C = K+1 = 4")}
+    del qs
+    torch.cuda.empty_cache()
+    return out
+
+
 def pass_with_kv(vp, dev, peak, tail_ms, context=32768, steps=20):
     """The verify pass with each layer's KV cache in its place (stack.KvPass: the window's keys
     and values appended, then attention over the layer's own cache, between its q|k|v and o
@@ -692,6 +725,9 @@ def run_svd(args, rank, world, local_rank):
                                   oracle_sample=(rank == 0 and world == 1
                                                  and not args.no_cpu_baseline))
         line["pass_with_kv"] = pass_with_kv(vp, dev, peak, line["stack"]["tail_ms"])
+    if not args.no_q4k and not args.stack_only:
+        line["q4k_stack"] = q4k_stack(dev, peak, line["stack"]["tail_ms"], layers=args.layers,
+                                      C=args.C if args.C <= 8 else 4)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         smp = OracleSample()  # one whole pass on every host thread
         times = [smp.step()]
@@ -727,6 +763,8 @@ def main():
                     help="print only the KV-read measurement")
     ap.add_argument("--kv-contexts", default=",".join(str(c) for c in KV_CONTEXTS),
                     help="comma-separated context lengths of the KV-read measurement")
+    ap.add_argument("--no-q4k", action="store_true",
+                    help="skip the stack in Q4_K super-block weights")
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the window-width sweep and the acceptance-throughput sample")
     ap.add_argument("--stack-only", action="store_true",

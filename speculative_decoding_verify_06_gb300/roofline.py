@@ -15,6 +15,12 @@ def linear_bytes(in_f: int, out_f: int, C: int) -> int:
     return out_f * in_f // 2 + out_f * (in_f // 32) * 2 + C * in_f * 2 + C * out_f * 4
 
 
+def q4k_linear_bytes(in_f: int, out_f: int, C: int) -> int:
+    """Algorithmic bytes of one verify-linear launch on Q4_K weights: 144 bytes per super-block
+    of 256 weights (the same 4.5 bits per weight as the symmetric format)."""
+    return out_f * (in_f // 256) * 144 + C * in_f * 2 + C * out_f * 4
+
+
 def linear_weight_bytes(in_f: int, out_f: int) -> int:
     return out_f * in_f // 2 + out_f * (in_f // 32) * 2
 

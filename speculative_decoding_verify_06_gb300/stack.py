@@ -210,6 +210,58 @@ class ColumnsView:
         return self.vp.layers * sum(roofline.linear_bytes(i, o, self.C) for i, o in self.vp.gemms)
 
 
+class Q4kStack:
+    """The 27B-shaped stack in the pages' own checkpoint format: every matrix drawn as Q4_K
+    super-blocks ("100 tokens per second ...", "The wall": UD-Q4_K_XL / Q4_K_M), repacked once
+    into the Q4_K native layout, and the 256 products run as one chain launch recorded in a CUDA
+    graph -- the same pass as VerifyPass's stack with the K-quant weights in place of the
+    symmetric 4.5-bit format (the same 144 bytes per 256 weights)."""
+
+    def __init__(self, layers: int = synth.LAYERS, C: int = 4, seed: int = 0, device="cuda",
+                 gemms=synth.LAYER_GEMMS):
+        self.device = torch.device(device)
+        self.C, self.layers, self.gemms = C, layers, tuple(gemms)
+        self.ops, self._keep = [], []
+        for l in range(layers):
+            for g, (i, o) in enumerate(self.gemms):
+                raw = synth.q4k_blocks_torch(o, i, seed * 100003 + 1000 * l + g, self.device)
+                cb, hb = svd.svd_q4k_native_sizes(i, o)
+                codes = torch.empty(cb, dtype=torch.uint8, device=self.device)
+                hdr = torch.empty(hb, dtype=torch.uint8, device=self.device)
+                svd.svd_repack_weights(svd.QWeight(raw, None, i, o, svd.SVD_LAYOUT_Q4K), codes, hdr)
+                del raw
+                W = svd.QWeight(codes, hdr, i, o, svd.SVD_LAYOUT_Q4K_NATIVE)
+                X = synth.activations_torch(C, i, seed * 100003 + 7919 + 1000 * l + g, self.device)
+                Y = torch.empty((C, o), dtype=torch.float32, device=self.device)
+                self.ops.append((W, X, Y))
+                self._keep.append((codes, hdr))
+        self.ws = torch.zeros(svd.svd_verify_chain_workspace_bytes(self.ops, C), dtype=torch.uint8,
+                              device=self.device)
+        self.graph = None
+        torch.cuda.synchronize(self.device)
+
+    def enqueue(self, stream=None):
+        svd.svd_verify_chain(self.ops, self.C, self.ws, stream=stream)
+
+    def capture(self):
+        s = torch.cuda.Stream(device=self.device)
+        s.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(s):
+            self.enqueue(s)
+            s.synchronize()
+            svd.svd_graph_begin(s)
+            self.enqueue(s)
+            self.graph = svd.svd_graph_end(s)
+        s.synchronize()
+        return self
+
+    def launch(self, stream=None):
+        self.graph.launch(stream)
+
+    def stack_bytes(self) -> int:
+        return self.layers * sum(roofline.q4k_linear_bytes(i, o, self.C) for i, o in self.gemms)
+
+
 class KvPass:
     """The resident weights of a VerifyPass with every layer's KV cache in its place, between the
     layer's q|k|v product and its o product: svd_kv_attention_append -- the window's keys and

@@ -227,3 +227,23 @@ def test_q4k_native_argument_errors():
     with pytest.raises(svd.SvdError) as e:
         svd.svd_verify_chain(ops, 4, cws)
     assert e.value.code == svd.SVD_ERR_INVALID_ARG
+
+
+def test_q4k_stack_graph_matches_oracle():
+    """stack.Q4kStack (the bench's Q4_K stack, one chain launch replayed from a CUDA graph) on a
+    small two-layer stack: every product matches the oracle on the weights read back from the
+    native layout, and no wait gave up."""
+    from speculative_decoding_verify_06_gb300 import stack
+    lib()
+    qs = stack.Q4kStack(layers=2, C=4, seed=3, device=DEV, gemms=((512, 768), (768, 256))).capture()
+    for Y in (op[2] for op in qs.ops):
+        Y.fill_(float("nan"))
+    qs.launch()
+    torch.cuda.synchronize()
+    assert svd.svd_verify_status(qs.ws) == (svd.SVD_OK, 0)
+    for W, X, Y in qs.ops:
+        raw = torch.empty((W.out_features, W.in_features // 256 * 144), dtype=torch.uint8, device=DEV)
+        svd.svd_unpack_weights(W, raw, None)
+        x = X.view(torch.int16).cpu().numpy().view(np.uint16)
+        y_ref, a_ref = kquant.verify_linear(raw.cpu().numpy(), W.in_features, x)
+        assert_gemm_parity(Y.cpu().numpy(), y_ref, a_ref)
