@@ -523,7 +523,7 @@ def kv_read(dev, peak, stack_ms, layers=64, contexts=KV_CONTEXTS, steps=10, C=4,
     return out
 
 
-def q4k_stack(dev, peak, tail_ms, layers=64, C=4, steps=20):
+def q4k_stack(dev, peak, tail_ms, layers=64, C=4, steps=20, oracle_sample=False):
     """The stack with Q4_K super-block weights (stack.Q4kStack: the pages' checkpoint format,
     repacked once into the Q4_K native layout; one chain launch in a CUDA graph), timed like the
     main stack; the pass rate adds the lm_head/sampler/acceptance tail of the main timed region."""
@@ -553,7 +553,27 @@ def q4k_stack(dev, peak, tail_ms, layers=64, C=4, steps=20):
                         "6-bit sub-block scales and mins, 4-bit codes), C = K+1 = 4")}
     del qs
     torch.cuda.empty_cache()
+    if oracle_sample:
+        out["cpu_baseline"] = q4k_oracle_sample()
     return out
+
+
+def q4k_oracle_sample(out_f=5120, in_f=5120, C=4, seed=12):
+    """The Q4_K oracle (fp64 numpy: dequantisation of every weight, then the product) on one
+    o-projection-shaped matrix, as Q4_K bytes per second."""
+    from oracle import kquant
+    from speculative_decoding_verify_06_gb300 import synth
+    blocks = synth.q4k_blocks(out_f, in_f, seed)
+    x = synth.activations(C, in_f, seed + 1)
+    t0 = time.perf_counter()
+    kquant.verify_linear(blocks, in_f, x)
+    dt = time.perf_counter() - t0
+    nbytes = out_f * (in_f // 256) * 144 + C * in_f * 2 + C * out_f * 4
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+            "seconds": dt,
+            "sample": (f"one {in_f}->{out_f} Q4_K matrix at C = {C} through oracle/kquant.py "
+                       "(fp64 numpy; the product on the BLAS threads numpy was built with, up to "
+                       "the host's cores); GB/s of its algorithmic bytes")}
 
 
 def pass_with_kv(vp, dev, peak, tail_ms, context=32768, steps=20):
@@ -727,7 +747,9 @@ def run_svd(args, rank, world, local_rank):
         line["pass_with_kv"] = pass_with_kv(vp, dev, peak, line["stack"]["tail_ms"])
     if not args.no_q4k and not args.stack_only:
         line["q4k_stack"] = q4k_stack(dev, peak, line["stack"]["tail_ms"], layers=args.layers,
-                                      C=args.C if args.C <= 8 else 4)
+                                      C=args.C if args.C <= 8 else 4,
+                                      oracle_sample=(rank == 0 and world == 1
+                                                     and not args.no_cpu_baseline))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         smp = OracleSample()  # one whole pass on every host thread
         times = [smp.step()]
