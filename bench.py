@@ -787,6 +787,8 @@ def main():
                     help="comma-separated context lengths of the KV-read measurement")
     ap.add_argument("--no-q4k", action="store_true",
                     help="skip the stack in Q4_K super-block weights")
+    ap.add_argument("--q4k-only", action="store_true",
+                    help="print only the Q4_K stack measurement (for profiling small stacks)")
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the window-width sweep and the acceptance-throughput sample")
     ap.add_argument("--stack-only", action="store_true",
@@ -811,6 +813,17 @@ def main():
         ctxs = tuple(int(c) for c in args.kv_contexts.split(","))
         print(json.dumps({"kv_read": kv_read(dev, peak, None, layers=args.layers,
                                              contexts=ctxs, steps=args.steps)}), flush=True)
+        return
+    if args.q4k_only:
+        import torch
+
+        from speculative_decoding_verify_06_gb300 import build
+        build.build_library()
+        dev = torch.device("cuda", local_rank)
+        torch.cuda.set_device(dev)
+        peak, _ = peaks()
+        print(json.dumps({"q4k_stack": q4k_stack(dev, peak, 0.0, layers=args.layers,
+                                                 C=args.C, steps=args.steps)}), flush=True)
         return
     if world > 1:
         import torch
