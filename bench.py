@@ -114,10 +114,10 @@ def kernel_source_sha16() -> str:
     return h.hexdigest()[:16]
 
 
-def kernel_traffic():
+def kernel_traffic(summary="vl_stream_kernel_27b_stack_c4.txt"):
     """DRAM traffic per launch of the stack's verify-linear kernel from the committed ncu
     summary, if it was taken on the current kernel source (else None)."""
-    prof = os.path.join(ROOT, "profiles", "vl_stream_kernel_27b_stack_c4.txt")
+    prof = os.path.join(ROOT, "profiles", summary)
     try:
         sha = kernel_source_sha16()
         txt = open(prof).read()
@@ -544,8 +544,10 @@ def q4k_stack(dev, peak, tail_ms, layers=64, C=4, steps=20, oracle_sample=False)
     ms = e0.elapsed_time(e1) / steps
     nbytes = qs.stack_bytes()
     rc, bits = svd.svd_verify_status(qs.ws)
+    traffic = kernel_traffic("vl_stream_kernel_q4k_27b_stack_c4.txt") if (layers == 64 and C == 4) else None
     out = {"C": C, "stack_ms": ms, "bytes": nbytes, "gb_s": nbytes / ms / 1e6,
            "frac": nbytes / ms / 1e6 / peak, "passes_per_s": 1000.0 / (ms + tail_ms),
+           "traffic": traffic,
            "status_bits": bits,
            "kernel": "vl_stream_kernel on Q4_K units (64 rows x 256 inputs), one chain launch",
            "workload": (f"{layers} layers x (q|k|v 5120->7168, o 5120->5120, gate|up "
