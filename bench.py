@@ -247,11 +247,32 @@ def lm_head_oracle_windows(n_windows: int = 16, threads: int = 0):
                                      f"+ sampler over 6 rows), fp64"}
 
 
+REF_BUDGET_S = 240.0  # host seconds the reference arm may take, warm-up included
+
+
+def ref_sample_layers(t_pass: float, n_steps: int, budget: float = REF_BUDGET_S,
+                      layers: int = 64) -> int:
+    """Layers per step so that n_steps more steps fit in what is left of the budget after the
+    first whole pass of t_pass seconds (all of them while whole passes fit; at least one)."""
+    left = budget - t_pass
+    if n_steps <= 0 or n_steps * t_pass <= left:
+        return layers
+    return max(1, min(layers, int(layers * left / (n_steps * t_pass))))
+
+
 def run_reference(args, rank):
+    """The oracle as the reference arm: one whole pass per step while (steps + warmup) whole
+    passes fit in REF_BUDGET_S, else each step a bounded sample of the pass (a share of the
+    layers and of the lm_head rows, sized from the first warm-up pass); ms_per_step is the time of
+    the work each step ran, and the value scales it to passes/s."""
     if rank != 0:
         return
     smp = OracleSample()  # one whole pass per step
-    for _ in range(args.warmup):
+    t_first = smp.step()  # the first warm-up step, which also sizes the others
+    layers = ref_sample_layers(t_first, args.warmup - 1 + args.steps)
+    if layers < 64:
+        smp = OracleSample(layers=layers)
+    for _ in range(args.warmup - 1):
         smp.step()
     times = [smp.step() for _ in range(args.steps)]
     v = smp.passes_per_s(times)
@@ -262,7 +283,8 @@ def run_reference(args, rank):
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "C": 4, "oracle": "fp64 C, OpenMP", "cpu": _cpu_model()},
         "cpu_baseline": {"value": v, "unit": UNIT, "cores": smp.threads, "kind": "oracle",
-                         "sample": smp.describe(args.steps)},
+                         "sample": smp.describe(args.steps), "pass_fraction_per_step": smp.fraction,
+                         "first_whole_pass_s": t_first},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

@@ -69,3 +69,16 @@ def test_reference_arm_prints_on_rank_zero_only():
     with contextlib.redirect_stdout(buf):
         bench.run_reference(args, rank=1)
     assert buf.getvalue() == ""
+
+
+def test_reference_arm_sample_sizing():
+    import bench
+    # 23 whole passes of 8.4 s fit in 240 s: whole passes
+    assert bench.ref_sample_layers(8.4, 22, budget=240.0) == 64
+    # 510 steps do not: a share of the layers so that they fit in what the first pass left
+    n = bench.ref_sample_layers(8.4, 509, budget=240.0)
+    assert n == int(64 * (240.0 - 8.4) / (509 * 8.4))
+    assert n * 509 * 8.4 / 64 <= 240.0 - 8.4
+    # never below one layer, never above all of them
+    assert bench.ref_sample_layers(100.0, 1000, budget=240.0) == 1
+    assert bench.ref_sample_layers(1.0, 0, budget=240.0) == 64
