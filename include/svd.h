@@ -270,12 +270,19 @@ int svd_sampler_probs(const float *logits, int rows, int64_t V, const svd_sample
 /* lm_head projection of every window position followed by the sampler: logits = W_lm^T H
  * ([positions][vocabulary], the HN thread's [4, vocabulary_size] tensor), then
  * svd_sampler_probs.  W_lm must be NATIVE (hidden x vocabulary).  H: bf16 [C][hidden].
- * logits: fp32 [C][V] (written).  The workspace (zero-filled before first use, as for
- * svd_verify_linear) holds svd_lm_head_workspace_bytes() bytes. */
+ * logits: fp32 [C][V] (written).  For C <= 8 the GEMM's epilogue also produces, per block of
+ * 64 vocabulary rows and position, the online-softmax statistics of the block -- its max, the
+ * sum of exp((l - max) / T) over it and its argmax (lowest id on ties, NaN logits skipped) --
+ * and the sampler merges those instead of scanning the logits for the row max (Milakov and
+ * Gimelshein's online normaliser; the pages' [positions, vocabulary] output).  lse (nullable,
+ * fp32 [C]) receives log sum_v exp(logits[c][v] / T), natural log, for a non-greedy sampler:
+ * from the epilogue's block sums when C <= 8, else from the sampler's exact mass.  The
+ * workspace (zero-filled before first use, as for svd_verify_linear) holds
+ * svd_lm_head_workspace_bytes() bytes. */
 size_t svd_lm_head_workspace_bytes(int64_t hidden, int64_t vocab, int C);
 int svd_lm_head_softmax(const svd_qweight *W_lm, const void *H, int C,
                         const svd_sampler *sampler, float *logits, float *probs,
-                        int32_t *argmax, void *workspace, size_t workspace_bytes,
+                        int32_t *argmax, float *lse, void *workspace, size_t workspace_bytes,
                         svd_stream_t stream);
 
 /* ---- (c) acceptance ----------------------------------------------------------------- */

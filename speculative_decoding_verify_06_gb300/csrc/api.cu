@@ -22,7 +22,11 @@ int verify_status(const void *ws, size_t ws_bytes, uint32_t *bits, cudaStream_t 
 int verify_inject_stall(void *ws, size_t ws_bytes, uint32_t polls, cudaStream_t stream);
 size_t sampler_ws_bytes(int rows, int64_t V);
 int sampler_probs(const float *logits, int rows, int64_t V, const svd_sampler *s, float *probs,
-                  int32_t *argmax, void *ws, size_t ws_bytes, cudaStream_t stream);
+                  int32_t *argmax, void *ws, size_t ws_bytes, cudaStream_t stream,
+                  const float4 *stats = nullptr, int n_sb = 0, float *lse = nullptr);
+int verify_linear_ex(const svd_qweight *W, const void *X, int C, float *Y, void *ws,
+                     size_t ws_bytes, int flags, float4 *stats, float stat_k, bool *stats_done,
+                     cudaStream_t stream);
 int accept(const float *p, const int64_t *p_rows, const float *q, const int64_t *q_rows,
            const int32_t *tgt_am, const int32_t *draft, int64_t n, int k, int64_t V,
            uint64_t seed, uint64_t woff, const float *uniforms, int32_t *out_tokens,
@@ -128,26 +132,37 @@ int svd_sampler_probs(const float *logits, int rows, int64_t V, const svd_sample
     return svd::sampler_probs(logits, rows, V, s, probs, argmax, ws, ws_bytes, (cudaStream_t)stream);
 }
 
+// lm_head workspace: [verify linear][the epilogue's block statistics: ceil(V / 64) x C float4]
+// [sampler], each part 256-byte aligned.
+static size_t lm_stats_bytes(int64_t vocab, int C) {
+    return svd::align_up((size_t)((vocab + 63) / 64) * (size_t)C * 16, 256);
+}
+
 size_t svd_lm_head_workspace_bytes(int64_t hidden, int64_t vocab, int C) {
     if (hidden <= 0 || vocab <= 0 || C < 1 || C > SVD_C_MAX || svd::sm_count() < 1) return 0;
-    return svd::align_up(svd::vl_workspace_bytes(hidden, vocab, C), 256) +
+    return svd::align_up(svd::vl_workspace_bytes(hidden, vocab, C), 256) + lm_stats_bytes(vocab, C) +
            svd::sampler_ws_bytes(C, vocab);
 }
 
 int svd_lm_head_softmax(const svd_qweight *W, const void *H, int C, const svd_sampler *s,
-                        float *logits, float *probs, int32_t *argmax, void *ws, size_t ws_bytes,
-                        svd_stream_t stream) {
+                        float *logits, float *probs, int32_t *argmax, float *lse, void *ws,
+                        size_t ws_bytes, svd_stream_t stream) {
     if (!W || !s || !logits || !probs) return SVD_ERR_INVALID_ARG;
     if (W->layout != SVD_LAYOUT_NATIVE) return SVD_ERR_INVALID_ARG;
     if (C < 1 || C > SVD_C_MAX || W->out_features > (1LL << 24)) return SVD_ERR_INVALID_ARG;
     const size_t need = svd_lm_head_workspace_bytes(W->in_features, W->out_features, C);
     if (!ws || need == 0 || ws_bytes < need) return SVD_ERR_WORKSPACE;
     const size_t vl = svd::align_up(svd::vl_workspace_bytes(W->in_features, W->out_features, C), 256);
-    int rc = svd::verify_linear(W, H, C, logits, ws, vl, 0, (cudaStream_t)stream);
+    const size_t sb = lm_stats_bytes(W->out_features, C);
+    float4 *stats = reinterpret_cast<float4 *>(reinterpret_cast<uint8_t *>(ws) + vl);
+    const float stat_k = s->greedy ? 0.f : 1.4426950408889634f / s->temperature;
+    bool fused = false;
+    int rc = svd::verify_linear_ex(W, H, C, logits, ws, vl, 0, stats, stat_k, &fused, (cudaStream_t)stream);
     if (rc != SVD_OK) return rc;
     return svd::sampler_probs(logits, C, W->out_features, s, probs, argmax,
-                              reinterpret_cast<uint8_t *>(ws) + vl, ws_bytes - vl,
-                              (cudaStream_t)stream);
+                              reinterpret_cast<uint8_t *>(ws) + vl + sb, ws_bytes - vl - sb,
+                              (cudaStream_t)stream, fused ? stats : nullptr,
+                              (int)((W->out_features + 63) / 64), lse);
 }
 
 int svd_accept(const float *p, const int64_t *p_rows, const float *q, const int64_t *q_rows,

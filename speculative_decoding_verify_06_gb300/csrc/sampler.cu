@@ -13,7 +13,10 @@
 // One launch per call: a cluster of kSmpSlices CTAs per row, each CTA one slice of the row,
 // sharing their partial results through distributed shared memory:
 //   1. each CTA's max and argmax (lowest id on ties, NaN skipped); after a cluster barrier
-//      every CTA merges the slices' into the row's;
+//      every CTA merges the slices' into the row's.  After the lm_head GEMM with its fused
+//      epilogue, the CTAs merge the epilogue's per-block maxima and argmaxes instead of
+//      scanning the logits (a share of the blocks each), and rank 0 also forms the row's
+//      log-normaliser log sum_v exp(l[v] / T) from the blocks' sums;
 //   2. e[v] written into the output buffer, mass sums in 2^-36 fixed point (exact integer
 //      sums, independent of the split), and the CTA's min-p survivors kept in shared memory;
 //   3. rank 0 finds the crossing: if the survivors fit (<= kSortCap) it gathers them from
@@ -117,9 +120,13 @@ struct SmpShared {
 };
 
 // One row per cluster of kSmpSlices CTAs (grid: slices x rows).
+// stats (nullable): the lm_head epilogue's per-block (max, sum of exp2((l - max) * log2e / T),
+// argmax bits) for block b of row r at stats[b * rows + r], n_sb blocks; lse (nullable): the
+// row's log-normaliser (natural log), written when the sampler is not greedy.
 __global__ void __launch_bounds__(kSmpThreads, 1)
 smp_fused_kernel(const float *__restrict__ logits, int64_t V, float T, float top_p, float min_p,
-                 int greedy, float *__restrict__ probs, int32_t *__restrict__ argmax_out) {
+                 int greedy, float *__restrict__ probs, int32_t *__restrict__ argmax_out,
+                 const float4 *__restrict__ stats, int n_sb, float *__restrict__ lse) {
     static_assert(kSmpSlices <= 32, "one warp merges the slices");
     cg::cluster_group cl = cg::this_cluster();
     const unsigned rank = cl.block_rank();
@@ -136,12 +143,21 @@ smp_fused_kernel(const float *__restrict__ logits, int64_t V, float T, float top
     float *P = probs + (int64_t)row * V;
 
     // ---- 1. max and argmax of the slice, then of the row ------------------------------------
+    const int rows = gridDim.y;
     {
         float bv = 0.f;
         int bi = -1;
-        for (int64_t v = lo + threadIdx.x; v < hi; v += kSmpThreads) {
-            const float f = L[v];
-            if (f == f) argmax_merge(bv, bi, f, (int)v);
+        if (stats) {
+            const int b0 = (int)((int64_t)n_sb * rank / kSmpSlices), b1 = (int)((int64_t)n_sb * (rank + 1) / kSmpSlices);
+            for (int b = b0 + (int)threadIdx.x; b < b1; b += kSmpThreads) {
+                const float4 st = stats[(size_t)b * rows + row];
+                argmax_merge(bv, bi, st.x, __float_as_int(st.z));
+            }
+        } else {
+            for (int64_t v = lo + threadIdx.x; v < hi; v += kSmpThreads) {
+                const float f = L[v];
+                if (f == f) argmax_merge(bv, bi, f, (int)v);
+            }
         }
         block_argmax_merge<kSmpThreads>(bv, bi);
         if (threadIdx.x == 0) {
@@ -274,6 +290,30 @@ smp_fused_kernel(const float *__restrict__ logits, int64_t V, float T, float top
         __syncthreads();
         const unsigned long long Z = s_Z;
         const double tgt = (double)top_p * (double)Z;
+        if (lse) {
+            // log sum_v exp(l[v] / T) = lmax / T + log sum_v e[v]: from the epilogue's block sums
+            // (each relative to its block's max) when there are any, else from the exact mass
+            __shared__ double s_part[kSmpThreads / 32];
+            double part = 0.0;
+            if (stats) {
+                const float k2 = 1.4426950408889634f / T;
+                for (int b = threadIdx.x; b < n_sb; b += kSmpThreads) {
+                    const float4 st = stats[(size_t)b * rows + row];
+                    if (__float_as_int(st.z) >= 0) part += (double)st.y * (double)exp2f((st.x - lmax) * k2);
+                }
+            } else if (threadIdx.x == 0) {
+                part = (double)Z / kFx;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+            if ((threadIdx.x & 31) == 0) s_part[threadIdx.x >> 5] = part;
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                double tot = 0.0;
+                for (int i = 0; i < kSmpThreads / 32; ++i) tot += s_part[i];
+                lse[row] = (float)((double)lmax / (double)T + log(tot));
+            }
+        }
         float e_cut;
         int id_cut;
         unsigned long long S;
@@ -491,7 +531,8 @@ size_t sampler_ws_bytes(int rows, int64_t V) {
 }
 
 int sampler_probs(const float *logits, int rows, int64_t V, const svd_sampler *s, float *probs,
-                  int32_t *argmax, void *ws, size_t ws_bytes, cudaStream_t stream) {
+                  int32_t *argmax, void *ws, size_t ws_bytes, cudaStream_t stream,
+                  const float4 *stats, int n_sb, float *lse) {
     if (!logits || !probs || !s || rows < 1 || rows > SVD_C_MAX || V < 1 || V > (1LL << 24))
         return SVD_ERR_INVALID_ARG;
     if (logits == probs) return SVD_ERR_INVALID_ARG;
@@ -512,7 +553,7 @@ int sampler_probs(const float *logits, int rows, int64_t V, const svd_sampler *s
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     SVD_CUDA_TRY(cudaLaunchKernelEx(&cfg, smp_fused_kernel, logits, V, s->temperature, s->top_p,
-                                    s->min_p, s->greedy ? 1 : 0, probs, argmax));
+                                    s->min_p, s->greedy ? 1 : 0, probs, argmax, stats, n_sb, lse));
     return SVD_OK;
 }
 

@@ -298,8 +298,22 @@ template <int MAXOPS>
 struct VlOps {
     int n;
     int C;
+    // lm_head epilogue (single-op launches with C <= 8 only, else null): per 64-row block rb and
+    // column c,
+    // stats[rb * C + c] = (max of the block's outputs, sum of exp2((y - max) * stat_k) over
+    // them, argmax as int bits, 0); NaN outputs and padding rows take no part.
+    float4 *stats = nullptr;
+    float stat_k = 0.f;  // log2(e) / T
     VlOp op[MAXOPS];
 };
+
+// (value, index) max with the lowest index on ties; index -1 is "none".
+__device__ __forceinline__ void stat_argmax(float &bv, int &bi, float ov, int oi) {
+    if (oi >= 0 && (bi < 0 || ov > bv || (ov == bv && oi < bi))) {
+        bv = ov;
+        bi = oi;
+    }
+}
 
 // ---- the tensor-core stream-K kernel ---------------------------------------------------
 // Every warp is an independent stream-K worker.  The units of an op (64-row block x 64-input
@@ -471,6 +485,7 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
     __shared__ uint32_t s_park_head[NW * 2];  // 1 if that partial starts at its block's start
     __shared__ uint32_t s_epoch, s_last;
     __shared__ WaitCtl s_wc;
+    __shared__ uint32_t s_own[2 * NW], s_nown;  // lm_head epilogue: blocks finished from partials
     float *park = reinterpret_cast<float *>(smem + Cfg::kRing);
     // The op descriptors live in shared memory: read from the parameter space with a
     // run-time index they would go through the small constant cache on every access.
@@ -603,6 +618,7 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
             s_park_rb[park_at(lane)] = kNone;
             s_park_head[park_at(lane)] = 0u;
         }
+        if (threadIdx.x == 0) s_nown = 0u;
 
         uint32_t lo, hi;
         range(o, &lo, &hi);
@@ -812,6 +828,43 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
                                     coords(lane, sub * TW + r, nt, q, rb, &row, &col);
                                     if (row < out_f && col < C) o.Y[(int64_t)col * out_f + row] = acc[r][nt][q];
                                 }
+                        if constexpr (NT == 1 && TW == kTiles && MAXOPS == 1) {
+                            // the lm_head epilogue from the registers: lane (g, t) holds rows
+                            // 16 r + g (+ 8) of every tile for columns 2 t and 2 t + 1
+                            if (P.stats != nullptr) {
+#pragma unroll
+                                for (int qc = 0; qc < 2; ++qc) {
+                                    float bv = 0.f;
+                                    int bi = -1;
+#pragma unroll
+                                    for (int r = 0; r < TW; ++r)
+#pragma unroll
+                                        for (int hh = 0; hh < 2; ++hh) {
+                                            const int64_t row = (int64_t)rb * kRowsPerBlock + 16 * r + g4 + 8 * hh;
+                                            const float v = acc[r][0][qc + 2 * hh];
+                                            if (row < out_f && v == v) stat_argmax(bv, bi, v, (int)row);
+                                        }
+#pragma unroll
+                                    for (int m = 4; m < 32; m <<= 1)
+                                        stat_argmax(bv, bi, __shfl_xor_sync(0xFFFFFFFFu, bv, m), __shfl_xor_sync(0xFFFFFFFFu, bi, m));
+                                    float sum = 0.f;
+#pragma unroll
+                                    for (int r = 0; r < TW; ++r)
+#pragma unroll
+                                        for (int hh = 0; hh < 2; ++hh) {
+                                            const int64_t row = (int64_t)rb * kRowsPerBlock + 16 * r + g4 + 8 * hh;
+                                            const float v = acc[r][0][qc + 2 * hh];
+                                            if (row < out_f && v == v) sum += exp2f((v - bv) * P.stat_k);
+                                        }
+#pragma unroll
+                                    for (int m = 4; m < 32; m <<= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, m);
+                                    const int col = 2 * t4 + qc;
+                                    if (g4 == 0 && col < C)
+                                        P.stats[(size_t)rb * C + col] =
+                                            make_float4(bi >= 0 ? bv : -INFINITY, sum, __int_as_float(bi), 0.f);
+                                }
+                            }
+                        }
                     } else {
                         const int k = seg_lo == lo ? 0 : 1;
                         float4 *dst = reinterpret_cast<float4 *>(park + park_at(k) * kParkW + lane * kAccW);
@@ -907,6 +960,59 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
                         o.Y[(int64_t)col * out_f + row] = v;
                     } else {
                         st_tagged(part + (size_t)b * kPartialMax + e, v, tag);
+                    }
+                }
+                if constexpr (NT == 1 && TW == kTiles && MAXOPS == 1) {
+                    // the lm_head epilogue of a block finished here: noted, done after the runs
+                    if (P.stats != nullptr && owner && threadIdx.x == 0 && s_nown < 2 * NW) s_own[s_nown++] = rb;
+                }
+            }
+        }
+        if constexpr (NT == 1 && TW == kTiles && MAXOPS == 1) {
+            // the lm_head epilogue of the blocks this CTA finished from partials: one warp per
+            // (block, column), from the outputs just written (read back through L2: rows lane
+            // and lane + 32), all of them at once
+            if (P.stats != nullptr) {
+                __syncthreads();
+                const int n_pairs = (int)s_nown * C;
+                constexpr int kPP = 4;  // (block, column) pairs per warp and round, loads first
+                for (int base = warp * kPP; base < n_pairs; base += NW * kPP) {
+                    float v2[kPP][2];
+#pragma unroll
+                    for (int i = 0; i < kPP; ++i) {
+                        const int pc = base + i;
+                        const uint32_t rb = pc < n_pairs ? s_own[pc / C] : 0u;
+                        const int col = pc < n_pairs ? pc % C : 0;
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int64_t row = (int64_t)rb * kRowsPerBlock + lane + 32 * hh;
+                            v2[i][hh] = (pc < n_pairs && row < out_f) ? __ldcg(o.Y + (int64_t)col * out_f + row)
+                                                                      : __int_as_float(0x7fc00000);
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < kPP; ++i) {
+                        const int pc = base + i;
+                        if (pc >= n_pairs) break;  // uniform across the warp
+                        const uint32_t rb = s_own[pc / C];
+                        const int col = pc % C;
+                        float bv = 0.f;
+                        int bi = -1;
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh)
+                            if (v2[i][hh] == v2[i][hh])
+                                stat_argmax(bv, bi, v2[i][hh], (int)((int64_t)rb * kRowsPerBlock + lane + 32 * hh));
+#pragma unroll
+                        for (int m = 1; m < 32; m <<= 1)
+                            stat_argmax(bv, bi, __shfl_xor_sync(0xFFFFFFFFu, bv, m), __shfl_xor_sync(0xFFFFFFFFu, bi, m));
+                        float sum = 0.f;
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh)
+                            if (v2[i][hh] == v2[i][hh]) sum += exp2f((v2[i][hh] - bv) * P.stat_k);
+#pragma unroll
+                        for (int m = 1; m < 32; m <<= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, m);
+                        if (lane == 0)
+                            P.stats[(size_t)rb * C + col] = make_float4(bi >= 0 ? bv : -INFINITY, sum, __int_as_float(bi), 0.f);
                     }
                 }
             }
@@ -1243,8 +1349,12 @@ static int check_native_size(const svd_qweight *W) {
     return SVD_OK;
 }
 
-int verify_linear(const svd_qweight *W, const void *X, int C, float *Y, void *ws,
-                  size_t ws_bytes, int flags, cudaStream_t stream) {
+// verify_linear with the lm_head epilogue: when stats is not null, C <= 8 and W is NATIVE, the
+// launch also writes the per-block statistics described at VlOps (and *stats_done = true).
+int verify_linear_ex(const svd_qweight *W, const void *X, int C, float *Y, void *ws,
+                     size_t ws_bytes, int flags, float4 *stats, float stat_k, bool *stats_done,
+                     cudaStream_t stream) {
+    if (stats_done) *stats_done = false;
     int rc = check_qweight(W);
     if (rc != SVD_OK) return rc;
     if (!X || !Y || C < 1 || C > SVD_C_MAX || !aligned16(X)) return SVD_ERR_INVALID_ARG;
@@ -1262,6 +1372,11 @@ int verify_linear(const svd_qweight *W, const void *X, int C, float *Y, void *ws
         P.n = 1;
         P.C = C;
         P.op[0] = make_op(W, X, Y);
+        if (stats && !q4k && ntiles_for(C) == 1) {
+            P.stats = stats;
+            P.stat_k = stat_k;
+            if (stats_done) *stats_done = true;
+        }
         SVD_CUDA_TRY(launch_ops(P, ws, pdl, stream, (flags & SVD_F_FRAGMENT_MMA) != 0, q4k));
         return SVD_OK;
     }
@@ -1285,6 +1400,11 @@ int verify_linear(const svd_qweight *W, const void *X, int C, float *Y, void *ws
     }
     SVD_CUDA_TRY(e);
     return SVD_OK;
+}
+
+int verify_linear(const svd_qweight *W, const void *X, int C, float *Y, void *ws,
+                  size_t ws_bytes, int flags, cudaStream_t stream) {
+    return verify_linear_ex(W, X, C, Y, ws, ws_bytes, flags, nullptr, 0.f, nullptr, stream);
 }
 
 size_t chain_workspace_bytes(const svd_linear_op *ops, int n_ops, int C) {

@@ -137,7 +137,7 @@ def load(path: str = LIB_PATH):
             "svd_sampler_workspace_bytes": (sz, [i32, i64]),
             "svd_sampler_probs": (i32, [P, i32, i64, P, P, P, P, sz, P]),
             "svd_lm_head_workspace_bytes": (sz, [i64, i64, i32]),
-            "svd_lm_head_softmax": (i32, [P, P, i32, P, P, P, P, P, sz, P]),
+            "svd_lm_head_softmax": (i32, [P, P, i32, P, P, P, P, P, P, sz, P]),
             "svd_accept": (i32, [P, P, P, P, P, P, i64, i32, i64, u64, u64, P, P, P, P, P]),
             "svd_graph_begin": (i32, [P]),
             "svd_graph_end": (i32, [P, P]),
@@ -323,14 +323,14 @@ def svd_lm_head_workspace_bytes(hidden: int, vocab: int, C: int) -> int:
 
 
 def svd_lm_head_softmax(W: QWeight, H, C: int, sampler: Sampler, logits, probs, argmax,
-                        workspace, workspace_bytes: int = 0, stream=None):
+                        workspace, workspace_bytes: int = 0, stream=None, lse=None):
     w = W._c()
     s = sampler._c()
     if not workspace_bytes:
         workspace_bytes = workspace.numel() * workspace.element_size()
     _check("svd_lm_head_softmax", load().svd_lm_head_softmax(
         ctypes.byref(w), _ptr(H), int(C), ctypes.byref(s), _ptr(logits), _ptr(probs),
-        _ptr(argmax), _ptr(workspace), int(workspace_bytes), _stream(stream)))
+        _ptr(argmax), _ptr(lse), _ptr(workspace), int(workspace_bytes), _stream(stream)))
 
 
 def svd_accept(p, draft, n_windows: int, k: int, V: int, out_tokens, n_emitted, status,

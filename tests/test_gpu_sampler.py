@@ -10,7 +10,7 @@ import torch
 
 import oracle
 from speculative_decoding_verify_06_gb300 import svd, synth
-from gpu_helpers import DEV, assert_gemm_parity, lib, sampler, to_dev
+from gpu_helpers import DEV, assert_gemm_parity, lib, native_weight, sampler, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -110,6 +110,57 @@ def test_hand_example_five_tokens():
     assert np.allclose(pg[0], np.r_[p[:3] / p[:3].sum(), 0, 0], rtol=1e-5)
 
 
+def log_partition(logits, T):
+    """log sum_v exp(l_v / T) per row in fp64 (the plain definition, shifted by the max)."""
+    z = logits.astype(np.float64) / T
+    m = np.max(z, axis=1, keepdims=True)
+    return (m[:, 0] + np.log(np.sum(np.exp(z - m), axis=1)))
+
+
+def _lm_head(hidden, vocab, C, seed, smp, want_lse=True):
+    codes, scales = synth.qweight(vocab, hidden, seed=seed)
+    W, _ = native_weight(codes, scales)
+    H = to_dev(synth.activations(C, hidden, seed=seed + 1))
+    logits = torch.empty((C, vocab), dtype=torch.float32, device=DEV)
+    probs = torch.empty_like(logits)
+    am = torch.empty(C, dtype=torch.int32, device=DEV)
+    lse = torch.full((C,), float("nan"), dtype=torch.float32, device=DEV) if want_lse else None
+    ws = torch.zeros(svd.svd_lm_head_workspace_bytes(hidden, vocab, C), dtype=torch.uint8, device=DEV)
+    svd.svd_lm_head_softmax(W, H, C, smp, logits, probs, am, ws, lse=lse)
+    torch.cuda.synchronize()
+    return (codes, scales, H, logits.cpu().numpy(), probs.cpu().numpy(), am.cpu().numpy(),
+            None if lse is None else lse.cpu().numpy())
+
+
+@pytest.mark.parametrize("hidden,vocab,C", [(512, 1000, 3), (256, 64, 8), (512, 4133, 5), (1024, 9000, 12)])
+def test_lm_head_epilogue_statistics(hidden, vocab, C):
+    """Ragged vocabularies (a last block of fewer than 64 rows), C <= 8 through the GEMM
+    epilogue's block statistics and C = 12 through the sampler's own max pass: the argmax, the
+    distribution and the log-normaliser match the oracle on the GPU's logits, and the logits
+    match the GEMM oracle."""
+    lib()
+    smp = svd.Sampler(0.7, 0.9, 0.02)
+    codes, scales, H, lg, pg, am, lse = _lm_head(hidden, vocab, C, seed=vocab + C, smp=smp)
+    y_ref, a_ref = oracle.verify_linear(codes, scales, H.view(torch.int16).cpu().numpy().view(np.uint16))
+    assert_gemm_parity(lg, y_ref, a_ref)
+    pr, amr, nk, fl = oracle.sampler(lg, F32(0.7), F32(0.9), F32(0.02))
+    assert np.array_equal(am, amr)
+    base, *_ = oracle.sampler(lg, F32(0.7), F32(1.0), F32(0.0))
+    for r in range(C):
+        if fl[r] == 0:
+            assert np.array_equal(pg[r] > 0, pr[r] > 0)
+            assert np.allclose(pg[r], pr[r], rtol=1e-5, atol=1e-12)
+        else:
+            check_flagged_row(pg[r], pr[r], base[r], int(fl[r]), float(F32(0.9)), float(F32(0.02)))
+    assert np.allclose(lse, log_partition(lg, 0.7), rtol=0, atol=2e-5)
+    # greedy: one-hot of the argmax, lse left untouched
+    g = svd.Sampler(greedy=True)
+    _, _, _, lg2, pg2, am2, lse2 = _lm_head(hidden, vocab, C, seed=vocab + C, smp=g)
+    assert np.array_equal(am2, np.argmax(lg2, axis=1))
+    assert np.all(pg2[np.arange(C), am2] == 1.0) and np.all(pg2.sum(axis=1) == 1.0)
+    assert np.all(np.isnan(lse2))
+
+
 def test_lm_head_softmax_matches_oracle():
     lib()
     hidden, vocab, C = synth.HIDDEN, synth.VOCAB, 6
@@ -125,9 +176,12 @@ def test_lm_head_softmax_matches_oracle():
     am = torch.empty(C, dtype=torch.int32, device=DEV)
     ws = torch.zeros(svd.svd_lm_head_workspace_bytes(hidden, vocab, C), dtype=torch.uint8, device=DEV)
     smp = svd.Sampler(0.6, 0.95, 0.05)
-    svd.svd_lm_head_softmax(W, H, C, smp, logits, probs, am, ws)
+    lse = torch.full((C,), float("nan"), dtype=torch.float32, device=DEV)
+    svd.svd_lm_head_softmax(W, H, C, smp, logits, probs, am, ws, lse=lse)
     torch.cuda.synchronize()
     lg = logits.cpu().numpy()
+    # C <= 8: the GEMM epilogue's block statistics give the max, the argmax and the normaliser
+    assert np.allclose(lse.cpu().numpy(), log_partition(lg, 0.6), rtol=0, atol=2e-5)
     rows = np.unique(np.r_[synth.rng(1).choice(vocab, 100, replace=False), 0, vocab - 1,
                            am.cpu().numpy()])
     y_ref, a_ref = oracle.verify_linear(codes[rows].cpu().numpy(),
