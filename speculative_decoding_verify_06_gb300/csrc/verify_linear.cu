@@ -648,8 +648,9 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
             };
 
             uint32_t rb = lo / n_kc, kc = lo - rb * n_kc, seg_lo = lo;
-            uint4 xr[NT][2];
+            uint4 xr[NT][2], xr2[NT][2];  // the next unit's (Q4_K: the next two sub-chunks') activations
             if constexpr (kPrefetchX) load_x(KQ ? kKqSub * kc : kc, xr);
+            if constexpr (kPrefetchX && KQ) load_x(kKqSub * kc + 1, xr2);
             for (uint32_t u = lo; u < hi; ++u) {
                 const uint32_t slot = c_used % R, in_slot = (u - lo) % U;
                 const uint32_t kn = (kc + 1 == n_kc) ? 0u : kc + 1;
@@ -701,10 +702,13 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
                     for (int s4 = 0; s4 < kKqSub; ++s4) {
                         uint4 xq[NT][2];
                         if constexpr (kPrefetchX) {
+                            // two sub-chunks ahead (into the next unit of the range at the end)
                             xq[0][0] = xr[0][0];
                             xq[0][1] = xr[0][1];
-                            if (s4 + 1 < kKqSub) load_x(kKqSub * kc + s4 + 1, xr);
-                            else if (u + 1 < hi) load_x(kKqSub * kn, xr);
+                            xr[0][0] = xr2[0][0];
+                            xr[0][1] = xr2[0][1];
+                            if (s4 + 2 < kKqSub) load_x(kKqSub * kc + s4 + 2, xr2);
+                            else if (u + 1 < hi) load_x(kKqSub * kn + s4 + 2 - kKqSub, xr2);
                         } else {
                             load_x(kKqSub * kc + s4, xq);
                         }
