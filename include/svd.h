@@ -82,7 +82,7 @@ enum {
                                  padded to 64): codes -> units of 64 rows x 256 inputs,
                                  8192 bytes of codes in fragment order; scales -> the
                                  units' 64 super-block headers (16 bytes each).  Streamed
-                                 by svd_verify_linear and svd_verify_chain, C <= 8      */
+                                 by svd_verify_linear and svd_verify_chain, C <= 16     */
 };
 
 /* Flags for svd_verify_linear. */

@@ -357,7 +357,7 @@ struct VlCfg {
     static constexpr int kKqScrW = TW * 288;
     static constexpr size_t kScratch = KQ ? (size_t)NW * kKqScrW * sizeof(float) : 0;
     static constexpr size_t kSmem = kRing + kPark + kScratch + (size_t)MAXOPS * sizeof(VlOp);
-    static_assert(!KQ || NT == 1, "Q4_K units take up to 8 columns");
+    static_assert(!KQ || NT <= 2, "Q4_K units take up to 16 columns");
     static_assert(kTiles % TW == 0 && NW % kWG == 0 && (kWG == 1 || kNG <= 15), "worker groups");
     static_assert(kPartial <= kPartialMax, "partial slot size");
     static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
@@ -650,7 +650,7 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
             uint32_t rb = lo / n_kc, kc = lo - rb * n_kc, seg_lo = lo;
             uint4 xr[NT][2], xr2[NT][2];  // the next unit's (Q4_K: the next two sub-chunks') activations
             if constexpr (kPrefetchX) load_x(KQ ? kKqSub * kc : kc, xr);
-            if constexpr (kPrefetchX && KQ) load_x(kKqSub * kc + 1, xr2);
+            if constexpr (kPrefetchX && KQ && NT == 1) load_x(kKqSub * kc + 1, xr2);
             for (uint32_t u = lo; u < hi; ++u) {
                 const uint32_t slot = c_used % R, in_slot = (u - lo) % U;
                 const uint32_t kn = (kc + 1 == n_kc) ? 0u : kc + 1;
@@ -693,15 +693,17 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
                     __syncwarp();
                     // per tile T = sum_j sc_j (sum_{i in j} (128 + q_i) x_i); and the sub-block sums
                     // of x as an MMA of X (rows = columns) against an indicator: D[col][j] = sum_{i in j} x
-                    float T[TW][4], xsd[4] = {0.f, 0.f, 0.f, 0.f};
+                    float T[TW][NT][4], xsd[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int r = 0; r < TW; ++r)
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) T[r][q] = 0.f;
+                        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) T[r][nt][q] = 0.f;
 #pragma unroll
                     for (int s4 = 0; s4 < kKqSub; ++s4) {
                         uint4 xq[NT][2];
-                        if constexpr (kPrefetchX) {
+                        if constexpr (kPrefetchX && NT == 1) {
                             // two sub-chunks ahead (into the next unit of the range at the end)
                             xq[0][0] = xr[0][0];
                             xq[0][1] = xr[0][1];
@@ -709,6 +711,15 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
                             xr[0][1] = xr2[0][1];
                             if (s4 + 2 < kKqSub) load_x(kKqSub * kc + s4 + 2, xr2);
                             else if (u + 1 < hi) load_x(kKqSub * kn + s4 + 2 - kKqSub, xr2);
+                        } else if constexpr (kPrefetchX) {
+                            // two n-tiles: one sub-chunk ahead (the registers go to the accumulators)
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt) {
+                                xq[nt][0] = xr[nt][0];
+                                xq[nt][1] = xr[nt][1];
+                            }
+                            if (s4 + 1 < kKqSub) load_x(kKqSub * kc + s4 + 1, xr);
+                            else if (u + 1 < hi) load_x(kKqSub * kn, xr);
                         } else {
                             load_x(kKqSub * kc + s4, xq);
                         }
@@ -721,45 +732,58 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
                                 dequant_word_b128(blk ? cw.z : cw.x, a0);
                                 dequant_word_b128(blk ? cw.w : cw.y, a1);
                                 const float2 sc2 = *reinterpret_cast<const float2 *>(sc_s + ((r * 8 + 2 * s4 + blk) * 8 + g4) * 2);
-                                float d4[4] = {0.f, 0.f, 0.f, 0.f};
-                                mma_bf16_16816(d4, a0, xq[0][blk].x, xq[0][blk].y);
-                                mma_bf16_16816(d4, a1, xq[0][blk].z, xq[0][blk].w);
-                                T[r][0] = fmaf(sc2.x, d4[0], T[r][0]);
-                                T[r][1] = fmaf(sc2.x, d4[1], T[r][1]);
-                                T[r][2] = fmaf(sc2.y, d4[2], T[r][2]);
-                                T[r][3] = fmaf(sc2.y, d4[3], T[r][3]);
+#pragma unroll
+                                for (int nt = 0; nt < NT; ++nt) {
+                                    float d4[4] = {0.f, 0.f, 0.f, 0.f};
+                                    mma_bf16_16816(d4, a0, xq[nt][blk].x, xq[nt][blk].y);
+                                    mma_bf16_16816(d4, a1, xq[nt][blk].z, xq[nt][blk].w);
+                                    T[r][nt][0] = fmaf(sc2.x, d4[0], T[r][nt][0]);
+                                    T[r][nt][1] = fmaf(sc2.x, d4[1], T[r][nt][1]);
+                                    T[r][nt][2] = fmaf(sc2.y, d4[2], T[r][nt][2]);
+                                    T[r][nt][3] = fmaf(sc2.y, d4[3], T[r][nt][3]);
+                                }
                             }
                         }
 #pragma unroll
                         for (int blk = 0; blk < 2; ++blk) {
                             const uint32_t ind = (g4 == 2 * s4 + blk) ? 0x3F803F80u : 0u;  // bf16 (1, 1)
-                            const uint32_t ax0[4] = {xq[0][blk].x, 0u, xq[0][blk].y, 0u};
-                            const uint32_t ax1[4] = {xq[0][blk].z, 0u, xq[0][blk].w, 0u};
+                            // A rows 0-7: columns 0-7; rows 8-15: columns 8-15 (the second n-tile)
+                            const uint32_t ax0[4] = {xq[0][blk].x, NT > 1 ? xq[NT - 1][blk].x : 0u, xq[0][blk].y,
+                                                     NT > 1 ? xq[NT - 1][blk].y : 0u};
+                            const uint32_t ax1[4] = {xq[0][blk].z, NT > 1 ? xq[NT - 1][blk].z : 0u, xq[0][blk].w,
+                                                     NT > 1 ? xq[NT - 1][blk].w : 0u};
                             mma_bf16_16816(xsd, ax0, ind, ind);
                             mma_bf16_16816(xsd, ax1, ind, ind);
                         }
                     }
-                    // lane (g, t) holds the sums of sub-blocks 2t, 2t+1 for column g: exactly the
-                    // B fragment of the products sum_j m_j xs_j (the mins) and sum_j sc_j xs_j (the
-                    // 128 offset of the codes), with xs split into bf16 hi + lo
-                    const __nv_bfloat162 hi2 = __floats2bfloat162_rn(xsd[0], xsd[1]);
-                    const float2 hif = __bfloat1622float2(hi2);
-                    const __nv_bfloat162 lo2 = __floats2bfloat162_rn(xsd[0] - hif.x, xsd[1] - hif.y);
-                    const uint32_t bh = *reinterpret_cast<const uint32_t *>(&hi2);
-                    const uint32_t bl = *reinterpret_cast<const uint32_t *>(&lo2);
+                    // lane (g, t) holds the sums of sub-blocks 2t, 2t+1 for column g (and g + 8):
+                    // exactly the B fragment of the products sum_j m_j xs_j (the mins) and
+                    // sum_j sc_j xs_j (the 128 offset of the codes), with xs split into bf16 hi + lo
+                    uint32_t bh[NT], bl[NT];
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const __nv_bfloat162 hi2 = __floats2bfloat162_rn(xsd[2 * nt], xsd[2 * nt + 1]);
+                        const float2 hif = __bfloat1622float2(hi2);
+                        const __nv_bfloat162 lo2 = __floats2bfloat162_rn(xsd[2 * nt] - hif.x, xsd[2 * nt + 1] - hif.y);
+                        bh[nt] = *reinterpret_cast<const uint32_t *>(&hi2);
+                        bl[nt] = *reinterpret_cast<const uint32_t *>(&lo2);
+                    }
 #pragma unroll
                     for (int r = 0; r < TW; ++r) {
                         const uint32_t *p0 = m_s + (16 * r + g4) * 8 + t4, *p1 = m_s + (16 * r + g4 + 8) * 8 + t4;
                         const uint32_t am[4] = {p0[0], p1[0], p0[0], p1[0]};
                         const uint32_t as[4] = {p0[4], p1[4], p0[4], p1[4]};
-                        float dm[4] = {0.f, 0.f, 0.f, 0.f}, ds[4] = {0.f, 0.f, 0.f, 0.f};
-                        mma_bf16_16816(dm, am, bh, bl);
-                        mma_bf16_16816(ds, as, bh, bl);
                         const float2 e0 = d_s[16 * r + g4], e1 = d_s[16 * r + g4 + 8];
-                        acc[r][0][0] = fmaf(e0.x, fmaf(-128.f, ds[0], T[r][0]), fmaf(-e0.y, dm[0], acc[r][0][0]));
-                        acc[r][0][1] = fmaf(e0.x, fmaf(-128.f, ds[1], T[r][1]), fmaf(-e0.y, dm[1], acc[r][0][1]));
-                        acc[r][0][2] = fmaf(e1.x, fmaf(-128.f, ds[2], T[r][2]), fmaf(-e1.y, dm[2], acc[r][0][2]));
-                        acc[r][0][3] = fmaf(e1.x, fmaf(-128.f, ds[3], T[r][3]), fmaf(-e1.y, dm[3], acc[r][0][3]));
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            float dm[4] = {0.f, 0.f, 0.f, 0.f}, ds[4] = {0.f, 0.f, 0.f, 0.f};
+                            mma_bf16_16816(dm, am, bh[nt], bl[nt]);
+                            mma_bf16_16816(ds, as, bh[nt], bl[nt]);
+                            acc[r][nt][0] = fmaf(e0.x, fmaf(-128.f, ds[0], T[r][nt][0]), fmaf(-e0.y, dm[0], acc[r][nt][0]));
+                            acc[r][nt][1] = fmaf(e0.x, fmaf(-128.f, ds[1], T[r][nt][1]), fmaf(-e0.y, dm[1], acc[r][nt][1]));
+                            acc[r][nt][2] = fmaf(e1.x, fmaf(-128.f, ds[2], T[r][nt][2]), fmaf(-e1.y, dm[2], acc[r][nt][2]));
+                            acc[r][nt][3] = fmaf(e1.x, fmaf(-128.f, ds[3], T[r][nt][3]), fmaf(-e1.y, dm[3], acc[r][nt][3]));
+                        }
                     }
                     __syncwarp();  // the scratch is rewritten for the next unit
                 } else {
@@ -1138,6 +1162,8 @@ constexpr int kNWq = SVD_NWQ;     // Q4_K units (64 rows x 256 inputs, 9 KB), C 
 constexpr int kTWq = SVD_TWQ;     // per unit, each on two 16-row tiles; one unit per slot, two
 constexpr int kRq = SVD_RQ;       // slots per worker group
 constexpr int kUq = 1;
+constexpr int kTWq2 = 1;          // Q4_K, 8 < C <= 16: four warps per unit, one 16-row tile each,
+constexpr int kRq2 = 4;           // four slots per group (the accumulators of two n-tiles)
 constexpr int kMaxCtasPerSm = 2;  // the workspace holds partial slots for this many
 constexpr int kChainMax = 256;    // ops per chain launch (kernel parameters, ~16 KB)
 
@@ -1291,7 +1317,10 @@ static cudaError_t launch_ops(const VlOps<MAXOPS> &P, void *ws, bool pdl, cudaSt
     for (int i = 0; i < P.n; ++i)
         max_units = (int64_t)P.op[i].n_units > max_units ? (int64_t)P.op[i].n_units : max_units;
     const bool coop = P.n > 1;
-    if (q4k) return launch_stream<1, kNWq, kTWq, kRq, kUq, MAXOPS, 1>(P, ws, pdl, coop, max_units, stream);
+    if (q4k) {
+        if (P.C <= 8) return launch_stream<1, kNWq, kTWq, kRq, kUq, MAXOPS, 1>(P, ws, pdl, coop, max_units, stream);
+        return launch_stream<2, kNWq, kTWq2, kRq2, kUq, MAXOPS, 1>(P, ws, pdl, coop, max_units, stream);
+    }
     switch (ntiles_for(P.C)) {
         case 1: return launch_stream<1, kNW1, kTiles, kR1, kU, MAXOPS>(P, ws, pdl, coop, max_units, stream);
         case 2: return launch_stream<2, kNW2, kTW2, kR2, kU, MAXOPS>(P, ws, pdl, coop, max_units, stream);
@@ -1367,7 +1396,7 @@ int verify_linear_ex(const svd_qweight *W, const void *X, int C, float *Y, void 
     if (sm_count() < 1) return SVD_ERR_CUDA;
     if (W->layout == SVD_LAYOUT_NATIVE || W->layout == SVD_LAYOUT_Q4K_NATIVE) {
         const bool q4k = W->layout == SVD_LAYOUT_Q4K_NATIVE;
-        if (q4k && C > 8) return SVD_ERR_UNSUPPORTED;
+        if (q4k && C > 16) return SVD_ERR_UNSUPPORTED;
         rc = check_native_size(W);
         if (rc != SVD_OK) return rc;
         if (!ws || ws_bytes < vl_workspace_bytes(W->in_features, W->out_features, C))
@@ -1424,7 +1453,7 @@ int verify_chain(const svd_linear_op *ops, int n_ops, int C, void *ws, size_t ws
     if (flags & ~(SVD_F_PDL | SVD_F_FRAGMENT_MMA)) return SVD_ERR_INVALID_ARG;
     // one layout for the whole chain: native, or Q4_K native (up to 8 columns)
     const bool q4k = ops[0].W.layout == SVD_LAYOUT_Q4K_NATIVE;
-    if (q4k && C > 8) return SVD_ERR_UNSUPPORTED;
+    if (q4k && C > 16) return SVD_ERR_UNSUPPORTED;
     for (int i = 0; i < n_ops; ++i) {
         const int rc = check_qweight(&ops[i].W);
         if (rc != SVD_OK) return rc;

@@ -103,6 +103,7 @@ def test_q4k_native_repack_round_trip(out_f, in_f):
 @pytest.mark.parametrize("out_f,in_f,C", [
     (37, 768, 1), (37, 768, 4), (64, 256, 8), (300, 5120, 3), (33, 2304, 5), (131, 4096, 2),
     (8, 2048, 6), (1, 256, 7), (200, 17408, 4), (1100, 1280, 8),
+    (37, 768, 9), (300, 5120, 12), (131, 4096, 16), (1100, 1280, 13), (1, 256, 10),
 ])
 def test_q4k_native_matches_oracle(out_f, in_f, C):
     lib()
@@ -147,7 +148,7 @@ def test_q4k_native_full_size_sampled_rows(out_f, in_f):
     assert_gemm_parity(y[:, rows], y_ref, a_ref)
 
 
-@pytest.mark.parametrize("C", [1, 4, 8])
+@pytest.mark.parametrize("C", [1, 4, 8, 12, 16])
 def test_q4k_native_chain_equals_single_launches_and_oracle(C):
     lib()
     shapes = [(5120, 1024), (96, 256), (544, 2048), (2048, 160), (64, 512), (1024, 3000)]
@@ -204,11 +205,11 @@ def test_q4k_native_argument_errors():
     lib()
     blocks = to_dev(synth.q4k_blocks(16, 512, seed=1))
     W, keep = q4k_native(blocks, 512, 16)
-    X = to_dev(synth.activations(9, 512, seed=2))
-    Y = torch.empty((9, 16), dtype=torch.float32, device=DEV)
-    ws = torch.zeros(svd.svd_verify_linear_workspace_bytes(512, 16, 9), dtype=torch.uint8, device=DEV)
-    with pytest.raises(svd.SvdError) as e:                       # C > 8
-        svd.svd_verify_linear(W, X, 9, Y, ws)
+    X = to_dev(synth.activations(17, 512, seed=2))
+    Y = torch.empty((17, 16), dtype=torch.float32, device=DEV)
+    ws = torch.zeros(svd.svd_verify_linear_workspace_bytes(512, 16, 17), dtype=torch.uint8, device=DEV)
+    with pytest.raises(svd.SvdError) as e:                       # C > 16
+        svd.svd_verify_linear(W, X, 17, Y, ws)
     assert e.value.code == svd.SVD_ERR_UNSUPPORTED
     with pytest.raises(svd.SvdError) as e:                       # no workspace
         svd.svd_verify_linear(W, X, 4, Y, None)
