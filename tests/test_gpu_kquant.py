@@ -248,3 +248,29 @@ def test_q4k_stack_graph_matches_oracle():
         x = X.view(torch.int16).cpu().numpy().view(np.uint16)
         y_ref, a_ref = kquant.verify_linear(raw.cpu().numpy(), W.in_features, x)
         assert_gemm_parity(Y.cpu().numpy(), y_ref, a_ref)
+
+
+@pytest.mark.parametrize("C", [4, 12])
+def test_q4k_native_wait_runs_out_and_is_reported(C):
+    """The stall hook on a Q4_K launch: no weight copy is issued, the first ring wait runs out,
+    the status word reports it, and the same workspace then gives the oracle's result."""
+    lib()
+    out_f, in_f = 7168, 5120
+    b = synth.q4k_blocks_torch(out_f, in_f, seed=31, device=DEV)
+    W, keep = q4k_native(b, in_f, out_f)
+    x = synth.activations(C, in_f, seed=32)
+    X = to_dev(x)
+    Y = torch.empty((C, out_f), dtype=torch.float32, device=DEV)
+    ws = torch.zeros(svd.svd_verify_linear_workspace_bytes(in_f, out_f, C), dtype=torch.uint8, device=DEV)
+    svd.svd_verify_inject_stall(ws, 0)
+    svd.svd_verify_linear(W, X, C, Y, ws)
+    rc, bits = svd.svd_verify_status(ws)
+    assert rc == svd.SVD_ERR_TIMEOUT and bits != 0 and bits & ~7 == 0
+    svd.svd_verify_inject_stall(ws, None)
+    Y.fill_(float("nan"))
+    svd.svd_verify_linear(W, X, C, Y, ws)
+    assert svd.svd_verify_status(ws) == (svd.SVD_OK, 0)
+    rows = np.r_[0:64, out_f - 64:out_f]
+    host = b[torch.as_tensor(rows, device=DEV)].cpu().numpy()
+    y_ref, a_ref = kquant.verify_linear(host, in_f, x)
+    assert_gemm_parity(Y.cpu().numpy()[:, rows], y_ref, a_ref)
