@@ -49,6 +49,37 @@ def test_native_sizes(lib):
         svd.svd_native_sizes(100, 64)
 
 
+def test_q4k_native_sizes(lib):
+    # 7168 x 5120: 112 row blocks x 20 super-block columns, 8192 + 1024 bytes each -- the
+    # format's own 144 bytes per 256 weights
+    cb, hb = svd.svd_q4k_native_sizes(5120, 7168)
+    assert (cb, hb) == (112 * 20 * 8192, 112 * 20 * 1024)
+    assert cb + hb == 7168 * 5120 // 256 * 144
+    cb, hb = svd.svd_q4k_native_sizes(512, 40)  # rows padded to 64
+    assert (cb, hb) == (2 * 8192, 2 * 1024)
+    for bad in ((480, 64), (0, 64), (256, 0)):
+        with pytest.raises(svd.SvdError):
+            svd.svd_q4k_native_sizes(*bad)
+
+
+def test_q4k_arguments_rejected_on_the_host(lib):
+    L = lib
+    # raw Q4_K: scales must be NULL, in_features % 256 == 0; Q4_K native: headers required
+    w = svd._QWeight(16, 16, 512, 64, svd.SVD_LAYOUT_Q4K, 0)
+    assert L.svd_verify_linear(ctypes.byref(w), 16, 4, 16, None, 0, 0, None) == svd.SVD_ERR_INVALID_ARG
+    w = svd._QWeight(16, None, 480, 64, svd.SVD_LAYOUT_Q4K, 0)
+    assert L.svd_verify_linear(ctypes.byref(w), 16, 4, 16, None, 0, 0, None) == svd.SVD_ERR_INVALID_ARG
+    w = svd._QWeight(16, None, 512, 64, svd.SVD_LAYOUT_Q4K_NATIVE, 0)
+    assert L.svd_verify_linear(ctypes.byref(w), 16, 4, 16, None, 0, 0, None) == svd.SVD_ERR_INVALID_ARG
+    w = svd._QWeight(16, 16, 480, 64, svd.SVD_LAYOUT_Q4K_NATIVE, 0)
+    assert L.svd_verify_linear(ctypes.byref(w), 16, 4, 16, None, 0, 0, None) == svd.SVD_ERR_INVALID_ARG
+    # repack: a Q4_K source with scales, or misaligned destinations
+    src = svd._QWeight(16, 16, 512, 64, svd.SVD_LAYOUT_Q4K, 0)
+    assert L.svd_repack_weights(ctypes.byref(src), 16, 16, None) == svd.SVD_ERR_INVALID_ARG
+    src = svd._QWeight(16, None, 512, 64, svd.SVD_LAYOUT_Q4K, 0)
+    assert L.svd_repack_weights(ctypes.byref(src), 8, 16, None) == svd.SVD_ERR_INVALID_ARG
+
+
 def test_bad_arguments_rejected_on_the_host(lib):
     L = lib
     assert L.svd_verify_linear(None, None, 4, None, None, 0, 0, None) == svd.SVD_ERR_INVALID_ARG
