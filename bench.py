@@ -545,6 +545,82 @@ def kv_read(dev, peak, stack_ms, layers=64, contexts=KV_CONTEXTS, steps=10, C=4,
     return out
 
 
+def lm_head_windows(vp, dev, peak, n_windows=10000, C=6, pool=16, seed=23):
+    """The lm_head + sampler workload with sampled acceptance: n_windows verify windows of K+1 = C
+    positions, each the 5120 x 151936 lm_head over the window's C hidden columns with the
+    production sampler (svd_lm_head_softmax) and then svd_accept of the window's C - 1 drafts
+    against a drafter q drawn from the target's perturbed logits (stack.DRAFTER_SIGMA, alpha about
+    0.5).  The hidden columns come from a pool of `pool` synthetic windows, the drafter's rows and
+    drafts are made from each pool entry once (untimed), and the timed loop runs the windows back
+    to back on the resident lm_head.  Reports windows/s, the lm_head's weight stream per window
+    against the copy peak and the tokens emitted per window."""
+    import torch
+
+    from speculative_decoding_verify_06_gb300 import stack, svd, synth
+    V, k, hid = synth.VOCAB, C - 1, synth.HIDDEN
+    W = vp.lm.W
+    smp = vp.sampler
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    Hs = [synth.activations_torch(C, hid, seed * 1000 + i, dev) for i in range(pool)]
+    logits = torch.empty((C, V), dtype=torch.float32, device=dev)
+    probs = torch.empty_like(logits)
+    am = torch.empty(C, dtype=torch.int32, device=dev)
+    ws = torch.zeros(svd.svd_lm_head_workspace_bytes(hid, V, C), dtype=torch.uint8, device=dev)
+    qws = torch.zeros(svd.svd_sampler_workspace_bytes(k, V), dtype=torch.uint8, device=dev)
+    qam = torch.empty(k, dtype=torch.int32, device=dev)
+    qs, drafts = [], []
+    for H in Hs:  # the drafter of each pool window (untimed)
+        svd.svd_lm_head_softmax(W, H, C, smp, logits, probs, am, ws)
+        noise = torch.empty((k, V), dtype=torch.float32, device=dev)
+        noise.normal_(0.0, stack.DRAFTER_SIGMA, generator=g)
+        q = torch.empty((k, V), dtype=torch.float32, device=dev)
+        svd.svd_sampler_probs((logits[:k] + noise).contiguous(), k, V, smp, q, qam, qws)
+        qs.append(q)
+        drafts.append(torch.multinomial(q, 1, generator=g).to(torch.int32).view(1, k).contiguous())
+    tok = torch.empty((n_windows, k + 1), dtype=torch.int32, device=dev)
+    ne = torch.empty(n_windows, dtype=torch.int32, device=dev)
+    st = torch.empty(n_windows, dtype=torch.int32, device=dev)
+    s = torch.cuda.current_stream(dev)
+
+    def window(w):
+        i = w % pool
+        svd.svd_lm_head_softmax(W, Hs[i], C, smp, logits, probs, am, ws, stream=s)
+        svd.svd_accept(probs, drafts[i], 1, k, V, tok[w], ne[w:w + 1], st[w:w + 1], q=qs[i],
+                       seed=seed, window_offset=w, stream=s)
+    for w in range(3):
+        window(w)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for w in range(n_windows):
+        window(w)
+    e1.record(s)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1)
+    per = ms / n_windows
+    wbytes = roofline_lm_bytes(hid, V, C)
+    out = {"windows": n_windows, "C": C, "ms_per_window": per, "windows_per_s": 1000.0 / per,
+           "lm_head_gb_s": wbytes / per / 1e6, "frac": wbytes / per / 1e6 / peak,
+           "tokens_per_window": float(ne.double().mean().item()),
+           "status_nonzero": int((st != 0).sum().item()),
+           "launches_per_window": 3,
+           "workload": (f"{n_windows} windows: lm_head {hid} x {V} over K+1 = {C} columns + sampler "
+                        f"(T 0.6, top-p 0.95, min-p 0.05) over {C} rows + svd_accept of {k} drafts "
+                        f"against the drafter's q (target logits + N(0, sigma^2), alpha about 0.5); "
+                        f"{pool} synthetic windows cycled")}
+    del Hs, qs, drafts, logits, probs, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+def roofline_lm_bytes(hid, V, C):
+    """Algorithmic bytes of one lm_head window: the weights and scales once, the C hidden columns
+    in and the C logit rows out."""
+    from speculative_decoding_verify_06_gb300 import roofline
+    return roofline.linear_bytes(hid, V, C)
+
+
 def q4k_stack(dev, peak, tail_ms, layers=64, C=4, steps=20, oracle_sample=False):
     """The stack with Q4_K super-block weights (stack.Q4kStack: the pages' checkpoint format,
     repacked once into the Q4_K native layout; one chain launch in a CUDA graph), timed like the
@@ -763,6 +839,8 @@ def run_svd(args, rank, world, local_rank):
         line["accept_throughput"] = accept_throughput(
             dev, peak, oracle_windows=2000 if (rank == 0 and world == 1
                                                and not args.no_cpu_baseline) else 0)
+    if not args.no_sweep and not args.stack_only and vp.head:
+        line["lm_head_windows"] = lm_head_windows(vp, dev, peak)
     if not args.no_kv and not args.stack_only:
         line["kv_read"] = kv_read(dev, peak, line["stack"]["ms"], layers=args.layers,
                                   contexts=tuple(int(c) for c in args.kv_contexts.split(",")),
