@@ -28,6 +28,16 @@
 //    block scale folded in, staged in shared memory, fp32 accumulators in tensor memory.
 //  * vl_simt_kernel (CANONICAL layout) -- the plain CUDA-core version: one warp per output
 //    row, each lane one 32-input block at a time, fp32 FMAs, warp-shuffle reduction.
+//
+// The stream-K kernel also serves two extensions:
+//  * Q4_K super-blocks (SVD_LAYOUT_Q4K_NATIVE, C <= 16): units of 64 rows x 256 inputs with
+//    the super-blocks' headers; the codes enter the MMA as bf16 (128 + q), each sub-block's sum
+//    is rescaled by its 6-bit scale in fp32, and the mins and the 128 offset leave through MMAs
+//    against the sub-block sums of the activations (the layout is described below);
+//  * the lm_head epilogue (single-op launches, C <= 8): per 64-row block and column the max,
+//    the sum of exp((y - max) / T) and the argmax, which the sampler merges instead of scanning
+//    the logits.
+// The Q4_K bytes as stored run on a CUDA-core kernel of their own (kquant.cu).
 #include <cooperative_groups.h>
 
 #include <memory>

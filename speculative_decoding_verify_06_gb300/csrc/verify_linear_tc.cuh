@@ -6,8 +6,8 @@
 // several sequences' windows amortises the one weight read of a pass over more columns.  At
 // C = 32 the legacy fragment path pays one fp32 FMA per weight for the per-block rescale and
 // reloads every activation fragment per warp; here the block scale is folded into the A operand
-// and the activations are staged once per CTA in shared memory, where the tensor core reads
-// them.
+// and the activations are converted once per op and staged per block in shared memory, where
+// the tensor core reads them.
 //
 // Arithmetic.  A = fp16(s * (c - 8)): (c - 8) is built exactly from the exponent pattern 0x6400
 // (1024 + c, minus 1032), then multiplied by the block's fp16 scale with one rounding (relative
@@ -19,14 +19,16 @@
 //
 // Decomposition.  An MMA unit is 128 weight rows (native row blocks 2q and 2q+1) x one 64-input
 // chunk; units are ordered row-group-major, and the grid splits them into contiguous ranges,
-// one per CTA (stream-K).  A CTA runs three PIPES of four warps and one MMA warp.  The CTA's
+// one per CTA (stream-K).  A CTA runs three PIPES of four warps, each with an MMA warp.  The CTA's
 // range is cut into blocks of up to two units of one row group, dealt to the pipes round-robin.
-// A pipe streams its blocks through a ring of two slots (per block four bulk copies, one per
-// warp: the codes and the scales of the two row blocks); its warps dequantise each unit into an
-// fp16 A stage (warp j: rows 32j..32j+31), convert the unit's activations into an fp16 B stage
-// (warp j: tokens 8j..8j+7), and arrive on the stage's barrier.  The MMA warp takes the pipes'
-// stages in order and issues four tcgen05.mma (M 128, N 32, K 16) per stage into the pipe's
-// accumulator (32 TMEM columns; two sets, by the parity of the row-group segment).  When a
+// At the start of each op all CTAs convert the op's activations from bf16 into fp16 B tiles
+// in the workspace (a share of the chunks each) and pass a grid barrier.  A pipe streams its
+// blocks through a ring of two slots (per block four bulk copies of weights, one per warp: the
+// codes and the scales of the two row blocks, and one of the block's B tiles); its warps
+// dequantise each unit into an fp16 A stage (warp j: rows 32j..32j+31) and arrive on the stage's
+// barrier.  The pipe's MMA warp takes its stages in order and issues four tcgen05.mma (M 128,
+// N 32, K 16) per stage into the pipe's accumulator (32 TMEM columns; two sets, by the parity of
+// the row-group segment).  When a
 // segment (one row group of the range) is done, the pipes' warps add the accumulators of the
 // segment in pipe order -- pipe p takes token groups p and p + 3 (8 TMEM columns each), warp j
 // of a pipe rows 32j..32j+31 (its TMEM lane quarter) -- and write Y, or store a tagged partial
