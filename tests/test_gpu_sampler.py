@@ -222,3 +222,21 @@ def test_vocabularies_smaller_than_the_cluster(V):
 def test_thirty_two_rows_one_call():
     """The largest window the ABI takes in one call (SVD_C_MAX rows), one cluster per row."""
     check(synth.normal_logits(32, 20000, seed=77, std=3.0), 0.6, 0.95, 0.05)
+
+
+@pytest.mark.parametrize("vocab", [1, 5, 63, 64, 65, 129])
+@pytest.mark.parametrize("C", [1, 8])
+def test_lm_head_epilogue_tiny_vocabularies(vocab, C):
+    """Vocabularies of one partial block, exactly one block, one block and a row: the epilogue's
+    padding rows take no part in the max, the argmax or the normaliser."""
+    lib()
+    smp = svd.Sampler(0.6, 0.95, 0.05)
+    codes, scales, H, lg, pg, am, lse = _lm_head(256, vocab, C, seed=vocab * 7 + C, smp=smp)
+    pr, amr, nk, fl = oracle.sampler(lg, F32(0.6), F32(0.95), F32(0.05))
+    assert np.array_equal(am, amr)
+    assert np.all(am >= 0) and np.all(am < vocab)
+    assert np.allclose(lse, log_partition(lg, 0.6), rtol=0, atol=2e-5)
+    for r in range(C):
+        if fl[r] == 0:
+            assert np.array_equal(pg[r] > 0, pr[r] > 0)
+            assert np.allclose(pg[r], pr[r], rtol=1e-5, atol=1e-12)
