@@ -18,11 +18,12 @@
 // first level streams the whole row from HBM, the deeper levels re-read a shrinking slice that
 // is still cached.
 //
-// Two kernels share that logic.  accept_kernel gives every window one CTA, which suits many
-// windows at once.  accept_cluster_kernel gives a window a cluster of eight CTAs on eight
-// SMs: the first level of the draw is split over the cluster (eight times the loads in
-// flight), the CTAs exchange their slice sums through distributed shared memory, and the CTA
-// whose slice holds the crossing finishes the search alone.  The host picks the cluster
+// Two kernels share that logic.  accept_kernel gives every window one CTA of 256 threads, which
+// suits many windows at once.  accept_cluster_kernel gives a window a cluster of eight CTAs of
+// 1024 threads on eight SMs: the first level of the draw is split over the cluster's 256 warps
+// (each warp's slice sum is one dependent 128-bit chain, so the width shortens it), the CTAs
+// exchange their slice sums through distributed shared memory, and the CTA whose slice holds the
+// crossing finishes the search alone.  The host picks the cluster
 // kernel when there are fewer sampled windows than SMs, the case of one verify pass.
 #include <cooperative_groups.h>
 
@@ -34,6 +35,11 @@ int sm_count();
 
 constexpr int kAccThreads = 256;
 constexpr int kAccWarps = kAccThreads / 32;
+// The cluster kernel (one window on eight SMs) runs wider CTAs: its first level of the draw is
+// one 128-bit sum chain per warp, so more warps shorten it.
+constexpr int kAccCThreads = 1024;
+constexpr int kAccCWarps = kAccCThreads / 32;
+constexpr int kAccMaxWarps = kAccCWarps > kAccWarps ? kAccCWarps : kAccWarps;
 typedef unsigned __int128 u128;
 
 // round(f * 2^62) for f in [0, 1] (round half up); NaN, infinities, negatives and values
@@ -141,10 +147,10 @@ __device__ u128 slice_sum(const float *rp, const float *rq, int64_t lo, int64_t 
 }
 
 struct AcceptShared {
-    u128 part[kAccWarps];
+    u128 part[kAccMaxWarps];
     u128 base, target, total;
     int64_t lo, hi;
-    int st_or[kAccWarps];
+    int st_or[kAccMaxWarps];
     int j;             // first rejected position (k when all accepted)
     uint32_t m2;       // resampling uniform as a 24-bit integer
     int64_t amax;      // greedy: argmax of the current row
@@ -475,7 +481,7 @@ __device__ __forceinline__ u128 warp_scan_u128(u128 x) {
     return ((u128)hi << 64) | lo;
 }
 
-__global__ void __cluster_dims__(kAccCluster, 1, 1) __launch_bounds__(kAccThreads)
+__global__ void __cluster_dims__(kAccCluster, 1, 1) __launch_bounds__(kAccCThreads, 1)
 accept_cluster_kernel(const float *__restrict__ p, const int64_t *__restrict__ p_rows,
                       const float *__restrict__ q, const int64_t *__restrict__ q_rows,
                       const int32_t *__restrict__ draft, int k, int64_t V, uint64_t seed,
@@ -485,7 +491,7 @@ accept_cluster_kernel(const float *__restrict__ p, const int64_t *__restrict__ p
     namespace cg = cooperative_groups;
     cg::cluster_group cluster = cg::this_cluster();
     __shared__ AcceptShared sh;
-    __shared__ u128 s_wsum[2][kAccWarps];  // this CTA's slice sums, per attempt
+    __shared__ u128 s_wsum[2][kAccCWarps];  // this CTA's slice sums, per attempt
     __shared__ int s_cst[2];               // status bits of this CTA's slices, per attempt
     const int crank = (int)cluster.block_rank();
     const int64_t w = blockIdx.x / kAccCluster;
@@ -509,7 +515,7 @@ accept_cluster_kernel(const float *__restrict__ p, const int64_t *__restrict__ p
     if (vec) piece = (piece + 3) & ~int64_t(3);
     auto slice_of = [&](int c, int i, int64_t *lo, int64_t *hi) {
         const int64_t c_lo = min(V, (int64_t)c * piece), c_hi = min(V, c_lo + piece);
-        int64_t part = (c_hi - c_lo + kAccWarps - 1) / kAccWarps;
+        int64_t part = (c_hi - c_lo + kAccCWarps - 1) / kAccCWarps;
         if (vec) part = (part + 3) & ~int64_t(3);
         *lo = min(c_hi, c_lo + part * i);
         *hi = min(c_hi, *lo + part);
@@ -528,14 +534,19 @@ accept_cluster_kernel(const float *__restrict__ p, const int64_t *__restrict__ p
         }
         cluster.sync();
         if (warp == 0) {
-            // lane t holds the cluster's slices 2t and 2t+1 (in row order)
-            const int i0 = 2 * lane, i1 = 2 * lane + 1;
-            const u128 x0 = *cluster.map_shared_rank(&s_wsum[attempt][i0 % kAccWarps], i0 / kAccWarps);
-            const u128 x1 = *cluster.map_shared_rank(&s_wsum[attempt][i1 % kAccWarps], i1 / kAccWarps);
+            // lane t holds the cluster's slices kPer t .. kPer t + kPer - 1 (in row order)
+            constexpr int kPer = kAccCluster * kAccCWarps / 32;
+            u128 xs[kPer], lt = 0;
+#pragma unroll
+            for (int e = 0; e < kPer; ++e) {
+                const int i = kPer * lane + e;
+                xs[e] = *cluster.map_shared_rank(&s_wsum[attempt][i % kAccCWarps], i / kAccCWarps);
+                lt += xs[e];
+            }
             int sts = lane < kAccCluster ? *cluster.map_shared_rank(&s_cst[attempt], lane) : 0;
             sts = __reduce_or_sync(0xffffffffu, sts);
-            const u128 incl = warp_scan_u128(x0 + x1);
-            const u128 excl = incl - (x0 + x1);
+            const u128 incl = warp_scan_u128(lt);
+            const u128 excl = incl - lt;
             const uint64_t tlo = __shfl_sync(0xffffffffu, (uint64_t)incl, 31);
             const uint64_t thi = __shfl_sync(0xffffffffu, (uint64_t)(incl >> 64), 31);
             const u128 R = ((u128)thi << 64) | tlo;
@@ -548,9 +559,11 @@ accept_cluster_kernel(const float *__restrict__ p, const int64_t *__restrict__ p
                 sh.found = -1;
             }
             if (hm && lane == __ffs(hm) - 1) {
-                const bool first = ((excl + x0) << 24) > tgt;
-                sh.found = first ? i0 : i1;
-                sh.base = first ? excl : excl + x0;
+                u128 run = excl;
+                int e = 0;
+                while (e < kPer - 1 && ((run + xs[e]) << 24) <= tgt) run += xs[e++];
+                sh.found = kPer * lane + e;
+                sh.base = run;
             }
         }
         cluster.sync();  // every read of another CTA's shared memory is done
@@ -566,15 +579,15 @@ accept_cluster_kernel(const float *__restrict__ p, const int64_t *__restrict__ p
         }
         break;
     }
-    const int finisher = found >= 0 ? found / kAccWarps : 0;
+    const int finisher = found >= 0 ? found / kAccCWarps : 0;
     if (crank != finisher) return;
 
     // ---- the CTA holding the crossing narrows its slice down to 32 elements ------------------
     int st = 0;
     if (found >= 0) {
-        slice_of(finisher, found % kAccWarps, &lo, &hi);
+        slice_of(finisher, found % kAccCWarps, &lo, &hi);
         while (hi - lo > 32) {
-            const int64_t part = (hi - lo + kAccWarps - 1) / kAccWarps;
+            const int64_t part = (hi - lo + kAccCWarps - 1) / kAccCWarps;
             const int64_t a = min(hi, lo + part * warp), bnd = min(hi, a + part);
             const u128 sum = (a < bnd) ? slice_sum(rp, rq, a, bnd, false, st) : (u128)0;
             if (lane == 0) sh.part[warp] = sum;
@@ -582,7 +595,7 @@ accept_cluster_kernel(const float *__restrict__ p, const int64_t *__restrict__ p
             if (threadIdx.x == 0) {
                 int chosen = -1;
                 u128 b = sh.base;
-                for (int i = 0; i < kAccWarps; ++i) {
+                for (int i = 0; i < kAccCWarps; ++i) {
                     if (((b + sh.part[i]) << 24) > target) {
                         chosen = i;
                         break;
@@ -624,7 +637,7 @@ accept_cluster_kernel(const float *__restrict__ p, const int64_t *__restrict__ p
     __syncthreads();
     if (threadIdx.x == 0) {
         int s2 = st_win;
-        for (int i = 0; i < kAccWarps; ++i) s2 |= sh.st_or[i];
+        for (int i = 0; i < kAccCWarps; ++i) s2 |= sh.st_or[i];
         for (int i = 0; i < j; ++i) tok[i] = draft[w * k + i];
         for (int i = j; i <= k; ++i) tok[i] = -1;
         if (token < 0) s2 |= SVD_ST_EMPTY;
@@ -646,7 +659,7 @@ int accept(const float *p, const int64_t *p_rows, const float *q, const int64_t 
     // sampled windows fewer than the SMs (one verify pass): a cluster of eight CTAs each
     if (q && n * kAccCluster <= (int64_t)kAccCluster * sm_count() && V > 32 * kAccCluster) {
         SVD_CUDA_TRY(launch(accept_cluster_kernel, dim3((unsigned)(n * kAccCluster)),
-                            dim3(kAccThreads), 0, stream, false, p, p_rows, q, q_rows, draft, k,
+                            dim3(kAccCThreads), 0, stream, false, p, p_rows, q, q_rows, draft, k,
                             V, seed, woff, uniforms, out_tokens, n_emitted, status, vec_ok));
         return SVD_OK;
     }
