@@ -38,6 +38,7 @@ constexpr int kSmpThreads = 1024;
 constexpr int kSortCap = 2048;                    // survivors sorted in shared memory
 constexpr int kSliceCap = kSortCap / kSmpSlices;  // survivors kept per CTA
 constexpr double kFx = 68719476736.0;             // 2^36
+constexpr int kSmpBatch = 8;                      // elements a thread loads before using them
 
 __device__ __forceinline__ unsigned long long fx36(float e) {
     return __float2ull_rn(e * 68719476736.0f);  // e in [0, 1]: exact scaling, then rounding
@@ -154,9 +155,16 @@ smp_fused_kernel(const float *__restrict__ logits, int64_t V, float T, float top
                 argmax_merge(bv, bi, st.x, __float_as_int(st.z));
             }
         } else {
-            for (int64_t v = lo + threadIdx.x; v < hi; v += kSmpThreads) {
-                const float f = L[v];
-                if (f == f) argmax_merge(bv, bi, f, (int)v);
+            for (int64_t v0 = lo + threadIdx.x; v0 < hi; v0 += kSmpBatch * kSmpThreads) {
+                float f[kSmpBatch];
+#pragma unroll
+                for (int u = 0; u < kSmpBatch; ++u) {  // the batch's loads first
+                    const int64_t v = v0 + (int64_t)u * kSmpThreads;
+                    f[u] = v < hi ? L[v] : __int_as_float(0x7fc00000);
+                }
+#pragma unroll
+                for (int u = 0; u < kSmpBatch; ++u)
+                    if (f[u] == f[u]) argmax_merge(bv, bi, f[u], (int)(v0 + (int64_t)u * kSmpThreads));
             }
         }
         block_argmax_merge<kSmpThreads>(bv, bi);
@@ -198,25 +206,36 @@ smp_fused_kernel(const float *__restrict__ logits, int64_t V, float T, float top
         unsigned long long z = 0, zc = 0;
         float cmin = 2.f;
         int cid = -1;
-        for (int64_t v = lo + threadIdx.x; v < hi; v += kSmpThreads) {
-            const float l = L[v];
-            float e;
-            if (l != l) e = 0.f;                       // NaN logits get no mass
-            else if (l == lmax) e = 1.f;
-            else e = expf((l - lmax) / T);
-            P[v] = e;
-            const unsigned long long f = fx36(e);
-            z += f;
-            if (e >= min_p) {
-                zc += f;
-                if (e < cmin || (e == cmin && (int)v > cid)) {
-                    cmin = e;
-                    cid = (int)v;
+        for (int64_t v0 = lo + threadIdx.x; v0 < hi; v0 += kSmpBatch * kSmpThreads) {
+            float lb[kSmpBatch];
+#pragma unroll
+            for (int ub = 0; ub < kSmpBatch; ++ub) {  // the batch's loads first
+                const int64_t vb = v0 + (int64_t)ub * kSmpThreads;
+                lb[ub] = vb < hi ? L[vb] : 0.f;
+            }
+#pragma unroll
+            for (int ub = 0; ub < kSmpBatch; ++ub) {
+                const int64_t v = v0 + (int64_t)ub * kSmpThreads;
+                if (v >= hi) break;
+                const float l = lb[ub];
+                float e;
+                if (l != l) e = 0.f;                       // NaN logits get no mass
+                else if (l == lmax) e = 1.f;
+                else e = expf((l - lmax) / T);
+                P[v] = e;
+                const unsigned long long f = fx36(e);
+                z += f;
+                if (e >= min_p) {
+                    zc += f;
+                    if (e < cmin || (e == cmin && (int)v > cid)) {
+                        cmin = e;
+                        cid = (int)v;
+                    }
+                    const unsigned slot = atomicAdd(&s_n, 1u);
+                    if (slot < kSliceCap)
+                        s_list[slot] = ((unsigned long long)__float_as_uint(e) << 32) |
+                                       (unsigned long long)(0xFFFFFFFFu - (unsigned)v);
                 }
-                const unsigned slot = atomicAdd(&s_n, 1u);
-                if (slot < kSliceCap)
-                    s_list[slot] = ((unsigned long long)__float_as_uint(e) << 32) |
-                                   (unsigned long long)(0xFFFFFFFFu - (unsigned)v);
             }
         }
         z = block_sum_u64<kSmpThreads>(z);
@@ -517,10 +536,20 @@ smp_fused_kernel(const float *__restrict__ logits, int64_t V, float T, float top
     __syncthreads();
     const float ec = s_ec, S = s_S;
     const int ic = s_ic;
-    for (int64_t v = lo + threadIdx.x; v < hi; v += kSmpThreads) {
-        const float e = P[v];
-        const bool kept = (e > ec) || (e == ec && v <= ic);
-        P[v] = kept ? e / S : 0.f;
+    for (int64_t v0 = lo + threadIdx.x; v0 < hi; v0 += kSmpBatch * kSmpThreads) {
+        float eb[kSmpBatch];
+#pragma unroll
+        for (int u = 0; u < kSmpBatch; ++u) {  // the batch's loads first
+            const int64_t v = v0 + (int64_t)u * kSmpThreads;
+            eb[u] = v < hi ? P[v] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kSmpBatch; ++u) {
+            const int64_t v = v0 + (int64_t)u * kSmpThreads;
+            if (v >= hi) break;
+            const bool kept = (eb[u] > ec) || (eb[u] == ec && v <= ic);
+            P[v] = kept ? eb[u] / S : 0.f;
+        }
     }
     cl.sync();  // rank 0 keeps its shared memory until every CTA has read the crossing
 }
