@@ -1151,8 +1151,10 @@ vl_simt_kernel(const uint8_t *__restrict__ codes, const uint16_t *__restrict__ s
 #define SVD_U 2
 #endif
 constexpr int kNW1 = SVD_NW1;     // warps per CTA, C <= 8
-constexpr int kR1 = SVD_R1;       // ring slots per warp, C <= 8
+constexpr int kR1 = SVD_R1;       // ring slots per warp, C <= 5
 constexpr int kU = SVD_U;         // units per slot (one pair of bulk copies)
+constexpr int kR1w = 4;           // 6..8 columns: four one-unit slots per warp (the same ring
+constexpr int kU1w = 1;           // bytes; 1-3 % faster there, no gain at 5 columns or fewer)
 constexpr int kNW2 = 16;          // warps per CTA, 8 < C <= 16: two warps per unit,
 constexpr int kTW2 = 2;           // each on two of its four 16-row tiles
 constexpr int kR2 = 2;            // ring slots per worker group, C <= 32
@@ -1332,7 +1334,9 @@ static cudaError_t launch_ops(const VlOps<MAXOPS> &P, void *ws, bool pdl, cudaSt
         return launch_stream<2, kNWq, kTWq2, kRq2, kUq, MAXOPS, 1>(P, ws, pdl, coop, max_units, stream);
     }
     switch (ntiles_for(P.C)) {
-        case 1: return launch_stream<1, kNW1, kTiles, kR1, kU, MAXOPS>(P, ws, pdl, coop, max_units, stream);
+        case 1:
+            if (P.C >= 6) return launch_stream<1, kNW1, kTiles, kR1w, kU1w, MAXOPS>(P, ws, pdl, coop, max_units, stream);
+            return launch_stream<1, kNW1, kTiles, kR1, kU, MAXOPS>(P, ws, pdl, coop, max_units, stream);
         case 2: return launch_stream<2, kNW2, kTW2, kR2, kU, MAXOPS>(P, ws, pdl, coop, max_units, stream);
         default:
             if (!fragment_mma) return launch_tc<MAXOPS>(P, ws, pdl, coop, stream);
