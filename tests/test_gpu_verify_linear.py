@@ -134,7 +134,7 @@ def _ops_for(shapes, C, seed):
     return mats, ops
 
 
-@pytest.mark.parametrize("C", [1, 4, 8, 16, 32])
+@pytest.mark.parametrize("C", [1, 4, 6, 8, 16, 32])
 def test_chain_equals_single_launches_and_oracle(C):
     """A chain mixing large, small and ragged matrices (some with fewer units than CTAs) equals
     one svd_verify_linear per op bit for bit, and matches the oracle."""
