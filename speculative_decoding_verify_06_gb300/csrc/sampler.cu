@@ -20,11 +20,14 @@
 //   2. e[v] written into the output buffer, mass sums in 2^-36 fixed point (exact integer
 //      sums, independent of the split), and the CTA's min-p survivors kept in shared memory;
 //   3. rank 0 finds the crossing: if the survivors fit (<= kSortCap) it gathers them from
-//      the cluster, bitonic-sorts them and finds the top-p crossing by a prefix scan;
+//      the cluster, bitonic-sorts them and finds the top-p crossing by a prefix scan (one warp
+//      in registers for up to 32 survivors, the whole CTA in shared memory above that);
 //      otherwise a four-pass radix select over the bit patterns of e (monotone for e >= 0)
 //      over the whole row finds the crossing value and a rank scan the crossing id;
 //   4. after a cluster barrier every CTA writes probs[v] = kept ? e[v] / S : 0 for its slice,
-//      S the kept mass.
+//      S the kept mass: when the slice's survivors all fit its list, as zeros over the slice
+//      and then e / S at the kept survivors (the kept set never reaches below min-p), else by
+//      reading e back.
 #include <cooperative_groups.h>
 
 #include "svd_common.cuh"
@@ -98,6 +101,25 @@ __device__ unsigned long long block_sum_u64(unsigned long long x) {
     x = s[0];
     __syncthreads();
     return x;
+}
+
+// Inclusive scan of u64 values over a warp.
+__device__ __forceinline__ unsigned long long warp_scan_u64(unsigned long long x) {
+    const unsigned lane = threadIdx.x & 31u;
+#pragma unroll
+    for (unsigned o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    return x;
+}
+
+// The survivor with the smallest e, the largest id among equals; id -1 is "none".
+__device__ __forceinline__ void cmin_merge(float &a, int &ai, float b, int bi) {
+    if (bi >= 0 && (ai < 0 || b < a || (b == a && bi > ai))) {
+        a = b;
+        ai = bi;
+    }
 }
 
 __device__ __forceinline__ void slice_bounds(int64_t V, int blk, int64_t *lo, int64_t *hi) {
@@ -238,31 +260,42 @@ smp_fused_kernel(const float *__restrict__ logits, int64_t V, float T, float top
                 }
             }
         }
-        z = block_sum_u64<kSmpThreads>(z);
-        zc = block_sum_u64<kSmpThreads>(zc);
+        // the CTA's sums and smallest survivor: warp shuffles, then warp 0 over the warps
+        __shared__ unsigned long long sz[kSmpThreads / 32], szc[kSmpThreads / 32];
         __shared__ float sv[kSmpThreads / 32];
         __shared__ int si[kSmpThreads / 32];
-        auto merge = [](float &a, int &ai, float b, int bi) {
-            if (bi >= 0 && (ai < 0 || b < a || (b == a && bi > ai))) {
-                a = b;
-                ai = bi;
-            }
-        };
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            merge(cmin, cid, __shfl_xor_sync(0xffffffffu, cmin, o), __shfl_xor_sync(0xffffffffu, cid, o));
+        for (int o = 16; o > 0; o >>= 1) {
+            z += __shfl_xor_sync(0xffffffffu, z, o);
+            zc += __shfl_xor_sync(0xffffffffu, zc, o);
+            cmin_merge(cmin, cid, __shfl_xor_sync(0xffffffffu, cmin, o), __shfl_xor_sync(0xffffffffu, cid, o));
+        }
         if ((threadIdx.x & 31) == 0) {
+            sz[threadIdx.x >> 5] = z;
+            szc[threadIdx.x >> 5] = zc;
             sv[threadIdx.x >> 5] = cmin;
             si[threadIdx.x >> 5] = cid;
         }
         __syncthreads();
-        if (threadIdx.x == 0) {
-            for (int i = 1; i < kSmpThreads / 32; ++i) merge(cmin, cid, sv[i], si[i]);
-            sh.z = z;
-            sh.zc = zc;
-            sh.cnt = s_n;
-            sh.cmin = cmin;
-            sh.cmin_id = cid;
+        if (threadIdx.x < 32) {
+            static_assert(kSmpThreads / 32 == 32, "warp 0 merges one value per warp");
+            z = sz[threadIdx.x];
+            zc = szc[threadIdx.x];
+            cmin = sv[threadIdx.x];
+            cid = si[threadIdx.x];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                z += __shfl_xor_sync(0xffffffffu, z, o);
+                zc += __shfl_xor_sync(0xffffffffu, zc, o);
+                cmin_merge(cmin, cid, __shfl_xor_sync(0xffffffffu, cmin, o), __shfl_xor_sync(0xffffffffu, cid, o));
+            }
+            if (threadIdx.x == 0) {
+                sh.z = z;
+                sh.zc = zc;
+                sh.cnt = s_n;
+                sh.cmin = cmin;
+                sh.cmin_id = cid;
+            }
         }
     }
     cl.sync();  // every slice's e (global) and summary (shared) are visible to the cluster
@@ -275,36 +308,49 @@ smp_fused_kernel(const float *__restrict__ logits, int64_t V, float T, float top
         __shared__ float s_cmin;
         __shared__ int s_cid, s_over;
         __shared__ unsigned s_M;
-        if (threadIdx.x == 0) {
+        if (threadIdx.x < 32) {
+            const unsigned b = threadIdx.x;
             unsigned long long Z = 0, Zc = 0;
-            unsigned M = 0;
-            int over = 0;
+            unsigned c = 0;
             float cmin = 2.f;
             int cid = -1;
-            s_off[0] = 0;
-            for (unsigned b = 0; b < (unsigned)kSmpSlices; ++b) {
+            if (b < (unsigned)kSmpSlices) {
                 const SmpShared *r = cl.map_shared_rank(&sh, b);
-                Z += r->z;
-                Zc += r->zc;
-                const unsigned c = r->cnt;
-                if (c > (unsigned)kSliceCap) over = 1;
-                M += c;
-                s_off[b + 1] = s_off[b] + min(c, (unsigned)kSliceCap);
+                Z = r->z;
+                Zc = r->zc;
+                c = r->cnt;
                 if (c > 0) {
-                    const float cm = r->cmin;
-                    const int ci = r->cmin_id;
-                    if (cid < 0 || cm < cmin || (cm == cmin && ci > cid)) {
-                        cmin = cm;
-                        cid = ci;
-                    }
+                    cmin = r->cmin;
+                    cid = r->cmin_id;
                 }
             }
-            s_Z = Z;
-            s_Zc = Zc;
-            s_M = M;
-            s_over = over || (M > (unsigned)kSortCap);
-            s_cmin = cmin;
-            s_cid = cid;
+            const int over = __any_sync(0xffffffffu, c > (unsigned)kSliceCap);
+            // offsets of the slices' kept survivors: an exclusive scan of min(c, kSliceCap)
+            const unsigned kept = min(c, (unsigned)kSliceCap);
+            unsigned incl = kept;
+#pragma unroll
+            for (unsigned o = 1; o < 32; o <<= 1) {
+                const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (b >= o) incl += y;
+            }
+            if (b < (unsigned)kSmpSlices) s_off[b + 1] = incl;
+            unsigned M = c;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                Z += __shfl_xor_sync(0xffffffffu, Z, o);
+                Zc += __shfl_xor_sync(0xffffffffu, Zc, o);
+                M += __shfl_xor_sync(0xffffffffu, M, o);
+                cmin_merge(cmin, cid, __shfl_xor_sync(0xffffffffu, cmin, o), __shfl_xor_sync(0xffffffffu, cid, o));
+            }
+            if (b == 0) {
+                s_off[0] = 0;
+                s_Z = Z;
+                s_Zc = Zc;
+                s_M = M;
+                s_over = over || (M > (unsigned)kSortCap);
+                s_cmin = cmin;
+                s_cid = cid;
+            }
         }
         __syncthreads();
         const unsigned long long Z = s_Z;
@@ -327,10 +373,11 @@ smp_fused_kernel(const float *__restrict__ logits, int64_t V, float T, float top
             for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
             if ((threadIdx.x & 31) == 0) s_part[threadIdx.x >> 5] = part;
             __syncthreads();
-            if (threadIdx.x == 0) {
-                double tot = 0.0;
-                for (int i = 0; i < kSmpThreads / 32; ++i) tot += s_part[i];
-                lse[row] = (float)((double)lmax / (double)T + log(tot));
+            if (threadIdx.x < 32) {
+                double tot = s_part[threadIdx.x];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+                if (threadIdx.x == 0) lse[row] = (float)((double)lmax / (double)T + log(tot));
             }
         }
         float e_cut;
@@ -346,6 +393,39 @@ smp_fused_kernel(const float *__restrict__ logits, int64_t V, float T, float top
             e_cut = s_cmin;
             id_cut = s_cid;
             S = s_Zc;
+        } else if (s_M <= 32u) {
+            // ---- at most 32 survivors (the usual case): warp 0 gathers them, sorts them with
+            // a bitonic network over its lanes (lane i ends with rank i, keys descending), scans
+            // their masses and finds the crossing; the keys, sums and decisions are those of the
+            // shared-memory path below
+            e_cut = 0.f;
+            id_cut = -1;
+            S = 0;
+            if (threadIdx.x < 32) {
+                const unsigned M = s_M, i = threadIdx.x;
+                unsigned long long key = 0ull;
+                if (i < M) {
+                    unsigned b = 0;
+                    while (i >= s_off[b + 1]) ++b;
+                    key = cl.map_shared_rank(s_list, b)[i - s_off[b]];
+                }
+#pragma unroll
+                for (unsigned size = 2; size <= 32; size <<= 1)
+#pragma unroll
+                    for (unsigned stride = size >> 1; stride > 0; stride >>= 1) {
+                        const unsigned long long o = __shfl_xor_sync(0xffffffffu, key, stride);
+                        const bool desc = (i & size) == 0, lower = (i & stride) == 0;
+                        key = (lower == desc) ? (key > o ? key : o) : (key < o ? key : o);
+                    }
+                const unsigned long long m = i < M ? fx36(__uint_as_float((unsigned)(key >> 32))) : 0ull;
+                const unsigned long long pre = warp_scan_u64(m);
+                const unsigned hits = __ballot_sync(0xffffffffu, i < M && (double)pre >= tgt);
+                const unsigned rc = hits ? (unsigned)(__ffs(hits) - 1) : M - 1;
+                const unsigned long long kc = __shfl_sync(0xffffffffu, key, rc);
+                S = __shfl_sync(0xffffffffu, pre, rc);
+                e_cut = __uint_as_float((unsigned)(kc >> 32));
+                id_cut = (int)(0xFFFFFFFFu - (unsigned)(kc & 0xFFFFFFFFu));
+            }
         } else if (!s_over) {
             // ---- fast path: gather the cluster's survivors and sort them ---------------------
             const unsigned M = s_M;
@@ -383,16 +463,17 @@ smp_fused_kernel(const float *__restrict__ logits, int64_t V, float T, float top
             const unsigned r0 = threadIdx.x * per, r1 = min(M, r0 + per);
             unsigned long long run = 0;
             for (unsigned r = r0; r < r1; ++r) run += fx36(__uint_as_float((unsigned)(s_key[r] >> 32)));
-            s_run[threadIdx.x] = run;
             if (threadIdx.x == 0) s_cross = 0xFFFFFFFFu;
+            // inclusive scan of the runs: each warp's, then warp 0 over the warps' totals
+            __shared__ unsigned long long s_wtot[kSmpThreads / 32];
+            run = warp_scan_u64(run);
+            if ((threadIdx.x & 31) == 31) s_wtot[threadIdx.x >> 5] = run;
             __syncthreads();
-            // inclusive scan of s_run (Hillis-Steele)
-            for (unsigned off = 1; off < (unsigned)kSmpThreads; off <<= 1) {
-                const unsigned long long add = threadIdx.x >= off ? s_run[threadIdx.x - off] : 0ull;
-                __syncthreads();
-                s_run[threadIdx.x] += add;
-                __syncthreads();
-            }
+            if (threadIdx.x < 32) s_wtot[threadIdx.x] = warp_scan_u64(s_wtot[threadIdx.x]);
+            __syncthreads();
+            if (threadIdx.x >= 32) run += s_wtot[(threadIdx.x >> 5) - 1];
+            s_run[threadIdx.x] = run;
+            __syncthreads();
             unsigned long long pre = threadIdx.x ? s_run[threadIdx.x - 1] : 0ull;
             for (unsigned r = r0; r < r1; ++r) {
                 pre += fx36(__uint_as_float((unsigned)(s_key[r] >> 32)));
@@ -406,14 +487,13 @@ smp_fused_kernel(const float *__restrict__ logits, int64_t V, float T, float top
             const unsigned long long key = s_key[rc];
             e_cut = __uint_as_float((unsigned)(key >> 32));
             id_cut = (int)(0xFFFFFFFFu - (unsigned)(key & 0xFFFFFFFFu));
-            // kept mass = prefix through rank rc
+            // kept mass = prefix through rank rc, from the thread whose run holds rc
             __shared__ unsigned long long s_S;
-            if (threadIdx.x == 0) s_S = 0;
-            __syncthreads();
-            unsigned long long part = 0;
-            for (unsigned r = threadIdx.x; r <= rc; r += kSmpThreads)
-                part += fx36(__uint_as_float((unsigned)(s_key[r] >> 32)));
-            atomicAdd(&s_S, part);
+            if (r0 <= rc && rc < r1) {
+                unsigned long long pk = threadIdx.x ? s_run[threadIdx.x - 1] : 0ull;
+                for (unsigned r = r0; r <= rc; ++r) pk += fx36(__uint_as_float((unsigned)(s_key[r] >> 32)));
+                s_S = pk;
+            }
             __syncthreads();
             S = s_S;
         } else {
@@ -536,19 +616,33 @@ smp_fused_kernel(const float *__restrict__ logits, int64_t V, float T, float top
     __syncthreads();
     const float ec = s_ec, S = s_S;
     const int ic = s_ic;
-    for (int64_t v0 = lo + threadIdx.x; v0 < hi; v0 += kSmpBatch * kSmpThreads) {
-        float eb[kSmpBatch];
-#pragma unroll
-        for (int u = 0; u < kSmpBatch; ++u) {  // the batch's loads first
-            const int64_t v = v0 + (int64_t)u * kSmpThreads;
-            eb[u] = v < hi ? P[v] : 0.f;
+    const unsigned n_list = s_n;
+    if (n_list <= (unsigned)kSliceCap) {
+        // the kept set lies inside the min-p survivors (the crossing is never below min_p), and
+        // this slice's are all in its list: zeros over the slice, then the kept survivors
+        for (int64_t v = lo + threadIdx.x; v < hi; v += kSmpThreads) P[v] = 0.f;
+        __syncthreads();
+        for (unsigned i = threadIdx.x; i < n_list; i += kSmpThreads) {
+            const unsigned long long key = s_list[i];
+            const float e = __uint_as_float((unsigned)(key >> 32));
+            const int v = (int)(0xFFFFFFFFu - (unsigned)(key & 0xFFFFFFFFu));
+            if ((e > ec) || (e == ec && v <= ic)) P[v] = e / S;
         }
+    } else {
+        for (int64_t v0 = lo + threadIdx.x; v0 < hi; v0 += kSmpBatch * kSmpThreads) {
+            float eb[kSmpBatch];
 #pragma unroll
-        for (int u = 0; u < kSmpBatch; ++u) {
-            const int64_t v = v0 + (int64_t)u * kSmpThreads;
-            if (v >= hi) break;
-            const bool kept = (eb[u] > ec) || (eb[u] == ec && v <= ic);
-            P[v] = kept ? eb[u] / S : 0.f;
+            for (int u = 0; u < kSmpBatch; ++u) {  // the batch's loads first
+                const int64_t v = v0 + (int64_t)u * kSmpThreads;
+                eb[u] = v < hi ? P[v] : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < kSmpBatch; ++u) {
+                const int64_t v = v0 + (int64_t)u * kSmpThreads;
+                if (v >= hi) break;
+                const bool kept = (eb[u] > ec) || (eb[u] == ec && v <= ic);
+                P[v] = kept ? eb[u] / S : 0.f;
+            }
         }
     }
     cl.sync();  // rank 0 keeps its shared memory until every CTA has read the crossing
