@@ -67,8 +67,21 @@ __device__ __forceinline__ double prob_clamped(float f, int &st) {
     return (double)f;
 }
 
+// A q value's status alone (where p is zero the residual is zero whatever q is).
+__device__ __forceinline__ void q_status(float f, int &st) {
+    if (!(f >= 0.f && f <= 1.f)) st |= SVD_ST_BAD_PROB;
+}
+
+// kSkipZero: rows from the sampler, where all but the kept tokens are zero (the one-window
+// cluster kernel); dense rows take the plain path, which the test would only slow down.
+template <bool kSkipZero = false>
 __device__ __forceinline__ uint64_t weight_fx(const float *rp, const float *rq, int64_t v, int &st) {
-    const uint64_t a = prob_fx(__ldg(rp + v), st);
+    const float fp = __ldg(rp + v);
+    if (kSkipZero && fp == 0.f) {  // a filtered-out token: no weight, no conversion
+        if (rq) q_status(__ldg(rq + v), st);
+        return 0ull;
+    }
+    const uint64_t a = prob_fx(fp, st);
     if (rq) {
         const uint64_t b = prob_fx(__ldg(rq + v), st);
         return a > b ? a - b : 0ull;
@@ -90,6 +103,7 @@ __device__ __forceinline__ u128 warp_sum_u128(u128 x) {
 }
 
 // Sum of the weights of [lo, hi) for this warp's slice; float4 loads when allowed.
+template <bool kSkipZero = false>
 __device__ u128 slice_sum(const float *rp, const float *rq, int64_t lo, int64_t hi, bool vec,
                           int &st) {
     const int lane = threadIdx.x & 31;
@@ -113,6 +127,14 @@ __device__ u128 slice_sum(const float *rp, const float *rq, int64_t lo, int64_t 
                 const float av[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
                 const float bv[4] = {q4 ? b[u].x : 0.f, q4 ? b[u].y : 0.f, q4 ? b[u].z : 0.f,
                                      q4 ? b[u].w : 0.f};
+                if (kSkipZero && av[0] == 0.f && av[1] == 0.f && av[2] == 0.f && av[3] == 0.f) {
+                    // four filtered-out tokens: no weight; q still reports a bad value
+                    if (q4) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) q_status(bv[e], st);
+                    }
+                    continue;
+                }
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const uint64_t x = prob_fx(av[e], st);
@@ -129,6 +151,13 @@ __device__ u128 slice_sum(const float *rp, const float *rq, int64_t lo, int64_t 
             const float4 a = __ldg(p4 + t);
             const float4 b = q4 ? __ldg(q4 + t) : make_float4(0.f, 0.f, 0.f, 0.f);
             const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+            if (kSkipZero && av[0] == 0.f && av[1] == 0.f && av[2] == 0.f && av[3] == 0.f) {
+                if (q4) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) q_status(bv[e], st);
+                }
+                continue;
+            }
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const uint64_t x = prob_fx(av[e], st);
@@ -142,7 +171,7 @@ __device__ u128 slice_sum(const float *rp, const float *rq, int64_t lo, int64_t 
         }
         v = lo + (nvec << 2);
     }
-    for (int64_t x = v + lane; x < hi; x += 32) acc += weight_fx(rp, rq, x, st);
+    for (int64_t x = v + lane; x < hi; x += 32) acc += weight_fx<kSkipZero>(rp, rq, x, st);
     return warp_sum_u128(acc);
 }
 
@@ -526,7 +555,7 @@ accept_cluster_kernel(const float *__restrict__ p, const int64_t *__restrict__ p
     u128 base = 0, total = 0, target = 0;
     for (int attempt = 0; attempt < 2; ++attempt) {
         int st = 0;
-        const u128 sum = (lo < hi) ? slice_sum(rp, rq, lo, hi, vec, st) : (u128)0;
+        const u128 sum = (lo < hi) ? slice_sum<true>(rp, rq, lo, hi, vec, st) : (u128)0;
         st = __reduce_or_sync(0xffffffffu, st);
         if (lane == 0) {
             s_wsum[attempt][warp] = sum;
@@ -589,7 +618,7 @@ accept_cluster_kernel(const float *__restrict__ p, const int64_t *__restrict__ p
         while (hi - lo > 32) {
             const int64_t part = (hi - lo + kAccCWarps - 1) / kAccCWarps;
             const int64_t a = min(hi, lo + part * warp), bnd = min(hi, a + part);
-            const u128 sum = (a < bnd) ? slice_sum(rp, rq, a, bnd, false, st) : (u128)0;
+            const u128 sum = (a < bnd) ? slice_sum<true>(rp, rq, a, bnd, false, st) : (u128)0;
             if (lane == 0) sh.part[warp] = sum;
             __syncthreads();
             if (threadIdx.x == 0) {
@@ -621,7 +650,7 @@ accept_cluster_kernel(const float *__restrict__ p, const int64_t *__restrict__ p
     int64_t token = -1;
     if (warp == 0 && found >= 0) {
         const int64_t v = lo + lane;
-        const u128 r = (v < hi) ? (u128)weight_fx(rp, rq, v, st) : (u128)0;
+        const u128 r = (v < hi) ? (u128)weight_fx<true>(rp, rq, v, st) : (u128)0;
         const u128 incl = warp_scan_u128(r);
         const bool hit = (v < hi) && (((base + incl) << 24) > target);
         const uint32_t hm = __ballot_sync(0xffffffffu, hit);

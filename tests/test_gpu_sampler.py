@@ -78,6 +78,47 @@ def test_plain_softmax_special_case_general_path():
     assert np.all(pg > 0)
 
 
+def _survivors(logits, T, min_p):
+    """Tokens with exp((l - max) / T) >= min_p, per row (fp64 count; the paths are chosen on it)."""
+    l = logits.astype(np.float64)
+    return ((l - l.max(axis=1, keepdims=True)) / T >= np.log(min_p)).sum(axis=1)
+
+
+def test_sorted_survivor_path():
+    """33 to 2048 min-p survivors per row: the CTA-wide shared-memory sort of the survivors (up
+    to 32 take the one-warp register sort)."""
+    logits = synth.normal_logits(3, 20000, seed=34, std=0.8)
+    m = _survivors(logits, 0.6, 0.05)
+    assert ((m > 32) & (m <= 2048)).all(), m
+    check(logits, 0.6, 0.95, 0.05)
+
+
+def test_min_p_survivors_beyond_the_sort_capacity():
+    """More than 2048 survivors with min-p on: the radix select over the whole row, and every
+    slice's survivor list overflows, so the renormalisation reads e back."""
+    logits = synth.normal_logits(2, synth.VOCAB, seed=32, std=0.5)
+    assert (_survivors(logits, 0.6, 0.05) > 8 * 256).all()
+    check(logits, 0.6, 0.95, 0.05)
+
+
+def test_survivors_crowded_into_one_slice():
+    """The first eighth of the row (the first CTA's slice) is all survivors and overflows its
+    list, while the other slices hold a few: that CTA reads e back, the others write zeros and
+    then their kept survivors (kept ones ranked above the crowd, and survivors ranked below
+    the top-p crossing)."""
+    rng = np.random.default_rng(33)
+    V = synth.VOCAB
+    logits = rng.normal(0.0, 0.1, size=(2, V)).astype(np.float32)
+    logits[:, : V // 8] += 5.0
+    for r in range(2):
+        idx = rng.choice(np.arange(V // 8, V), size=40, replace=False)
+        logits[r, idx[:20]] = (5.6 + 0.05 * rng.standard_normal(20)).astype(np.float32)
+        logits[r, idx[20:]] = (4.2 + 0.05 * rng.standard_normal(20)).astype(np.float32)
+    assert (_survivors(logits, 0.6, 0.05) > 2048).all()
+    pg, pr, fl = check(logits, 0.6, 0.95, 0.05)
+    assert (pg[:, V // 8:] > 0).sum() >= 20
+
+
 def test_top_p_general_path_radix_select():
     check(synth.normal_logits(3, synth.VOCAB, seed=3, std=1.5), 0.8, 0.9, 0.0)
 
