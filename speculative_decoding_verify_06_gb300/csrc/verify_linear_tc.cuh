@@ -574,19 +574,50 @@ vl_tc_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__rest
                                 st_tagged(part + (size_t)b * kTcPartial + (size_t)(c0 + e) * kTcRows + rl, v[gq][e], tag);
                     } else if (row < out_f) {
                         if (!whole) {
+                            // the later CTAs' partials, two CTAs at a time: all sixteen loads in
+                            // flight together, the missing ones polled together, then added in
+                            // CTA order
                             const uint32_t b_last = tc_cta_of(o, G, (sg.rg + 1u) * n_kc - 1u);
-                            for (uint32_t bb = b + 1u; bb <= b_last; ++bb) {
+                            for (uint32_t bb = b + 1u; bb <= b_last; bb += 2u) {
+                                const bool two = bb + 1u <= b_last;
                                 const unsigned long long *src = part + (size_t)bb * kTcPartial + rl;
-                                unsigned long long w[8];
+                                unsigned long long w[2][8];
+                                uint32_t pend = 0u;
+#pragma unroll
+                                for (int i = 0; i < 2; ++i)
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e) {
+                                        w[i][e] = 0ull;
+                                        if (c0 + e < C && (i == 0 || two)) {
+                                            w[i][e] = ld_tagged(src + (size_t)i * kTcPartial + (size_t)(c0 + e) * kTcRows);
+                                            pend |= 1u << (8 * i + e);
+                                        }
+                                    }
+                                for (uint32_t it = 0;; ++it) {
+#pragma unroll
+                                    for (int i = 0; i < 2; ++i)
+#pragma unroll
+                                        for (int e = 0; e < 8; ++e)
+                                            if ((uint32_t)(w[i][e] >> 32) == tag) pend &= ~(1u << (8 * i + e));
+                                    if (pend == 0u) break;
+                                    if (it >= s_wc.limit || wait_stopped(&s_wc)) {
+                                        wait_fail(&s_wc, kStPartial);
+                                        break;
+                                    }
+                                    if (it > 64) __nanosleep(64);
+#pragma unroll
+                                    for (int i = 0; i < 2; ++i)
+#pragma unroll
+                                        for (int e = 0; e < 8; ++e)
+                                            if (pend & (1u << (8 * i + e)))
+                                                w[i][e] = ld_tagged(src + (size_t)i * kTcPartial + (size_t)(c0 + e) * kTcRows);
+                                }
 #pragma unroll
                                 for (int e = 0; e < 8; ++e)
-                                    if (c0 + e < C) w[e] = ld_tagged(src + (size_t)(c0 + e) * kTcRows);
-#pragma unroll
-                                for (int e = 0; e < 8; ++e)
-                                    if (c0 + e < C)
-                                        v[gq][e] += (uint32_t)(w[e] >> 32) == tag
-                                                        ? __uint_as_float((uint32_t)w[e])
-                                                        : wait_tagged(src + (size_t)(c0 + e) * kTcRows, tag, &s_wc);
+                                    if (c0 + e < C) {
+                                        v[gq][e] += __uint_as_float((uint32_t)w[0][e]);
+                                        if (two) v[gq][e] += __uint_as_float((uint32_t)w[1][e]);
+                                    }
                             }
                         }
 #pragma unroll
