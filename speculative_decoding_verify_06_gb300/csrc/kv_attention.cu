@@ -281,10 +281,21 @@ __global__ void __launch_bounds__(kThreads, 1) kv_attention_kernel(const KvaPara
     const unsigned char *head = P.cache + (size_t)g * P.units_cap * kUnitBytes;
     const uint32_t ring = smem_u32(smem) + warp * kRing * kUnitBytes;
     const uint32_t mb0 = smem_u32(smem + kRingBytes) + warp * kRing * 8;
+    // Units wholly before the window's first position hold only positions written by earlier
+    // passes (an append before this kernel writes from n_past on), so this warp's first copies of
+    // them go out before the dependency wait.
+    const int early_end = min(we, P.n_past / kUnitPos);
     if (lane == 0) {
 #pragma unroll
         for (int r = 0; r < kRing; ++r) mbar_init(mb0 + 8 * r, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+#pragma unroll
+        for (int r = 0; r < kRing; ++r)
+            if (wb + r < early_end) {
+                mbar_expect_tx(mb0 + 8 * r, kUnitBytes);
+                bulk_g2s(ring + r * kUnitBytes, head + (size_t)(wb + r) * kUnitBytes, kUnitBytes,
+                         mb0 + 8 * r);
+            }
     }
     griddep_wait();  // queries and cache written by the kernels before this one
     // polls after which a ring wait gives up: word 1 of the workspace minus one when it is set
@@ -325,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) kv_attention_kernel(const KvaPara
     if (lane == 0) {
 #pragma unroll
         for (int r = 0; r < kRing; ++r)
-            if (wb + r < we) {
+            if (wb + r < we && wb + r >= early_end) {
                 mbar_expect_tx(mb0 + 8 * r, kUnitBytes);
                 bulk_g2s(ring + r * kUnitBytes, head + (size_t)(wb + r) * kUnitBytes, kUnitBytes,
                          mb0 + 8 * r);
