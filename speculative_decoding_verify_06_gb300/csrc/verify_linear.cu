@@ -979,20 +979,53 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
                     for (uint32_t mm = members & sub_mask[h]; mm != 0u; mm &= mm - 1u)
                         v += park[(__ffs(mm) - 1) * kParkW + off];
                     if (owner) {
-                        // the other CTAs' partials, in CTA order: four loads in flight at a
-                        // time, then each waited for (normally already there) and added
-                        for (uint32_t bb = b + 1; bb <= b_last; bb += 4) {
-                            unsigned long long w4[4];
+                        // the other CTAs' partials, in CTA order, four loads in flight at a time;
+                        // with two ring slots per worker the missing ones are polled together,
+                        // with four (6 to 8 columns, whose registers are tighter) one at a time
+                        if constexpr (R == 2) {
+                            for (uint32_t bb = b + 1; bb <= b_last; bb += 4) {
+                                unsigned long long w4[4];
+                                uint32_t pend = 0u;
 #pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                if (bb + i <= b_last) w4[i] = ld_tagged(part + (size_t)(bb + i) * kPartialMax + e);
+                                for (int i = 0; i < 4; ++i) {
+                                    w4[i] = 0ull;
+                                    if (bb + i <= b_last) {
+                                        w4[i] = ld_tagged(part + (size_t)(bb + i) * kPartialMax + e);
+                                        pend |= 1u << i;
+                                    }
+                                }
+                                for (uint32_t it = 0;; ++it) {
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                if (bb + i > b_last) break;
-                                const float x = (uint32_t)(w4[i] >> 32) == tag
-                                                    ? __uint_as_float((uint32_t)w4[i])
-                                                    : wait_tagged(part + (size_t)(bb + i) * kPartialMax + e, tag, &s_wc);
-                                v += x;
+                                    for (int i = 0; i < 4; ++i)
+                                        if ((uint32_t)(w4[i] >> 32) == tag) pend &= ~(1u << i);
+                                    if (pend == 0u) break;
+                                    if (it >= s_wc.limit || wait_stopped(&s_wc)) {
+                                        wait_fail(&s_wc, kStPartial);
+                                        break;
+                                    }
+                                    if (it > 64) __nanosleep(64);
+#pragma unroll
+                                    for (int i = 0; i < 4; ++i)
+                                        if (pend & (1u << i)) w4[i] = ld_tagged(part + (size_t)(bb + i) * kPartialMax + e);
+                                }
+#pragma unroll
+                                for (int i = 0; i < 4; ++i)
+                                    if (bb + i <= b_last) v += __uint_as_float((uint32_t)w4[i]);
+                            }
+                        } else {
+                            for (uint32_t bb = b + 1; bb <= b_last; bb += 4) {
+                                unsigned long long w4[4];
+#pragma unroll
+                                for (int i = 0; i < 4; ++i)
+                                    if (bb + i <= b_last) w4[i] = ld_tagged(part + (size_t)(bb + i) * kPartialMax + e);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    if (bb + i > b_last) break;
+                                    const float x = (uint32_t)(w4[i] >> 32) == tag
+                                                        ? __uint_as_float((uint32_t)w4[i])
+                                                        : wait_tagged(part + (size_t)(bb + i) * kPartialMax + e, tag, &s_wc);
+                                    v += x;
+                                }
                             }
                         }
                         o.Y[(int64_t)col * out_f + row] = v;
