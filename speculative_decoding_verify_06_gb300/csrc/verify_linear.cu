@@ -980,9 +980,9 @@ vl_stream_kernel(const __grid_constant__ VlOps<MAXOPS> P, unsigned long long *__
                         v += park[(__ffs(mm) - 1) * kParkW + off];
                     if (owner) {
                         // the other CTAs' partials, in CTA order, four loads in flight at a time;
-                        // with two ring slots per worker the missing ones are polled together,
-                        // with four (6 to 8 columns, whose registers are tighter) one at a time
-                        if constexpr (R == 2) {
+                        // the missing ones polled together where the registers allow it (one
+                        // n-tile, two ring slots per worker, symmetric units), else one at a time
+                        if constexpr (NT == 1 && R == 2 && !KQ) {
                             for (uint32_t bb = b + 1; bb <= b_last; bb += 4) {
                                 unsigned long long w4[4];
                                 uint32_t pend = 0u;
