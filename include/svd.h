@@ -362,7 +362,10 @@ int svd_device_sm_count(void);
  *   kernel gave up (zero it once to watch it); its second word, when non-zero, is one more than
  *   the number of polls after which such a wait gives up (a test hook: 1 makes every wait give
  *   up at once; 0, the zero-filled value, keeps the default of about a second).  Two kernels are enqueued (the split pass and its
- *   merge, the latter a programmatic dependent launch).  Errors: SVD_ERR_INVALID_ARG for null or
+ *   merge, the latter a programmatic dependent launch).  The split pass starts copying cache
+ *   units that lie wholly before position n_past before it waits for the kernel ahead of it on
+ *   the stream: positions before n_past must not be written by a kernel still in flight there
+ *   (an append of positions n_past.. is fine).  Errors: SVD_ERR_INVALID_ARG for null or
  *   misaligned pointers, Hq % Hkv != 0, C < 1, n_past < 0, n_past + C > capacity or a scale that
  *   is not positive and finite; SVD_ERR_WORKSPACE for a short workspace.
  */
