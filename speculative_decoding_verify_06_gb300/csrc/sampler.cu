@@ -10,7 +10,8 @@
 // Both are prefixes of the same order, so the kept set is described by its last element
 // (e_cut, id_cut): v is kept iff e[v] > e_cut or (e[v] == e_cut and v <= id_cut).
 //
-// One launch per call: a cluster of kSmpSlices CTAs per row, each CTA one slice of the row,
+// One launch per call: a cluster of 16 CTAs per row (8 above 8 rows, or where a cluster of 16
+// does not fit), each CTA one slice of the row,
 // sharing their partial results through distributed shared memory:
 //   1. each CTA's max and argmax (lowest id on ties, NaN skipped); after a cluster barrier
 //      every CTA merges the slices' into the row's.  After the lm_head GEMM with its fused
@@ -36,10 +37,11 @@ namespace svd {
 
 namespace cg = cooperative_groups;
 
-constexpr int kSmpSlices = 8;                     // CTAs (one cluster) per row
+constexpr int kSmpSlicesFew = 16;                 // CTAs (one cluster) per row, up to 8 rows
+constexpr int kSmpSlicesMany = 8;                 // ... above 8 rows (the clusters fit in fewer waves)
+constexpr int kSmpFewRows = 8;
 constexpr int kSmpThreads = 1024;
 constexpr int kSortCap = 2048;                    // survivors sorted in shared memory
-constexpr int kSliceCap = kSortCap / kSmpSlices;  // survivors kept per CTA
 constexpr double kFx = 68719476736.0;             // 2^36
 constexpr int kSmpBatch = 8;                      // elements a thread loads before using them
 
@@ -122,8 +124,8 @@ __device__ __forceinline__ void cmin_merge(float &a, int &ai, float b, int bi) {
     }
 }
 
-__device__ __forceinline__ void slice_bounds(int64_t V, int blk, int64_t *lo, int64_t *hi) {
-    const int64_t S = (V + kSmpSlices - 1) / kSmpSlices;
+__device__ __forceinline__ void slice_bounds(int64_t V, int slices, int blk, int64_t *lo, int64_t *hi) {
+    const int64_t S = (V + slices - 1) / slices;
     *lo = min(V, S * blk);
     *hi = min(V, *lo + S);
 }
@@ -135,22 +137,24 @@ struct SmpShared {
     int pidx;
     unsigned long long z;    // slice mass, 2^-36 fixed point
     unsigned long long zc;   // mass of the slice's min-p survivors
-    unsigned cnt;            // survivors of the slice (may exceed kSliceCap)
+    unsigned cnt;            // survivors of the slice (may exceed the list's capacity)
     float cmin;              // smallest survivor e, largest id among equals
     int cmin_id;
     float e_cut, s_kept;     // rank 0: the row's crossing and kept mass
     int id_cut;
 };
 
-// One row per cluster of kSmpSlices CTAs (grid: slices x rows).
+// One row per cluster of SL CTAs (grid: SL x rows).
 // stats (nullable): the lm_head epilogue's per-block (max, sum of exp2((l - max) * log2e / T),
 // argmax bits) for block b of row r at stats[b * rows + r], n_sb blocks; lse (nullable): the
 // row's log-normaliser (natural log), written when the sampler is not greedy.
+template <int SL>
 __global__ void __launch_bounds__(kSmpThreads, 1)
 smp_fused_kernel(const float *__restrict__ logits, int64_t V, float T, float top_p, float min_p,
                  int greedy, float *__restrict__ probs, int32_t *__restrict__ argmax_out,
                  const float4 *__restrict__ stats, int n_sb, float *__restrict__ lse) {
-    static_assert(kSmpSlices <= 32, "one warp merges the slices");
+    static_assert(SL <= 32, "one warp merges the slices");
+    constexpr int kSliceCap = kSortCap / SL;  // survivors kept per CTA
     cg::cluster_group cl = cg::this_cluster();
     const unsigned rank = cl.block_rank();
     const int row = blockIdx.y;
@@ -161,7 +165,7 @@ smp_fused_kernel(const float *__restrict__ logits, int64_t V, float T, float top
     __shared__ int s_am;
     griddep_wait();
     int64_t lo, hi;
-    slice_bounds(V, (int)rank, &lo, &hi);
+    slice_bounds(V, SL, (int)rank, &lo, &hi);
     const float *L = logits + (int64_t)row * V;
     float *P = probs + (int64_t)row * V;
 
@@ -171,7 +175,7 @@ smp_fused_kernel(const float *__restrict__ logits, int64_t V, float T, float top
         float bv = 0.f;
         int bi = -1;
         if (stats) {
-            const int b0 = (int)((int64_t)n_sb * rank / kSmpSlices), b1 = (int)((int64_t)n_sb * (rank + 1) / kSmpSlices);
+            const int b0 = (int)((int64_t)n_sb * rank / SL), b1 = (int)((int64_t)n_sb * (rank + 1) / SL);
             for (int b = b0 + (int)threadIdx.x; b < b1; b += kSmpThreads) {
                 const float4 st = stats[(size_t)b * rows + row];
                 argmax_merge(bv, bi, st.x, __float_as_int(st.z));
@@ -200,7 +204,7 @@ smp_fused_kernel(const float *__restrict__ logits, int64_t V, float T, float top
     if (threadIdx.x < 32) {
         float bv = 0.f;
         int bi = -1;
-        if (threadIdx.x < kSmpSlices) {
+        if (threadIdx.x < SL) {
             const SmpShared *r = cl.map_shared_rank(&sh, threadIdx.x);
             bv = r->pmax;
             bi = r->pidx;
@@ -303,7 +307,7 @@ smp_fused_kernel(const float *__restrict__ logits, int64_t V, float T, float top
     // ---- 3. rank 0: the crossing (e_cut, id_cut) and the kept mass --------------------------
     if (rank == 0) {
         __shared__ unsigned long long s_key[kSortCap];
-        __shared__ unsigned s_off[kSmpSlices + 1];
+        __shared__ unsigned s_off[SL + 1];
         __shared__ unsigned long long s_Z, s_Zc;
         __shared__ float s_cmin;
         __shared__ int s_cid, s_over;
@@ -314,7 +318,7 @@ smp_fused_kernel(const float *__restrict__ logits, int64_t V, float T, float top
             unsigned c = 0;
             float cmin = 2.f;
             int cid = -1;
-            if (b < (unsigned)kSmpSlices) {
+            if (b < (unsigned)SL) {
                 const SmpShared *r = cl.map_shared_rank(&sh, b);
                 Z = r->z;
                 Zc = r->zc;
@@ -333,7 +337,7 @@ smp_fused_kernel(const float *__restrict__ logits, int64_t V, float T, float top
                 const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
                 if (b >= o) incl += y;
             }
-            if (b < (unsigned)kSmpSlices) s_off[b + 1] = incl;
+            if (b < (unsigned)SL) s_off[b + 1] = incl;
             unsigned M = c;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
@@ -663,20 +667,50 @@ int sampler_probs(const float *logits, int rows, int64_t V, const svd_sampler *s
                         s->min_p >= 0.f && s->min_p < 1.f))
         return SVD_ERR_INVALID_ARG;
     if (!ws || ws_bytes < sampler_ws_bytes(rows, V)) return SVD_ERR_WORKSPACE;
+    // 16 CTAs per row where the rows' clusters of 16 can all be resident at once on this GPU (the
+    // count is asked once), else 8
+    static int few_max = -1;
+    if (few_max < 0) {
+        int ok = 0;
+        if (cudaFuncSetAttribute(smp_fused_kernel<kSmpSlicesFew>,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+            cudaLaunchConfig_t qc = {};
+            qc.gridDim = dim3(kSmpSlicesFew, 1);
+            qc.blockDim = dim3(kSmpThreads);
+            cudaLaunchAttribute qa[1];
+            qa[0].id = cudaLaunchAttributeClusterDimension;
+            qa[0].val.clusterDim.x = kSmpSlicesFew;
+            qa[0].val.clusterDim.y = 1;
+            qa[0].val.clusterDim.z = 1;
+            qc.attrs = qa;
+            qc.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, smp_fused_kernel<kSmpSlicesFew>, &qc) == cudaSuccess)
+                ok = n;
+        }
+        (void)cudaGetLastError();
+        few_max = ok;
+    }
+    const bool few = rows <= kSmpFewRows && rows <= few_max;
+    const int slices = few ? kSmpSlicesFew : kSmpSlicesMany;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kSmpSlices, rows);
+    cfg.gridDim = dim3(slices, rows);
     cfg.blockDim = dim3(kSmpThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kSmpSlices;
+    attr[0].val.clusterDim.x = slices;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    SVD_CUDA_TRY(cudaLaunchKernelEx(&cfg, smp_fused_kernel, logits, V, s->temperature, s->top_p,
-                                    s->min_p, s->greedy ? 1 : 0, probs, argmax, stats, n_sb, lse));
+    if (few)
+        SVD_CUDA_TRY(cudaLaunchKernelEx(&cfg, smp_fused_kernel<kSmpSlicesFew>, logits, V, s->temperature,
+                                        s->top_p, s->min_p, s->greedy ? 1 : 0, probs, argmax, stats, n_sb, lse));
+    else
+        SVD_CUDA_TRY(cudaLaunchKernelEx(&cfg, smp_fused_kernel<kSmpSlicesMany>, logits, V, s->temperature,
+                                        s->top_p, s->min_p, s->greedy ? 1 : 0, probs, argmax, stats, n_sb, lse));
     return SVD_OK;
 }
 
