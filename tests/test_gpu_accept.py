@@ -195,6 +195,23 @@ def test_status_edge_cases_match_oracle():
     assert st[0] & 8 and tok[0, 0] == 5
 
 
+def test_sampler_rows_report_a_bad_q_where_p_is_zero():
+    """One window over sampler-style p rows (zero outside the kept set): the one-window cluster
+    kernel skips the residual's fixed-point work where p is zero, and must still report an
+    invalid q value there, and draw the same token as the oracle."""
+    V, k = 4096, 3
+    logits = synth.normal_logits(k + 1, V, seed=41, std=2.0)
+    pk, *_ = oracle.sampler(logits, np.float32(0.6), np.float32(0.95), np.float32(0.05))
+    p = pk.astype(np.float32)
+    q = softmax_rows(logits[:k] + synth.normal_logits(k, V, seed=42, std=1.0))
+    zero = np.nonzero(p[0] == 0)[0]
+    assert len(zero) > V // 2
+    draft = zero[:k].astype(np.int32)[None]      # p(x) = 0: rejected at the first position
+    q[0, zero[k + 5]] = np.nan                   # in the residual's row, where p is zero
+    tok, ne, st, _ = compare(p, draft, q=q, seed=5)
+    assert st[0] & 4 and ne[0] == 1 and p[0, tok[0, 0]] > 0
+
+
 def test_uniform_hook_equals_philox():
     n, k, V = 200, 3, 512
     p, q = window_pq(n, k, V, seed=77)

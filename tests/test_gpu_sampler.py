@@ -119,6 +119,18 @@ def test_survivors_crowded_into_one_slice():
     assert (pg[:, V // 8:] > 0).sum() >= 20
 
 
+def test_cluster_sizes_give_the_same_bits():
+    """Up to 8 rows run on clusters of 16 CTAs per row, more rows on clusters of 8: the slices
+    differ, the probabilities, argmaxes and kept sets must not (the masses are exact integer sums
+    and every element's value is computed alone)."""
+    logits = synth.normal_logits(12, synth.VOCAB, seed=43, std=4.389)
+    smp = svd.Sampler(0.6, 0.95, 0.05)
+    p12, a12 = sampler(logits, smp)
+    p4, a4 = sampler(logits[:4], smp)
+    assert np.array_equal(a12[:4], a4)
+    assert np.array_equal(p12[:4].view(np.uint32), p4.view(np.uint32))
+
+
 def test_top_p_general_path_radix_select():
     check(synth.normal_logits(3, synth.VOCAB, seed=3, std=1.5), 0.8, 0.9, 0.0)
 
